@@ -1,0 +1,187 @@
+"""CPU oracle for the W4A16 group-quantized linear layer (fp64, plain C).
+
+TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
+CPU-baseline leg may import this package; the product path never does. The C
+source (``oracle.c``) shares no code with the CUDA library.
+
+What it follows: the LLM170 page, introduction ("W4A16 (int4 sym g128, f16
+activations)", group 32 for the MoE models) and its Repository layout section
+(GPU kernel outputs must match the CPU reference quant lane). The quantizer
+(s = fp16(max|w|/7), q = clamp(rint(w/s), -8, 7), nibble q+8, even k in the
+low nibble) is the workload specification's reading of "int4 sym".
+
+Every function here is pinned by ``tests/test_oracle.py`` against closed
+forms, exact rational arithmetic, numpy's own binary16 conversion and the
+hand-worked fixtures in ``tests/golden/``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_CFLAGS = ["-std=c99", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc into oracle/_build/liboracle.so."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".{os.getpid()}.tmp"
+        subprocess.run(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I64 = ctypes.c_int64
+            I32 = ctypes.c_int32
+            lib.oracle_half_to_double_n.argtypes = [P, I64, P]
+            lib.oracle_float_to_half_rn_n.argtypes = [P, I64, P]
+            lib.oracle_quantize.argtypes = [P, I64, I64, I32, P, P]
+            lib.oracle_unpack.argtypes = [P, I64, I64, P]
+            lib.oracle_pack_q.argtypes = [P, I64, I64, P]
+            lib.oracle_dequantize.argtypes = [P, I64, I64, I64, I32, P]
+            lib.oracle_linear.argtypes = [P, P, P, I64, I64, I64, I32, P, P]
+            lib.oracle_grouped_linear.argtypes = [P, P, P, P, I32, I64, I64, I64, I32, P, P]
+            for f in (lib.oracle_half_to_double_n, lib.oracle_float_to_half_rn_n,
+                      lib.oracle_quantize, lib.oracle_unpack, lib.oracle_pack_q,
+                      lib.oracle_dequantize, lib.oracle_linear, lib.oracle_grouped_linear):
+                f.restype = None
+            _lib = lib
+    return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _p(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def half_bits(x) -> np.ndarray:
+    """fp16 array (or uint16 bits) -> uint16 bit patterns, no arithmetic."""
+    a = np.asarray(x)
+    if a.dtype == np.float16:
+        return np.ascontiguousarray(a).view(np.uint16)
+    return _c(a, np.uint16)
+
+
+def half_to_double(bits) -> np.ndarray:
+    b = half_bits(bits)
+    out = np.empty(b.shape, np.float64)
+    _load().oracle_half_to_double_n(_p(b), b.size, _p(out))
+    return out
+
+
+def float_to_half_bits(f) -> np.ndarray:
+    a = _c(f, np.float32)
+    out = np.empty(a.shape, np.uint16)
+    _load().oracle_float_to_half_rn_n(_p(a), a.size, _p(out))
+    return out
+
+
+def quantize(w: np.ndarray, group: int):
+    """fp32 [N, K] -> (qw uint8 [N, K/2], s fp16-bits uint16 [N, K/group])."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    assert K % group == 0 and K % 2 == 0
+    qw = np.empty((N, K // 2), np.uint8)
+    s = np.empty((N, K // group), np.uint16)
+    _load().oracle_quantize(_p(w), N, K, group, _p(qw), _p(s))
+    return qw, s
+
+
+def unpack(qw: np.ndarray, K: int) -> np.ndarray:
+    qw = _c(qw, np.uint8)
+    N = qw.shape[0]
+    q = np.empty((N, K), np.int8)
+    _load().oracle_unpack(_p(qw), N, K, _p(q))
+    return q
+
+
+def pack_q(q: np.ndarray) -> np.ndarray:
+    q = _c(q, np.int8)
+    N, K = q.shape
+    qw = np.empty((N, K // 2), np.uint8)
+    _load().oracle_pack_q(_p(q), N, K, _p(qw))
+    return qw
+
+
+def dequantize(qw: np.ndarray, s: np.ndarray, K: int, group: int) -> np.ndarray:
+    qw = _c(qw, np.uint8)
+    s = half_bits(s)
+    N = qw.shape[0]
+    out = np.empty((N, K), np.float64)
+    _load().oracle_dequantize(_p(qw), _p(s), N, K, group, _p(out))
+    return out
+
+
+def linear(x, qw, s, group: int, threads: int = 1):
+    """y = x @ W^T in fp64 and sum_k |x W^| ; x fp16 [M, K]. Returns (y, absdot).
+
+    ``threads > 1`` splits the output columns n over threads (each element's
+    sum is computed exactly as in the single-threaded case)."""
+    xb = half_bits(x)
+    M, K = xb.shape
+    qw = _c(qw, np.uint8)
+    s = half_bits(s)
+    N = qw.shape[0]
+    assert qw.shape == (N, K // 2) and s.shape == (N, K // group)
+    if threads <= 1 or N < 2 * threads:
+        y = np.empty((M, N), np.float64)
+        a = np.empty((M, N), np.float64)
+        _load().oracle_linear(_p(xb), _p(qw), _p(s), M, N, K, group, _p(y), _p(a))
+        return y, a
+    lib = _load()
+    bounds = np.linspace(0, N, threads + 1).astype(np.int64)
+
+    def part(i):
+        n0, n1 = int(bounds[i]), int(bounds[i + 1])
+        qs, ss = np.ascontiguousarray(qw[n0:n1]), np.ascontiguousarray(s[n0:n1])
+        yp = np.empty((M, n1 - n0), np.float64)
+        ap = np.empty((M, n1 - n0), np.float64)
+        lib.oracle_linear(_p(xb), _p(qs), _p(ss), M, n1 - n0, K, group, _p(yp), _p(ap))
+        return yp, ap
+
+    with ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(part, range(threads)))
+    return np.concatenate([p[0] for p in parts], 1), np.concatenate([p[1] for p in parts], 1)
+
+
+def grouped_linear(x, qw, s, offsets, group: int):
+    """Routed-expert linear over expert-sorted rows. x fp16 [R, K], qw [E, N, K/2],
+    s [E, N, K/g], offsets int32 [E+1]. Returns (y, absdot) fp64 [R, N]."""
+    xb = half_bits(x)
+    R, K = xb.shape
+    qw = _c(qw, np.uint8)
+    s = half_bits(s)
+    off = _c(offsets, np.int32)
+    E, N = qw.shape[0], qw.shape[1]
+    assert off.shape == (E + 1,) and off[0] == 0 and off[-1] == R
+    y = np.zeros((R, N), np.float64)
+    a = np.zeros((R, N), np.float64)
+    _load().oracle_grouped_linear(_p(xb), _p(qw), _p(s), _p(off), E, R, N, K, group, _p(y), _p(a))
+    return y, a
+
+
+def tolerance(y_ref: np.ndarray, absdot: np.ndarray) -> np.ndarray:
+    """Per-element bound |y - y_ref| <= 2^-9 |y_ref| + 1e-4 sum_k |x_k W^_nk|."""
+    return np.ldexp(np.abs(y_ref), -9) + 1e-4 * absdot

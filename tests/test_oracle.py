@@ -1,0 +1,303 @@
+"""Pins for the CPU oracle (no GPU needed).
+
+Each test checks the oracle against something other than itself: numpy's own
+binary16 conversion, hand-worked fixtures (tests/golden/), exact rational
+arithmetic, closed forms and invariants of y = x W^T with W^ = s * q.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from conftest import GOLDEN
+
+
+# ------------------------------------------------------------------ fixtures
+
+def _golden_lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield line
+
+
+def _quantize_cases():
+    cases, cur = [], None
+    for line in _golden_lines("quantize_groups.txt"):
+        key, _, rest = line.partition(" ")
+        if key == "case":
+            name, g = rest.split()
+            cur = dict(name=name, g=int(g))
+            cases.append(cur)
+        elif key == "w":
+            cur["w"] = [np.float32(v) for v in rest.split()]
+        elif key == "s":
+            cur["s"] = [int(v, 16) for v in rest.split()]
+        elif key == "q":
+            cur["q"] = {int(a): int(b) for a, b in (t.split(":") for t in rest.split())}
+        elif key == "bytes":
+            cur["bytes"] = [int(v, 16) for v in rest.split()]
+    return cases
+
+
+# -------------------------------------------------------------- fp16 pins
+
+def test_half_to_double_all_bit_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.half_to_double(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert np.signbit(ours[0x8000]) and not np.signbit(ours[0])
+
+
+def test_float_to_half_matches_numpy():
+    g = np.random.default_rng(1)
+    parts = [
+        g.normal(0, 1, 200_000),
+        g.normal(0, 1e-5, 50_000),                       # subnormal fp16 range
+        g.normal(0, 3e4, 50_000),                        # near overflow
+        np.ldexp(g.uniform(1, 2, 50_000), g.integers(-30, 18, 50_000)),
+    ]
+    f = np.concatenate(parts).astype(np.float32)
+    # exact ties between two fp16 neighbours, normal and subnormal
+    h = g.integers(0, 0x7BFF, 20_000).astype(np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    ties = ((lo + hi) / 2).astype(np.float32)
+    f = np.concatenate([f, ties, -ties, np.float32([65504, 65519.99, 65520, 1e9, -1e9, 0.0, -0.0,
+                                                     np.inf, -np.inf])])
+    ours = oracle.float_to_half_bits(f)
+    ref = f.astype(np.float16).view(np.uint16)
+    assert np.array_equal(ours, ref)
+    assert np.isnan(oracle.half_to_double(oracle.float_to_half_bits(np.float32([np.nan])))[0])
+
+
+# ---------------------------------------------------------- format pins
+
+def test_nibble_order_golden():
+    rows = [line.split() for line in _golden_lines("nibble_order.txt")]
+    b = np.array([[int(r[0], 16) for r in rows]], np.uint8)
+    q = oracle.unpack(b, 2 * b.shape[1])
+    assert q[0, 0::2].tolist() == [int(r[1]) for r in rows]
+    assert q[0, 1::2].tolist() == [int(r[2]) for r in rows]
+
+
+def test_pack_unpack_round_trip_all_bytes():
+    b = np.arange(256, dtype=np.uint8).reshape(4, 64)
+    q = oracle.unpack(b, 128)
+    assert q.min() == -8 and q.max() == 7
+    assert np.array_equal(oracle.pack_q(q), b)
+    # every (even, odd) pair of q values appears exactly once
+    pairs = set(zip(q[:, 0::2].ravel().tolist(), q[:, 1::2].ravel().tolist()))
+    assert len(pairs) == 256
+
+
+@pytest.mark.parametrize("case", _quantize_cases(), ids=lambda c: c["name"])
+def test_quantize_golden(case):
+    g = case["g"]
+    K = g * len(case["s"])
+    w = np.zeros((1, K), np.float32)
+    w[0, :len(case["w"])] = case["w"]
+    qw, s = oracle.quantize(w, g)
+    assert s[0].tolist() == case["s"]
+    q = oracle.unpack(qw, K)[0]
+    want = np.zeros(K, np.int64)
+    for k, v in case["q"].items():
+        want[k] = v
+    assert q.tolist() == want.tolist()
+    bytes_want = [0x88] * (K // 2)
+    bytes_want[:len(case["bytes"])] = case["bytes"]
+    assert qw[0].tolist() == bytes_want
+
+
+def test_quantize_invariants():
+    g = workloads.rng(3)
+    for group in (32, 64, 128):
+        W = workloads.weights(g, 48, 512)
+        qw, s = oracle.quantize(W, group)
+        q = oracle.unpack(qw, 512).astype(np.float64)
+        sd = oracle.half_to_double(s)
+        sk = np.repeat(sd, group, axis=1)
+        Wg = W.astype(np.float64).reshape(48, -1, group)
+        amax = np.abs(Wg).max(axis=2)
+        # the scale is amax/7 to within fp16 rounding (relative 2^-11)
+        assert np.all(np.abs(sd * 7 - amax) <= amax * 2.0 ** -11 * 7 / 6.9)
+        # the element of largest magnitude lands on +-7
+        arg = np.abs(Wg).argmax(axis=2)
+        qg = q.reshape(48, -1, group)
+        assert np.all(np.abs(np.take_along_axis(qg, arg[..., None], 2)) == 7)
+        # round to nearest: |w - s q| <= s/2 (plus fp32 quotient rounding)
+        err = np.abs(W - sk * q)
+        assert np.all(err <= sk * (0.5 + 2.0 ** -20))
+        assert q.min() >= -8 and q.max() <= 7
+        # odd symmetry and power-of-two scale invariance
+        qw_n, s_n = oracle.quantize(-W, group)
+        assert np.array_equal(s_n, s)
+        assert np.array_equal(oracle.unpack(qw_n, 512), -oracle.unpack(qw, 512))
+        qw_2, s_2 = oracle.quantize(W * np.float32(4), group)
+        assert np.array_equal(qw_2, qw)
+        assert np.array_equal(oracle.half_to_double(s_2), 4 * sd)
+
+
+# ---------------------------------------------------------- linear pins
+
+def _raw(seed, M, N, K, g):
+    r = workloads.rng(seed)
+    qw, s = workloads.raw_packed(r, N, K, g)
+    x = workloads.activations(r, M, K)
+    return x, qw, s
+
+
+def test_linear_golden_tiny():
+    cases = {c["name"]: c for c in _quantize_cases()}
+    rows = []
+    for name in ("A", "B"):
+        w = np.zeros((1, 32), np.float32)
+        w[0, :len(cases[name]["w"])] = cases[name]["w"]
+        rows.append(oracle.quantize(w, 32))
+    qw = np.concatenate([r[0] for r in rows])
+    s = np.concatenate([r[1] for r in rows])
+    x = np.zeros((2, 32), np.float16)
+    x[0, :] = 1
+    x[1, 0], x[1, 1] = 1, 2
+    y, _ = oracle.linear(x, qw, s, 32)
+    for line in _golden_lines("linear_tiny.txt"):
+        _, m, n, v = line.split()
+        assert y[int(m), int(n)] == float(v)
+
+
+@pytest.mark.parametrize("M,N,K,g", [(1, 3, 32, 32), (2, 5, 64, 32), (3, 4, 128, 64),
+                                     (2, 3, 256, 128), (1, 2, 384, 128)])
+def test_linear_exact_rational(M, N, K, g):
+    """fp64 oracle vs the exact sum (fp16 values are dyadic rationals)."""
+    x, qw, s = _raw(7 + K, M, N, K, g)
+    y, absdot = oracle.linear(x, qw, s, g)
+    xb = x.view(np.uint16)
+    sb = s.view(np.uint16)
+    for m in range(M):
+        for n in range(N):
+            exact = Fraction(0)
+            for j in range(K // g):
+                sc = Fraction(float(np.uint16(sb[n, j]).view(np.float16)))
+                for k in range(j * g, (j + 1) * g):
+                    byte = int(qw[n, k // 2])
+                    nib = (byte >> 4) if (k % 2) else (byte & 15)
+                    xv = Fraction(float(np.uint16(xb[m, k]).view(np.float16)))
+                    exact += xv * sc * (nib - 8)
+            assert abs(Fraction(y[m, n]) - exact) <= Fraction(K * 2.0 ** -52) * Fraction(absdot[m, n])
+
+
+def test_linear_zero_weights_give_zero():
+    x, _, s = _raw(11, 3, 7, 256, 64)
+    qw = np.full((7, 128), 0x88, np.uint8)      # every q = 0
+    y, a = oracle.linear(x, qw, s, 64)
+    assert np.all(y == 0) and np.all(a == 0)
+
+
+def test_linear_one_hot_x_reads_one_weight():
+    K, N, g = 256, 6, 32
+    _, qw, s = _raw(12, 1, N, K, g)
+    q = oracle.unpack(qw, K)
+    sd = oracle.half_to_double(s)
+    for k in (0, 1, 31, 32, 77, 255):
+        x = np.zeros((1, K), np.float16)
+        x[0, k] = 1
+        y, _ = oracle.linear(x, qw, s, g)
+        assert np.array_equal(y[0], sd[:, k // g] * q[:, k])
+
+
+@pytest.mark.parametrize("c", [-8, -3, 0, 5, 7])
+def test_linear_constant_q_closed_form(c):
+    K, N, g = 512, 5, 128
+    _, _, s = _raw(13, 1, N, K, g)
+    qw = np.full((N, K // 2), ((c + 8) | ((c + 8) << 4)), np.uint8)
+    x = np.ones((1, K), np.float16)
+    y, _ = oracle.linear(x, qw, s, g)
+    sd = oracle.half_to_double(s)
+    assert np.array_equal(y[0], c * g * sd.sum(axis=1))
+
+
+def test_linear_unit_scales_match_numpy_matmul():
+    M, N, K, g = 4, 33, 640, 64
+    x, qw, _ = _raw(14, M, N, K, g)
+    s = np.ones((N, K // g), np.float16)
+    q = oracle.unpack(qw, K).astype(np.float64)
+    y, a = oracle.linear(x, qw, s, g)
+    ref = x.astype(np.float64) @ q.T
+    assert np.all(np.abs(y - ref) <= K * 2.0 ** -52 * a)
+
+
+def test_linear_is_linear_in_x():
+    M, N, K, g = 2, 9, 512, 128
+    _, qw, s = _raw(15, 1, N, K, g)
+    r = workloads.rng(16)
+    x1 = r.integers(-32, 33, (M, K)).astype(np.float16)   # small integers: sums exact
+    x2 = r.integers(-32, 33, (M, K)).astype(np.float16)
+    x3 = (3 * x1.astype(np.float64) - 2 * x2.astype(np.float64)).astype(np.float16)
+    y1, a1 = oracle.linear(x1, qw, s, g)
+    y2, a2 = oracle.linear(x2, qw, s, g)
+    y3, a3 = oracle.linear(x3, qw, s, g)
+    assert np.all(np.abs(y3 - (3 * y1 - 2 * y2)) <= K * 2.0 ** -50 * (a3 + 3 * a1 + 2 * a2))
+
+
+def test_linear_group_permutation_invariance():
+    M, N, K, g = 3, 8, 512, 64
+    x, qw, s = _raw(17, M, N, K, g)
+    perm = workloads.rng(18).permutation(K // g)
+    kidx = np.concatenate([np.arange(p * g, (p + 1) * g) for p in perm])
+    bidx = np.concatenate([np.arange(p * g // 2, (p + 1) * g // 2) for p in perm])
+    y, a = oracle.linear(x, qw, s, g)
+    yp, _ = oracle.linear(np.ascontiguousarray(x[:, kidx]), np.ascontiguousarray(qw[:, bidx]),
+                          np.ascontiguousarray(s[:, perm]), g)
+    assert np.all(np.abs(yp - y) <= K * 2.0 ** -51 * a)
+
+
+def test_grouped_equals_loop_of_dense_calls():
+    E, N, K, g = 6, 10, 256, 32
+    r = workloads.rng(19)
+    qw = r.integers(0, 256, (E, N, K // 2), dtype=np.uint8)
+    s = (np.abs(r.normal(0, 0.02, (E, N, K // g))) / 7).astype(np.float16)
+    counts = np.array([3, 0, 5, 1, 0, 7])                 # empty experts included
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    x = workloads.activations(r, int(off[-1]), K)
+    y, a = oracle.grouped_linear(x, qw, s, off, g)
+    for e in range(E):
+        if counts[e]:
+            ye, ae = oracle.linear(x[off[e]:off[e + 1]], qw[e], s[e], g)
+            assert np.array_equal(y[off[e]:off[e + 1]], ye)
+            assert np.array_equal(a[off[e]:off[e + 1]], ae)
+    y1, _ = oracle.grouped_linear(x, qw[:1], s[:1], np.int32([0, off[-1]]), g)
+    assert np.array_equal(y1, oracle.linear(x, qw[0], s[0], g)[0])
+
+
+def test_threaded_linear_equals_single_thread():
+    x, qw, s = _raw(20, 3, 101, 256, 128)
+    y1, a1 = oracle.linear(x, qw, s, 128)
+    y4, a4 = oracle.linear(x, qw, s, 128, threads=4)
+    assert np.array_equal(y1, y4) and np.array_equal(a1, a4)
+
+
+# ------------------------------------------------------------ workloads
+
+def test_workloads_are_seeded_and_shaped():
+    W, x, g = workloads.config0()
+    W2, x2, _ = workloads.config0()
+    assert W.shape == (256, 1024) and x.shape == (1, 1024) and g == 128
+    assert np.array_equal(W, W2) and np.array_equal(x, x2)
+    assert abs(W.std() - 0.02) < 0.001
+    _, xp, _ = workloads.prefill(8, K=1000, N=4)
+    big = np.abs(xp.astype(np.float32)).max(axis=0) > 0
+    assert xp.dtype == np.float16 and big.all()
+    r = workloads.routing(workloads.rng(0), 64, 16, 4)
+    assert r.offsets[0] == 0 and r.offsets[-1] == 256
+    assert np.all(np.diff(r.offsets) >= 0)
+    assert np.all(np.diff(r.expert_of_row) >= 0)
+    pairs = set(zip(r.token_of_row.tolist(), r.expert_of_row.tolist()))
+    assert len(pairs) == 256                               # distinct experts per token
