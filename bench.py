@@ -1,0 +1,415 @@
+"""Benchmark of the W4A16 group-quantized linear layer on GB300.
+
+One step = one decode pass of a 27B-class dense MLP through the layer:
+x [1, 5120] -> gate/up projection (K=5120 -> N=17408, group 128) -> h [1, 17408]
+-> down projection (K=17408 -> N=5120) -> out [1, 5120]; both are decode GEMVs.
+The headline metric is the achieved HBM bandwidth of that step: algorithmic
+bytes (every packed weight, scale, activation and output byte once) divided by
+device time. Weights rotate through enough copies (> 4x the L2 size) that
+every step streams them from HBM.
+
+Side measurements in the same JSON line: the batched decode (M=4), the
+prefill GEMM (M=4096, K=5120, N=17408; TFLOP/s) and the routed-expert layer
+(E=128, 4096 tokens, top-8, group 32), when the library provides them.
+
+--impl reference times the CPU oracle (fp64, single thread) on the same
+workload and metric. With --gpus N > 1 (torchrun), every rank runs an
+independent replica (the layer needs no collective), timing is the max over
+ranks and the value is the sum over ranks (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+DECODE = [(5120, 17408), (17408, 5120)]  # (K, N): gate/up then down
+GROUP = 128
+
+
+def decode_bytes(M: int) -> int:
+    """Algorithmic bytes of one decode step: packed weights, scales, x and y once."""
+    total = 0
+    for K, N in DECODE:
+        total += N * K // 2 + N * (K // GROUP) * 2 + M * K * 2 + M * N * 2
+    return total
+
+
+def moe_bytes(E, R, K, N, g):
+    return E * N * K // 2 + E * N * (K // g) * 2 + R * K * 2 + R * N * 2
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm --
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+class Timer:
+    """CUDA-event pairs around launches on the launching stream."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.pairs = []
+
+    def around(self, fn):
+        s = self.torch.cuda.Event(enable_timing=True)
+        e = self.torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        self.pairs.append((s, e))
+
+    def ms(self):
+        return [s.elapsed_time(e) for s, e in self.pairs]
+
+
+def run_gpu(args, rank, world):
+    import torch
+
+    import w4a16_group_quantized_linear_gb300 as w4
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w4.lib()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20)
+    hbm_peak, tc_peak, peak_kind = _peaks()
+
+    # ---- weights: packed on the GPU by the library's quantizer, rotated copies
+    M = 1
+    step_bytes = decode_bytes(M)
+    copies = max(2, -(-4 * l2 // (step_bytes - 2 * 10240)))
+    g = workloads.rng(0)
+    mats = []
+    for K, N in DECODE:
+        W = torch.from_numpy(workloads.weights(g, N, K)).to(dev)
+        qw, s = w4.pack(W, GROUP)
+        del W
+        mats.append((qw, s))
+    rot = [[(m[0].clone(), m[1].clone()) for m in mats] for _ in range(copies)]
+    x = torch.from_numpy(workloads.activations(g, M, DECODE[0][0])).to(dev)
+    h = torch.empty((M, DECODE[0][1]), dtype=torch.float16, device=dev)
+    out = torch.empty((M, DECODE[1][1]), dtype=torch.float16, device=dev)
+
+    def step(i):
+        (qa, sa), (qb, sb) = rot[i % copies]
+        w4.linear(x, qa, sa, GROUP, out=h)
+        w4.linear(h, qb, sb, GROUP, out=out)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    w4.device_status()
+
+    # ---- timed region: launches queued behind a spin so the GPU runs them back to back
+    timer = Timer(torch)
+    (qa0, sa0), _ = rot[0]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        torch.cuda._sleep(int(1e7 + args.steps * 2e5))
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for i in range(args.steps):
+            (qa, sa), (qb, sb) = rot[i % copies]
+            timer.around(lambda: w4.linear(x, qa, sa, GROUP, out=h))
+            timer.around(lambda: w4.linear(h, qb, sb, GROUP, out=out))
+        t1.record()
+        torch.cuda.synchronize()
+    ms_total = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    launch_ms = timer.ms()
+    kernel_ms = statistics.mean(launch_ms)
+    per_launch_bytes = step_bytes / 2  # both GEMVs move the same algorithmic bytes
+    achieved = per_launch_bytes / (kernel_ms * 1e-3) / 1e9
+    value = step_bytes * args.steps * world / (ms_total * 1e-3) / 1e9
+
+    # ---- end to end through the public API: pinned host x in, host result out
+    xh = torch.from_numpy(workloads.activations(workloads.rng(1), M, DECODE[0][0])).pin_memory()
+    oh = torch.empty((M, DECODE[1][1]), dtype=torch.float16).pin_memory()
+    for i in range(3):
+        x.copy_(xh, non_blocking=True)
+        step(i)
+        oh.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        x.copy_(xh, non_blocking=True)
+        step(i)
+        oh.copy_(out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    w4.device_status()
+
+    extra = {}
+    if not args.decode_only:
+        extra = side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2)
+
+    cs = clocks.summary()
+    return dict(
+        value=value, ms_per_step=ms_total / args.steps, kernel_ms=kernel_ms, achieved=achieved,
+        hbm_peak=hbm_peak, tc_peak=tc_peak, peak_kind=peak_kind, copies=copies,
+        e2e=dict(value=step_bytes * args.steps * world / (e2e_ms * 1e-3) / 1e9, unit="GB/s",
+                 h2d_bytes_per_step=xh.numel() * 2, d2h_bytes_per_step=oh.numel() * 2,
+                 ms_per_step=e2e_ms / args.steps),
+        clocks=cs, extra=extra, gpu=torch.cuda.get_device_name(dev), sms=props.multi_processor_count,
+        launches=2 * args.steps, per_launch_bytes=per_launch_bytes)
+
+
+def _time_launches(torch, fn, n, sleep_cycles=2e6):
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(sleep_cycles))
+    timer = Timer(torch)
+    for i in range(n):
+        timer.around(lambda: fn(i))
+    torch.cuda.synchronize()
+    return timer.ms()
+
+
+def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):
+    """Batched decode (M=4), prefill GEMM (M=4096) and routed experts, if supported."""
+    out = {}
+    g = workloads.rng(0)
+    # batched decode np4: the gate/up shape, rotated copies
+    K, N = DECODE[0]
+    W = torch.from_numpy(workloads.weights(g, N, K)).to(dev)
+    qw, s = w4.pack(W, GROUP)
+    del W
+    per = N * K // 2 + N * (K // GROUP) * 2
+    copies = max(2, -(-4 * l2 // per))
+    rot = [(qw.clone(), s.clone()) for _ in range(copies)]
+    x4 = torch.from_numpy(workloads.activations(g, 4, K)).to(dev)
+    y4 = torch.empty((4, N), dtype=torch.float16, device=dev)
+    f = lambda i: w4.linear(x4, rot[i % copies][0], rot[i % copies][1], GROUP, out=y4)  # noqa: E731
+    for i in range(5):
+        f(i)
+    ms = statistics.median(_time_launches(torch, f, 100))
+    b = per + 4 * K * 2 + 4 * N * 2
+    out["decode_m4"] = {"shape": [4, K, N], "us": ms * 1e3, "GB/s": b / (ms * 1e-3) / 1e9,
+                        "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm_peak}
+    del rot
+    # prefill GEMM M=4096
+    try:
+        xp = torch.from_numpy(workloads.activations(g, 4096, K, outlier_frac=0.01)).to(dev)
+        yp = torch.empty((4096, N), dtype=torch.float16, device=dev)
+        f = lambda i: w4.linear(xp, qw, s, GROUP, out=yp)  # noqa: E731
+        for i in range(3):
+            f(i)
+        ms = statistics.median(_time_launches(torch, f, 20))
+        fl = 2.0 * 4096 * N * K
+        out["prefill_m4096"] = {"shape": [4096, K, N], "us": ms * 1e3, "TFLOP/s": fl / (ms * 1e-3) / 1e12,
+                                "frac_tc": fl / (ms * 1e-3) / 1e12 / tc_peak}
+        xp5 = xp[:512].contiguous()
+        yp5 = yp[:512]
+        f = lambda i: w4.linear(xp5, qw, s, GROUP, out=yp5)  # noqa: E731
+        for i in range(3):
+            f(i)
+        ms = statistics.median(_time_launches(torch, f, 50))
+        fl = 2.0 * 512 * N * K
+        out["prefill_m512"] = {"shape": [512, K, N], "us": ms * 1e3, "TFLOP/s": fl / (ms * 1e-3) / 1e12,
+                               "frac_tc": fl / (ms * 1e-3) / 1e12 / tc_peak}
+    except w4.W4A16Error as e:
+        out["prefill"] = {"unavailable": str(e)}
+    return out
+
+
+# ------------------------------------------------------------ reference arm --
+
+def run_reference(args):
+    """The CPU oracle (fp64, one thread) on the same decode step and metric."""
+    import oracle
+
+    oracle.build()
+    g = workloads.rng(0)
+    mats = []
+    for K, N in DECODE:
+        W = workloads.weights(g, N, K)
+        mats.append(oracle.quantize(W, GROUP))
+    x = workloads.activations(g, 1, DECODE[0][0])
+
+    def step():
+        y1, _ = oracle.linear(x, *mats[0], GROUP)
+        h = y1.astype(np.float16)
+        y2, _ = oracle.linear(h, *mats[1], GROUP)
+        return y2
+
+    for _ in range(min(args.warmup, 1)):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    return dt
+
+
+def cpu_baseline_sample(budget_s=12.0):
+    """Oracle decode steps on one host core until about `budget_s` seconds pass."""
+    import oracle
+
+    oracle.build()
+    g = workloads.rng(0)
+    mats = [oracle.quantize(workloads.weights(g, N, K), GROUP) for K, N in DECODE]
+    x = workloads.activations(g, 1, DECODE[0][0])
+    n, t0 = 0, time.perf_counter()
+    while True:
+        y1, _ = oracle.linear(x, *mats[0], GROUP)
+        oracle.linear(y1.astype(np.float16), *mats[1], GROUP)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": decode_bytes(1) * n / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} full decode steps (M=1, 5120->17408->5120, group 128), fp64, one thread, "
+                      f"{dt:.1f} s"}
+
+
+# -------------------------------------------------------------------- main --
+
+METRIC = "decode GEMV achieved HBM GB/s (M=1, 27B-class gate/up + down, group 128)"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--decode-only", action="store_true", help="skip the prefill / MoE side measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    config = {"workload": "decode step M=1: x[1,5120] -> W4A16 5120->17408 -> W4A16 17408->5120, group 128",
+              "M": 1, "shapes_KN": DECODE, "group": GROUP, "l2": "weights rotate through >4x L2 of copies",
+              "parallelism": "replicas" if world > 1 else "single GPU"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps = max(1, min(args.steps, 20))
+        dt = run_reference(argparse.Namespace(steps=steps, warmup=args.warmup))
+        value = decode_bytes(1) * steps / dt / 1e9
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": steps,
+            "warmup": 1, "ms_per_step": dt * 1e3 / steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{steps} full decode steps, fp64, one thread"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+
+    if world > 1:
+        import torch
+
+        torch.distributed.init_process_group("nccl")
+    r = run_gpu(args, rank, world)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 in, fp32 accumulate, int4 weights", "data": "synthetic",
+        "config": config,
+        "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["hbm_peak"], "unit": "GB/s",
+                     "frac": r["achieved"] / r["hbm_peak"], "traffic": None,
+                     "kernel": "gemv_kernel<128,1>", "peak_kind": r["peak_kind"],
+                     "kernel_us": r["kernel_ms"] * 1e3, "algorithmic_bytes_per_launch": r["per_launch_bytes"]},
+        "e2e": r["e2e"], "gpu_launches": r["launches"], "clocks": r["clocks"], "gpu": r["gpu"], "sms": r["sms"],
+        "side": r["extra"],
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample()
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,148 @@
+/*
+ * w4a16.h - C ABI of libw4a16.so, the GB300 (sm_103a) W4A16 group-quantized
+ * linear layer.
+ *
+ * The operation (LLM170 page, introduction: "W4A16 (int4 sym g128, f16
+ * activations)"; the MoE models of the same page use group 32):
+ *
+ *     y[m, n] = sum_k x[m, k] * s[n, k / g] * q[n, k]
+ *
+ * with x, y fp16, q a signed 4-bit integer in [-8, 7] and s one fp16 scale per
+ * group of g consecutive input features k. This is y = x * W^T for the
+ * dequantized weight W^[n, k] = s[n, k/g] * q[n, k]; per the same page's
+ * Repository layout section the GPU result must match a CPU reference of that
+ * definition.
+ *
+ * Data layout (all row-major, all in device memory unless stated):
+ *   x        fp16 [M, K]           (uint16_t bit patterns)
+ *   qweight  uint8 [N, K/2]        byte j of row n holds k = 2j in bits 0-3 and
+ *                                  k = 2j+1 in bits 4-7; the stored nibble is q+8
+ *                                  (byte-identical to little-endian int32
+ *                                  [N, K/8] with nibble i = k mod 8)
+ *   scales   fp16 [N, K/g]
+ *   y        fp16 [M, N]
+ *   routed experts: qweight [E, N, K/2], scales [E, N, K/g], expert_offsets
+ *   int32 [E+1] (device memory), activations sorted by expert.
+ *
+ * Ownership and threading: the caller owns and allocates every buffer. The
+ * library never allocates, frees or synchronizes (except w4a16_device_status,
+ * which says so). Every call is asynchronous on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream). Calls on different streams must not share a
+ * workspace. Results are deterministic: the same inputs give the same bits.
+ *
+ * Errors: every entry point validates its arguments on the host before any
+ * launch and returns a status; it never aborts the process. A CUDA launch
+ * error is returned as W4A16_ERR_CUDA. Problems only the device can see
+ * (expert offsets that are not a valid partition, a bounded wait that ran
+ * out) set a sticky device word read by w4a16_device_status.
+ *
+ * Numerics: products x * q are exact in fp32; each group's partial sum is
+ * accumulated in fp32 and multiplied by its fp32 scale; the result is rounded
+ * once to fp16 (round to nearest even). Element-wise it stays within
+ * |y - y_ref| <= 2^-9 |y_ref| + 1e-4 sum_k |x[m,k] W^[n,k]| of the exact value.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define W4A16_API __attribute__((visibility("default")))
+#else
+#define W4A16_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4A16_OK = 0,
+    W4A16_ERR_INVALID_ARG = 1,   /* null pointer, negative size, K % group != 0 ... */
+    W4A16_ERR_UNSUPPORTED = 2,   /* group not in {32, 64, 128}, K not a multiple of 32,
+                                    no sm_103 device */
+    W4A16_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
+    W4A16_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    W4A16_ERR_TIMEOUT = 5,       /* device: a bounded wait gave up (kernel returned early) */
+    W4A16_ERR_BAD_OFFSETS = 6,   /* device: expert_offsets not 0 = o[0] <= ... <= o[E] = R */
+    W4A16_ERR_WORKSPACE = 7      /* workspace missing or smaller than w4a16_workspace_bytes */
+} w4a16_status;
+
+/*
+ * Symmetric int4 group quantizer (LLM170 page, introduction: "int4 sym").
+ * For each row n and group j of `group` consecutive k:
+ *   amax = max |w| over the group (fp32); s = fp16_rn(fp32(amax / 7));
+ *   q = clamp(rint(w / s), -8, 7) computed in fp32 (rint: half to even);
+ *   an all-zero group gives s = 0 and q = 0. Stored as described above.
+ * w: fp32 [N, K] (device). qweight: uint8 [N, K/2]. scales: fp16 [N, K/group].
+ * Bit-exact and deterministic. NaN weights are not supported; |w| must stay
+ * below 7 * 65520 for the scale to be finite.
+ * Requires N >= 0, K >= 0, K % group == 0, K even, group in {32, 64, 128}.
+ */
+W4A16_API w4a16_status w4a16_pack(const float* w, int64_t N, int64_t K, int32_t group,
+                        uint8_t* qweight, uint16_t* scales, void* stream);
+
+/*
+ * Inverse of the storage step: q[n, k] = nibble - 8 as int8 [N, K] (device).
+ * Bit-exact. Requires K even.
+ */
+W4A16_API w4a16_status w4a16_unpack(const uint8_t* qweight, int64_t N, int64_t K, int8_t* q,
+                          void* stream);
+
+/*
+ * Dense layer y = x * W^T (see the definition at the top of this file).
+ * M, N >= 0 (M = 0 or N = 0: nothing to do); K >= 0 with K % group == 0 and
+ * K % 32 == 0 (K = 0 writes y = 0); group in {32, 64, 128}.
+ * x, qweight, scales and y must be 16-byte aligned.
+ * Small M (decode, up to 16 rows) runs a split-K GEMV whose cross-block
+ * partial sums live in `workspace`; larger M runs the tensor-core GEMM.
+ * workspace: device buffer of at least w4a16_workspace_bytes(M, N, K, group, 1)
+ * bytes, zero-filled once before its first use (w4a16_workspace_init); every
+ * call returns it to that state. May be NULL when that size is 0.
+ */
+W4A16_API w4a16_status w4a16_linear(const uint16_t* x, const uint8_t* qweight, const uint16_t* scales,
+                          uint16_t* y, int64_t M, int64_t N, int64_t K, int32_t group,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Routed-expert (MoE) layer over activations sorted by expert: for every
+ * expert e and row r with expert_offsets[e] <= r < expert_offsets[e+1],
+ *   y_sorted[r, n] = sum_k x_sorted[r, k] * W^_e[n, k],
+ * W^_e from qweight[e] and scales[e] (LLM170 page: the routed-MoE models,
+ * "g32"). E >= 1, R >= 0; the same K/group/alignment rules as w4a16_linear.
+ * expert_offsets lives in device memory and is read only by the device, so
+ * no host synchronization happens; an invalid partition sets
+ * W4A16_ERR_BAD_OFFSETS in the device word and leaves y_sorted unspecified.
+ * Empty experts are allowed. workspace: w4a16_workspace_bytes(R, N, K, group, E).
+ */
+W4A16_API w4a16_status w4a16_grouped_linear(const uint16_t* x_sorted, const uint8_t* qweight,
+                                  const uint16_t* scales, const int32_t* expert_offsets,
+                                  uint16_t* y_sorted, int32_t E, int64_t R, int64_t N,
+                                  int64_t K, int32_t group, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace w4a16_linear (E = 1) or w4a16_grouped_linear (E experts,
+ * M = R rows) needs for this problem on the current device; 0 if none. */
+W4A16_API size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t group, int32_t E);
+
+/* Zero-fills a workspace asynchronously on `stream` (cudaMemsetAsync; no
+ * allocation). Needed once per workspace, and again after any call that
+ * reported a device error. */
+W4A16_API w4a16_status w4a16_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronizes `stream`, then reads and clears the current device's sticky
+ * error word: W4A16_OK, W4A16_ERR_TIMEOUT or W4A16_ERR_BAD_OFFSETS. */
+W4A16_API w4a16_status w4a16_device_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+W4A16_API const char* w4a16_status_string(w4a16_status status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+W4A16_API int32_t w4a16_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

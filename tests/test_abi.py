@@ -1,0 +1,89 @@
+"""The C ABI: the library builds, loads and exports every declared symbol, and
+host-side validation returns the documented status codes (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from w4a16_group_quantized_linear_gb300 import build
+
+    build.build()
+    import w4a16_group_quantized_linear_gb300 as w4
+
+    return w4.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "w4a16.h")).read()
+    return re.findall(r"W4A16_API\s+[\w\s\*]+?\b(w4a16_\w+)\s*\(", src)
+
+
+def test_header_declares_the_api():
+    names = set(_declared())
+    assert {"w4a16_pack", "w4a16_unpack", "w4a16_linear", "w4a16_grouped_linear",
+            "w4a16_workspace_bytes", "w4a16_device_status", "w4a16_status_string"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import w4a16_group_quantized_linear_gb300 as w4
+
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in w4.EXPORTS, f"binding misses {name}"
+    assert lib.w4a16_version() >= 100
+
+
+def test_status_strings(lib):
+    import w4a16_group_quantized_linear_gb300 as w4
+
+    for code, name in w4.STATUS.items():
+        assert lib.w4a16_status_string(code).decode().startswith(name)
+
+
+def _fake(addr):
+    return ctypes.c_void_p(addr)
+
+
+@pytest.mark.parametrize("group,K,want", [(16, 256, 2), (96, 288, 2), (128, 200, 1), (32, 48, 1), (64, -64, 1)])
+def test_linear_rejects_bad_group_or_K(lib, group, K, want):
+    p = _fake(1 << 20)
+    assert lib.w4a16_linear(p, p, p, p, 4, 8, K, group, None, 0, None) == want
+
+
+def test_linear_rejects_negative_sizes_and_nulls(lib):
+    p = _fake(1 << 20)
+    assert lib.w4a16_linear(p, p, p, p, -1, 8, 128, 128, None, 0, None) == 1
+    assert lib.w4a16_linear(p, p, p, p, 4, -8, 128, 128, None, 0, None) == 1
+    assert lib.w4a16_linear(None, p, p, p, 4, 8, 128, 128, None, 0, None) == 1
+    assert lib.w4a16_linear(p, p, p, None, 4, 8, 128, 128, None, 0, None) == 1
+
+
+def test_linear_rejects_misaligned(lib):
+    p, q = _fake(1 << 20), _fake((1 << 20) + 8)
+    assert lib.w4a16_linear(q, p, p, p, 4, 8, 128, 128, None, 0, None) == 3
+    assert lib.w4a16_linear(p, q, p, p, 4, 8, 128, 128, None, 0, None) == 3
+    assert lib.w4a16_linear(p, p, q, p, 4, 8, 128, 128, None, 0, None) == 3
+
+
+def test_empty_problems_are_no_ops(lib):
+    p = _fake(1 << 20)
+    assert lib.w4a16_linear(p, p, p, p, 0, 8, 128, 128, None, 0, None) == 0
+    assert lib.w4a16_linear(p, p, p, p, 4, 0, 128, 128, None, 0, None) == 0
+    assert lib.w4a16_pack(p, 0, 128, 128, p, p, None) == 0
+    assert lib.w4a16_unpack(p, 0, 128, p, None) == 0
+
+
+def test_grouped_and_pack_validation(lib):
+    p = _fake(1 << 20)
+    assert lib.w4a16_grouped_linear(p, p, p, p, p, 0, 16, 8, 128, 32, None, 0, None) == 1   # E < 1
+    assert lib.w4a16_grouped_linear(p, p, p, None, p, 4, 16, 8, 128, 32, None, 0, None) == 1
+    assert lib.w4a16_grouped_linear(p, p, p, p, p, 4, 16, 8, 100, 32, None, 0, None) == 1
+    assert lib.w4a16_pack(p, 4, 100, 32, p, p, None) == 1
+    assert lib.w4a16_pack(p, 4, 128, 48, p, p, None) == 2
+    assert lib.w4a16_unpack(p, 4, 7, p, None) == 1

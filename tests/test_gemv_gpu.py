@@ -1,0 +1,117 @@
+"""Decode GEMV (M <= 16) on the GPU against the oracle, within
+|y - y_ref| <= 2^-9 |y_ref| + 1e-4 sum_k |x W^| per element."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from helpers import assert_within_bound, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def w4(cuda_device):
+    import w4a16_group_quantized_linear_gb300 as m
+
+    m.lib()
+    return m
+
+
+def _run(w4, dev, x, qw, s, g):
+    return w4.linear(to_dev(x, dev), to_dev(qw, dev), to_dev(s.view(np.float16), dev), g).cpu().numpy()
+
+
+def test_config0(w4, cuda_device):
+    W, x, g = workloads.config0()
+    qw, s = oracle.quantize(W, g)
+    y = _run(w4, cuda_device, x, qw, s, g)
+    y_ref, a = oracle.linear(x, qw, s, g)
+    print("config0 max err/bound", assert_within_bound(y, y_ref, a, "config0"))
+
+
+@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("K,N", [(5120, 17408), (17408, 5120)])
+def test_decode_full_size(w4, cuda_device, M, K, N):
+    W, x, g = workloads.decode(M, K, N)
+    qw, s = oracle.quantize(W, g)
+    y = _run(w4, cuda_device, x, qw, s, g)
+    y_ref, a = oracle.linear(x, qw, s, g, threads=8)
+    print(f"decode M={M} K={K} N={N} max err/bound", assert_within_bound(y, y_ref, a, "decode"))
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8, 9, 13, 16])
+@pytest.mark.parametrize("g", [32, 64, 128])
+def test_raw_nibbles_all_M(w4, cuda_device, M, g):
+    r = workloads.rng(100 * M + g)
+    N, K = 203, 1536
+    qw, s = workloads.raw_packed(r, N, K, g)
+    x = workloads.activations(r, M, K)
+    y = _run(w4, cuda_device, x, qw, s, g)
+    y_ref, a = oracle.linear(x, qw, s, g)
+    assert_within_bound(y, y_ref, a, f"M={M} g={g}")
+
+
+@pytest.mark.parametrize("N,K,g", [(1, 32, 32), (7, 96, 32), (17, 192, 64), (100, 640, 128), (1000, 2080, 32),
+                                   (4099, 384, 128), (16, 128, 128), (31, 8192, 64)])
+def test_ragged_shapes(w4, cuda_device, N, K, g):
+    r = workloads.rng(N * 7 + K)
+    qw, s = workloads.raw_packed(r, N, K, g)
+    for M in (1, 4, 11):
+        x = workloads.activations(r, M, K)
+        y = _run(w4, cuda_device, x, qw, s, g)
+        y_ref, a = oracle.linear(x, qw, s, g)
+        assert_within_bound(y, y_ref, a, f"N={N} K={K} g={g} M={M}")
+
+
+def test_zero_weights_give_exact_zero(w4, cuda_device):
+    r = workloads.rng(21)
+    x = workloads.activations(r, 3, 1024)
+    qw = np.full((300, 512), 0x88, np.uint8)
+    s = (np.abs(r.normal(0, 0.02, (300, 8))) / 7).astype(np.float16)
+    y = _run(w4, cuda_device, x, qw, s, 128)
+    assert np.all(y == 0)
+
+
+def test_one_hot_x_reads_one_weight_exactly(w4, cuda_device):
+    r = workloads.rng(22)
+    N, K, g = 300, 1024, 64
+    qw, s = workloads.raw_packed(r, N, K, g)
+    ks = [0, 1, 63, 64, 500, 1023]
+    x = np.zeros((len(ks), K), np.float16)
+    for i, k in enumerate(ks):
+        x[i, k] = 1
+    y = _run(w4, cuda_device, x, qw, s, g)
+    q = oracle.unpack(qw, K).astype(np.float64)
+    sd = oracle.half_to_double(s.view(np.uint16))
+    for i, k in enumerate(ks):
+        want = (sd[:, k // g] * q[:, k]).astype(np.float16)   # one exact product, rounded once
+        assert np.array_equal(y[i], want)
+
+
+def test_deterministic_and_workspace_reuse(w4, cuda_device):
+    r = workloads.rng(23)
+    qw, s = workloads.raw_packed(r, 5000, 4096, 128)
+    x = workloads.activations(r, 4, 4096)
+    y1 = _run(w4, cuda_device, x, qw, s, 128)
+    # a different shape in between reuses (and must leave clean) the workspace counters
+    qw2, s2 = workloads.raw_packed(r, 77, 1024, 32)
+    _run(w4, cuda_device, x[:, :1024], qw2, s2, 32)
+    y2 = _run(w4, cuda_device, x, qw, s, 128)
+    assert np.array_equal(y1.view(np.uint16), y2.view(np.uint16))
+
+
+def test_output_canary_untouched(w4, cuda_device):
+    import torch
+
+    r = workloads.rng(24)
+    N, K = 100, 512
+    qw, s = workloads.raw_packed(r, N, K, 128)
+    x = workloads.activations(r, 3, K)
+    buf = torch.full((3 * N + 64,), 12345, dtype=torch.int16, device=cuda_device)
+    out = buf[: 3 * N].view(torch.float16).view(3, N)
+    w4.linear(to_dev(x, cuda_device), to_dev(qw, cuda_device), to_dev(s, cuda_device), 128, out=out)
+    tail = buf[3 * N:].cpu().numpy()
+    assert np.all(tail == 12345)
+    y_ref, a = oracle.linear(x, qw, s, 128)
+    assert_within_bound(out.cpu().numpy(), y_ref, a, "canary")

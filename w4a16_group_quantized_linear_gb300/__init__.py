@@ -1,0 +1,191 @@
+"""W4A16 group-quantized linear layer for GB300 (sm_103a).
+
+y = x W^T with int4-symmetric weights (nibble q+8, even k in the low nibble),
+one fp16 scale per group of 32/64/128 input features and fp16 activations
+(LLM170 page, introduction: "W4A16 (int4 sym g128, f16 activations)").
+
+This module is a thin ctypes binding over the C ABI of ``libw4a16.so``
+(declared in ``include/w4a16.h``): it checks tensor dtypes and shapes,
+allocates outputs with PyTorch and passes raw device pointers and the current
+CUDA stream. Every step of the computation runs in the library's CUDA
+kernels; there is no fallback. If the library is missing, every call raises.
+Build it with ``python -m w4a16_group_quantized_linear_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["pack", "unpack", "linear", "grouped_linear", "workspace_bytes", "device_status",
+           "W4A16Error", "lib", "LIB_PATH", "EXPORTS", "STATUS"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libw4a16.so")
+
+STATUS = {0: "W4A16_OK", 1: "W4A16_ERR_INVALID_ARG", 2: "W4A16_ERR_UNSUPPORTED", 3: "W4A16_ERR_MISALIGNED",
+          4: "W4A16_ERR_CUDA", 5: "W4A16_ERR_TIMEOUT", 6: "W4A16_ERR_BAD_OFFSETS", 7: "W4A16_ERR_WORKSPACE"}
+
+_P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+# name -> (restype, argtypes); mirrors include/w4a16.h
+EXPORTS = {
+    "w4a16_pack": (_I32, [_P, _I64, _I64, _I32, _P, _P, _P]),
+    "w4a16_unpack": (_I32, [_P, _I64, _I64, _P, _P]),
+    "w4a16_linear": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
+    "w4a16_grouped_linear": (_I32, [_P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
+    "w4a16_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32, _I32]),
+    "w4a16_workspace_init": (_I32, [_P, _SZ, _P]),
+    "w4a16_device_status": (_I32, [_P]),
+    "w4a16_status_string": (ctypes.c_char_p, [_I32]),
+    "w4a16_version": (_I32, []),
+}
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libw4a16.so not built ({LIB_PATH}); run "
+                                   "python -m w4a16_group_quantized_linear_gb300.build")
+            h = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in EXPORTS.items():
+                f = getattr(h, name)
+                f.restype, f.argtypes = res, args
+            _lib = h
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise W4A16Error(status, where)
+
+
+def _stream(dev: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _ptr(t: torch.Tensor):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype, dim: int):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or t.dim() != dim or not t.is_cuda:
+        raise ValueError(f"{name}: expected a {dim}-d {dtype} CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+# one zero-initialised workspace per (device, stream), grown on demand
+_ws: dict = {}
+
+
+def _workspace(dev: torch.device, stream, nbytes: int):
+    if nbytes == 0:
+        return None
+    key = (dev.index, stream.value)
+    buf = _ws.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=dev)
+        _check(lib().w4a16_workspace_init(_ptr(buf), buf.numel(), stream), "w4a16_workspace_init")
+        _ws[key] = buf
+    return buf
+
+
+def workspace_bytes(M: int, N: int, K: int, group: int, E: int = 1) -> int:
+    return int(lib().w4a16_workspace_bytes(M, N, K, group, E))
+
+
+def pack(w: torch.Tensor, group: int = 128):
+    """fp32 [N, K] -> (qweight uint8 [N, K/2], scales fp16 [N, K/group])."""
+    _need(w, "w", torch.float32, 2)
+    N, K = w.shape
+    qw = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    s = torch.empty((N, K // group if group else 0), dtype=torch.float16, device=w.device)
+    _check(lib().w4a16_pack(_ptr(w), N, K, group, _ptr(qw), _ptr(s), _stream(w.device)), "w4a16_pack")
+    return qw, s
+
+
+def unpack(qw: torch.Tensor, K: int) -> torch.Tensor:
+    """uint8 [N, K/2] -> int8 q [N, K] in [-8, 7]."""
+    _need(qw, "qweight", torch.uint8, 2)
+    N = qw.shape[0]
+    if qw.shape[1] * 2 != K:
+        raise ValueError("qweight must be [N, K/2]")
+    q = torch.empty((N, K), dtype=torch.int8, device=qw.device)
+    _check(lib().w4a16_unpack(_ptr(qw), N, K, _ptr(q), _stream(qw.device)), "w4a16_unpack")
+    return q
+
+
+def linear(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, group: int = 128,
+           out: torch.Tensor | None = None) -> torch.Tensor:
+    """y = x W^T for x fp16 [M, K], qweight uint8 [N, K/2], scales fp16 [N, K/group]."""
+    _need(x, "x", torch.float16, 2)
+    _need(qweight, "qweight", torch.uint8, 2)
+    _need(scales, "scales", torch.float16, 2)
+    M, K = x.shape
+    N = qweight.shape[0]
+    if qweight.shape[1] * 2 != K or (group and tuple(scales.shape) != (N, K // group)):
+        raise ValueError("shape mismatch between x, qweight and scales")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    else:
+        _need(out, "out", torch.float16, 2)
+        if tuple(out.shape) != (M, N):
+            raise ValueError("out must be [M, N]")
+    st = _stream(x.device)
+    nb = workspace_bytes(M, N, K, group, 1)
+    ws = _workspace(x.device, st, nb)
+    _check(lib().w4a16_linear(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(out), M, N, K, group,
+                              _ptr(ws) if ws is not None else None, ws.numel() if ws is not None else 0, st),
+           "w4a16_linear")
+    return out
+
+
+def grouped_linear(x_sorted: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
+                   expert_offsets: torch.Tensor, group: int = 32,
+                   out: torch.Tensor | None = None) -> torch.Tensor:
+    """Routed experts: x_sorted fp16 [R, K] (rows sorted by expert), qweight uint8
+    [E, N, K/2], scales fp16 [E, N, K/group], expert_offsets int32 [E+1] on the device."""
+    _need(x_sorted, "x_sorted", torch.float16, 2)
+    _need(qweight, "qweight", torch.uint8, 3)
+    _need(scales, "scales", torch.float16, 3)
+    _need(expert_offsets, "expert_offsets", torch.int32, 1)
+    R, K = x_sorted.shape
+    E, N = qweight.shape[0], qweight.shape[1]
+    if qweight.shape[2] * 2 != K or tuple(scales.shape) != (E, N, K // group) or expert_offsets.numel() != E + 1:
+        raise ValueError("shape mismatch between x_sorted, qweight, scales and expert_offsets")
+    if out is None:
+        out = torch.empty((R, N), dtype=torch.float16, device=x_sorted.device)
+    else:
+        _need(out, "out", torch.float16, 2)
+    st = _stream(x_sorted.device)
+    nb = workspace_bytes(R, N, K, group, E)
+    ws = _workspace(x_sorted.device, st, nb)
+    _check(lib().w4a16_grouped_linear(_ptr(x_sorted), _ptr(qweight), _ptr(scales), _ptr(expert_offsets),
+                                      _ptr(out), E, R, N, K, group,
+                                      _ptr(ws) if ws is not None else None, ws.numel() if ws is not None else 0,
+                                      st), "w4a16_grouped_linear")
+    return out
+
+
+def device_status(raise_on_error: bool = True) -> int:
+    """Synchronizes the current stream and reads/clears the device error word."""
+    st = _stream(torch.device("cuda", torch.cuda.current_device()))
+    status = int(lib().w4a16_device_status(st))
+    if raise_on_error:
+        _check(status, "device")
+    return status

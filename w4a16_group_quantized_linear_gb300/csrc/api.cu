@@ -1,0 +1,170 @@
+// C ABI of libw4a16.so: argument validation, per-device state and dispatch.
+// The entry points and their contracts are documented in include/w4a16.h.
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace w4a16 {
+
+// Sticky device error word, one per device (module global).
+__device__ unsigned int g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kGemvMaxM = 16;
+
+std::mutex g_info_mutex;
+DeviceInfo g_info[kMaxDevices];
+bool g_info_ready[kMaxDevices];
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+w4a16_status check_group(int64_t K, int32_t group) {
+    if (group != 32 && group != 64 && group != 128) return W4A16_ERR_UNSUPPORTED;
+    if (K < 0 || K % group != 0) return W4A16_ERR_INVALID_ARG;
+    return W4A16_OK;
+}
+
+}  // namespace
+
+const DeviceInfo* device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_info_mutex);
+    if (!g_info_ready[dev]) {
+        DeviceInfo d{};
+        d.device = dev;
+        int smem = 0;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return nullptr;
+        d.smem_optin = (size_t)smem;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.error_word), g_error_word) != cudaSuccess)
+            return nullptr;
+        g_info[dev] = d;
+        g_info_ready[dev] = true;
+    }
+    return &g_info[dev];
+}
+
+namespace {
+
+// Common validation of w4a16_linear / w4a16_grouped_linear.
+w4a16_status check_linear(const void* x, const void* qw, const void* s, const void* y, int64_t M, int64_t N,
+                          int64_t K, int32_t group, const DeviceInfo** dev) {
+    if (M < 0 || N < 0 || K < 0) return W4A16_ERR_INVALID_ARG;
+    const w4a16_status g = check_group(K, group);
+    if (g != W4A16_OK) return g;
+    if (M == 0 || N == 0) return W4A16_OK;
+    if (!y || (K > 0 && (!x || !qw || !s))) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(qw) || !aligned16(s) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
+    *dev = device_info();
+    if (!*dev) return W4A16_ERR_CUDA;
+    if ((*dev)->cc_major != 10 || (*dev)->cc_minor != 3) return W4A16_ERR_UNSUPPORTED;
+    return W4A16_OK;
+}
+
+}  // namespace
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+int32_t w4a16_version(void) { return 100; }
+
+const char* w4a16_status_string(w4a16_status status) {
+    switch (status) {
+        case W4A16_OK: return "W4A16_OK";
+        case W4A16_ERR_INVALID_ARG: return "W4A16_ERR_INVALID_ARG: invalid argument";
+        case W4A16_ERR_UNSUPPORTED: return "W4A16_ERR_UNSUPPORTED: unsupported group, shape or device";
+        case W4A16_ERR_MISALIGNED: return "W4A16_ERR_MISALIGNED: pointer not 16-byte aligned";
+        case W4A16_ERR_CUDA: return "W4A16_ERR_CUDA: CUDA runtime error";
+        case W4A16_ERR_TIMEOUT: return "W4A16_ERR_TIMEOUT: a device wait gave up";
+        case W4A16_ERR_BAD_OFFSETS: return "W4A16_ERR_BAD_OFFSETS: expert offsets are not a partition of the rows";
+        case W4A16_ERR_WORKSPACE: return "W4A16_ERR_WORKSPACE: workspace missing or too small";
+    }
+    return "W4A16: unknown status";
+}
+
+w4a16_status w4a16_pack(const float* w, int64_t N, int64_t K, int32_t group, uint8_t* qweight, uint16_t* scales,
+                        void* stream) {
+    if (N < 0 || K < 0) return W4A16_ERR_INVALID_ARG;
+    const w4a16_status g = check_group(K, group);
+    if (g != W4A16_OK) return g;
+    if (N == 0 || K == 0) return W4A16_OK;
+    if (!w || !qweight || !scales) return W4A16_ERR_INVALID_ARG;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return W4A16_ERR_CUDA;
+    if (dev->cc_major != 10 || dev->cc_minor != 3) return W4A16_ERR_UNSUPPORTED;
+    return pack_launch(w, N, K, group, qweight, scales, (cudaStream_t)stream);
+}
+
+w4a16_status w4a16_unpack(const uint8_t* qweight, int64_t N, int64_t K, int8_t* q, void* stream) {
+    if (N < 0 || K < 0 || (K & 1)) return W4A16_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return W4A16_OK;
+    if (!qweight || !q) return W4A16_ERR_INVALID_ARG;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return W4A16_ERR_CUDA;
+    if (dev->cc_major != 10 || dev->cc_minor != 3) return W4A16_ERR_UNSUPPORTED;
+    return unpack_launch(qweight, N, K, q, (cudaStream_t)stream);
+}
+
+size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t group, int32_t E) {
+    if (M <= 0 || N <= 0 || K <= 0 || E < 1 || check_group(K, group) != W4A16_OK) return 0;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return 0;
+    if (E == 1 && M <= kGemvMaxM) return gemv_workspace_bytes(*dev, M, N, K);
+    return 0;
+}
+
+w4a16_status w4a16_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+    if (workspace_bytes == 0) return W4A16_OK;
+    if (!workspace) return W4A16_ERR_INVALID_ARG;
+    return cuda_status(cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream));
+}
+
+w4a16_status w4a16_linear(const uint16_t* x, const uint8_t* qweight, const uint16_t* scales, uint16_t* y,
+                          int64_t M, int64_t N, int64_t K, int32_t group, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+    const DeviceInfo* dev = nullptr;
+    const w4a16_status v = check_linear(x, qweight, scales, y, M, N, K, group, &dev);
+    if (v != W4A16_OK || M == 0 || N == 0) return v;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(uint16_t), st));
+    if (M <= kGemvMaxM)
+        return gemv_launch(*dev, x, qweight, scales, y, M, N, K, group, workspace, workspace_bytes, st);
+    return gemm_launch(*dev, x, qweight, scales, y, M, N, K, group, nullptr, 1, st);
+}
+
+w4a16_status w4a16_grouped_linear(const uint16_t* x_sorted, const uint8_t* qweight, const uint16_t* scales,
+                                  const int32_t* expert_offsets, uint16_t* y_sorted, int32_t E, int64_t R,
+                                  int64_t N, int64_t K, int32_t group, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    if (E < 1 || !expert_offsets) return W4A16_ERR_INVALID_ARG;
+    const DeviceInfo* dev = nullptr;
+    const w4a16_status v = check_linear(x_sorted, qweight, scales, y_sorted, R, N, K, group, &dev);
+    if (v != W4A16_OK || R == 0 || N == 0) return v;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (K == 0) return cuda_status(cudaMemsetAsync(y_sorted, 0, (size_t)(R * N) * sizeof(uint16_t), st));
+    return gemm_launch(*dev, x_sorted, qweight, scales, y_sorted, R, N, K, group, expert_offsets, E, st);
+}
+
+w4a16_status w4a16_device_status(void* stream) {
+    const DeviceInfo* dev = device_info();
+    if (!dev) return W4A16_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    unsigned int word = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return W4A16_ERR_CUDA;
+    if (cudaMemcpyAsync(&word, dev->error_word, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemsetAsync(dev->error_word, 0, sizeof(word), st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+        return W4A16_ERR_CUDA;
+    return (w4a16_status)word;
+}
+
+}  // extern "C"

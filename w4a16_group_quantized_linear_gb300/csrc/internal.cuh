@@ -1,0 +1,93 @@
+// Internal declarations shared by the translation units of libw4a16.so.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "w4a16.h"
+
+namespace w4a16 {
+
+// ----------------------------------------------------------------- device --
+
+// Bit-select (a & b) | c in one instruction.
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Eight packed nibbles (k0..k7 at bits 4i, value q+8) -> four fp16 pairs of
+// the exact integers q, in the order (k0,k4), (k1,k5), (k2,k6), (k3,k7).
+// A nibble placed in the low mantissa bits of the fp16 1024 (0x6400) reads as
+// 1024 + nib; one at bits 4-7 reads as 1024 + 16 nib. Subtracting 1032, or
+// scaling by 1/16 and subtracting 72, leaves nib - 8 exactly.
+__device__ __forceinline__ void nibbles_to_half2(uint32_t v, uint32_t& h04, uint32_t& h15,
+                                                 uint32_t& h26, uint32_t& h37) {
+    const uint32_t lo_mask = 0x000F000Fu, hi_mask = 0x00F000F0u, magic = 0x64006400u;
+    uint32_t t0 = lop3_and_or(v, lo_mask, magic);
+    uint32_t t1 = lop3_and_or(v, hi_mask, magic);
+    uint32_t v8 = v >> 8;
+    uint32_t t2 = lop3_and_or(v8, lo_mask, magic);
+    uint32_t t3 = lop3_and_or(v8, hi_mask, magic);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+    const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
+    const __half2 bias16 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480)); // -72
+    __half2 r0 = __hsub2(*reinterpret_cast<__half2*>(&t0), bias);
+    __half2 r1 = __hfma2(*reinterpret_cast<__half2*>(&t1), sixteenth, bias16);
+    __half2 r2 = __hsub2(*reinterpret_cast<__half2*>(&t2), bias);
+    __half2 r3 = __hfma2(*reinterpret_cast<__half2*>(&t3), sixteenth, bias16);
+    h04 = *reinterpret_cast<uint32_t*>(&r0);
+    h15 = *reinterpret_cast<uint32_t*>(&r1);
+    h26 = *reinterpret_cast<uint32_t*>(&r2);
+    h37 = *reinterpret_cast<uint32_t*>(&r3);
+}
+
+// D = A * B + C, m16n8k16, fp16 inputs, fp32 accumulators (register operands).
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Sticky device error word (one per device, in api.cu's module).
+__device__ __forceinline__ void raise_device_error(unsigned int* word, unsigned int code) {
+    if (word) atomicCAS(word, 0u, code);
+}
+
+// ------------------------------------------------------------------- host --
+
+struct DeviceInfo {
+    int device;
+    int sms;
+    int cc_major, cc_minor;
+    size_t smem_optin;
+    unsigned int* error_word;  // device address of the sticky error word
+};
+
+// Cached per-device properties of the current device (nullptr on failure).
+const DeviceInfo* device_info();
+
+// GEMV (decode, M <= 16).
+size_t gemv_workspace_bytes(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K);
+w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw,
+                         const uint16_t* s, uint16_t* y, int64_t M, int64_t N, int64_t K,
+                         int group, void* workspace, size_t workspace_bytes, cudaStream_t st);
+
+// Quantizer / unpack.
+w4a16_status pack_launch(const float* w, int64_t N, int64_t K, int group, uint8_t* qw,
+                         uint16_t* s, cudaStream_t st);
+w4a16_status unpack_launch(const uint8_t* qw, int64_t N, int64_t K, int8_t* q, cudaStream_t st);
+
+// Tensor-core GEMM (prefill and routed experts).
+w4a16_status gemm_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw,
+                         const uint16_t* s, uint16_t* y, int64_t M, int64_t N, int64_t K,
+                         int group, const int32_t* expert_offsets, int E, cudaStream_t st);
+
+inline w4a16_status cuda_status(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA; }
+
+}  // namespace w4a16
