@@ -123,6 +123,22 @@ def _peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def max_over_ranks(ms: float, device, world: int) -> float:
+    """The slowest rank's time (replicas run the same work; the job ends with the last)."""
+    if world <= 1:
+        return ms
+    import torch
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 class Timer:
     """CUDA-event pairs around launches on the launching stream."""
 
@@ -197,16 +213,12 @@ def run_gpu(args, rank, world):
             timer.around(lambda: w4.linear(h, qb, sb, GROUP, out=out))
         t1.record()
         torch.cuda.synchronize()
-    ms_total = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(t0.elapsed_time(t1), dev, world)
     launch_ms = timer.ms()
     kernel_ms = statistics.mean(launch_ms)
     per_launch_bytes = step_bytes / 2  # both GEMVs move the same algorithmic bytes
     achieved = per_launch_bytes / (kernel_ms * 1e-3) / 1e9
-    value = step_bytes * args.steps * world / (ms_total * 1e-3) / 1e9
+    value = job_throughput(step_bytes * args.steps, world, ms_total) / 1e9
 
     # ---- end to end through the public API: pinned host x in, host result out
     xh = torch.from_numpy(workloads.activations(workloads.rng(1), M, DECODE[0][0])).pin_memory()
@@ -297,6 +309,32 @@ def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):
                                "frac_tc": fl / (ms * 1e-3) / 1e12 / tc_peak}
     except w4.W4A16Error as e:
         out["prefill"] = {"unavailable": str(e)}
+    # routed experts: E=128, 4096 tokens, top-8 (R = 32768 rows), group 32
+    try:
+        for name, (Km, Nm) in (("moe_gate_up", (2048, 512)), ("moe_down", (512, 2048))):
+            W, xs, rt = workloads.moe(Km, Nm)
+            E = W.shape[0]
+            Wd = torch.from_numpy(W.reshape(E * Nm, Km)).to(dev)
+            qm, sm = w4.pack(Wd, 32)
+            del Wd, W
+            qm, sm = qm.view(E, Nm, Km // 2), sm.view(E, Nm, Km // 32)
+            xd = torch.from_numpy(xs).to(dev)
+            off = torch.from_numpy(rt.offsets).to(dev)
+            yd = torch.empty((xs.shape[0], Nm), dtype=torch.float16, device=dev)
+            f = lambda i: w4.grouped_linear(xd, qm, sm, off, 32, out=yd)  # noqa: E731
+            for i in range(3):
+                f(i)
+            ms = statistics.median(_time_launches(torch, f, 30))
+            R = xs.shape[0]
+            fl = 2.0 * R * Nm * Km
+            b = moe_bytes(E, R, Km, Nm, 32)
+            out[name] = {"E": E, "R": R, "K": Km, "N": Nm, "us": ms * 1e3, "TFLOP/s": fl / (ms * 1e-3) / 1e12,
+                         "frac_tc": fl / (ms * 1e-3) / 1e12 / tc_peak, "GB/s": b / (ms * 1e-3) / 1e9,
+                         "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm_peak}
+            del qm, sm, xd, yd
+        w4.device_status()
+    except w4.W4A16Error as e:
+        out["moe"] = {"unavailable": str(e)}
     return out
 
 

@@ -44,27 +44,42 @@ def build(force: bool = False) -> str:
     return _SO
 
 
+def _bind(path: str):
+    """Load a compiled oracle library and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    I64 = ctypes.c_int64
+    I32 = ctypes.c_int32
+    lib.oracle_half_to_double_n.argtypes = [P, I64, P]
+    lib.oracle_float_to_half_rn_n.argtypes = [P, I64, P]
+    lib.oracle_quantize.argtypes = [P, I64, I64, I32, P, P]
+    lib.oracle_unpack.argtypes = [P, I64, I64, P]
+    lib.oracle_pack_q.argtypes = [P, I64, I64, P]
+    lib.oracle_dequantize.argtypes = [P, I64, I64, I64, I32, P]
+    lib.oracle_linear.argtypes = [P, P, P, I64, I64, I64, I32, P, P]
+    lib.oracle_grouped_linear.argtypes = [P, P, P, P, I32, I64, I64, I64, I32, P, P]
+    for f in (lib.oracle_half_to_double_n, lib.oracle_float_to_half_rn_n,
+              lib.oracle_quantize, lib.oracle_unpack, lib.oracle_pack_q,
+              lib.oracle_dequantize, lib.oracle_linear, lib.oracle_grouped_linear):
+        f.restype = None
+    return lib
+
+
+def compile_variant(src_text: str, out_dir: str) -> str:
+    """Compile C source text with the oracle's flags (used by the mutation tests)."""
+    src = os.path.join(out_dir, "variant.c")
+    so = os.path.join(out_dir, "libvariant.so")
+    with open(src, "w") as f:
+        f.write(src_text)
+    subprocess.run(["gcc", *_CFLAGS, "-o", so, src, "-lm"], check=True)
+    return so
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            P = ctypes.c_void_p
-            I64 = ctypes.c_int64
-            I32 = ctypes.c_int32
-            lib.oracle_half_to_double_n.argtypes = [P, I64, P]
-            lib.oracle_float_to_half_rn_n.argtypes = [P, I64, P]
-            lib.oracle_quantize.argtypes = [P, I64, I64, I32, P, P]
-            lib.oracle_unpack.argtypes = [P, I64, I64, P]
-            lib.oracle_pack_q.argtypes = [P, I64, I64, P]
-            lib.oracle_dequantize.argtypes = [P, I64, I64, I64, I32, P]
-            lib.oracle_linear.argtypes = [P, P, P, I64, I64, I64, I32, P, P]
-            lib.oracle_grouped_linear.argtypes = [P, P, P, P, I32, I64, I64, I64, I32, P, P]
-            for f in (lib.oracle_half_to_double_n, lib.oracle_float_to_half_rn_n,
-                      lib.oracle_quantize, lib.oracle_unpack, lib.oracle_pack_q,
-                      lib.oracle_dequantize, lib.oracle_linear, lib.oracle_grouped_linear):
-                f.restype = None
-            _lib = lib
+            _lib = _bind(build())
     return _lib
 
 

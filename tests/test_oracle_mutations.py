@@ -1,0 +1,64 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case copies oracle.c, plants one mistake in the copy (on the CPU),
+compiles it with the oracle's flags, swaps it in for the real oracle and runs
+the pins of test_oracle.py: at least one must fail. The real oracle passes
+all of them (test_oracle.py itself)."""
+import os
+import tempfile
+
+import pytest
+
+import oracle
+import test_oracle as pins
+
+SRC = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+
+MUTANTS = {
+    "nibble order swapped": ("4 * (k & 1)", "4 * (1 - (k & 1))"),
+    "bias -7 instead of -8": ("& 0xF) - 8;", "& 0xF) - 7;"),
+    "scale amax/8": ("amax / 7.0f", "amax / 8.0f"),
+    "round half away from zero": ("rintf(r)", "roundf(r)"),
+    "symmetric clamp [-7, 7]": ("if (rr < -8.0f) rr = -8.0f;", "if (rr < -7.0f) rr = -7.0f;"),
+    "scale indexed by byte, not k": ("s[n * G + k / g]", "s[n * G + (k / 2) / g]"),
+    "abs dropped in the bound": ("aacc += fabs(p);", "aacc += p;"),
+    "subnormal exponent off by one": ("ldexp((double)f, -24)", "ldexp((double)f, -25)"),
+    "dot product skips the last k": ("for (int64_t k = 0; k < K; ++k) {\n                double p",
+                                     "for (int64_t k = 0; k < K - 1; ++k) {\n                double p"),
+}
+
+
+def _all_pins():
+    yield pins.test_half_to_double_all_bit_patterns, ()
+    yield pins.test_float_to_half_matches_numpy, ()
+    yield pins.test_nibble_order_golden, ()
+    yield pins.test_pack_unpack_round_trip_all_bytes, ()
+    for case in pins._quantize_cases():
+        yield pins.test_quantize_golden, (case,)
+    yield pins.test_quantize_invariants, ()
+    yield pins.test_linear_golden_tiny, ()
+    for args in [(1, 3, 32, 32), (2, 5, 64, 32), (3, 4, 128, 64)]:
+        yield pins.test_linear_exact_rational, args
+    yield pins.test_linear_zero_weights_give_zero, ()
+    yield pins.test_linear_one_hot_x_reads_one_weight, ()
+    for c in (-8, 5):
+        yield pins.test_linear_constant_q_closed_form, (c,)
+    yield pins.test_linear_unit_scales_match_numpy_matmul, ()
+    yield pins.test_linear_is_linear_in_x, ()
+    yield pins.test_grouped_equals_loop_of_dense_calls, ()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, monkeypatch):
+    old, new = MUTANTS[name]
+    assert old in SRC, f"mutation anchor not found: {old!r}"
+    with tempfile.TemporaryDirectory() as d:
+        so = oracle.compile_variant(SRC.replace(old, new), d)
+        monkeypatch.setattr(oracle, "_lib", oracle._bind(so))
+        failed = []
+        for fn, args in _all_pins():
+            try:
+                fn(*args)
+            except AssertionError:
+                failed.append(fn.__name__)
+        assert failed, f"no pin caught: {name}"
