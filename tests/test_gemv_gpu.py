@@ -115,3 +115,18 @@ def test_output_canary_untouched(w4, cuda_device):
     assert np.all(tail == 12345)
     y_ref, a = oracle.linear(x, qw, s, 128)
     assert_within_bound(out.cpu().numpy(), y_ref, a, "canary")
+
+
+def test_workspace_shared_across_shapes(w4, cuda_device):
+    """Calls of different M and N share one workspace; each must see clean counters."""
+    r = workloads.rng(25)
+    cases = [(16, 64, 2048), (1, 20000, 1024), (9, 333, 4096), (4, 7000, 640), (1, 64, 128)]
+    data = []
+    for M, N, K in cases:
+        qw, s = workloads.raw_packed(r, N, K, 128)
+        data.append((workloads.activations(r, M, K), qw, s))
+    for _ in range(2):
+        for x, qw, s in data:
+            y = _run(w4, cuda_device, x, qw, s, 128)
+            y_ref, a = oracle.linear(x, qw, s, 128)
+            assert_within_bound(y, y_ref, a, f"M={x.shape[0]} N={qw.shape[0]}")
