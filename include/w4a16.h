@@ -122,6 +122,31 @@ W4A16_API w4a16_status w4a16_grouped_linear(const uint16_t* x_sorted, const uint
                                   int64_t K, int32_t group, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
+/*
+ * Allocation-free variant of w4a16_linear, for callers that cannot allocate
+ * device memory: code that runs inside an allocator or memory-pool callback,
+ * a plugin host that hands a kernel only its input and output buffers, or a
+ * runtime that forbids allocation while it captures or replays work. The
+ * pages this library follows have no counterpart to it.
+ *
+ * Same arguments and results as w4a16_linear, minus the workspace. The
+ * scratch the decode GEMV needs (cross-block fp32 partial sums and per-row-
+ * block arrival counters) lives in one fixed device array of
+ * W4A16_NOALLOC_SCRATCH_BYTES that every GPU which loads the library keeps
+ * until the process exits. A problem whose scratch would not fit is rejected
+ * with W4A16_ERR_WORKSPACE before anything runs. The entry point calls no
+ * cudaMalloc, cudaFree or other allocating routine. Its first call on a
+ * device looks up the array's device address, so make that first call
+ * before any stream capture. Each call clears the counters it uses
+ * (cudaMemsetAsync on `stream`). All calls share the one array and it keeps
+ * the last call's contents, so calls that overlap on the GPU (for example on
+ * two streams) race with each other: serialize them.
+ */
+#define W4A16_NOALLOC_SCRATCH_BYTES (8u << 20)
+W4A16_API w4a16_status w4a16_linear_noalloc(const uint16_t* x, const uint8_t* qweight, const uint16_t* scales,
+                                            uint16_t* y, int64_t M, int64_t N, int64_t K, int32_t group,
+                                            void* stream);
+
 /* Bytes of workspace w4a16_linear (E = 1) or w4a16_grouped_linear (E experts,
  * M = R rows) needs for this problem on the current device; 0 if none. */
 W4A16_API size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t group, int32_t E);

@@ -34,6 +34,7 @@ EXPORTS = {
     "w4a16_pack": (_I32, [_P, _I64, _I64, _I32, _P, _P, _P]),
     "w4a16_unpack": (_I32, [_P, _I64, _I64, _P, _P]),
     "w4a16_linear": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
+    "w4a16_linear_noalloc": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]),
     "w4a16_grouped_linear": (_I32, [_P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
     "w4a16_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32, _I32]),
     "w4a16_workspace_init": (_I32, [_P, _SZ, _P]),
