@@ -439,7 +439,7 @@ def main():
         "config": config,
         "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["hbm_peak"], "unit": "GB/s",
                      "frac": r["achieved"] / r["hbm_peak"], "traffic": None,
-                     "kernel": "gemv_kernel<128,1>", "peak_kind": r["peak_kind"],
+                     "kernel": "gemv_kernel<group 128, M<=8>", "peak_kind": r["peak_kind"],
                      "kernel_us": r["kernel_ms"] * 1e3, "algorithmic_bytes_per_launch": r["per_launch_bytes"]},
         "e2e": r["e2e"], "gpu_launches": r["launches"], "clocks": r["clocks"], "gpu": r["gpu"], "sms": r["sms"],
         "side": r["extra"],

@@ -163,6 +163,11 @@ W4A16_API w4a16_status w4a16_device_status(void* stream);
 /* Static, human-readable name of a status code. */
 W4A16_API const char* w4a16_status_string(w4a16_status status);
 
+/* Text of the most recent CUDA runtime failure that made a call of this host
+ * thread return W4A16_ERR_CUDA (which call, error name and message). The
+ * string stays valid until this thread's next failing call. */
+W4A16_API const char* w4a16_last_cuda_error(void);
+
 /* Library version as major * 10000 + minor * 100 + patch. */
 W4A16_API int32_t w4a16_version(void);
 

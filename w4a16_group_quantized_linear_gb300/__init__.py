@@ -41,13 +41,17 @@ EXPORTS = {
     "w4a16_device_status": (_I32, [_P]),
     "w4a16_status_string": (ctypes.c_char_p, [_I32]),
     "w4a16_version": (_I32, []),
+    "w4a16_last_cuda_error": (ctypes.c_char_p, []),
 }
 
 
 class W4A16Error(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        detail = ""
+        if status == 4 and _lib is not None:
+            detail = " (" + _lib.w4a16_last_cuda_error().decode(errors="replace") + ")"
+        super().__init__(f"{where}: {STATUS.get(status, status)}{detail}")
 
 
 _lock = threading.Lock()

@@ -4,10 +4,20 @@
 
 #include "internal.cuh"
 
+#include <cstdio>
+
 namespace w4a16 {
 
 // Sticky device error word, one per device (module global).
 __device__ unsigned int g_error_word;
+
+namespace {
+thread_local char t_last_error[256] = "no CUDA error recorded";
+}
+
+void note_cuda_error(cudaError_t e, const char* where) {
+    snprintf(t_last_error, sizeof(t_last_error), "%s: %s (%s)", where, cudaGetErrorString(e), cudaGetErrorName(e));
+}
 
 namespace {
 
@@ -75,6 +85,8 @@ using namespace w4a16;
 extern "C" {
 
 int32_t w4a16_version(void) { return 100; }
+
+const char* w4a16_last_cuda_error(void) { return t_last_error; }
 
 const char* w4a16_status_string(w4a16_status status) {
     switch (status) {

@@ -1,34 +1,42 @@
 // Decode GEMV for the W4A16 layer, M <= 16 activation rows (LLM170 page:
 // "CUDA-graph decode", np4 = four sequences per step).
 //
-// Decode streams every packed weight byte once and does almost no arithmetic
-// per byte, so the kernel is bound by HBM bandwidth. Design:
+// Decode streams every packed weight byte once and does little arithmetic per
+// byte: the kernel is bound by HBM bandwidth, and on the instruction budget
+// of its dequantization. Design (one block of kConsumers warps per SM):
 //
-// * Work unit = 16 output features (rows n of W) x 128 input features k:
-//   1 KB of packed weights plus their scales. Units are ordered row-block
-//   major, k minor, and each warp of a persistent grid takes an equal
-//   contiguous range of units (stream-K split), so every SM streams the same
-//   number of bytes whatever N and K are.
-// * Each thread loads 16 B of two weight rows per unit with 128-bit
-//   coalesced, L1-bypassing loads, kDepth units ahead of the math.
-// * The activations (M x K fp16, at most 200 KB) are copied once per block
-//   into shared memory with bulk asynchronous copies while the first weight
-//   loads are in flight; larger x is read through the L1 instead.
+// * Work unit = 16 weight rows x 512 input features (4 KB packed). Units are
+//   ordered row-block major, k minor; every consumer warp of a persistent
+//   grid owns an equal contiguous range of them (stream-K split), so each SM
+//   streams the same number of bytes whatever N and K are.
+// * Every warp streams its units through a private ring of kSlots shared-
+//   memory slots with TMA, refilling a slot as soon as it has consumed it (no
+//   coupling between warps): a unit is four 16-row x 64-byte boxes issued back
+//   to back, i.e. 256 contiguous bytes per weight row per unit. Slots are laid
+//   out [k-step][row][64 B], so the fragment reads below are free of bank
+//   conflicts.
+// * The activations (M x K fp16, when small enough) are staged once per block
+//   in shared memory, permuted into MMA fragment order, while the first weight
+//   boxes are in flight; larger x is read through the L1.
 // * Nibbles become exact fp16 integers in registers (lop3 + one half2 op per
 //   pair) and go straight into mma.sync m16n8k16 as the A operand (rows =
-//   weight rows, columns = tokens padded to 8): the tensor core does the
-//   x*q products (exact) and their fp32 sum within one scale group, which
-//   keeps the ALU cost per weight near one instruction. The k order inside a
-//   group is permuted identically on the activation side, which leaves every
-//   group sum unchanged.
+//   weight rows, columns = tokens padded to 8): the tensor core does the x*q
+//   products (exact) and their fp32 sum within one scale group. The k order
+//   inside a group is permuted identically on the activation side, which
+//   leaves every group sum unchanged.
 // * After each group the fp32 partial is multiplied by the group's scale and
 //   added into fp32 accumulators: acc += s[n, grp] * sum_{k in grp} x q.
 // * A row-block whose units span several warps is finished by the last warp
 //   to arrive: each contributor stores its fp32 partial in the workspace,
 //   bumps a per-row-block counter, and the last one sums all partials in
 //   warp order (deterministic), rounds once to fp16 and resets the counter.
-//   A warp publishes its (at most two) partials after its last load, so the
-//   memory fence never waits on weight loads still in flight.
+//   A warp publishes its (at most two) partials after its last unit.
+//
+// Waits on the slot barriers are bounded in time; one that gives up records
+// W4A16_ERR_TIMEOUT in the device error word and the block unwinds after its
+// own TMA loads land.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "internal.cuh"
@@ -37,51 +45,39 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kWarps = 16;       // warps per block, one block per SM
-constexpr int kBlocksPerSM = 1;
-constexpr size_t kXSmemMax = 200 * 1024;  // x staged in shared memory up to this size
-constexpr int kStepK = 128;      // input features per unit
-constexpr int kRows = 16;        // output features per unit
-constexpr int kDepth = 4;        // units in flight per warp
+constexpr int kConsumers = 12;   // warps per block (one block per SM; 3 per scheduler)
+constexpr int kThreads = kConsumers * 32;
+constexpr int kSlots = 3;        // ring slots per consumer warp
+constexpr int kStepK = 128;      // k per step (one 64-byte piece of a row)
+constexpr int kUnitSteps = 4;    // steps per unit
+constexpr int kUnitK = kStepK * kUnitSteps;
+constexpr int kRows = 16;        // weight rows per unit
+constexpr int kSlotBytes = kUnitSteps * kRows * 64;  // 4 KB
+constexpr int kRingBytes = kConsumers * kSlots * kSlotBytes;
 constexpr int kMaxM = 16;        // activation rows handled by the GEMV
+constexpr size_t kXSmemMax = 80 * 1024;  // x staged in shared memory up to this size
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct GemvArgs {
     const uint16_t* x;
-    const uint8_t* qw;
     const uint16_t* s;
     uint16_t* y;
     int M;
     int64_t N, K;
-    int64_t KS;  // k-steps per row: ceil(K / 128)
-    int64_t U;   // units: ceil(N / 16) * KS
-    int64_t P;   // active warps (each owns >= 1 unit)
+    int64_t KS;  // 128-k steps per row: ceil(K / 128)
+    int64_t KU;  // 512-k units per row: ceil(K / 512)
+    int64_t U;   // units: ceil(N / 16) * KU
+    int64_t P;   // consumer warps taking part (each owns >= 1 unit)
     float* partial;  // [P][2][16 * M] fp32 partial sums (first / last segment)
     int* counter;    // [ceil(N/16)] arrivals per row-block, zero between calls
     unsigned int* err;
 };
 
-template <int G>
-struct Unit {
-    uint32_t wa[4], wb[4];     // rows gid and gid + 8: 32 nibbles each
-    uint32_t sc[kStepK / G];   // per group: scale of row gid (low) and gid + 8 (high)
+struct Bars {
+    uint64_t full[kConsumers][kSlots];
+    int abort;
 };
 
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-    uint4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
-    uint2 v;
-    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
-    uint32_t v;
-    asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
 __device__ __forceinline__ uint4 ld_cached_v4(const void* p) {
     uint4 v;
     asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
@@ -100,130 +96,115 @@ __device__ __forceinline__ uint4 permute_x8(uint4 v) {
                       __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
 }
 
-// Load cursor: per-thread addresses of one unit (rows gid and gid + 8 of
-// row-block rb, k-step ks). Rows past N point at row N-1 and get a zero
-// scale, so the hot loop needs no predicates.
-template <int G>
-struct Cursor {
-    const uint8_t* pa;
-    const uint8_t* pb;
-    const uint16_t* sa;
-    const uint16_t* sb;
-    int64_t rb, ks;
-    bool va, vb;
-
-    __device__ __forceinline__ void seek(const GemvArgs& p, int64_t rb_, int64_t ks_, int gid, int t4) {
-        rb = rb_;
-        ks = ks_;
-        int64_t r0 = rb * kRows + gid, r1 = r0 + 8;
-        va = r0 < p.N;
-        vb = r1 < p.N;
-        if (!va) r0 = p.N - 1;
-        if (!vb) r1 = p.N - 1;
-        const int64_t rowbytes = p.K >> 1, gpr = p.K / G;
-        const int64_t byte = ks * (kStepK / 2) + t4 * (G / 8);
-        pa = p.qw + r0 * rowbytes + byte;
-        pb = p.qw + r1 * rowbytes + byte;
-        sa = p.s + r0 * gpr + ks * (kStepK / G);
-        sb = p.s + r1 * gpr + ks * (kStepK / G);
-    }
-    __device__ __forceinline__ void next(const GemvArgs& p, int gid, int t4) {
-        if (++ks == p.KS) {
-            seek(p, rb + 1, 0, gid, t4);
-        } else {
-            pa += kStepK / 2;
-            pb += kStepK / 2;
-            sa += kStepK / G;
-            sb += kStepK / G;
-        }
-    }
-};
-
-template <int G>
-__device__ __forceinline__ void load_unit(Unit<G>& u, const Cursor<G>& c, const GemvArgs& p) {
-    constexpr int WPP = G / 32;  // 32-bit words per thread per row per group
-#pragma unroll
-    for (int j = 0; j < kStepK / G; ++j) {
-        // a group past K (ragged last step, G < 128) re-reads group 0 with a zero scale
-        const bool vk = (G == kStepK) || (c.ks * kStepK + j * G < p.K);
-        const int off = vk ? j * (G / 2) : 0;
-        if constexpr (WPP == 4) {
-            const uint4 va = ld_stream_v4(c.pa + off);
-            const uint4 vb = ld_stream_v4(c.pb + off);
-            u.wa[0] = va.x; u.wa[1] = va.y; u.wa[2] = va.z; u.wa[3] = va.w;
-            u.wb[0] = vb.x; u.wb[1] = vb.y; u.wb[2] = vb.z; u.wb[3] = vb.w;
-        } else if constexpr (WPP == 2) {
-            const uint2 va = ld_stream_v2(c.pa + off);
-            const uint2 vb = ld_stream_v2(c.pb + off);
-            u.wa[2 * j] = va.x; u.wa[2 * j + 1] = va.y;
-            u.wb[2 * j] = vb.x; u.wb[2 * j + 1] = vb.y;
-        } else {
-            u.wa[j] = ld_stream_u32(c.pa + off);
-            u.wb[j] = ld_stream_u32(c.pb + off);
-        }
-        const uint32_t s0 = ld_cached_u16(c.sa + (vk ? j : 0));
-        const uint32_t s1 = ld_cached_u16(c.sb + (vk ? j : 0));
-        u.sc[j] = ((c.va && vk) ? s0 : 0u) | ((c.vb && vk) ? (s1 << 16) : 0u);
-    }
-}
-
-// Shared-memory activations: per token a row of ceil(K/128) units x 16 chunks
-// of 16 bytes (+64 B pad), each chunk pre-permuted by permute_x8 and placed so
-// that the four threads of a quad read consecutive chunks.
+// Shared-memory activations: per token a row of 4 KU steps x 16 chunks of 16
+// bytes (+64 B pad), each chunk pre-permuted by permute_x8 and placed so that
+// the four threads of a quad read consecutive chunks.
 __device__ __forceinline__ int xs_pos(int c_local, int G) {
-    const int cpp = G / 8;              // chunks per group
+    const int cpp = G / 8;  // chunks per group
     const int j = c_local / cpp, rem = c_local % cpp;
     const int t4 = rem / (G / 32), wi = rem % (G / 32);
     return (j * (G / 32) + wi) * 4 + t4;
 }
 
+// Scales of one unit for rows gid and gid+8: per group, row gid in the low
+// half and row gid+8 in the high half. Rows past N and groups past K get 0.
+template <int G>
+struct UnitScales {
+    uint32_t v[kUnitK / G];
+};
+
+template <int G>
+__device__ __forceinline__ void load_scales(UnitScales<G>& sc, const GemvArgs& p, int64_t rb, int64_t ku,
+                                            int gid) {
+    const int64_t gpr = p.K / G;
+    const int64_t r0 = rb * kRows + gid, r1 = r0 + 8;
+    const bool v0 = r0 < p.N, v1 = r1 < p.N;
+    const uint16_t* s0 = p.s + (v0 ? r0 : 0) * gpr;
+    const uint16_t* s1 = p.s + (v1 ? r1 : 0) * gpr;
+#pragma unroll
+    for (int j = 0; j < kUnitK / G; ++j) {
+        const int64_t g = ku * (kUnitK / G) + j;
+        const bool vg = g < gpr;
+        const uint32_t a = (v0 && vg) ? ld_cached_u16(s0 + g) : 0u;
+        const uint32_t b = (v1 && vg) ? ld_cached_u16(s1 + g) : 0u;
+        sc.v[j] = a | (b << 16);
+    }
+}
+
+// One unit from its ring slot: for every 128-k step and scale group, the
+// quad's share of rows gid and gid+8, x from shared memory (XS) or global.
 template <int G, int NT, bool XS>
-__device__ __forceinline__ void compute_unit(const Unit<G>& u, const GemvArgs& p, const uint8_t* xs_unit,
-                                             int64_t xstride, int64_t ks, int gid, int t4, float (&acc)[NT][4]) {
-    constexpr int WPP = G / 32;
+__device__ __forceinline__ void compute_unit(const uint8_t* slot, const UnitScales<G>& sc, const GemvArgs& p,
+                                             const uint8_t* xs, int64_t xstride, int64_t ku, int gid, int t4,
+                                             float (&acc)[NT][4]) {
+    constexpr int WPP = G / 32;      // words per thread per row per group
+    constexpr int GPS = kStepK / G;  // groups per step
 #pragma unroll
-    for (int j = 0; j < kStepK / G; ++j) {
-        float c0[NT][4], c1[NT][4];  // two independent MMA chains per group
+    for (int step = 0; step < kUnitSteps; ++step) {
+        const int64_t ks = ku * kUnitSteps + step;
+        const uint8_t* ra = slot + step * (kRows * 64) + gid * 64;
+        const uint8_t* rbp = ra + 8 * 64;
 #pragma unroll
-        for (int t = 0; t < NT; ++t)
+        for (int j = 0; j < GPS; ++j) {
+            uint32_t wa[WPP], wb[WPP];
+            const int off = j * (G / 2) + t4 * (G / 8);
+            if constexpr (WPP == 4) {
+                const uint4 a = *reinterpret_cast<const uint4*>(ra + off);
+                const uint4 b = *reinterpret_cast<const uint4*>(rbp + off);
+                wa[0] = a.x; wa[1] = a.y; wa[2] = a.z; wa[3] = a.w;
+                wb[0] = b.x; wb[1] = b.y; wb[2] = b.z; wb[3] = b.w;
+            } else if constexpr (WPP == 2) {
+                const uint2 a = *reinterpret_cast<const uint2*>(ra + off);
+                const uint2 b = *reinterpret_cast<const uint2*>(rbp + off);
+                wa[0] = a.x; wa[1] = a.y;
+                wb[0] = b.x; wb[1] = b.y;
+            } else {
+                wa[0] = *reinterpret_cast<const uint32_t*>(ra + off);
+                wb[0] = *reinterpret_cast<const uint32_t*>(rbp + off);
+            }
+            float c0[NT][4], c1[NT][4];  // two independent MMA chains per group
 #pragma unroll
-            for (int i = 0; i < 4; ++i) c0[t][i] = c1[t][i] = 0.0f;
+            for (int t = 0; t < NT; ++t)
 #pragma unroll
-        for (int wi = 0; wi < WPP; ++wi) {
-            uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
-            nibbles_to_half2(u.wa[j * WPP + wi], a04, a15, a26, a37);
-            nibbles_to_half2(u.wb[j * WPP + wi], b04, b15, b26, b37);
+                for (int i = 0; i < 4; ++i) c0[t][i] = c1[t][i] = 0.0f;
+#pragma unroll
+            for (int wi = 0; wi < WPP; ++wi) {
+                uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
+                nibbles_to_half2(wa[wi], a04, a15, a26, a37);
+                nibbles_to_half2(wb[wi], b04, b15, b26, b37);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const int m = 8 * t + gid;
+                    uint4 xv = make_uint4(0, 0, 0, 0);
+                    if (XS) {
+                        if (m < p.M)
+                            xv = *reinterpret_cast<const uint4*>(xs + m * xstride + ks * (kStepK * 2) +
+                                                                 ((j * WPP + wi) * 4 + t4) * 16);
+                    } else {
+                        const int64_t k0 = ks * kStepK + j * G + t4 * (G / 4) + 8 * wi;
+                        if (m < p.M && k0 < p.K) xv = permute_x8(ld_cached_v4(p.x + (int64_t)m * p.K + k0));
+                    }
+                    mma_16816(c0[t], a04, b04, a15, b15, xv.x, xv.y);
+                    mma_16816(c1[t], a26, b26, a37, b37, xv.z, xv.w);
+                }
+            }
+            const uint32_t sp = sc.v[step * GPS + j];
+            const float s0 = __half2float(__ushort_as_half((unsigned short)(sp & 0xFFFFu)));
+            const float s1 = __half2float(__ushort_as_half((unsigned short)(sp >> 16)));
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                const int m = 8 * t + gid;
-                uint4 xv = make_uint4(0, 0, 0, 0);
-                if (XS) {
-                    if (m < p.M)
-                        xv = *reinterpret_cast<const uint4*>(xs_unit + m * xstride + ((j * WPP + wi) * 4 + t4) * 16);
-                } else {
-                    const int64_t k0 = ks * kStepK + j * G + t4 * (G / 4) + 8 * wi;
-                    if (m < p.M && k0 < p.K) xv = permute_x8(ld_cached_v4(p.x + (int64_t)m * p.K + k0));
-                }
-                mma_16816(c0[t], a04, b04, a15, b15, xv.x, xv.y);
-                mma_16816(c1[t], a26, b26, a37, b37, xv.z, xv.w);
+                acc[t][0] = fmaf(s0, c0[t][0] + c1[t][0], acc[t][0]);
+                acc[t][1] = fmaf(s0, c0[t][1] + c1[t][1], acc[t][1]);
+                acc[t][2] = fmaf(s1, c0[t][2] + c1[t][2], acc[t][2]);
+                acc[t][3] = fmaf(s1, c0[t][3] + c1[t][3], acc[t][3]);
             }
-        }
-        const float s0 = __half2float(__ushort_as_half((unsigned short)(u.sc[j] & 0xFFFFu)));
-        const float s1 = __half2float(__ushort_as_half((unsigned short)(u.sc[j] >> 16)));
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            acc[t][0] = fmaf(s0, c0[t][0] + c1[t][0], acc[t][0]);
-            acc[t][1] = fmaf(s0, c0[t][1] + c1[t][1], acc[t][1]);
-            acc[t][2] = fmaf(s1, c0[t][2] + c1[t][2], acc[t][2]);
-            acc[t][3] = fmaf(s1, c0[t][3] + c1[t][3], acc[t][3]);
         }
     }
 }
 
 // Accumulator element i of tile t: row gid + 8 (i >> 1), token 8 t + 2 t4 + (i & 1).
 template <int NT>
-__device__ __forceinline__ void store_y(const GemvArgs& p, int64_t rb, const float (&v)[NT][4], int gid,
-                                        int t4) {
+__device__ __forceinline__ void store_y(const GemvArgs& p, int64_t rb, const float (&v)[NT][4], int gid, int t4) {
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -238,8 +219,6 @@ __device__ __forceinline__ int64_t warp_of_unit(int64_t u, const GemvArgs& p) {
     return ((u + 1) * p.P + p.U - 1) / p.U - 1;  // largest w with w*U/P <= u
 }
 
-// Stores a row-block's fp32 partial in this warp's slot (0: first segment,
-// 1: last segment).
 template <int NT>
 __device__ __forceinline__ void store_partial(const GemvArgs& p, int64_t w, int slot, const float (&acc)[NT][4],
                                               int gid, int t4) {
@@ -257,12 +236,12 @@ __device__ __forceinline__ void store_partial(const GemvArgs& p, int64_t w, int 
 // the last contributor sums every contributor's partial in warp order,
 // rounds once to fp16, stores y and resets the counter.
 template <int NT>
-__device__ __noinline__ void arrive_row_block(const GemvArgs& p, int64_t rb, int gid, int t4, int lane) {
+__device__ __forceinline__ void arrive_row_block(const GemvArgs& p, int64_t rb, int gid, int t4, int lane) {
     int old = 0;
     if (lane == 0) old = atomicAdd(p.counter + rb, 1);
     old = __shfl_sync(0xffffffffu, old, 0);
-    const int64_t wa = warp_of_unit(rb * p.KS, p);
-    const int64_t wb = warp_of_unit(rb * p.KS + p.KS - 1, p);
+    const int64_t wa = warp_of_unit(rb * p.KU, p);
+    const int64_t wb = warp_of_unit(rb * p.KU + p.KU - 1, p);
     if ((int64_t)old != wb - wa) return;  // another warp finishes this row-block
     __threadfence();
     const int64_t slot_elems = (int64_t)kRows * p.M;
@@ -271,7 +250,7 @@ __device__ __noinline__ void arrive_row_block(const GemvArgs& p, int64_t rb, int
     for (int t = 0; t < NT; ++t) sum[t][0] = sum[t][1] = sum[t][2] = sum[t][3] = 0.0f;
     for (int64_t v = wa; v <= wb; ++v) {
         // rb is the first segment of every contributor except possibly wa
-        const bool wa_started_inside = (v * p.U / p.P) == rb * p.KS;
+        const bool wa_started_inside = (v * p.U / p.P) == rb * p.KU;
         const int slot = (v == wa && !wa_started_inside) ? 1 : 0;
         const float* src = p.partial + (v * 2 + slot) * slot_elems;
 #pragma unroll
@@ -287,82 +266,120 @@ __device__ __noinline__ void arrive_row_block(const GemvArgs& p, int64_t rb, int
 }
 
 template <int G, int NT, bool XS>
-__global__ void __launch_bounds__(kWarps * 32, kBlocksPerSM) gemv_kernel(const GemvArgs p) {
-    extern __shared__ __align__(16) uint8_t xs[];
-    const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
-    const int64_t w = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    const bool active = w < p.P;
-    const int64_t u_begin = active ? w * p.U / p.P : 0, u_end = active ? (w + 1) * p.U / p.P : 0;
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const GemvArgs p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    Bars* bars = reinterpret_cast<Bars*>(ring + kRingBytes);
+    uint8_t* xs = reinterpret_cast<uint8_t*>(bars) + ((sizeof(Bars) + 127) & ~(size_t)127);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
+    const int64_t xsteps = p.KU * kUnitSteps;             // staged steps per token (whole units)
+    const int64_t xstride = xsteps * (kStepK * 2) + 64;  // bytes per token row of staged x
+    volatile int* abort = &bars->abort;
 
-    // weight loads for the first kDepth units go out before anything else
-    Unit<G> buf[kDepth];
-    Cursor<G> lc;
-    lc.seek(p, u_begin / p.KS, u_begin % p.KS, gid, t4);
-#pragma unroll
-    for (int d = 0; d < kDepth; ++d) {
-        if (u_begin + d < u_end) {
-            load_unit<G>(buf[d], lc, p);
-            lc.next(p, gid, t4);
-        }
+    if (threadIdx.x == 0) {
+        for (int w = 0; w < kConsumers; ++w)
+            for (int sl = 0; sl < kSlots; ++sl) ptx::mbar_init(&bars->full[w][sl], 1);
+        bars->abort = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tensormap(&tmap_w);
     }
+    __syncthreads();
 
-    const int64_t xstride = p.KS * (kStepK * 2) + 64;  // bytes per token row
+    // unit range of every consumer warp of this block
+    auto range = [&](int cw, int64_t& ub, int64_t& ue) {
+        const int64_t w = (int64_t)blockIdx.x * kConsumers + cw;
+        ub = w < p.P ? w * p.U / p.P : 0;
+        ue = w < p.P ? (w + 1) * p.U / p.P : 0;
+    };
+    auto issue = [&](int cw, int64_t u, int sl) {  // one unit into a slot: four 16-row x 64-byte boxes
+        const int64_t rb = u / p.KU, ku = u % p.KU;
+        uint64_t* bar = &bars->full[cw][sl];
+        uint8_t* dst = ring + (cw * kSlots + sl) * kSlotBytes;
+        ptx::mbar_arrive_expect_tx(bar, kSlotBytes);
+#pragma unroll
+        for (int step = 0; step < kUnitSteps; ++step)
+            ptx::tma_load_2d(dst + step * (kRows * 64), &tmap_w, bar, (int)((ku * kUnitSteps + step) * 64),
+                             (int)(rb * kRows));
+    };
+
+    const int cw = warp;
+    int64_t u_begin, u_end;
+    range(cw, u_begin, u_end);
+    if (lane == 0)  // first loads of this warp go out before x is staged
+        for (int r = 0; r < kSlots && u_begin + r < u_end; ++r) issue(cw, u_begin + r, r);
     if (XS) {
-        // stage x: coalesced 16-byte loads, permuted into MMA fragment order, zero past K
-        const int64_t chunks = (int64_t)p.M * p.KS * 16;
+        const int64_t chunks = (int64_t)p.M * xsteps * 16;  // zero past K
         for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) {
-            const int64_t m = c / (p.KS * 16), cc = c % (p.KS * 16);
+            const int64_t m = c / (xsteps * 16), cc = c % (xsteps * 16);
             const int64_t k0 = cc * 8;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (k0 < p.K) v = permute_x8(ld_cached_v4(p.x + m * p.K + k0));
-            const int unit = (int)(cc >> 4), pos = xs_pos((int)(cc & 15), G);
-            *reinterpret_cast<uint4*>(xs + m * xstride + unit * (kStepK * 2) + pos * 16) = v;
+            *reinterpret_cast<uint4*>(xs + m * xstride + (cc >> 4) * (kStepK * 2) + xs_pos((int)(cc & 15), G) * 16) = v;
         }
         __syncthreads();
     }
-    if (!active) return;
 
-    int64_t rb = u_begin / p.KS, ks = u_begin % p.KS;
+    // ------------------------------------------------------------ consumers
+    const int64_t w = (int64_t)blockIdx.x * kConsumers + cw;
+    if (w >= p.P) return;
+
+    int64_t rb = u_begin / p.KU, ku = u_begin % p.KU;
     const int64_t first_rb = rb;
-    int64_t seg_ks0 = ks;
+    int64_t seg_ku0 = ku;
     float acc[NT][4], acc_first[NT][4];
     bool has_first = false;
     int64_t last_rb = -1;
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+    UnitScales<G> sc;
+    load_scales<G>(sc, p, rb, ku, gid);
 
-    for (int64_t u = u_begin; u < u_end; u += kDepth) {
-#pragma unroll
-        for (int d = 0; d < kDepth; ++d) {
-            if (u + d < u_end) {
-                compute_unit<G, NT, XS>(buf[d], p, xs + ks * (kStepK * 2), xstride, ks, gid, t4, acc);
-                if (u + d + kDepth < u_end) {
-                    load_unit<G>(buf[d], lc, p);
-                    lc.next(p, gid, t4);
-                }
-                const bool seg_end = (ks == p.KS - 1) || (u + d == u_end - 1);
-                if (seg_end) {
-                    if (seg_ks0 == 0 && ks == p.KS - 1) {
-                        store_y<NT>(p, rb, acc, gid, t4);  // whole row-block in this warp
-                    } else if (rb == first_rb) {
-                        // partial first segment: published after the last load (a fence
-                        // here would wait for the loads in flight)
-                        has_first = true;
-#pragma unroll
-                        for (int t = 0; t < NT; ++t)
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) acc_first[t][i] = acc[t][i];
-                    } else {
-                        store_partial<NT>(p, w, 1, acc, gid, t4);  // partial last segment
-                        last_rb = rb;
-                    }
-#pragma unroll
-                    for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
-                }
-                if (++ks == p.KS) { ks = 0; ++rb; }
-                if (seg_end) seg_ks0 = ks;
+    for (int64_t u = u_begin; u < u_end; ++u) {
+        const int64_t r = u - u_begin;
+        const int sl = (int)(r % kSlots);
+        if (!__all_sync(0xffffffffu,
+                        ptx::mbar_wait(&bars->full[cw][sl], (uint32_t)((r / kSlots) & 1), abort, kWaitLimitNs))) {
+            raise_device_error(p.err, W4A16_ERR_TIMEOUT);
+            *abort = 1;
+            if (lane == 0) {  // this warp's own loads still in flight land before it exits
+                volatile int never = 0;
+                for (int64_t q = r + 1; q < r + kSlots && u_begin + q < u_end; ++q)
+                    ptx::mbar_wait(&bars->full[cw][q % kSlots], (uint32_t)((q / kSlots) & 1), &never, kWaitLimitNs);
             }
+            return;
         }
+        UnitScales<G> sc_next;
+        const int64_t nrb = ku + 1 == p.KU ? rb + 1 : rb, nku = ku + 1 == p.KU ? 0 : ku + 1;
+        if (u + 1 < u_end) load_scales<G>(sc_next, p, nrb, nku, gid);
+        compute_unit<G, NT, XS>(ring + (cw * kSlots + sl) * kSlotBytes, sc, p, xs, xstride, ku, gid, t4, acc);
+        __syncwarp();  // every lane has read the slot
+        if (lane == 0 && u + kSlots < u_end) {
+            ptx::fence_proxy_async_smem();
+            issue(cw, u + kSlots, sl);
+        }
+        if (u + 1 < u_end) sc = sc_next;
+
+        const bool seg_end = (ku == p.KU - 1) || (u == u_end - 1);
+        if (seg_end) {
+            if (seg_ku0 == 0 && ku == p.KU - 1) {
+                store_y<NT>(p, rb, acc, gid, t4);  // whole row-block in this warp
+            } else if (rb == first_rb) {
+                has_first = true;  // published after the last unit
+#pragma unroll
+                for (int t = 0; t < NT; ++t)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc_first[t][i] = acc[t][i];
+            } else {
+                store_partial<NT>(p, w, 1, acc, gid, t4);  // partial last segment
+                last_rb = rb;
+            }
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+        }
+        rb = nrb;
+        ku = nku;
+        if (seg_end) seg_ku0 = ku;
     }
     if (has_first) store_partial<NT>(p, w, 0, acc_first, gid, t4);
     if (has_first || last_rb >= 0) {
@@ -373,23 +390,42 @@ __global__ void __launch_bounds__(kWarps * 32, kBlocksPerSM) gemv_kernel(const G
     }
 }
 
-int64_t max_warps(const DeviceInfo& dev) { return (int64_t)dev.sms * kBlocksPerSM * kWarps; }
-
-template <int G, int NT, bool XS>
-w4a16_status launch_one(const GemvArgs& a, unsigned blocks, size_t smem, cudaStream_t st) {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    if (XS)
-        std::call_once(once, [] {
-            attr = cudaFuncSetAttribute(gemv_kernel<G, NT, XS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kXSmemMax);
-        });
-    if (attr != cudaSuccess) return W4A16_ERR_CUDA;
-    gemv_kernel<G, NT, XS><<<blocks, kWarps * 32, smem, st>>>(a);
-    return cuda_status(cudaGetLastError());
-}
+int64_t max_warps(const DeviceInfo& dev) { return (int64_t)dev.sms * kConsumers; }
 
 size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* q = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault, &r) ==
+                cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(q);
+    });
+    return fn;
+}
+
+size_t smem_bytes(bool xs, int64_t M, int64_t steps) {
+    size_t b = 1024 + kRingBytes + ((sizeof(Bars) + 127) & ~(size_t)127);
+    if (xs) b += (size_t)M * (size_t)(steps * kStepK * 2 + 64);
+    return b;
+}
+
+template <int G, int NT, bool XS>
+w4a16_status launch_one(const CUtensorMap& map, const GemvArgs& a, unsigned blocks, size_t smem, cudaStream_t st) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(gemv_kernel<G, NT, XS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)(smem_bytes(false, 0, 0) + kXSmemMax));
+    });
+    if (attr != cudaSuccess) return cuda_status(attr, "gemv: cudaFuncSetAttribute");
+    gemv_kernel<G, NT, XS><<<blocks, kThreads, smem, st>>>(map, a);
+    return cuda_status(cudaGetLastError(), "gemv: kernel launch");
+}
 
 }  // namespace
 
@@ -413,26 +449,47 @@ w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     const size_t need = gemv_workspace_bytes(dev, M, N, K);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return W4A16_ERR_WORKSPACE;
     if (((uintptr_t)workspace & 255) != 0) return W4A16_ERR_MISALIGNED;
+    if (M > kMaxM || N > 0x7fffffffLL || K / 2 > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cuda_status(cudaErrorNotSupported, "gemv: cuTensorMapEncodeTiled entry point");
+    CUtensorMap map;
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
+        cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+        cuuint32_t box[2] = {64, (cuuint32_t)kRows};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(qw), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cuda_status(cudaErrorInvalidValue, "gemv: cuTensorMapEncodeTiled");
+    }
     GemvArgs a;
-    a.x = x; a.qw = qw; a.s = s; a.y = y;
-    a.M = (int)M; a.N = N; a.K = K;
+    a.x = x;
+    a.s = s;
+    a.y = y;
+    a.M = (int)M;
+    a.N = N;
+    a.K = K;
     a.KS = (K + kStepK - 1) / kStepK;
+    a.KU = (K + kUnitK - 1) / kUnitK;
     const int64_t RB = (N + kRows - 1) / kRows;
-    a.U = RB * a.KS;
-    int64_t blocks = (a.U + kWarps - 1) / kWarps;
-    const int64_t max_blocks = (int64_t)dev.sms * kBlocksPerSM;
-    if (blocks > max_blocks) blocks = max_blocks;
-    a.P = blocks * kWarps < a.U ? blocks * kWarps : a.U;
+    a.U = RB * a.KU;
+    int64_t blocks = (a.U + kConsumers - 1) / kConsumers;
+    if (blocks > dev.sms) blocks = dev.sms;
+    a.P = blocks * kConsumers < a.U ? blocks * kConsumers : a.U;
     a.partial = reinterpret_cast<float*>(workspace);
     a.counter = reinterpret_cast<int*>(reinterpret_cast<char*>(workspace) + partial_region_bytes(dev));
     a.err = dev.error_word;
+    const int64_t xsteps = a.KU * kUnitSteps;
+    const size_t xbytes = (size_t)M * (size_t)(xsteps * kStepK * 2 + 64);
+    const bool xs = xbytes <= kXSmemMax && smem_bytes(true, M, xsteps) <= dev.smem_optin;
+    const size_t smem = smem_bytes(xs, M, xsteps);
+    if (smem > dev.smem_optin) return W4A16_ERR_UNSUPPORTED;
     const int nt = M <= 8 ? 1 : 2;
-    const size_t xbytes = (size_t)M * (size_t)(a.KS * kStepK * 2 + 64);
-    const bool xs = xbytes <= kXSmemMax && xbytes <= dev.smem_optin;
-    w4a16_status st_ = W4A16_OK;
-#define W4A16_GEMV(G_, NT_)                                                                  \
-    st_ = xs ? launch_one<G_, NT_, true>(a, (unsigned)blocks, xbytes, st)                    \
-             : launch_one<G_, NT_, false>(a, (unsigned)blocks, 0, st)
+    w4a16_status r = W4A16_OK;
+#define W4A16_GEMV(G_, NT_)                                                           \
+    r = xs ? launch_one<G_, NT_, true>(map, a, (unsigned)blocks, smem, st)            \
+           : launch_one<G_, NT_, false>(map, a, (unsigned)blocks, smem, st)
     if (nt == 1) {
         if (group == 128) W4A16_GEMV(128, 1);
         else if (group == 64) W4A16_GEMV(64, 1);
@@ -443,7 +500,7 @@ w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
         else W4A16_GEMV(32, 2);
     }
 #undef W4A16_GEMV
-    return st_;
+    return r;
 }
 
 }  // namespace w4a16

@@ -90,6 +90,13 @@ w4a16_status gemm_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
                          const uint16_t* s, uint16_t* y, int64_t M, int64_t N, int64_t K,
                          int group, const int32_t* expert_offsets, int E, cudaStream_t st);
 
-inline w4a16_status cuda_status(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA; }
+// Records a failed CUDA runtime call for w4a16_last_cuda_error (per host thread).
+void note_cuda_error(cudaError_t e, const char* where);
+
+inline w4a16_status cuda_status(cudaError_t e, const char* where = "CUDA call") {
+    if (e == cudaSuccess) return W4A16_OK;
+    note_cuda_error(e, where);
+    return W4A16_ERR_CUDA;
+}
 
 }  // namespace w4a16

@@ -73,7 +73,7 @@ w4a16_status pack_launch(const float* w, int64_t N, int64_t K, int group, uint8_
         case 128: pack_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(w, N, K, qw, s); break;
         default: return W4A16_ERR_UNSUPPORTED;
     }
-    return cuda_status(cudaGetLastError());
+    return cuda_status(cudaGetLastError(), "pack: kernel launch");
 }
 
 w4a16_status unpack_launch(const uint8_t* qw, int64_t N, int64_t K, int8_t* q, cudaStream_t st) {
@@ -82,7 +82,7 @@ w4a16_status unpack_launch(const uint8_t* qw, int64_t N, int64_t K, int8_t* q, c
     int64_t blocks = (bytes + 255) / 256;
     if (blocks > 65536) blocks = 65536;
     unpack_kernel<<<(unsigned)blocks, 256, 0, st>>>(qw, bytes, q);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(cudaGetLastError(), "unpack: kernel launch");
 }
 
 }  // namespace w4a16
