@@ -196,9 +196,9 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     w4.device_status()
 
-    # ---- timed region: launches queued behind a spin so the GPU runs them back to back
-    timer = Timer(torch)
-    (qa0, sa0), _ = rot[0]
+    # ---- timed region: launches queued behind a spin so the GPU runs them back to
+    # back (consecutive GEMVs overlap through programmatic dependent launch); CUDA
+    # events only at the two ends, on the launching stream
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -208,14 +208,12 @@ def run_gpu(args, rank, world):
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
         for i in range(args.steps):
-            (qa, sa), (qb, sb) = rot[i % copies]
-            timer.around(lambda: w4.linear(x, qa, sa, GROUP, out=h))
-            timer.around(lambda: w4.linear(h, qb, sb, GROUP, out=out))
+            step(i)
         t1.record()
         torch.cuda.synchronize()
-    ms_total = max_over_ranks(t0.elapsed_time(t1), dev, world)
-    launch_ms = timer.ms()
-    kernel_ms = statistics.mean(launch_ms)
+    ms_local = t0.elapsed_time(t1)
+    ms_total = max_over_ranks(ms_local, dev, world)
+    kernel_ms = ms_local / (2 * args.steps)  # mean GEMV launch duration in the stream
     per_launch_bytes = step_bytes / 2  # both GEMVs move the same algorithmic bytes
     achieved = per_launch_bytes / (kernel_ms * 1e-3) / 1e9
     value = job_throughput(step_bytes * args.steps, world, ms_total) / 1e9
@@ -255,14 +253,18 @@ def run_gpu(args, rank, world):
         launches=2 * args.steps, per_launch_bytes=per_launch_bytes)
 
 
-def _time_launches(torch, fn, n, sleep_cycles=2e6):
+def _time_launches(torch, fn, n, sleep_cycles=2e7):
+    """Mean device time per launch of n back-to-back launches (CUDA events at the ends)."""
     torch.cuda.synchronize()
     torch.cuda._sleep(int(sleep_cycles))
-    timer = Timer(torch)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
     for i in range(n):
-        timer.around(lambda: fn(i))
+        fn(i)
+    t1.record()
     torch.cuda.synchronize()
-    return timer.ms()
+    return [t0.elapsed_time(t1) / n]
 
 
 def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):

@@ -30,7 +30,10 @@
 //   to arrive: each contributor stores its fp32 partial in the workspace,
 //   bumps a per-row-block counter, and the last one sums all partials in
 //   warp order (deterministic), rounds once to fp16 and resets the counter.
-//   A warp publishes its (at most two) partials after its last unit.
+//   A warp publishes each partial as soon as its segment ends, with one
+//   acquire-release atomic on the counter.
+// * Programmatic dependent launch: the weight loads of the first units go out
+//   before griddepcontrol.wait, so they overlap the previous kernel's tail.
 //
 // Waits on the slot barriers are bounded in time; one that gives up records
 // W4A16_ERR_TIMEOUT in the device error word and the block unwinds after its
@@ -76,6 +79,7 @@ struct GemvArgs {
 struct Bars {
     uint64_t full[kConsumers][kSlots];
     int abort;
+    alignas(16) uint8_t zero[256];  // x fragment of lanes without a token
 };
 
 __device__ __forceinline__ uint4 ld_cached_v4(const void* p) {
@@ -106,11 +110,11 @@ __device__ __forceinline__ int xs_pos(int c_local, int G) {
     return (j * (G / 32) + wi) * 4 + t4;
 }
 
-// Scales of one unit for rows gid and gid+8: per group, row gid in the low
-// half and row gid+8 in the high half. Rows past N and groups past K get 0.
+// Scales of one unit for rows gid and gid+8, per group, as fp32. Rows past N
+// and groups past K get 0.
 template <int G>
 struct UnitScales {
-    uint32_t v[kUnitK / G];
+    float lo[kUnitK / G], hi[kUnitK / G];
 };
 
 template <int G>
@@ -127,21 +131,23 @@ __device__ __forceinline__ void load_scales(UnitScales<G>& sc, const GemvArgs& p
         const bool vg = g < gpr;
         const uint32_t a = (v0 && vg) ? ld_cached_u16(s0 + g) : 0u;
         const uint32_t b = (v1 && vg) ? ld_cached_u16(s1 + g) : 0u;
-        sc.v[j] = a | (b << 16);
+        sc.lo[j] = __half2float(__ushort_as_half((unsigned short)a));
+        sc.hi[j] = __half2float(__ushort_as_half((unsigned short)b));
     }
 }
 
 // One unit from its ring slot: for every 128-k step and scale group, the
-// quad's share of rows gid and gid+8, x from shared memory (XS) or global.
+// quad's share of rows gid and gid+8. XS: x comes from shared memory; each
+// lane's row pointer (xrow) and per-step stride (xstep) point lanes without a
+// token at a zero block instead, so no load is predicated.
 template <int G, int NT, bool XS>
 __device__ __forceinline__ void compute_unit(const uint8_t* slot, const UnitScales<G>& sc, const GemvArgs& p,
-                                             const uint8_t* xs, int64_t xstride, int64_t ku, int gid, int t4,
-                                             float (&acc)[NT][4]) {
+                                             const uint8_t* const (&xrow)[NT], const int (&xstep)[NT],
+                                             int64_t ku, int gid, int t4, float (&acc)[NT][4]) {
     constexpr int WPP = G / 32;      // words per thread per row per group
     constexpr int GPS = kStepK / G;  // groups per step
 #pragma unroll
     for (int step = 0; step < kUnitSteps; ++step) {
-        const int64_t ks = ku * kUnitSteps + step;
         const uint8_t* ra = slot + step * (kRows * 64) + gid * 64;
         const uint8_t* rbp = ra + 8 * 64;
 #pragma unroll
@@ -162,11 +168,7 @@ __device__ __forceinline__ void compute_unit(const uint8_t* slot, const UnitScal
                 wa[0] = *reinterpret_cast<const uint32_t*>(ra + off);
                 wb[0] = *reinterpret_cast<const uint32_t*>(rbp + off);
             }
-            float c0[NT][4], c1[NT][4];  // two independent MMA chains per group
-#pragma unroll
-            for (int t = 0; t < NT; ++t)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) c0[t][i] = c1[t][i] = 0.0f;
+            float c[NT][4];  // this group's fp32 sum of x*q
 #pragma unroll
             for (int wi = 0; wi < WPP; ++wi) {
                 uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
@@ -174,29 +176,28 @@ __device__ __forceinline__ void compute_unit(const uint8_t* slot, const UnitScal
                 nibbles_to_half2(wb[wi], b04, b15, b26, b37);
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
-                    const int m = 8 * t + gid;
-                    uint4 xv = make_uint4(0, 0, 0, 0);
+                    uint4 xv;
                     if (XS) {
-                        if (m < p.M)
-                            xv = *reinterpret_cast<const uint4*>(xs + m * xstride + ks * (kStepK * 2) +
-                                                                 ((j * WPP + wi) * 4 + t4) * 16);
+                        xv = *reinterpret_cast<const uint4*>(xrow[t] + step * xstep[t] +
+                                                             ((j * WPP + wi) * 4 + t4) * 16);
                     } else {
-                        const int64_t k0 = ks * kStepK + j * G + t4 * (G / 4) + 8 * wi;
+                        const int m = 8 * t + gid;
+                        const int64_t k0 = (ku * kUnitSteps + step) * kStepK + j * G + t4 * (G / 4) + 8 * wi;
+                        xv = make_uint4(0, 0, 0, 0);
                         if (m < p.M && k0 < p.K) xv = permute_x8(ld_cached_v4(p.x + (int64_t)m * p.K + k0));
                     }
-                    mma_16816(c0[t], a04, b04, a15, b15, xv.x, xv.y);
-                    mma_16816(c1[t], a26, b26, a37, b37, xv.z, xv.w);
+                    if (wi == 0) mma_16816_zero(c[t], a04, b04, a15, b15, xv.x, xv.y);
+                    else mma_16816(c[t], a04, b04, a15, b15, xv.x, xv.y);
+                    mma_16816(c[t], a26, b26, a37, b37, xv.z, xv.w);
                 }
             }
-            const uint32_t sp = sc.v[step * GPS + j];
-            const float s0 = __half2float(__ushort_as_half((unsigned short)(sp & 0xFFFFu)));
-            const float s1 = __half2float(__ushort_as_half((unsigned short)(sp >> 16)));
+            const float s0 = sc.lo[step * GPS + j], s1 = sc.hi[step * GPS + j];
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                acc[t][0] = fmaf(s0, c0[t][0] + c1[t][0], acc[t][0]);
-                acc[t][1] = fmaf(s0, c0[t][1] + c1[t][1], acc[t][1]);
-                acc[t][2] = fmaf(s1, c0[t][2] + c1[t][2], acc[t][2]);
-                acc[t][3] = fmaf(s1, c0[t][3] + c1[t][3], acc[t][3]);
+                acc[t][0] = fmaf(s0, c[t][0], acc[t][0]);
+                acc[t][1] = fmaf(s0, c[t][1], acc[t][1]);
+                acc[t][2] = fmaf(s1, c[t][2], acc[t][2]);
+                acc[t][3] = fmaf(s1, c[t][3], acc[t][3]);
             }
         }
     }
@@ -232,18 +233,21 @@ __device__ __forceinline__ void store_partial(const GemvArgs& p, int64_t w, int 
         }
 }
 
-// After this warp's partial for row-block rb is visible: count the arrival;
-// the last contributor sums every contributor's partial in warp order,
+// Publishes this warp's fp32 partial of row-block rb (slot 0: the warp's first
+// segment, 1: its last) and counts the arrival with one acquire-release
+// atomic; the last contributor sums every contributor's partial in warp order,
 // rounds once to fp16, stores y and resets the counter.
 template <int NT>
-__device__ __forceinline__ void arrive_row_block(const GemvArgs& p, int64_t rb, int gid, int t4, int lane) {
+__device__ __noinline__ void publish_partial(const GemvArgs& p, int64_t w, int slot, int64_t rb,
+                                             const float (&acc)[NT][4], int gid, int t4, int lane) {
+    store_partial<NT>(p, w, slot, acc, gid, t4);
+    __syncwarp();  // the lanes' stores happen before lane 0's release
     int old = 0;
-    if (lane == 0) old = atomicAdd(p.counter + rb, 1);
+    if (lane == 0) old = ptx::atom_add_acq_rel_gpu(p.counter + rb, 1);
     old = __shfl_sync(0xffffffffu, old, 0);
     const int64_t wa = warp_of_unit(rb * p.KU, p);
     const int64_t wb = warp_of_unit(rb * p.KU + p.KU - 1, p);
     if ((int64_t)old != wb - wa) return;  // another warp finishes this row-block
-    __threadfence();
     const int64_t slot_elems = (int64_t)kRows * p.M;
     float sum[NT][4];
 #pragma unroll
@@ -251,8 +255,8 @@ __device__ __forceinline__ void arrive_row_block(const GemvArgs& p, int64_t rb, 
     for (int64_t v = wa; v <= wb; ++v) {
         // rb is the first segment of every contributor except possibly wa
         const bool wa_started_inside = (v * p.U / p.P) == rb * p.KU;
-        const int slot = (v == wa && !wa_started_inside) ? 1 : 0;
-        const float* src = p.partial + (v * 2 + slot) * slot_elems;
+        const int sl = (v == wa && !wa_started_inside) ? 1 : 0;
+        const float* src = p.partial + (v * 2 + sl) * slot_elems;
 #pragma unroll
         for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -284,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&tmap_w);
     }
+    if (threadIdx.x < 16) reinterpret_cast<uint4*>(bars->zero)[threadIdx.x] = make_uint4(0, 0, 0, 0);
     __syncthreads();
 
     // unit range of every consumer warp of this block
@@ -292,8 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ub = w < p.P ? w * p.U / p.P : 0;
         ue = w < p.P ? (w + 1) * p.U / p.P : 0;
     };
-    auto issue = [&](int cw, int64_t u, int sl) {  // one unit into a slot: four 16-row x 64-byte boxes
-        const int64_t rb = u / p.KU, ku = u % p.KU;
+    auto issue = [&](int cw, int64_t rb, int64_t ku, int sl) {  // one unit: four 16-row x 64-byte boxes
         uint64_t* bar = &bars->full[cw][sl];
         uint8_t* dst = ring + (cw * kSlots + sl) * kSlotBytes;
         ptx::mbar_arrive_expect_tx(bar, kSlotBytes);
@@ -306,8 +310,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cw = warp;
     int64_t u_begin, u_end;
     range(cw, u_begin, u_end);
-    if (lane == 0)  // first loads of this warp go out before x is staged
-        for (int r = 0; r < kSlots && u_begin + r < u_end; ++r) issue(cw, u_begin + r, r);
+    // refill cursor: the next unit to load into this warp's ring
+    int64_t f_rb = u_begin / p.KU, f_ku = u_begin % p.KU;
+    auto advance = [&](int64_t& rb_, int64_t& ku_) {
+        if (++ku_ == p.KU) {
+            ku_ = 0;
+            ++rb_;
+        }
+    };
+    for (int r = 0; r < kSlots && u_begin + r < u_end; ++r) {  // first loads go out before x is staged
+        if (lane == 0) issue(cw, f_rb, f_ku, r);
+        advance(f_rb, f_ku);
+    }
+    // weights and scales never change between calls; x, y and the workspace may
+    // belong to the previous kernel on the stream: touch them only after this
+    ptx::grid_dependency_wait();
     if (XS) {
         const int64_t chunks = (int64_t)p.M * xsteps * 16;  // zero past K
         for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) {
@@ -327,13 +344,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t rb = u_begin / p.KU, ku = u_begin % p.KU;
     const int64_t first_rb = rb;
     int64_t seg_ku0 = ku;
-    float acc[NT][4], acc_first[NT][4];
-    bool has_first = false;
-    int64_t last_rb = -1;
+    float acc[NT][4];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
     UnitScales<G> sc;
     load_scales<G>(sc, p, rb, ku, gid);
+    // x row of each of this lane's tokens (the zero block for lanes without one)
+    const uint8_t* xbase[NT];
+    int xstep[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const bool has = 8 * t + gid < p.M;
+        xbase[t] = has ? xs + (8 * t + gid) * xstride : bars->zero;
+        xstep[t] = has ? kStepK * 2 : 0;
+    }
 
     for (int64_t u = u_begin; u < u_end; ++u) {
         const int64_t r = u - u_begin;
@@ -352,41 +376,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         UnitScales<G> sc_next;
         const int64_t nrb = ku + 1 == p.KU ? rb + 1 : rb, nku = ku + 1 == p.KU ? 0 : ku + 1;
         if (u + 1 < u_end) load_scales<G>(sc_next, p, nrb, nku, gid);
-        compute_unit<G, NT, XS>(ring + (cw * kSlots + sl) * kSlotBytes, sc, p, xs, xstride, ku, gid, t4, acc);
+        const uint8_t* xrow[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) xrow[t] = xbase[t] + ku * kUnitSteps * xstep[t];
+        compute_unit<G, NT, XS>(ring + (cw * kSlots + sl) * kSlotBytes, sc, p, xrow, xstep, ku, gid, t4, acc);
         __syncwarp();  // every lane has read the slot
-        if (lane == 0 && u + kSlots < u_end) {
-            ptx::fence_proxy_async_smem();
-            issue(cw, u + kSlots, sl);
+        if (u + kSlots < u_end) {
+            if (lane == 0) issue(cw, f_rb, f_ku, sl);
+            advance(f_rb, f_ku);
         }
         if (u + 1 < u_end) sc = sc_next;
 
         const bool seg_end = (ku == p.KU - 1) || (u == u_end - 1);
         if (seg_end) {
-            if (seg_ku0 == 0 && ku == p.KU - 1) {
+            if (u == u_end - 1) ptx::launch_dependents();  // only the epilogue of this warp remains
+            if (seg_ku0 == 0 && ku == p.KU - 1)
                 store_y<NT>(p, rb, acc, gid, t4);  // whole row-block in this warp
-            } else if (rb == first_rb) {
-                has_first = true;  // published after the last unit
-#pragma unroll
-                for (int t = 0; t < NT; ++t)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) acc_first[t][i] = acc[t][i];
-            } else {
-                store_partial<NT>(p, w, 1, acc, gid, t4);  // partial last segment
-                last_rb = rb;
-            }
+            else  // partial: published now, so its latency overlaps the units that follow
+                publish_partial<NT>(p, w, rb == first_rb ? 0 : 1, rb, acc, gid, t4, lane);
 #pragma unroll
             for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
         }
         rb = nrb;
         ku = nku;
         if (seg_end) seg_ku0 = ku;
-    }
-    if (has_first) store_partial<NT>(p, w, 0, acc_first, gid, t4);
-    if (has_first || last_rb >= 0) {
-        __threadfence();
-        __syncwarp();
-        if (has_first) arrive_row_block<NT>(p, first_rb, gid, t4, lane);
-        if (last_rb >= 0) arrive_row_block<NT>(p, last_rb, gid, t4, lane);
     }
 }
 
@@ -415,16 +428,26 @@ size_t smem_bytes(bool xs, int64_t M, int64_t steps) {
 }
 
 template <int G, int NT, bool XS>
-w4a16_status launch_one(const CUtensorMap& map, const GemvArgs& a, unsigned blocks, size_t smem, cudaStream_t st) {
+w4a16_status launch_one(const DeviceInfo& dev, const CUtensorMap& map, const GemvArgs& a, unsigned blocks,
+                        size_t smem, cudaStream_t st) {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
+    std::call_once(once, [&dev] {  // the device's opt-in maximum; each launch checks its own size
         attr = cudaFuncSetAttribute(gemv_kernel<G, NT, XS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)(smem_bytes(false, 0, 0) + kXSmemMax));
+                                    (int)dev.smem_optin);
     });
     if (attr != cudaSuccess) return cuda_status(attr, "gemv: cudaFuncSetAttribute");
-    gemv_kernel<G, NT, XS><<<blocks, kThreads, smem, st>>>(map, a);
-    return cuda_status(cudaGetLastError(), "gemv: kernel launch");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, gemv_kernel<G, NT, XS>, map, a), "gemv: kernel launch");
 }
 
 }  // namespace
@@ -488,8 +511,8 @@ w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     const int nt = M <= 8 ? 1 : 2;
     w4a16_status r = W4A16_OK;
 #define W4A16_GEMV(G_, NT_)                                                           \
-    r = xs ? launch_one<G_, NT_, true>(map, a, (unsigned)blocks, smem, st)            \
-           : launch_one<G_, NT_, false>(map, a, (unsigned)blocks, smem, st)
+    r = xs ? launch_one<G_, NT_, true>(dev, map, a, (unsigned)blocks, smem, st)       \
+           : launch_one<G_, NT_, false>(dev, map, a, (unsigned)blocks, smem, st)
     if (nt == 1) {
         if (group == 128) W4A16_GEMV(128, 1);
         else if (group == 64) W4A16_GEMV(64, 1);
