@@ -130,3 +130,26 @@ def test_workspace_shared_across_shapes(w4, cuda_device):
             y = _run(w4, cuda_device, x, qw, s, 128)
             y_ref, a = oracle.linear(x, qw, s, 128)
             assert_within_bound(y, y_ref, a, f"M={x.shape[0]} N={qw.shape[0]}")
+
+
+def test_weights_written_by_previous_kernel(w4, cuda_device):
+    """The GEMV may start before the kernel ahead of it on the stream ends; it
+    must still read the weights that kernel wrote. The quantizer writes the
+    packed weights and the GEMV follows at once on the same stream, several
+    times over; the allocator hands back the same memory with the previous
+    round's contents, so reading too early would give the old weights."""
+    import torch
+
+    K, N, g = 2048, 1536, 128
+    x = workloads.activations(workloads.rng(77), 1, K)
+    xd = to_dev(x, cuda_device)
+    for i in range(6):
+        W = workloads.weights(workloads.rng(100 + i), N, K)
+        Wd = torch.from_numpy(W).to(cuda_device)
+        torch.cuda.synchronize()
+        qw, s = w4.pack(Wd, g)
+        y = w4.linear(xd, qw, s, g).cpu().numpy()
+        del qw, s
+        qh, sh = oracle.quantize(W, g)
+        y_ref, a = oracle.linear(x, qh, sh, g)
+        assert_within_bound(y, y_ref, a, f"pack then GEMV, round {i}")

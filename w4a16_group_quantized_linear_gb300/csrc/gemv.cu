@@ -32,8 +32,11 @@
 //   warp order (deterministic), rounds once to fp16 and resets the counter.
 //   A warp publishes each partial as soon as its segment ends, with one
 //   acquire-release atomic on the counter.
-// * Programmatic dependent launch: the weight loads of the first units go out
-//   before griddepcontrol.wait, so they overlap the previous kernel's tail.
+// * Programmatic dependent launch: the block starts while the kernel before it
+//   is still finishing. Until griddepcontrol.wait returns it only prefetches
+//   the weights of its first units into L2 (L2 is the point of coherence, so
+//   this is safe even if that kernel wrote them); after it, x is loaded first
+//   and the ring's TMA loads then hit L2.
 //
 // Waits on the slot barriers are bounded in time; one that gives up records
 // W4A16_ERR_TIMEOUT in the device error word and the block unwinds after its
@@ -59,6 +62,7 @@ constexpr int kSlotBytes = kUnitSteps * kRows * 64;  // 4 KB
 constexpr int kRingBytes = kConsumers * kSlots * kSlotBytes;
 constexpr int kMaxM = 16;        // activation rows handled by the GEMV
 constexpr size_t kXSmemMax = 80 * 1024;  // x staged in shared memory up to this size
+constexpr int kXLoads = (int)((kXSmemMax / 16 + kThreads - 1) / kThreads);  // x loads per thread
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct GemvArgs {
@@ -82,14 +86,23 @@ struct Bars {
     alignas(16) uint8_t zero[256];  // x fragment of lanes without a token
 };
 
-__device__ __forceinline__ uint4 ld_cached_v4(const void* p) {
+// Every input may have been written by the kernel just before this one on
+// the stream (its completion is awaited with griddepcontrol.wait), so none is
+// read through the non-coherent path. One-shot reads bypass L1 (.cg); x read
+// repeatedly from global memory uses the L1 (.ca).
+__device__ __forceinline__ uint4 ld_l2_v4(const void* p) {
     uint4 v;
-    asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }
-__device__ __forceinline__ uint32_t ld_cached_u16(const uint16_t* p) {
+__device__ __forceinline__ uint4 ld_l1_v4(const void* p) {
+    uint4 v;
+    asm("ld.global.ca.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_l2_u16(const uint16_t* p) {
     unsigned short v;
-    asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p));
     return v;
 }
 
@@ -129,8 +142,8 @@ __device__ __forceinline__ void load_scales(UnitScales<G>& sc, const GemvArgs& p
     for (int j = 0; j < kUnitK / G; ++j) {
         const int64_t g = ku * (kUnitK / G) + j;
         const bool vg = g < gpr;
-        const uint32_t a = (v0 && vg) ? ld_cached_u16(s0 + g) : 0u;
-        const uint32_t b = (v1 && vg) ? ld_cached_u16(s1 + g) : 0u;
+        const uint32_t a = (v0 && vg) ? ld_l2_u16(s0 + g) : 0u;
+        const uint32_t b = (v1 && vg) ? ld_l2_u16(s1 + g) : 0u;
         sc.lo[j] = __half2float(__ushort_as_half((unsigned short)a));
         sc.hi[j] = __half2float(__ushort_as_half((unsigned short)b));
     }
@@ -184,7 +197,7 @@ __device__ __forceinline__ void compute_unit(const uint8_t* slot, const UnitScal
                         const int m = 8 * t + gid;
                         const int64_t k0 = (ku * kUnitSteps + step) * kStepK + j * G + t4 * (G / 4) + 8 * wi;
                         xv = make_uint4(0, 0, 0, 0);
-                        if (m < p.M && k0 < p.K) xv = permute_x8(ld_cached_v4(p.x + (int64_t)m * p.K + k0));
+                        if (m < p.M && k0 < p.K) xv = permute_x8(ld_l1_v4(p.x + (int64_t)m * p.K + k0));
                     }
                     if (wi == 0) mma_16816_zero(c[t], a04, b04, a15, b15, xv.x, xv.y);
                     else mma_16816(c[t], a04, b04, a15, b15, xv.x, xv.y);
@@ -318,21 +331,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++rb_;
         }
     };
-    for (int r = 0; r < kSlots && u_begin + r < u_end; ++r) {  // first loads go out before x is staged
+    // Every input, the weights included, may come from the kernel before this
+    // one on the stream, which may still be running: until griddepcontrol.wait
+    // returns, the first units of this warp are only prefetched into L2.
+    if (lane == 0) {
+        int64_t rb_ = f_rb, ku_ = f_ku;
+        for (int r = 0; r < kSlots && u_begin + r < u_end; ++r) {
+#pragma unroll
+            for (int step = 0; step < kUnitSteps; ++step)
+                ptx::tma_prefetch_l2_2d(&tmap_w, (int)((ku_ * kUnitSteps + step) * 64), (int)(rb_ * kRows));
+            advance(rb_, ku_);
+        }
+    }
+    ptx::grid_dependency_wait();
+    // x loads first (every unit waits for them), then the ring, then the x stores
+    const int64_t chunks = XS ? (int64_t)p.M * xsteps * 16 : 0;  // 16-byte chunks, zero past K
+    uint4 xv[XS ? kXLoads : 1];
+    if (XS) {
+#pragma unroll
+        for (int i = 0; i < kXLoads; ++i) {
+            const int64_t c = threadIdx.x + i * kThreads;
+            xv[i] = make_uint4(0, 0, 0, 0);
+            if (c < chunks) {
+                const int64_t m = c / (xsteps * 16), k0 = (c % (xsteps * 16)) * 8;
+                if (k0 < p.K) xv[i] = ld_l2_v4(p.x + m * p.K + k0);
+            }
+        }
+    }
+    for (int r = 0; r < kSlots && u_begin + r < u_end; ++r) {
         if (lane == 0) issue(cw, f_rb, f_ku, r);
         advance(f_rb, f_ku);
     }
-    // weights and scales never change between calls; x, y and the workspace may
-    // belong to the previous kernel on the stream: touch them only after this
-    ptx::grid_dependency_wait();
     if (XS) {
-        const int64_t chunks = (int64_t)p.M * xsteps * 16;  // zero past K
-        for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) {
-            const int64_t m = c / (xsteps * 16), cc = c % (xsteps * 16);
-            const int64_t k0 = cc * 8;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (k0 < p.K) v = permute_x8(ld_cached_v4(p.x + m * p.K + k0));
-            *reinterpret_cast<uint4*>(xs + m * xstride + (cc >> 4) * (kStepK * 2) + xs_pos((int)(cc & 15), G) * 16) = v;
+#pragma unroll
+        for (int i = 0; i < kXLoads; ++i) {
+            const int64_t c = threadIdx.x + i * kThreads;
+            if (c < chunks) {
+                const int64_t m = c / (xsteps * 16), cc = c % (xsteps * 16);
+                *reinterpret_cast<uint4*>(xs + m * xstride + (cc >> 4) * (kStepK * 2) +
+                                          xs_pos((int)(cc & 15), G) * 16) = permute_x8(xv[i]);
+            }
         }
         __syncthreads();
     }
