@@ -390,6 +390,68 @@ def cpu_baseline_sample(budget_s=12.0):
                       f"{dt:.1f} s"}
 
 
+# ----------------------------------------------------------------- profile --
+
+PROFILE_CASES = ("decode", "decode_down", "decode_m4", "prefill", "prefill_m512", "moe_gate_up", "moe_down")
+
+
+def run_profile(case: str, launches: int):
+    """A few launches of one workload, for ncu: no timing, no clocks, no oracle."""
+    import torch
+
+    import w4a16_group_quantized_linear_gb300 as w4
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w4.lib()
+    g = workloads.rng(0)
+    if case.startswith("moe"):
+        Km, Nm = (2048, 512) if case == "moe_gate_up" else (512, 2048)
+        W, xs, rt = workloads.moe(Km, Nm)
+        E = W.shape[0]
+        qm, sm = w4.pack(torch.from_numpy(W.reshape(E * Nm, Km)).to(dev), 32)
+        qm, sm = qm.view(E, Nm, Km // 2), sm.view(E, Nm, Km // 32)
+        xd = torch.from_numpy(xs).to(dev)
+        off = torch.from_numpy(rt.offsets).to(dev)
+        yd = torch.empty((xs.shape[0], Nm), dtype=torch.float16, device=dev)
+        for _ in range(launches):
+            w4.grouped_linear(xd, qm, sm, off, 32, out=yd)
+    else:
+        K, N = DECODE[1] if case == "decode_down" else DECODE[0]
+        M = {"decode": 1, "decode_down": 1, "decode_m4": 4, "prefill": 4096, "prefill_m512": 512}[case]
+        qw, s = w4.pack(torch.from_numpy(workloads.weights(g, N, K)).to(dev), GROUP)
+        copies = [(qw, s)] + [(qw.clone(), s.clone()) for _ in range(3)]  # successive launches miss in L2
+        x = torch.from_numpy(workloads.activations(g, M, K, outlier_frac=0.01 if M > 16 else 0.0)).to(dev)
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        for i in range(launches):
+            w4.linear(x, *copies[i % 4], GROUP, out=y)
+    torch.cuda.synchronize()
+    w4.device_status()
+    print(f"profile {case}: {launches} launches done")
+
+
+def measured_traffic(kernel_file: str, profile: str):
+    """DRAM bytes per launch from a committed ncu summary, or None once the
+    kernel source has changed since that capture (the summary records the
+    sha256 of the source it was taken on)."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", profile)
+    src = os.path.join(ROOT, "w4a16_group_quantized_linear_gb300", "csrc", kernel_file)
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(("source_sha256:", "dram_bytes_per_launch:")))
+    if fields.get("source_sha256", "").strip() != sha:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 # -------------------------------------------------------------------- main --
 
 METRIC = "decode GEMV achieved HBM GB/s (M=1, 27B-class gate/up + down, group 128)"
@@ -403,7 +465,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--decode-only", action="store_true", help="skip the prefill / MoE side measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=PROFILE_CASES, help="only run a few launches of one workload (for ncu)")
+    ap.add_argument("--launches", type=int, default=6, help="launches in --profile mode")
     args = ap.parse_args()
+    if args.profile:
+        run_profile(args.profile, args.launches)
+        return
     args.warmup = max(args.warmup, 3)
 
     rank = int(os.environ.get("RANK", 0))
@@ -440,7 +507,8 @@ def main():
         "vs_baseline": None, "dtype": "f16 in, fp32 accumulate, int4 weights", "data": "synthetic",
         "config": config,
         "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["hbm_peak"], "unit": "GB/s",
-                     "frac": r["achieved"] / r["hbm_peak"], "traffic": None,
+                     "frac": r["achieved"] / r["hbm_peak"],
+                     "traffic": measured_traffic("gemv.cu", "gemv_decode_m1.md"),
                      "kernel": "gemv_kernel<group 128, M<=8>", "peak_kind": r["peak_kind"],
                      "kernel_us": r["kernel_ms"] * 1e3, "algorithmic_bytes_per_launch": r["per_launch_bytes"]},
         "e2e": r["e2e"], "gpu_launches": r["launches"], "clocks": r["clocks"], "gpu": r["gpu"], "sms": r["sms"],
