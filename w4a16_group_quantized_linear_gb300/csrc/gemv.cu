@@ -78,12 +78,14 @@ struct GemvArgs {
     float* partial;  // [P][2][16 * M] fp32 partial sums (first / last segment)
     int* counter;    // [ceil(N/16)] arrivals per row-block, zero between calls
     unsigned int* err;
+    int gpr;         // scale groups per row: K / G
+    int svec;        // scale rows start 16-byte aligned (gpr % 8 == 0): whole units load as vectors
 };
 
 struct Bars {
     uint64_t full[kConsumers][kSlots];
     int abort;
-    alignas(16) uint8_t zero[256];  // x fragment of lanes without a token
+    alignas(16) uint8_t zero[1024];  // x of one unit for lanes without a token
 };
 
 // Every input may have been written by the kernel just before this one on
@@ -98,6 +100,28 @@ __device__ __forceinline__ uint4 ld_l2_v4(const void* p) {
 __device__ __forceinline__ uint4 ld_l1_v4(const void* p) {
     uint4 v;
     asm("ld.global.ca.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ld_l2_v2(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+// Shared-memory loads by 32-bit shared address (the offsets fold into the
+// instruction); volatile keeps them after the barrier wait that guards them.
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds_v2(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
     return v;
 }
 __device__ __forceinline__ uint32_t ld_l2_u16(const uint16_t* p) {
@@ -123,64 +147,118 @@ __device__ __forceinline__ int xs_pos(int c_local, int G) {
     return (j * (G / 32) + wi) * 4 + t4;
 }
 
-// Scales of one unit for rows gid and gid+8, per group, as fp32. Rows past N
-// and groups past K get 0.
+// Scales of one unit for rows gid and gid+8 as raw fp16: word j of a row holds
+// the unit's groups 2j (low half) and 2j+1 (high half). They are converted
+// only when used, so the loads stay in flight during the previous unit.
 template <int G>
 struct UnitScales {
-    float lo[kUnitK / G], hi[kUnitK / G];
+    static constexpr int W = kUnitK / G / 2;
+    uint32_t lo[W], hi[W];
 };
 
+// The scale rows of this lane (rows gid and gid+8 of a row-block); a row past
+// N reads row 0 and is zeroed.
+struct ScaleRows {
+    const uint16_t* r0;
+    const uint16_t* r1;
+    bool v0, v1;
+};
+
+__device__ __forceinline__ ScaleRows scale_rows(const GemvArgs& p, int rb, int gid) {
+    const int64_t n0 = (int64_t)rb * kRows + gid, n1 = n0 + 8;
+    ScaleRows r;
+    r.v0 = n0 < p.N;
+    r.v1 = n1 < p.N;
+    r.r0 = p.s + (r.v0 ? n0 : 0) * p.gpr;
+    r.r1 = p.s + (r.v1 ? n1 : 0) * p.gpr;
+    return r;
+}
+
 template <int G>
-__device__ __forceinline__ void load_scales(UnitScales<G>& sc, const GemvArgs& p, int64_t rb, int64_t ku,
-                                            int gid) {
-    const int64_t gpr = p.K / G;
-    const int64_t r0 = rb * kRows + gid, r1 = r0 + 8;
-    const bool v0 = r0 < p.N, v1 = r1 < p.N;
-    const uint16_t* s0 = p.s + (v0 ? r0 : 0) * gpr;
-    const uint16_t* s1 = p.s + (v1 ? r1 : 0) * gpr;
+__device__ __forceinline__ void load_scales(UnitScales<G>& sc, const GemvArgs& p, const ScaleRows& sr, int ku) {
+    constexpr int GPU = kUnitK / G;  // groups per unit: 4, 8 or 16
+    const int g0 = ku * GPU;
+    if (p.svec && g0 + GPU <= p.gpr) {  // whole unit from aligned rows: vector loads
+        if constexpr (GPU == 4) {
+            const uint2 a = sr.v0 ? ld_l2_v2(sr.r0 + g0) : make_uint2(0, 0);
+            const uint2 b = sr.v1 ? ld_l2_v2(sr.r1 + g0) : make_uint2(0, 0);
+            sc.lo[0] = a.x; sc.lo[1] = a.y;
+            sc.hi[0] = b.x; sc.hi[1] = b.y;
+        } else {
 #pragma unroll
-    for (int j = 0; j < kUnitK / G; ++j) {
-        const int64_t g = ku * (kUnitK / G) + j;
-        const bool vg = g < gpr;
-        const uint32_t a = (v0 && vg) ? ld_l2_u16(s0 + g) : 0u;
-        const uint32_t b = (v1 && vg) ? ld_l2_u16(s1 + g) : 0u;
-        sc.lo[j] = __half2float(__ushort_as_half((unsigned short)a));
-        sc.hi[j] = __half2float(__ushort_as_half((unsigned short)b));
+            for (int q = 0; q < GPU / 8; ++q) {
+                const uint4 a = sr.v0 ? ld_l2_v4(sr.r0 + g0 + 8 * q) : make_uint4(0, 0, 0, 0);
+                const uint4 b = sr.v1 ? ld_l2_v4(sr.r1 + g0 + 8 * q) : make_uint4(0, 0, 0, 0);
+                sc.lo[4 * q] = a.x; sc.lo[4 * q + 1] = a.y; sc.lo[4 * q + 2] = a.z; sc.lo[4 * q + 3] = a.w;
+                sc.hi[4 * q] = b.x; sc.hi[4 * q + 1] = b.y; sc.hi[4 * q + 2] = b.z; sc.hi[4 * q + 3] = b.w;
+            }
+        }
+    } else {  // ragged or unaligned: one scale at a time, groups past K read as 0
+#pragma unroll
+        for (int w = 0; w < GPU / 2; ++w) {
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int g = g0 + 2 * w + h;
+                const bool vg = g < p.gpr;
+                lo |= ((sr.v0 && vg) ? ld_l2_u16(sr.r0 + g) : 0u) << (16 * h);
+                hi |= ((sr.v1 && vg) ? ld_l2_u16(sr.r1 + g) : 0u) << (16 * h);
+            }
+            sc.lo[w] = lo;
+            sc.hi[w] = hi;
+        }
     }
 }
 
+__device__ __forceinline__ float half_bits(uint32_t w, int h) {
+    return __half2float(__ushort_as_half((unsigned short)(h ? (w >> 16) : (w & 0xffffu))));
+}
+
 // One unit from its ring slot: for every 128-k step and scale group, the
-// quad's share of rows gid and gid+8. XS: x comes from shared memory; each
-// lane's row pointer (xrow) and per-step stride (xstep) point lanes without a
-// token at a zero block instead, so no load is predicated.
+// quad's share of rows gid and gid+8. `wlane` is the shared address of this
+// lane's first weight bytes in the slot (row gid, its quad's offset). XS: x
+// comes from shared memory at xlane[t] (this lane's 16-byte chunk of the
+// unit's x for token 8t+gid, or of the zero block for lanes without a token),
+// so no load is predicated and every offset below is a constant.
 template <int G, int NT, bool XS>
-__device__ __forceinline__ void compute_unit(const uint8_t* slot, const UnitScales<G>& sc, const GemvArgs& p,
-                                             const uint8_t* const (&xrow)[NT], const int (&xstep)[NT],
-                                             int64_t ku, int gid, int t4, float (&acc)[NT][4]) {
+__device__ __forceinline__ void compute_unit(uint32_t wlane, const UnitScales<G>& sc, const GemvArgs& p,
+                                             const uint32_t (&xlane)[NT], int ku, int gid, int t4,
+                                             float (&acc)[NT][4]) {
     constexpr int WPP = G / 32;      // words per thread per row per group
     constexpr int GPS = kStepK / G;  // groups per step
 #pragma unroll
     for (int step = 0; step < kUnitSteps; ++step) {
-        const uint8_t* ra = slot + step * (kRows * 64) + gid * 64;
-        const uint8_t* rbp = ra + 8 * 64;
 #pragma unroll
         for (int j = 0; j < GPS; ++j) {
             uint32_t wa[WPP], wb[WPP];
-            const int off = j * (G / 2) + t4 * (G / 8);
+            const uint32_t ra = wlane + step * (kRows * 64) + j * (G / 2);
+            const uint32_t rbp = ra + 8 * 64;
             if constexpr (WPP == 4) {
-                const uint4 a = *reinterpret_cast<const uint4*>(ra + off);
-                const uint4 b = *reinterpret_cast<const uint4*>(rbp + off);
+                const uint4 a = lds_v4(ra), b = lds_v4(rbp);
                 wa[0] = a.x; wa[1] = a.y; wa[2] = a.z; wa[3] = a.w;
                 wb[0] = b.x; wb[1] = b.y; wb[2] = b.z; wb[3] = b.w;
             } else if constexpr (WPP == 2) {
-                const uint2 a = *reinterpret_cast<const uint2*>(ra + off);
-                const uint2 b = *reinterpret_cast<const uint2*>(rbp + off);
+                const uint2 a = lds_v2(ra), b = lds_v2(rbp);
                 wa[0] = a.x; wa[1] = a.y;
                 wb[0] = b.x; wb[1] = b.y;
             } else {
-                wa[0] = *reinterpret_cast<const uint32_t*>(ra + off);
-                wb[0] = *reinterpret_cast<const uint32_t*>(rbp + off);
+                wa[0] = lds_u32(ra);
+                wb[0] = lds_u32(rbp);
             }
+            uint4 xv[WPP][NT];
+#pragma unroll
+            for (int wi = 0; wi < WPP; ++wi)
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    if (XS) {
+                        xv[wi][t] = lds_v4(xlane[t] + step * (kStepK * 2) + (j * WPP + wi) * 64);
+                    } else {
+                        const int m = 8 * t + gid;
+                        const int64_t k0 = ((int64_t)ku * kUnitSteps + step) * kStepK + j * G + t4 * (G / 4) + 8 * wi;
+                        xv[wi][t] = make_uint4(0, 0, 0, 0);
+                        if (m < p.M && k0 < p.K) xv[wi][t] = permute_x8(ld_l1_v4(p.x + (int64_t)m * p.K + k0));
+                    }
+                }
             float c[NT][4];  // this group's fp32 sum of x*q
 #pragma unroll
             for (int wi = 0; wi < WPP; ++wi) {
@@ -189,22 +267,13 @@ __device__ __forceinline__ void compute_unit(const uint8_t* slot, const UnitScal
                 nibbles_to_half2(wb[wi], b04, b15, b26, b37);
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
-                    uint4 xv;
-                    if (XS) {
-                        xv = *reinterpret_cast<const uint4*>(xrow[t] + step * xstep[t] +
-                                                             ((j * WPP + wi) * 4 + t4) * 16);
-                    } else {
-                        const int m = 8 * t + gid;
-                        const int64_t k0 = (ku * kUnitSteps + step) * kStepK + j * G + t4 * (G / 4) + 8 * wi;
-                        xv = make_uint4(0, 0, 0, 0);
-                        if (m < p.M && k0 < p.K) xv = permute_x8(ld_l1_v4(p.x + (int64_t)m * p.K + k0));
-                    }
-                    if (wi == 0) mma_16816_zero(c[t], a04, b04, a15, b15, xv.x, xv.y);
-                    else mma_16816(c[t], a04, b04, a15, b15, xv.x, xv.y);
-                    mma_16816(c[t], a26, b26, a37, b37, xv.z, xv.w);
+                    if (wi == 0) mma_16816_zero(c[t], a04, b04, a15, b15, xv[wi][t].x, xv[wi][t].y);
+                    else mma_16816(c[t], a04, b04, a15, b15, xv[wi][t].x, xv[wi][t].y);
+                    mma_16816(c[t], a26, b26, a37, b37, xv[wi][t].z, xv[wi][t].w);
                 }
             }
-            const float s0 = sc.lo[step * GPS + j], s1 = sc.hi[step * GPS + j];
+            const int gi = step * GPS + j;
+            const float s0 = half_bits(sc.lo[gi >> 1], gi & 1), s1 = half_bits(sc.hi[gi >> 1], gi & 1);
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
                 acc[t][0] = fmaf(s0, c[t][0], acc[t][0]);
@@ -301,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&tmap_w);
     }
-    if (threadIdx.x < 16) reinterpret_cast<uint4*>(bars->zero)[threadIdx.x] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x < 64) reinterpret_cast<uint4*>(bars->zero)[threadIdx.x] = make_uint4(0, 0, 0, 0);
     __syncthreads();
 
     // unit range of every consumer warp of this block
@@ -379,56 +448,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t w = (int64_t)blockIdx.x * kConsumers + cw;
     if (w >= p.P) return;
 
-    int64_t rb = u_begin / p.KU, ku = u_begin % p.KU;
-    const int64_t first_rb = rb;
-    int64_t seg_ku0 = ku;
+    const int n_units = (int)(u_end - u_begin);
+    int rb = (int)(u_begin / p.KU), ku = (int)(u_begin % p.KU);
+    const int first_rb = rb, KU = (int)p.KU;
+    int seg_ku0 = ku;
     float acc[NT][4];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+    ScaleRows sr = scale_rows(p, rb, gid);
     UnitScales<G> sc;
-    load_scales<G>(sc, p, rb, ku, gid);
-    // x row of each of this lane's tokens (the zero block for lanes without one)
-    const uint8_t* xbase[NT];
-    int xstep[NT];
+    load_scales<G>(sc, p, sr, ku);
+    // shared address of this lane's x chunk in unit 0 (the zero block for lanes
+    // without a token) and its stride per unit
+    uint32_t xlane0[NT], xunit[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         const bool has = 8 * t + gid < p.M;
-        xbase[t] = has ? xs + (8 * t + gid) * xstride : bars->zero;
-        xstep[t] = has ? kStepK * 2 : 0;
+        xlane0[t] = (has ? ptx::smem_u32(xs) + (8 * t + gid) * (uint32_t)xstride : ptx::smem_u32(bars->zero)) + t4 * 16;
+        xunit[t] = has ? kUnitSteps * kStepK * 2 : 0;
     }
+    const uint32_t wlane0 = ptx::smem_u32(ring) + cw * (kSlots * kSlotBytes) + gid * 64 + t4 * (G / 8);
 
-    for (int64_t u = u_begin; u < u_end; ++u) {
-        const int64_t r = u - u_begin;
-        const int sl = (int)(r % kSlots);
-        if (!__all_sync(0xffffffffu,
-                        ptx::mbar_wait(&bars->full[cw][sl], (uint32_t)((r / kSlots) & 1), abort, kWaitLimitNs))) {
+    int sl = 0;
+    uint32_t phase = 0;
+    for (int r = 0; r < n_units; ++r) {
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bars->full[cw][sl], phase, abort, kWaitLimitNs))) {
             raise_device_error(p.err, W4A16_ERR_TIMEOUT);
             *abort = 1;
             if (lane == 0) {  // this warp's own loads still in flight land before it exits
                 volatile int never = 0;
-                for (int64_t q = r + 1; q < r + kSlots && u_begin + q < u_end; ++q)
+                for (int q = r + 1; q < r + kSlots && q < n_units; ++q)
                     ptx::mbar_wait(&bars->full[cw][q % kSlots], (uint32_t)((q / kSlots) & 1), &never, kWaitLimitNs);
             }
             return;
         }
+        int nrb = rb, nku = ku + 1;
+        if (nku == KU) {
+            nku = 0;
+            ++nrb;
+        }
+        const ScaleRows nsr = nku == 0 ? scale_rows(p, nrb, gid) : sr;
         UnitScales<G> sc_next;
-        const int64_t nrb = ku + 1 == p.KU ? rb + 1 : rb, nku = ku + 1 == p.KU ? 0 : ku + 1;
-        if (u + 1 < u_end) load_scales<G>(sc_next, p, nrb, nku, gid);
-        const uint8_t* xrow[NT];
+        if (r + 1 < n_units) load_scales<G>(sc_next, p, nsr, nku);
+        uint32_t xlane[NT];
 #pragma unroll
-        for (int t = 0; t < NT; ++t) xrow[t] = xbase[t] + ku * kUnitSteps * xstep[t];
-        compute_unit<G, NT, XS>(ring + (cw * kSlots + sl) * kSlotBytes, sc, p, xrow, xstep, ku, gid, t4, acc);
+        for (int t = 0; t < NT; ++t) xlane[t] = xlane0[t] + ku * xunit[t];
+        compute_unit<G, NT, XS>(wlane0 + sl * kSlotBytes, sc, p, xlane, ku, gid, t4, acc);
         __syncwarp();  // every lane has read the slot
-        if (u + kSlots < u_end) {
+        if (r + kSlots < n_units) {
             if (lane == 0) issue(cw, f_rb, f_ku, sl);
             advance(f_rb, f_ku);
         }
-        if (u + 1 < u_end) sc = sc_next;
+        if (r + 1 < n_units) sc = sc_next;
+        sr = nsr;
 
-        const bool seg_end = (ku == p.KU - 1) || (u == u_end - 1);
+        const bool seg_end = (ku == KU - 1) || (r == n_units - 1);
         if (seg_end) {
-            if (u == u_end - 1) ptx::launch_dependents();  // only the epilogue of this warp remains
-            if (seg_ku0 == 0 && ku == p.KU - 1)
+            if (r == n_units - 1) ptx::launch_dependents();  // only the epilogue of this warp remains
+            if (seg_ku0 == 0 && ku == KU - 1)
                 store_y<NT>(p, rb, acc, gid, t4);  // whole row-block in this warp
             else  // partial: published now, so its latency overlaps the units that follow
                 publish_partial<NT>(p, w, rb == first_rb ? 0 : 1, rb, acc, gid, t4, lane);
@@ -438,6 +515,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         rb = nrb;
         ku = nku;
         if (seg_end) seg_ku0 = ku;
+        if (++sl == kSlots) {
+            sl = 0;
+            phase ^= 1u;
+        }
     }
 }
 
@@ -541,6 +622,8 @@ w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     a.partial = reinterpret_cast<float*>(workspace);
     a.counter = reinterpret_cast<int*>(reinterpret_cast<char*>(workspace) + partial_region_bytes(dev));
     a.err = dev.error_word;
+    a.gpr = (int)(K / group);
+    a.svec = (K / group) % 8 == 0;
     const int64_t xsteps = a.KU * kUnitSteps;
     const size_t xbytes = (size_t)M * (size_t)(xsteps * kStepK * 2 + 64);
     const bool xs = xbytes <= kXSmemMax && smem_bytes(true, M, xsteps) <= dev.smem_optin;
