@@ -2,22 +2,25 @@
 // "CUDA-graph decode", np4 = four sequences per step).
 //
 // Decode streams every packed weight byte once and does little arithmetic per
-// byte: the kernel is bound by HBM bandwidth, and on the instruction budget
-// of its dequantization. Design (one block of kConsumers warps per SM):
+// byte: the kernel is bound by HBM bandwidth, by the issue rate of its
+// dequantization and legacy tensor-core MMAs, and by the latency of the
+// kernel before it. Design (one block per SM: kConsumers compute warps and
+// one producer warp):
 //
 // * Work unit = 16 weight rows x 512 input features (4 KB packed). Units are
-//   ordered row-block major, k minor; every consumer warp of a persistent
-//   grid owns an equal contiguous range of them (stream-K split), so each SM
+//   ordered row-block major, k minor; every compute warp of a persistent grid
+//   owns an equal contiguous range of them (stream-K split), so each SM
 //   streams the same number of bytes whatever N and K are.
-// * Every warp streams its units through a private ring of kSlots shared-
-//   memory slots with TMA, refilling a slot as soon as it has consumed it (no
-//   coupling between warps): a unit is four 16-row x 64-byte boxes issued back
-//   to back, i.e. 256 contiguous bytes per weight row per unit. Slots are laid
-//   out [k-step][row][64 B], so the fragment reads below are free of bank
-//   conflicts.
+// * Each compute warp has a private ring of kSlots shared-memory slots. Lane c
+//   of the producer warp keeps compute warp c's ring full: one TMA copy per
+//   unit (a 3-D box that lands as [k-step][row][64 B], so the fragment reads
+//   are free of bank conflicts; four 2-D boxes when K % 128 != 0) plus the
+//   unit's box of scales, refilled as soon as the warp releases the slot on
+//   its "empty" barrier. Compute warps neither issue copies nor compute
+//   addresses for them, and no warp waits behind another.
 // * The activations (M x K fp16, when small enough) are staged once per block
-//   in shared memory, permuted into MMA fragment order, while the first weight
-//   boxes are in flight; larger x is read through the L1.
+//   in shared memory, permuted into MMA fragment order; larger x is read
+//   through the L1.
 // * Nibbles become exact fp16 integers in registers (lop3 + one half2 op per
 //   pair) and go straight into mma.sync m16n8k16 as the A operand (rows =
 //   weight rows, columns = tokens padded to 8): the tensor core does the x*q
@@ -33,14 +36,12 @@
 //   A warp publishes each partial as soon as its segment ends, with one
 //   acquire-release atomic on the counter.
 // * Programmatic dependent launch: the block starts while the kernel before it
-//   is still finishing. Until griddepcontrol.wait returns it only prefetches
-//   the weights of its first units into L2 (L2 is the point of coherence, so
-//   this is safe even if that kernel wrote them); after it, x is loaded first
-//   and the ring's TMA loads then hit L2.
+//   is still finishing, and reads nothing (weights included, which that kernel
+//   may have written) before griddepcontrol.wait returns.
 //
-// Waits on the slot barriers are bounded in time; one that gives up records
-// W4A16_ERR_TIMEOUT in the device error word and the block unwinds after its
-// own TMA loads land.
+// Every wait is bounded in time; one that gives up records W4A16_ERR_TIMEOUT in
+// the device error word, and the block leaves only after the copies it issued
+// have landed.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -51,18 +52,26 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kConsumers = 12;   // warps per block (one block per SM; 3 per scheduler)
-constexpr int kThreads = kConsumers * 32;
+constexpr int kConsumers = 12;   // compute warps per block (one block per SM; 3 per scheduler)
+constexpr int kProducer = kConsumers;  // warp index of the block's TMA producer
+constexpr int kThreads = (kConsumers + 1) * 32;
+constexpr int kConsumerThreads = kConsumers * 32;
 constexpr int kSlots = 3;        // ring slots per consumer warp
 constexpr int kStepK = 128;      // k per step (one 64-byte piece of a row)
 constexpr int kUnitSteps = 4;    // steps per unit
 constexpr int kUnitK = kStepK * kUnitSteps;
 constexpr int kRows = 16;        // weight rows per unit
-constexpr int kSlotBytes = kUnitSteps * kRows * 64;  // 4 KB
-constexpr int kRingBytes = kConsumers * kSlots * kSlotBytes;
+constexpr int kWBytes = kUnitSteps * kRows * 64;  // packed weights of a unit: 4 KB
+// Scales travel with the weights (TS) as one TMA box of 16 rows x kScaleBox<G>
+// groups: 16 or 32 bytes a row, the smallest box that holds a unit's groups
+// and starts on a 16-byte boundary (for group 128 it holds two units' groups).
+template <int G>
+constexpr int kScaleBox = G == 32 ? 16 : 8;
+template <int G, bool TS>
+constexpr int kSlotBytes = kWBytes + (TS ? kRows * kScaleBox<G> * 2 : 0);
 constexpr int kMaxM = 16;        // activation rows handled by the GEMV
 constexpr size_t kXSmemMax = 80 * 1024;  // x staged in shared memory up to this size
-constexpr int kXLoads = (int)((kXSmemMax / 16 + kThreads - 1) / kThreads);  // x loads per thread
+constexpr int kXLoads = (int)((kXSmemMax / 16 + kConsumerThreads - 1) / kConsumerThreads);  // x loads per thread
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct GemvArgs {
@@ -80,10 +89,12 @@ struct GemvArgs {
     unsigned int* err;
     int gpr;         // scale groups per row: K / G
     int svec;        // scale rows start 16-byte aligned (gpr % 8 == 0): whole units load as vectors
+    int w3d;         // the weight map is 3-D: one TMA box per unit
 };
 
 struct Bars {
-    uint64_t full[kConsumers][kSlots];
+    uint64_t full[kConsumers][kSlots];   // a unit's bytes have landed in the slot
+    uint64_t empty[kConsumers][kSlots];  // the compute warp has finished with the slot
     int abort;
     alignas(16) uint8_t zero[1024];  // x of one unit for lanes without a token
 };
@@ -210,6 +221,27 @@ __device__ __forceinline__ void load_scales(UnitScales<G>& sc, const GemvArgs& p
     }
 }
 
+// Scales from the unit's TMA box in its slot (rows and groups outside the
+// tensor were filled with zeros by the copy).
+template <int G>
+__device__ __forceinline__ void load_scales_smem(UnitScales<G>& sc, uint32_t box, int ku, int gid) {
+    constexpr int GPU = kUnitK / G;
+    const uint32_t r0 = box + gid * (kScaleBox<G> * 2) + (G == 128 ? (ku & 1) * 8 : 0);
+    const uint32_t r1 = r0 + 8 * (kScaleBox<G> * 2);
+    if constexpr (GPU == 4) {
+        const uint2 a = lds_v2(r0), b = lds_v2(r1);
+        sc.lo[0] = a.x; sc.lo[1] = a.y;
+        sc.hi[0] = b.x; sc.hi[1] = b.y;
+    } else {
+#pragma unroll
+        for (int q = 0; q < GPU / 8; ++q) {
+            const uint4 a = lds_v4(r0 + 16 * q), b = lds_v4(r1 + 16 * q);
+            sc.lo[4 * q] = a.x; sc.lo[4 * q + 1] = a.y; sc.lo[4 * q + 2] = a.z; sc.lo[4 * q + 3] = a.w;
+            sc.hi[4 * q] = b.x; sc.hi[4 * q + 1] = b.y; sc.hi[4 * q + 2] = b.z; sc.hi[4 * q + 3] = b.w;
+        }
+    }
+}
+
 __device__ __forceinline__ float half_bits(uint32_t w, int h) {
     return __half2float(__ushort_as_half((unsigned short)(h ? (w >> 16) : (w & 0xffffu))));
 }
@@ -298,6 +330,8 @@ __device__ __forceinline__ void store_y(const GemvArgs& p, int64_t rb, const flo
         }
 }
 
+__device__ __forceinline__ int unit_begin(int w, const GemvArgs& p) { return (int)((int64_t)w * p.U / p.P); }
+
 __device__ __forceinline__ int64_t warp_of_unit(int64_t u, const GemvArgs& p) {
     return ((u + 1) * p.P + p.U - 1) / p.U - 1;  // largest w with w*U/P <= u
 }
@@ -351,113 +385,154 @@ __device__ __noinline__ void publish_partial(const GemvArgs& p, int64_t w, int s
     if (lane == 0) p.counter[rb] = 0;
 }
 
-template <int G, int NT, bool XS>
+// The producer warp: lane c streams compute warp c's units into that warp's
+// ring, refilling a slot as soon as the warp releases it. The lanes issue
+// their copies side by side, so no compute warp waits behind another.
+template <int G, bool TS>
+__device__ __forceinline__ void produce(const CUtensorMap* tmap_w, const CUtensorMap* tmap_s, const GemvArgs& p,
+                                        Bars* bars, uint8_t* ring, volatile int* abort, int lane) {
+    constexpr int SLOT = kSlotBytes<G, TS>;
+    const int KU = (int)p.KU;
+    const int c = lane < kConsumers ? lane : 0;
+    const int w = blockIdx.x * kConsumers + c;
+    const int ub = (lane < kConsumers && w < p.P) ? unit_begin(w, p) : 0;
+    const int n = (lane < kConsumers && w < p.P) ? unit_begin(w + 1, p) - ub : 0;
+    int ri = 0;  // units issued into the ring
+    auto scale_x = [](int ku) { return G == 128 ? (ku >> 1) * 8 : ku * kScaleBox<G>; };
+    auto issue = [&](int sl, int u) {
+        const int rb = u / KU, ku = u % KU;
+        uint64_t* bar = &bars->full[c][sl];
+        uint8_t* dst = ring + (c * kSlots + sl) * SLOT;
+        ptx::mbar_arrive_expect_tx(bar, SLOT);
+        if (p.w3d) {
+            ptx::tma_load_3d(dst, tmap_w, bar, 0, rb * kRows, ku * kUnitSteps);
+        } else {
+#pragma unroll
+            for (int step = 0; step < kUnitSteps; ++step)
+                ptx::tma_load_2d(dst + step * (kRows * 64), tmap_w, bar, (ku * kUnitSteps + step) * 64, rb * kRows);
+        }
+        if (TS) ptx::tma_load_2d(dst + kWBytes, tmap_s, bar, scale_x(ku), rb * kRows);
+    };
+
+    // Every input, the weights included, may come from the kernel before this
+    // one on the stream, which may still be running: nothing is read before
+    // griddepcontrol.wait returns. (Prefetching the first units into L2 before
+    // the wait is safe, but measured slower: the extra traffic delays the
+    // previous kernel's completion and this kernel's x loads.)
+    ptx::grid_dependency_wait();
+    for (; ri < kSlots && ri < n; ++ri) issue(ri, ub + ri);
+    uint64_t idle_since = 0;
+    bool failed = false;
+    while (__any_sync(0xffffffffu, ri < n && !failed)) {
+        bool moved = false;
+        if (ri < n && !failed) {
+            const int sl = ri % kSlots;
+            // the slot's previous unit (ri - kSlots) completed phase ri / kSlots - 1
+            if (ptx::mbar_try_wait(&bars->empty[c][sl], (uint32_t)((ri / kSlots + 1) & 1))) {
+                issue(sl, ub + ri);
+                ++ri;
+                moved = true;
+            }
+        }
+        if (__any_sync(0xffffffffu, moved)) {
+            idle_since = 0;
+            continue;
+        }
+        const uint64_t now = ptx::globaltimer_ns();
+        if (idle_since == 0) idle_since = now;
+        if (*abort || now - idle_since > kWaitLimitNs) {
+            if (lane == 0 && !*abort) {
+                raise_device_error(p.err, W4A16_ERR_TIMEOUT);
+                *abort = 1;
+            }
+            failed = true;
+        }
+    }
+    // leave only when every load issued has landed (the block's shared memory
+    // must not be released under an outstanding copy)
+    volatile int never = 0;
+    for (int q = ri > kSlots ? ri - kSlots : 0; q < ri; ++q)
+        ptx::mbar_wait(&bars->full[c][q % kSlots], (uint32_t)((q / kSlots) & 1), &never, kWaitLimitNs);
+}
+
+template <int G, int NT, bool XS, bool TS>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const GemvArgs p) {
+    gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
+                const GemvArgs p) {
+    constexpr int SLOT = kSlotBytes<G, TS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    Bars* bars = reinterpret_cast<Bars*>(ring + kRingBytes);
+    Bars* bars = reinterpret_cast<Bars*>(ring + kConsumers * kSlots * SLOT);
     uint8_t* xs = reinterpret_cast<uint8_t*>(bars) + ((sizeof(Bars) + 127) & ~(size_t)127);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
-    const int64_t xsteps = p.KU * kUnitSteps;             // staged steps per token (whole units)
-    const int64_t xstride = xsteps * (kStepK * 2) + 64;  // bytes per token row of staged x
+    const int xsteps = (int)p.KU * kUnitSteps;     // staged steps per token (whole units)
+    const int xstride = xsteps * (kStepK * 2) + 64;  // bytes per token row of staged x
     volatile int* abort = &bars->abort;
 
     if (threadIdx.x == 0) {
         for (int w = 0; w < kConsumers; ++w)
-            for (int sl = 0; sl < kSlots; ++sl) ptx::mbar_init(&bars->full[w][sl], 1);
+            for (int sl = 0; sl < kSlots; ++sl) {
+                ptx::mbar_init(&bars->full[w][sl], 1);
+                ptx::mbar_init(&bars->empty[w][sl], 1);
+            }
         bars->abort = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&tmap_w);
+        if (TS) ptx::prefetch_tensormap(&tmap_s);
     }
     if (threadIdx.x < 64) reinterpret_cast<uint4*>(bars->zero)[threadIdx.x] = make_uint4(0, 0, 0, 0);
     __syncthreads();
 
-    // unit range of every consumer warp of this block
-    auto range = [&](int cw, int64_t& ub, int64_t& ue) {
-        const int64_t w = (int64_t)blockIdx.x * kConsumers + cw;
-        ub = w < p.P ? w * p.U / p.P : 0;
-        ue = w < p.P ? (w + 1) * p.U / p.P : 0;
-    };
-    auto issue = [&](int cw, int64_t rb, int64_t ku, int sl) {  // one unit: four 16-row x 64-byte boxes
-        uint64_t* bar = &bars->full[cw][sl];
-        uint8_t* dst = ring + (cw * kSlots + sl) * kSlotBytes;
-        ptx::mbar_arrive_expect_tx(bar, kSlotBytes);
-#pragma unroll
-        for (int step = 0; step < kUnitSteps; ++step)
-            ptx::tma_load_2d(dst + step * (kRows * 64), &tmap_w, bar, (int)((ku * kUnitSteps + step) * 64),
-                             (int)(rb * kRows));
-    };
+    if (warp == kProducer) {
+        produce<G, TS>(&tmap_w, &tmap_s, p, bars, ring, abort, lane);
+        return;
+    }
 
+    // ------------------------------------------------------------ compute warps
     const int cw = warp;
-    int64_t u_begin, u_end;
-    range(cw, u_begin, u_end);
-    // refill cursor: the next unit to load into this warp's ring
-    int64_t f_rb = u_begin / p.KU, f_ku = u_begin % p.KU;
-    auto advance = [&](int64_t& rb_, int64_t& ku_) {
-        if (++ku_ == p.KU) {
-            ku_ = 0;
-            ++rb_;
-        }
-    };
-    // Every input, the weights included, may come from the kernel before this
-    // one on the stream, which may still be running: until griddepcontrol.wait
-    // returns, the first units of this warp are only prefetched into L2.
-    if (lane == 0) {
-        int64_t rb_ = f_rb, ku_ = f_ku;
-        for (int r = 0; r < kSlots && u_begin + r < u_end; ++r) {
-#pragma unroll
-            for (int step = 0; step < kUnitSteps; ++step)
-                ptx::tma_prefetch_l2_2d(&tmap_w, (int)((ku_ * kUnitSteps + step) * 64), (int)(rb_ * kRows));
-            advance(rb_, ku_);
-        }
-    }
+    const int w = blockIdx.x * kConsumers + cw;
+    const int u_begin = w < p.P ? unit_begin(w, p) : 0;
+    const int n_units = w < p.P ? unit_begin(w + 1, p) - u_begin : 0;
+    int rb = u_begin / (int)p.KU, ku = u_begin % (int)p.KU;
     ptx::grid_dependency_wait();
-    // x loads first (every unit waits for them), then the ring, then the x stores
-    const int64_t chunks = XS ? (int64_t)p.M * xsteps * 16 : 0;  // 16-byte chunks, zero past K
-    uint4 xv[XS ? kXLoads : 1];
+    // the first unit's scales (global path) and x go out at once
+    ScaleRows sr = scale_rows(p, rb, gid);
+    UnitScales<G> sc;
+    if (!TS && n_units > 0) load_scales<G>(sc, p, sr, ku);
     if (XS) {
+        // chunk c = threadIdx.x + i * kConsumerThreads is token m, chunk cc of its
+        // row (16 bytes, zero past K); (m, cc) advance without division
+        const int per_tok = xsteps * 16;
+        uint4 xv[kXLoads];
+        int m = 0, cc = threadIdx.x;
+        while (cc >= per_tok) cc -= per_tok, ++m;
 #pragma unroll
         for (int i = 0; i < kXLoads; ++i) {
-            const int64_t c = threadIdx.x + i * kThreads;
             xv[i] = make_uint4(0, 0, 0, 0);
-            if (c < chunks) {
-                const int64_t m = c / (xsteps * 16), k0 = (c % (xsteps * 16)) * 8;
-                if (k0 < p.K) xv[i] = ld_l2_v4(p.x + m * p.K + k0);
-            }
+            if (m < p.M && cc * 8 < p.K) xv[i] = ld_l2_v4(p.x + (int64_t)m * p.K + cc * 8);
+            cc += kConsumerThreads;
+            while (cc >= per_tok) cc -= per_tok, ++m;
         }
-    }
-    for (int r = 0; r < kSlots && u_begin + r < u_end; ++r) {
-        if (lane == 0) issue(cw, f_rb, f_ku, r);
-        advance(f_rb, f_ku);
-    }
-    if (XS) {
+        m = 0;
+        cc = threadIdx.x;
+        while (cc >= per_tok) cc -= per_tok, ++m;
 #pragma unroll
         for (int i = 0; i < kXLoads; ++i) {
-            const int64_t c = threadIdx.x + i * kThreads;
-            if (c < chunks) {
-                const int64_t m = c / (xsteps * 16), cc = c % (xsteps * 16);
-                *reinterpret_cast<uint4*>(xs + m * xstride + (cc >> 4) * (kStepK * 2) +
-                                          xs_pos((int)(cc & 15), G) * 16) = permute_x8(xv[i]);
-            }
+            if (m < p.M)
+                *reinterpret_cast<uint4*>(xs + m * xstride + (cc >> 4) * (kStepK * 2) + xs_pos(cc & 15, G) * 16) =
+                    permute_x8(xv[i]);
+            cc += kConsumerThreads;
+            while (cc >= per_tok) cc -= per_tok, ++m;
         }
-        __syncthreads();
+        ptx::named_bar_sync(1, kConsumerThreads);  // compute warps only; the producer runs on
     }
+    if (n_units == 0) return;
 
-    // ------------------------------------------------------------ consumers
-    const int64_t w = (int64_t)blockIdx.x * kConsumers + cw;
-    if (w >= p.P) return;
-
-    const int n_units = (int)(u_end - u_begin);
-    int rb = (int)(u_begin / p.KU), ku = (int)(u_begin % p.KU);
     const int first_rb = rb, KU = (int)p.KU;
     int seg_ku0 = ku;
     float acc[NT][4];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
-    ScaleRows sr = scale_rows(p, rb, gid);
-    UnitScales<G> sc;
-    load_scales<G>(sc, p, sr, ku);
     // shared address of this lane's x chunk in unit 0 (the zero block for lanes
     // without a token) and its stride per unit
     uint32_t xlane0[NT], xunit[NT];
@@ -467,19 +542,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         xlane0[t] = (has ? ptx::smem_u32(xs) + (8 * t + gid) * (uint32_t)xstride : ptx::smem_u32(bars->zero)) + t4 * 16;
         xunit[t] = has ? kUnitSteps * kStepK * 2 : 0;
     }
-    const uint32_t wlane0 = ptx::smem_u32(ring) + cw * (kSlots * kSlotBytes) + gid * 64 + t4 * (G / 8);
+    const uint32_t slot0 = ptx::smem_u32(ring) + cw * (kSlots * SLOT);
+    const uint32_t wlane = gid * 64 + t4 * (G / 8);
 
     int sl = 0;
     uint32_t phase = 0;
     for (int r = 0; r < n_units; ++r) {
         if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bars->full[cw][sl], phase, abort, kWaitLimitNs))) {
-            raise_device_error(p.err, W4A16_ERR_TIMEOUT);
-            *abort = 1;
-            if (lane == 0) {  // this warp's own loads still in flight land before it exits
-                volatile int never = 0;
-                for (int q = r + 1; q < r + kSlots && q < n_units; ++q)
-                    ptx::mbar_wait(&bars->full[cw][q % kSlots], (uint32_t)((q / kSlots) & 1), &never, kWaitLimitNs);
-            }
+            if (!*abort) raise_device_error(p.err, W4A16_ERR_TIMEOUT);
+            *abort = 1;  // the producer stops and waits for the loads it issued
             return;
         }
         int nrb = rb, nku = ku + 1;
@@ -487,20 +558,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             nku = 0;
             ++nrb;
         }
-        const ScaleRows nsr = nku == 0 ? scale_rows(p, nrb, gid) : sr;
+        const uint32_t slot = slot0 + sl * SLOT;
         UnitScales<G> sc_next;
-        if (r + 1 < n_units) load_scales<G>(sc_next, p, nsr, nku);
+        ScaleRows nsr = sr;
+        if (TS) {
+            load_scales_smem<G>(sc, slot + kWBytes, ku, gid);
+        } else {
+            if (nku == 0) nsr = scale_rows(p, nrb, gid);
+            if (r + 1 < n_units) load_scales<G>(sc_next, p, nsr, nku);
+        }
         uint32_t xlane[NT];
 #pragma unroll
         for (int t = 0; t < NT; ++t) xlane[t] = xlane0[t] + ku * xunit[t];
-        compute_unit<G, NT, XS>(wlane0 + sl * kSlotBytes, sc, p, xlane, ku, gid, t4, acc);
+        compute_unit<G, NT, XS>(slot + wlane, sc, p, xlane, ku, gid, t4, acc);
         __syncwarp();  // every lane has read the slot
-        if (r + kSlots < n_units) {
-            if (lane == 0) issue(cw, f_rb, f_ku, sl);
-            advance(f_rb, f_ku);
+        if (lane == 0) ptx::mbar_arrive(&bars->empty[cw][sl]);
+        if (!TS) {
+            if (r + 1 < n_units) sc = sc_next;
+            sr = nsr;
         }
-        if (r + 1 < n_units) sc = sc_next;
-        sr = nsr;
 
         const bool seg_end = (ku == KU - 1) || (r == n_units - 1);
         if (seg_end) {
@@ -540,19 +616,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-size_t smem_bytes(bool xs, int64_t M, int64_t steps) {
-    size_t b = 1024 + kRingBytes + ((sizeof(Bars) + 127) & ~(size_t)127);
+size_t smem_bytes(size_t slot_bytes, bool xs, int64_t M, int64_t steps) {
+    size_t b = 1024 + (size_t)kConsumers * kSlots * slot_bytes + ((sizeof(Bars) + 127) & ~(size_t)127);
     if (xs) b += (size_t)M * (size_t)(steps * kStepK * 2 + 64);
     return b;
 }
 
-template <int G, int NT, bool XS>
-w4a16_status launch_one(const DeviceInfo& dev, const CUtensorMap& map, const GemvArgs& a, unsigned blocks,
+template <int G, int NT, bool XS, bool TS>
+w4a16_status launch_one(const DeviceInfo& dev, const CUtensorMap (&map)[2], const GemvArgs& a, unsigned blocks,
                         size_t smem, cudaStream_t st) {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [&dev] {  // the device's opt-in maximum; each launch checks its own size
-        attr = cudaFuncSetAttribute(gemv_kernel<G, NT, XS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr = cudaFuncSetAttribute(gemv_kernel<G, NT, XS, TS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)dev.smem_optin);
     });
     if (attr != cudaSuccess) return cuda_status(attr, "gemv: cudaFuncSetAttribute");
@@ -566,7 +642,25 @@ w4a16_status launch_one(const DeviceInfo& dev, const CUtensorMap& map, const Gem
     attrs[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = 1;
-    return cuda_status(cudaLaunchKernelEx(&cfg, gemv_kernel<G, NT, XS>, map, a), "gemv: kernel launch");
+    return cuda_status(cudaLaunchKernelEx(&cfg, gemv_kernel<G, NT, XS, TS>, map[0], map[1], a),
+                       "gemv: kernel launch");
+}
+
+template <int G, int NT>
+w4a16_status launch_group(const DeviceInfo& dev, const CUtensorMap (&map)[2], const GemvArgs& a, unsigned blocks,
+                          bool xs, bool ts, size_t smem, cudaStream_t st) {
+    if (xs) return ts ? launch_one<G, NT, true, true>(dev, map, a, blocks, smem, st)
+                      : launch_one<G, NT, true, false>(dev, map, a, blocks, smem, st);
+    return ts ? launch_one<G, NT, false, true>(dev, map, a, blocks, smem, st)
+              : launch_one<G, NT, false, false>(dev, map, a, blocks, smem, st);
+}
+
+bool encode(CUtensorMap* map, CUtensorMapDataType type, const void* base, cuuint32_t rank, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box) {
+    const cuuint32_t es[3] = {1, 1, 1};
+    return encode_fn()(map, type, rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -592,18 +686,34 @@ w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return W4A16_ERR_WORKSPACE;
     if (((uintptr_t)workspace & 255) != 0) return W4A16_ERR_MISALIGNED;
     if (M > kMaxM || N > 0x7fffffffLL || K / 2 > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (!enc) return cuda_status(cudaErrorNotSupported, "gemv: cuTensorMapEncodeTiled entry point");
-    CUtensorMap map;
+    if (!encode_fn()) return cuda_status(cudaErrorNotSupported, "gemv: cuTensorMapEncodeTiled entry point");
+    const int64_t gpr = K / group;
+    const bool ts = (gpr * 2) % 16 == 0;  // scale rows can be TMA boxes
+    // [0] the ring's weight boxes: one 3-D box per unit ([step][row][64 B] in
+    //     shared memory) when every 64-byte step piece lies inside its row,
+    //     else four 2-D boxes of 16 rows x 64 B; [1] the scales' 16-row boxes
+    CUtensorMap map[2];
+    memset(map, 0, sizeof(map));
+    bool w3d = false;
+    if ((K / 2) % 64 == 0) {
+        const cuuint64_t dims[3] = {64, (cuuint64_t)N, (cuuint64_t)(K / 128)};
+        const cuuint64_t strides[2] = {(cuuint64_t)(K / 2), 64};
+        const cuuint32_t box[3] = {64, (cuuint32_t)kRows, (cuuint32_t)kUnitSteps};
+        w3d = encode(&map[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, 3, dims, strides, box);
+    }
     {
-        cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
-        cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-        cuuint32_t box[2] = {64, (cuuint32_t)kRows};
-        cuuint32_t es[2] = {1, 1};
-        if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(qw), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cuda_status(cudaErrorInvalidValue, "gemv: cuTensorMapEncodeTiled");
+        const cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+        const cuuint32_t box[2] = {64, (cuuint32_t)kRows};
+        if (!w3d && !encode(&map[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, 2, dims, strides, box))
+            return cuda_status(cudaErrorInvalidValue, "gemv: cuTensorMapEncodeTiled (weights)");
+    }
+    if (ts) {
+        const cuuint64_t dims[2] = {(cuuint64_t)gpr, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)(gpr * 2)};
+        const cuuint32_t box[2] = {(cuuint32_t)(group == 32 ? 16 : 8), (cuuint32_t)kRows};
+        if (!encode(&map[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, s, 2, dims, strides, box))
+            return cuda_status(cudaErrorInvalidValue, "gemv: cuTensorMapEncodeTiled (scales)");
     }
     GemvArgs a;
     a.x = x;
@@ -616,35 +726,31 @@ w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     a.KU = (K + kUnitK - 1) / kUnitK;
     const int64_t RB = (N + kRows - 1) / kRows;
     a.U = RB * a.KU;
+    if (a.U > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
     int64_t blocks = (a.U + kConsumers - 1) / kConsumers;
     if (blocks > dev.sms) blocks = dev.sms;
     a.P = blocks * kConsumers < a.U ? blocks * kConsumers : a.U;
     a.partial = reinterpret_cast<float*>(workspace);
     a.counter = reinterpret_cast<int*>(reinterpret_cast<char*>(workspace) + partial_region_bytes(dev));
     a.err = dev.error_word;
-    a.gpr = (int)(K / group);
-    a.svec = (K / group) % 8 == 0;
+    a.gpr = (int)gpr;
+    a.svec = gpr % 8 == 0;
+    a.w3d = w3d;
+    const size_t slot = (size_t)kWBytes + (ts ? (size_t)kRows * (group == 32 ? 32 : 16) : 0);
     const int64_t xsteps = a.KU * kUnitSteps;
     const size_t xbytes = (size_t)M * (size_t)(xsteps * kStepK * 2 + 64);
-    const bool xs = xbytes <= kXSmemMax && smem_bytes(true, M, xsteps) <= dev.smem_optin;
-    const size_t smem = smem_bytes(xs, M, xsteps);
+    const bool xs = xbytes <= kXSmemMax && smem_bytes(slot, true, M, xsteps) <= dev.smem_optin;
+    const size_t smem = smem_bytes(slot, xs, M, xsteps);
     if (smem > dev.smem_optin) return W4A16_ERR_UNSUPPORTED;
-    const int nt = M <= 8 ? 1 : 2;
-    w4a16_status r = W4A16_OK;
-#define W4A16_GEMV(G_, NT_)                                                           \
-    r = xs ? launch_one<G_, NT_, true>(dev, map, a, (unsigned)blocks, smem, st)       \
-           : launch_one<G_, NT_, false>(dev, map, a, (unsigned)blocks, smem, st)
-    if (nt == 1) {
-        if (group == 128) W4A16_GEMV(128, 1);
-        else if (group == 64) W4A16_GEMV(64, 1);
-        else W4A16_GEMV(32, 1);
-    } else {
-        if (group == 128) W4A16_GEMV(128, 2);
-        else if (group == 64) W4A16_GEMV(64, 2);
-        else W4A16_GEMV(32, 2);
+    const unsigned nb = (unsigned)blocks;
+    if (M <= 8) {
+        if (group == 128) return launch_group<128, 1>(dev, map, a, nb, xs, ts, smem, st);
+        if (group == 64) return launch_group<64, 1>(dev, map, a, nb, xs, ts, smem, st);
+        return launch_group<32, 1>(dev, map, a, nb, xs, ts, smem, st);
     }
-#undef W4A16_GEMV
-    return r;
+    if (group == 128) return launch_group<128, 2>(dev, map, a, nb, xs, ts, smem, st);
+    if (group == 64) return launch_group<64, 2>(dev, map, a, nb, xs, ts, smem, st);
+    return launch_group<32, 2>(dev, map, a, nb, xs, ts, smem, st);
 }
 
 }  // namespace w4a16
