@@ -50,7 +50,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s
 constexpr int kRowsPerTile = 128;
 
-template <int G_, int BN_, int KSTAGE_, int STAGES_, int ASTAGES_, int DEQW_, int EPIW_, bool STREAMK_>
+template <int G_, int BN_, int KSTAGE_, int STAGES_, int ASTAGES_, int DEQW_, int EPIW_, bool STREAMK_, int ND_ = 2>
 struct Cfg {
     static constexpr int G = G_;              // scale group
     static constexpr int BN = BN_;            // tokens per tile (MMA N)
@@ -60,6 +60,7 @@ struct Cfg {
     static constexpr int DEQW = DEQW_;        // dequant warps (multiple of 4)
     static constexpr int EPIW = EPIW_;        // epilogue warps (multiple of 4)
     static constexpr bool STREAMK = STREAMK_;
+    static constexpr int ND = ND_;            // group-partial buffers in TMEM
 
     static constexpr int THREADS = (2 + DEQW + EPIW) * 32;
     static constexpr int PBYTES = kRowsPerTile * KSTAGE / 2;  // packed weights per stage
@@ -68,7 +69,7 @@ struct Cfg {
     static constexpr int XBYTES = XBOXES * XBOX_BYTES;
     static constexpr int STAGE_BYTES = PBYTES + XBYTES;        // both multiples of 1024
     static constexpr int ACOLS = KSTAGE / 2;                   // TMEM columns per A stage
-    static constexpr int DCOLS = 2 * BN;                       // two group-partial buffers
+    static constexpr int DCOLS = ND * BN;                      // group-partial buffers
     static constexpr int TMEM_COLS = 512;
     static constexpr int NPART = DEQW / 4;                     // dequant threads per row
     static constexpr int PART_K = KSTAGE / NPART;              // k per dequant thread per stage
@@ -84,13 +85,14 @@ struct Cfg {
     static_assert(DCOLS + ASTAGES * ACOLS <= TMEM_COLS, "TMEM budget");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
     static_assert(PART_K % 64 == 0 && BNP % 16 == 0, "per-thread shares");
-    static_assert(STAGES <= 8 && ASTAGES <= 8, "barrier arrays");
+    static_assert(STAGES <= 8 && ASTAGES <= 8 && ND <= 4, "barrier arrays");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
-// Prefill / routed experts: 128 tokens, 64-k stages, one tile per CTA.
+// Prefill / routed experts: 128 tokens, 256-k stages, one tile per CTA. Large
+// stages amortise the MMA thread's per-stage waits and commits over 16 MMAs.
 template <int G>
-using PrefillCfg = Cfg<G, 128, 64, 8, 8, 4, 8, false>;
+using PrefillCfg = Cfg<G, 128, 256, 2, 2, 4, 8, false>;
 
 struct Args {
     const uint16_t* s;
@@ -112,8 +114,8 @@ struct Smem {
     uint64_t empty[8];   // MMAs reading the stage finished
     uint64_t afull[8];   // TMEM A stage written
     uint64_t aempty[8];  // MMAs reading the TMEM A stage finished
-    uint64_t dfull[2];   // group partial ready in TMEM buffer b
-    uint64_t dempty[2];  // epilogue done reading TMEM buffer b
+    uint64_t dfull[4];   // group partial ready in TMEM buffer b
+    uint64_t dempty[4];  // epilogue done reading TMEM buffer b
     uint64_t mma_done;
     uint64_t pstored;    // stream-K: every epilogue thread stored its partial
     uint64_t pflag;      // stream-K: last_flag is set
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 ptx::mbar_init(&sm->afull[i], C::DEQW * 32);
                 ptx::mbar_init(&sm->aempty[i], 1);
             }
-            for (int b = 0; b < 2; ++b) {
+            for (int b = 0; b < C::ND; ++b) {
                 ptx::mbar_init(&sm->dfull[b], 1);
                 ptx::mbar_init(&sm->dempty[b], C::EPIW * 32);
             }
@@ -336,8 +338,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             while (ok && sched.next(a, seg)) {
                 for (int64_t kc = seg.k0; ok && kc < seg.k1; kc += C::KSTAGE, ++c) {
                     const int st = (int)(c % C::STAGES), as = (int)(c % C::ASTAGES);
-                    if (!ptx::mbar_wait(&sm->full[st], (uint32_t)((c / C::STAGES) & 1), abort, kWaitLimitNs) ||
-                        !ptx::mbar_wait(&sm->afull[as], (uint32_t)((c / C::ASTAGES) & 1), abort, kWaitLimitNs)) {
+                    // afull implies full: the dequant warps saw the stage's bytes land before arriving
+                    if (!ptx::mbar_wait(&sm->afull[as], (uint32_t)((c / C::ASTAGES) & 1), abort, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
@@ -356,9 +358,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         const bool last = C::KSTAGE >= C::G ? (kk % GPS == GPS - 1)
                                                             : (kk == C::KSTAGE / 16 - 1 && stage_closes);
                         if (first) {
-                            cur_b = (int)(grp & 1);
-                            if (grp >= 2) {
-                                if (!ptx::mbar_wait(&sm->dempty[cur_b], (uint32_t)(((grp >> 1) - 1) & 1), abort,
+                            cur_b = (int)(grp % C::ND);
+                            if (grp >= C::ND) {
+                                if (!ptx::mbar_wait(&sm->dempty[cur_b], (uint32_t)((grp / C::ND - 1) & 1), abort,
                                                     kWaitLimitNs)) {
                                     ok = false;
                                     break;
@@ -376,7 +378,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                     if (!ok) break;
                     ptx::mma_commit(&sm->empty[st]);
-                    ptx::mma_commit(&sm->aempty[as]);
+                    if (C::ASTAGES != C::STAGES) ptx::mma_commit(&sm->aempty[as]);
                 }
             }
             if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
@@ -399,7 +401,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const int64_t around = c / C::ASTAGES;
                 if (!ptx::mbar_wait(&sm->full[st], (uint32_t)((c / C::STAGES) & 1), abort, kWaitLimitNs) ||
                     (around > 0 &&
-                     !ptx::mbar_wait(&sm->aempty[as], (uint32_t)((around - 1) & 1), abort, kWaitLimitNs))) {
+                     !ptx::mbar_wait(C::ASTAGES != C::STAGES ? &sm->aempty[as] : &sm->empty[st],
+                                     (uint32_t)((around - 1) & 1), abort, kWaitLimitNs))) {
                     ok = false;
                     break;
                 }
@@ -463,9 +466,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < SB; ++i) {
                     if (gb + i >= g1 || !ok) break;
-                    const int b = (int)(grp & 1);
+                    const int b = (int)(grp % C::ND);
                     if (!__all_sync(0xffffffffu,
-                                    ptx::mbar_wait(&sm->dfull[b], (uint32_t)((grp >> 1) & 1), abort, kWaitLimitNs))) {
+                                    ptx::mbar_wait(&sm->dfull[b], (uint32_t)((grp / C::ND) & 1), abort, kWaitLimitNs))) {
                         ok = false;
                         break;
                     }
