@@ -52,11 +52,11 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kConsumers = 12;   // compute warps per block (one block per SM; 3 per scheduler)
+constexpr int kConsumers = 8;    // compute warps per block (one block per SM; 2 per scheduler)
 constexpr int kProducer = kConsumers;  // warp index of the block's TMA producer
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kConsumerThreads = kConsumers * 32;
-constexpr int kSlots = 3;        // ring slots per consumer warp
+constexpr int kSlots = 4;        // ring slots per compute warp (8 x 4 measured best of 4..16 x 2..8)
 constexpr int kStepK = 128;      // k per step (one 64-byte piece of a row)
 constexpr int kUnitSteps = 4;    // steps per unit
 constexpr int kUnitK = kStepK * kUnitSteps;
