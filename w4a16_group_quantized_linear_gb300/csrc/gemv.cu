@@ -63,10 +63,11 @@ constexpr int kUnitK = kStepK * kUnitSteps;
 constexpr int kRows = 16;        // weight rows per unit
 constexpr int kWBytes = kUnitSteps * kRows * 64;  // packed weights of a unit: 4 KB
 // Scales travel with the weights (TS) as one TMA box of 16 rows x kScaleBox<G>
-// groups: 16 or 32 bytes a row, the smallest box that holds a unit's groups
-// and starts on a 16-byte boundary (for group 128 it holds two units' groups).
+// groups: the unit's groups, or 8 (16 bytes, the smallest box that starts on
+// a 16-byte boundary) when a unit has fewer; then the box also holds the
+// groups of neighbouring units.
 template <int G>
-constexpr int kScaleBox = G == 32 ? 16 : 8;
+constexpr int kScaleBox = kUnitK / G > 8 ? kUnitK / G : 8;
 template <int G, bool TS>
 constexpr int kSlotBytes = kWBytes + (TS ? kRows * kScaleBox<G> * 2 : 0);
 constexpr int kMaxM = 16;        // activation rows handled by the GEMV
@@ -226,7 +227,7 @@ __device__ __forceinline__ void load_scales(UnitScales<G>& sc, const GemvArgs& p
 template <int G>
 __device__ __forceinline__ void load_scales_smem(UnitScales<G>& sc, uint32_t box, int ku, int gid) {
     constexpr int GPU = kUnitK / G;
-    const uint32_t r0 = box + gid * (kScaleBox<G> * 2) + (G == 128 ? (ku & 1) * 8 : 0);
+    const uint32_t r0 = box + gid * (kScaleBox<G> * 2) + ((ku * GPU) % kScaleBox<G>) * 2;
     const uint32_t r1 = r0 + 8 * (kScaleBox<G> * 2);
     if constexpr (GPU == 4) {
         const uint2 a = lds_v2(r0), b = lds_v2(r1);
@@ -398,7 +399,8 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmap_w, const CUtenso
     const int ub = (lane < kConsumers && w < p.P) ? unit_begin(w, p) : 0;
     const int n = (lane < kConsumers && w < p.P) ? unit_begin(w + 1, p) - ub : 0;
     int ri = 0;  // units issued into the ring
-    auto scale_x = [](int ku) { return G == 128 ? (ku >> 1) * 8 : ku * kScaleBox<G>; };
+    // first group of the box holding unit ku's groups (a multiple of 8: 16-byte aligned)
+    auto scale_x = [](int ku) { return (ku * (kUnitK / G)) / kScaleBox<G> * kScaleBox<G>; };
     auto issue = [&](int sl, int u) {
         const int rb = u / KU, ku = u % KU;
         uint64_t* bar = &bars->full[c][sl];
@@ -616,6 +618,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+int scale_box(int group) { return kUnitK / group > 8 ? kUnitK / group : 8; }  // = kScaleBox<group>
+
 size_t smem_bytes(size_t slot_bytes, bool xs, int64_t M, int64_t steps) {
     size_t b = 1024 + (size_t)kConsumers * kSlots * slot_bytes + ((sizeof(Bars) + 127) & ~(size_t)127);
     if (xs) b += (size_t)M * (size_t)(steps * kStepK * 2 + 64);
@@ -711,7 +715,7 @@ w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     if (ts) {
         const cuuint64_t dims[2] = {(cuuint64_t)gpr, (cuuint64_t)N};
         const cuuint64_t strides[1] = {(cuuint64_t)(gpr * 2)};
-        const cuuint32_t box[2] = {(cuuint32_t)(group == 32 ? 16 : 8), (cuuint32_t)kRows};
+        const cuuint32_t box[2] = {(cuuint32_t)scale_box(group), (cuuint32_t)kRows};
         if (!encode(&map[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, s, 2, dims, strides, box))
             return cuda_status(cudaErrorInvalidValue, "gemv: cuTensorMapEncodeTiled (scales)");
     }
@@ -736,7 +740,7 @@ w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     a.gpr = (int)gpr;
     a.svec = gpr % 8 == 0;
     a.w3d = w3d;
-    const size_t slot = (size_t)kWBytes + (ts ? (size_t)kRows * (group == 32 ? 32 : 16) : 0);
+    const size_t slot = (size_t)kWBytes + (ts ? (size_t)kRows * scale_box(group) * 2 : 0);
     const int64_t xsteps = a.KU * kUnitSteps;
     const size_t xbytes = (size_t)M * (size_t)(xsteps * kStepK * 2 + 64);
     const bool xs = xbytes <= kXSmemMax && smem_bytes(slot, true, M, xsteps) <= dev.smem_optin;
