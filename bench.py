@@ -288,6 +288,36 @@ def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):
     b = per + 4 * K * 2 + 4 * N * 2
     out["decode_m4"] = {"shape": [4, K, N], "us": ms * 1e3, "GB/s": b / (ms * 1e-3) / 1e9,
                         "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm_peak}
+    # small-batch continuum: M = 8, 16 (decode GEMV) and 32, 64 (narrow-tile GEMM)
+    for Ms in (8, 16, 32, 64):
+        xs_ = torch.from_numpy(workloads.activations(g, Ms, K)).to(dev)
+        ys_ = torch.empty((Ms, N), dtype=torch.float16, device=dev)
+        f = lambda i: w4.linear(xs_, rot[i % copies][0], rot[i % copies][1], GROUP, out=ys_)  # noqa: E731
+        for i in range(5):
+            f(i)
+        ms = statistics.median(_time_launches(torch, f, 100))
+        b = per + Ms * K * 2 + Ms * N * 2
+        fl = 2.0 * Ms * N * K
+        out[f"batch_m{Ms}"] = {"shape": [Ms, K, N], "us": ms * 1e3, "GB/s": b / (ms * 1e-3) / 1e9,
+                               "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm_peak, "TFLOP/s": fl / (ms * 1e-3) / 1e12}
+    # fused gate + up pair with the SiLU * up epilogue (one launch, both matrices streamed)
+    try:
+        W2 = torch.from_numpy(workloads.weights(workloads.rng(7), N, K)).to(dev)
+        qw2, s2 = w4.pack(W2, GROUP)
+        del W2
+        pairs = [(rot[i][0], rot[i][1], qw2.clone(), s2.clone()) for i in range(copies)]
+        x1 = torch.from_numpy(workloads.activations(g, 1, K)).to(dev)
+        y1 = torch.empty((1, N), dtype=torch.float16, device=dev)
+        f = lambda i: w4.linear_gated(x1, *pairs[i % copies], GROUP, out=y1)  # noqa: E731
+        for i in range(5):
+            f(i)
+        ms = statistics.median(_time_launches(torch, f, 100))
+        b = 2 * per + K * 2 + N * 2
+        out["decode_gated_m1"] = {"shape": [1, K, N], "us": ms * 1e3, "GB/s": b / (ms * 1e-3) / 1e9,
+                                  "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm_peak}
+        del pairs
+    except w4.W4A16Error as e:
+        out["decode_gated_m1"] = {"unavailable": str(e)}
     del rot
     # prefill GEMM M=4096
     try:

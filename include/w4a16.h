@@ -123,6 +123,31 @@ W4A16_API w4a16_status w4a16_grouped_linear(const uint16_t* x_sorted, const uint
                                   size_t workspace_bytes, void* stream);
 
 /*
+ * Gate and up projections of a gated (SwiGLU) MLP fused into one decode pass:
+ *   g = x * Wg^T,  u = x * Wu^T,  y[m, n] = silu(g[m, n]) * u[m, n],
+ *   silu(v) = v / (1 + exp(-v)),
+ * (rust-inference page, list of accuracy fixes, item 5: the SiLU-activated
+ * gate projection multiplies the up projection). Wg and Wu have the same
+ * shape [N, K] and group, in the format of w4a16_linear; g and u are formed
+ * exactly as w4a16_linear forms y (fp32 group sums, scale in fp32) and stay
+ * in fp32; silu and the product are fp32; y is rounded once to fp16.
+ * Decode only: 1 <= M <= 16, else W4A16_ERR_UNSUPPORTED. Same alignment rules
+ * as w4a16_linear. workspace: w4a16_linear_gated_workspace_bytes(M, N, K,
+ * group) bytes, zero-filled once (w4a16_workspace_init); every call returns
+ * it to that state. One launch streams both weight matrices once and never
+ * writes g or u to y's buffer.
+ */
+W4A16_API w4a16_status w4a16_linear_gated(const uint16_t* x, const uint8_t* qweight_gate,
+                                          const uint16_t* scales_gate, const uint8_t* qweight_up,
+                                          const uint16_t* scales_up, uint16_t* y, int64_t M, int64_t N,
+                                          int64_t K, int32_t group, void* workspace, size_t workspace_bytes,
+                                          void* stream);
+
+/* Bytes of workspace w4a16_linear_gated needs on the current device; 0 if the
+ * problem is not one it runs. */
+W4A16_API size_t w4a16_linear_gated_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t group);
+
+/*
  * Allocation-free variant of w4a16_linear, for callers that cannot allocate
  * device memory: code that runs inside an allocator or memory-pool callback,
  * a plugin host that hands a kernel only its input and output buffers, or a

@@ -200,3 +200,33 @@ def grouped_linear(x, qw, s, offsets, group: int):
 def tolerance(y_ref: np.ndarray, absdot: np.ndarray) -> np.ndarray:
     """Per-element bound |y - y_ref| <= 2^-9 |y_ref| + 1e-4 sum_k |x_k W^_nk|."""
     return np.ldexp(np.abs(y_ref), -9) + 1e-4 * absdot
+
+
+def silu(v):
+    """SiLU(v) = v / (1 + e^(-v)) in fp64: the activation of the gated MLP
+    (rust-inference page, list of accuracy fixes, item 5: the SiLU-activated
+    gate projection multiplies the up projection)."""
+    v = np.asarray(v, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return v / (1.0 + np.exp(-v))
+
+
+def gated_linear(x, qw_gate, s_gate, qw_up, s_up, group: int, threads: int = 1):
+    """y = silu(x Wg^T) * (x Wu^T) in fp64, the two projections as linear()
+    forms them. Returns (y, g, u, absdot_g, absdot_u)."""
+    g, ag = linear(x, qw_gate, s_gate, group, threads)
+    u, au = linear(x, qw_up, s_up, group, threads)
+    return silu(g) * u, g, u, ag, au
+
+
+def gated_tolerance(g, u, absdot_g, absdot_u):
+    """Per-element bound on |y - y_ref| for a kernel whose g and u each meet
+    the linear bound (tolerance()) and which evaluates silu(g) * u in fp32 and
+    rounds once to fp16. First-order propagation with |silu'| <= 1.1 on the
+    real line, the cross term of the two errors, and 2^-9 |y| for the fp32
+    evaluation and the final rounding."""
+    eg = tolerance(g, absdot_g)
+    eu = tolerance(u, absdot_u)
+    y = silu(g) * u
+    return 1.1 * eg * np.abs(u) + np.abs(silu(g)) * eu + 1.1 * eg * eu + np.ldexp(np.abs(y), -9)
+

@@ -25,7 +25,11 @@ def _run(w4, dev, x, qw, s, g):
 
 
 @pytest.mark.parametrize("M,N,K,g", [
-    (17, 128, 128, 128),      # smallest GEMM M, one tile
+    (17, 128, 128, 128),      # smallest GEMM M, one tile (32-token tiles up to M=32)
+    (32, 384, 2048, 128),     # 32-token tile, full
+    (33, 200, 512, 64),       # 64-token tiles from M=33, ragged N
+    (64, 300, 1024, 32),      # 64-token tile, full, group 32
+    (65, 130, 768, 128),      # first M on 128-token tiles, K % 256 != 0
     (128, 128, 64, 64),       # one chunk
     (200, 384, 512, 128),     # several tiles, ragged M
     (300, 257, 1024, 32),     # ragged N (one row past a tile), g32

@@ -301,3 +301,71 @@ def test_workloads_are_seeded_and_shaped():
     assert np.all(np.diff(r.expert_of_row) >= 0)
     pairs = set(zip(r.token_of_row.tolist(), r.expert_of_row.tolist()))
     assert len(pairs) == 256                               # distinct experts per token
+
+
+# ------------------------------------------------------------ gated MLP pins
+
+def test_silu_closed_forms():
+    # sigmoid(ln 3) = 3/4 and sigmoid(-ln 3) = 1/4, so silu(+-ln 3) = +-ln 3 * (3/4 | 1/4)
+    l3 = np.log(3.0)
+    assert oracle.silu(l3) == pytest.approx(0.75 * l3, rel=1e-15)
+    assert oracle.silu(-l3) == pytest.approx(-0.25 * l3, rel=1e-15)
+    assert oracle.silu(0.0) == 0.0
+    # silu(v) - silu(-v) = v (sigmoid(v) + sigmoid(-v) = 1), across magnitudes
+    v = np.concatenate([np.linspace(-30, 30, 601), [1e-8, -1e-8, 700.0, -700.0]])
+    assert np.allclose(oracle.silu(v) - oracle.silu(-v), v, rtol=1e-14, atol=1e-300)
+    # far tails: silu(v) -> v for large v, -> -0 for very negative v, never NaN
+    assert oracle.silu(60.0) == pytest.approx(60.0, rel=1e-15)
+    assert oracle.silu(-1000.0) == 0.0 and not np.isnan(oracle.silu(-1000.0))
+
+
+def test_gated_zero_up_or_gate_gives_zero():
+    x, qw, s = _raw(31, 3, 9, 256, 64)
+    zero = np.full_like(qw, 0x88)                # every q = 0
+    y, g, u, _, _ = oracle.gated_linear(x, qw, s, zero, s, 64)
+    assert np.all(u == 0) and np.all(y == 0)
+    y, g, u, _, _ = oracle.gated_linear(x, zero, s, qw, s, 64)
+    assert np.all(g == 0) and np.all(y == 0)     # silu(0) = 0
+
+
+def test_gated_one_hot_closed_form():
+    """One-hot x picks one weight of each matrix: y = silu(sg qg) * (su qu),
+    with silu evaluated independently through math.exp; swapping gate and up
+    (a plausible slip) changes every value checked here."""
+    import math
+
+    K, N, g = 128, 5, 32
+    _, qg, sg = _raw(32, 1, N, K, g)
+    _, qu, su = _raw(33, 1, N, K, g)
+    # scales of order 1 put g and u where silu is far from linear
+    sg = oracle.float_to_half_bits(np.float32(16.0) * oracle.half_to_double(sg).astype(np.float32))
+    su = oracle.float_to_half_bits(np.float32(16.0) * oracle.half_to_double(su).astype(np.float32))
+    Wg = oracle.half_to_double(sg)[:, :, None] * oracle.unpack(qg, K).reshape(N, K // g, g)
+    Wu = oracle.half_to_double(su)[:, :, None] * oracle.unpack(qu, K).reshape(N, K // g, g)
+    Wg, Wu = Wg.reshape(N, K), Wu.reshape(N, K)
+    for k in (0, 33, 127):
+        x = np.zeros((1, K), np.float16)
+        x[0, k] = 1
+        y, _, _, _, _ = oracle.gated_linear(x, qg, sg, qu, su, g)
+        for n in range(N):
+            a, b = Wg[n, k], Wu[n, k]
+            assert y[0, n] == pytest.approx(a / (1.0 + math.exp(-a)) * b, rel=1e-14, abs=1e-300)
+        swapped = oracle.silu(Wu[:, k]) * Wg[:, k]
+        assert np.max(np.abs(y[0] - swapped)) > 1e-3 * np.max(np.abs(y[0]))
+
+
+def test_gated_tolerance_covers_linear_errors():
+    """Perturbing g and u by their full linear bounds (worst signs) moves
+    silu(g) * u by no more than the gated bound (fp64 check of the first-order
+    propagation with the cross term)."""
+    r = np.random.default_rng(5)
+    g = r.normal(0, 3, 20000)
+    u = r.normal(0, 3, 20000)
+    ag, au = np.abs(g) * 5 + 1, np.abs(u) * 5 + 1
+    eg, eu = oracle.tolerance(g, ag), oracle.tolerance(u, au)
+    bound = oracle.gated_tolerance(g, u, ag, au)
+    y = oracle.silu(g) * u
+    for sg_ in (-1, 1):
+        for su_ in (-1, 1):
+            yp = oracle.silu(g + sg_ * eg) * (u + su_ * eu)
+            assert np.all(np.abs(yp - y) <= bound)

@@ -20,7 +20,7 @@ import threading
 
 import torch
 
-__all__ = ["pack", "unpack", "linear", "grouped_linear", "workspace_bytes", "device_status",
+__all__ = ["pack", "unpack", "linear", "linear_gated", "grouped_linear", "workspace_bytes", "device_status",
            "W4A16Error", "lib", "LIB_PATH", "EXPORTS", "STATUS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libw4a16.so")
@@ -35,6 +35,8 @@ EXPORTS = {
     "w4a16_unpack": (_I32, [_P, _I64, _I64, _P, _P]),
     "w4a16_linear": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
     "w4a16_linear_noalloc": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]),
+    "w4a16_linear_gated": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
+    "w4a16_linear_gated_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
     "w4a16_grouped_linear": (_I32, [_P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
     "w4a16_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32, _I32]),
     "w4a16_workspace_init": (_I32, [_P, _SZ, _P]),
@@ -157,6 +159,37 @@ def linear(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, group: 
     _check(lib().w4a16_linear(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(out), M, N, K, group,
                               _ptr(ws) if ws is not None else None, ws.numel() if ws is not None else 0, st),
            "w4a16_linear")
+    return out
+
+
+def linear_gated(x: torch.Tensor, qweight_gate: torch.Tensor, scales_gate: torch.Tensor,
+                 qweight_up: torch.Tensor, scales_up: torch.Tensor, group: int = 128,
+                 out: torch.Tensor | None = None) -> torch.Tensor:
+    """y = silu(x Wg^T) * (x Wu^T) in one decode pass (M <= 16); both weight
+    matrices uint8 [N, K/2] with fp16 scales [N, K/group]."""
+    _need(x, "x", torch.float16, 2)
+    for t, name in ((qweight_gate, "qweight_gate"), (qweight_up, "qweight_up")):
+        _need(t, name, torch.uint8, 2)
+    for t, name in ((scales_gate, "scales_gate"), (scales_up, "scales_up")):
+        _need(t, name, torch.float16, 2)
+    M, K = x.shape
+    N = qweight_gate.shape[0]
+    if (qweight_gate.shape[1] * 2 != K or tuple(qweight_up.shape) != tuple(qweight_gate.shape)
+            or tuple(scales_gate.shape) != (N, K // group) or tuple(scales_up.shape) != (N, K // group)):
+        raise ValueError("shape mismatch between x, the weights and the scales")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    else:
+        _need(out, "out", torch.float16, 2)
+        if tuple(out.shape) != (M, N):
+            raise ValueError("out must be [M, N]")
+    st = _stream(x.device)
+    nb = int(lib().w4a16_linear_gated_workspace_bytes(M, N, K, group))
+    ws = _workspace(x.device, st, nb)
+    _check(lib().w4a16_linear_gated(_ptr(x), _ptr(qweight_gate), _ptr(scales_gate), _ptr(qweight_up),
+                                    _ptr(scales_up), _ptr(out), M, N, K, group,
+                                    _ptr(ws) if ws is not None else None, ws.numel() if ws is not None else 0, st),
+           "w4a16_linear_gated")
     return out
 
 

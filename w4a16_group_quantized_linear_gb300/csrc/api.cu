@@ -152,6 +152,29 @@ w4a16_status w4a16_linear(const uint16_t* x, const uint8_t* qweight, const uint1
     return gemm_launch(*dev, x, qweight, scales, y, M, N, K, group, nullptr, 1, st);
 }
 
+w4a16_status w4a16_linear_gated(const uint16_t* x, const uint8_t* qweight_gate, const uint16_t* scales_gate,
+                                const uint8_t* qweight_up, const uint16_t* scales_up, uint16_t* y, int64_t M,
+                                int64_t N, int64_t K, int32_t group, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+    const DeviceInfo* dev = nullptr;
+    w4a16_status v = check_linear(x, qweight_gate, scales_gate, y, M, N, K, group, &dev);
+    if (v != W4A16_OK || M == 0 || N == 0) return v;
+    if (K > 0 && (!qweight_up || !scales_up)) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(qweight_up) || !aligned16(scales_up)) return W4A16_ERR_MISALIGNED;
+    if (M > kGemvMaxM) return W4A16_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(uint16_t), st));  // silu(0) * 0
+    return gemv_gated_launch(*dev, x, qweight_gate, scales_gate, qweight_up, scales_up, y, M, N, K, group, workspace,
+                             workspace_bytes, st);
+}
+
+size_t w4a16_linear_gated_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t group) {
+    if (M <= 0 || M > kGemvMaxM || N <= 0 || K <= 0 || check_group(K, group) != W4A16_OK) return 0;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return 0;
+    return gemv_workspace_bytes(*dev, M, N, K, true);
+}
+
 w4a16_status w4a16_grouped_linear(const uint16_t* x_sorted, const uint8_t* qweight, const uint16_t* scales,
                                   const int32_t* expert_offsets, uint16_t* y_sorted, int32_t E, int64_t R,
                                   int64_t N, int64_t K, int32_t group, void* workspace, size_t workspace_bytes,

@@ -71,7 +71,7 @@ constexpr int kScaleBox = kUnitK / G > 8 ? kUnitK / G : 8;
 template <int G, bool TS>
 constexpr int kSlotBytes = kWBytes + (TS ? kRows * kScaleBox<G> * 2 : 0);
 constexpr int kMaxM = 16;        // activation rows handled by the GEMV
-constexpr size_t kXSmemMax = 80 * 1024;  // x staged in shared memory up to this size
+constexpr size_t kXSmemMax = 84 * 1024;  // x staged in shared memory up to this size (M = 8 at K = 5120)
 constexpr int kXLoads = (int)((kXSmemMax / 16 + kConsumerThreads - 1) / kConsumerThreads);  // x loads per thread
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -91,6 +91,17 @@ struct GemvArgs {
     int gpr;         // scale groups per row: K / G
     int svec;        // scale rows start 16-byte aligned (gpr % 8 == 0): whole units load as vectors
     int w3d;         // the weight map is 3-D: one TMA box per unit
+};
+
+// Gated pair (gate and up projections of one MLP, fused; a parameter of the
+// gated kernel only, which keeps the plain kernel's parameters as small as
+// they measure fastest): row-block rb of the output is virtual row-blocks 2 rb
+// (gate) and 2 rb + 1 (up); the second of the two to finish writes
+// y = silu(gate) * up.
+struct GatedArgs {
+    const uint16_t* s2;  // scales of the up projection
+    float* gres;         // [2][M][N] fp32 gate and up results
+    int* pair;           // [ceil(N/16)] finished halves per row-block, zero between calls
 };
 
 struct Bars {
@@ -176,13 +187,15 @@ struct ScaleRows {
     bool v0, v1;
 };
 
-__device__ __forceinline__ ScaleRows scale_rows(const GemvArgs& p, int rb, int gid) {
-    const int64_t n0 = (int64_t)rb * kRows + gid, n1 = n0 + 8;
+template <bool GT>
+__device__ __forceinline__ ScaleRows scale_rows(const GemvArgs& p, const GatedArgs& ga, int vrb, int gid) {
+    const int64_t n0 = (int64_t)(GT ? vrb >> 1 : vrb) * kRows + gid, n1 = n0 + 8;
+    const uint16_t* s = (GT && (vrb & 1)) ? ga.s2 : p.s;
     ScaleRows r;
     r.v0 = n0 < p.N;
     r.v1 = n1 < p.N;
-    r.r0 = p.s + (r.v0 ? n0 : 0) * p.gpr;
-    r.r1 = p.s + (r.v1 ? n1 : 0) * p.gpr;
+    r.r0 = s + (r.v0 ? n0 : 0) * p.gpr;
+    r.r1 = s + (r.v1 ? n1 : 0) * p.gpr;
     return r;
 }
 
@@ -331,6 +344,51 @@ __device__ __forceinline__ void store_y(const GemvArgs& p, int64_t rb, const flo
         }
 }
 
+// The finished fp32 sums of virtual row-block vrb. Plain: round once to fp16
+// and store y. Gated: park them in the workspace; the second half of the pair
+// to finish computes y = silu(gate) * up in fp32 and rounds once to fp16
+// (rust-inference README, list of accuracy fixes, item 5: the SiLU-activated
+// gate multiplies the up projection).
+template <int NT, bool GT>
+__device__ __forceinline__ void finish_row_block(const GemvArgs& p, const GatedArgs& ga, int vrb,
+                                                 const float (&v)[NT][4], int gid, int t4, int lane) {
+    if constexpr (!GT) {
+        store_y<NT>(p, vrb, v, gid, t4);
+        return;
+    }
+    const int rb = vrb >> 1, mat = vrb & 1;
+    const int64_t half = (int64_t)p.M * p.N;
+    float* mine = ga.gres + mat * half;
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int m = 8 * t + 2 * t4 + (i & 1);
+            const int64_t n = (int64_t)rb * kRows + gid + 8 * (i >> 1);
+            if (m < p.M && n < p.N) __stcg(mine + (int64_t)m * p.N + n, v[t][i]);
+        }
+    __syncwarp();  // the lanes' stores happen before lane 0's release
+    int old = 0;
+    if (lane == 0) old = ptx::atom_add_acq_rel_gpu(ga.pair + rb, 1);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old == 0) return;  // the other half finishes the pair
+    const float* other = ga.gres + (mat ^ 1) * half;
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int m = 8 * t + 2 * t4 + (i & 1);
+            const int64_t n = (int64_t)rb * kRows + gid + 8 * (i >> 1);
+            if (m < p.M && n < p.N) {
+                const float o = __ldcg(other + (int64_t)m * p.N + n);
+                const float g = mat == 0 ? v[t][i] : o, u = mat == 0 ? o : v[t][i];
+                const float silu = g / (1.0f + expf(-g));
+                p.y[(int64_t)m * p.N + n] = __half_as_ushort(__float2half_rn(silu * u));
+            }
+        }
+    if (lane == 0) ga.pair[rb] = 0;
+}
+
 __device__ __forceinline__ int unit_begin(int w, const GemvArgs& p) { return (int)((int64_t)w * p.U / p.P); }
 
 __device__ __forceinline__ int64_t warp_of_unit(int64_t u, const GemvArgs& p) {
@@ -354,8 +412,8 @@ __device__ __forceinline__ void store_partial(const GemvArgs& p, int64_t w, int 
 // segment, 1: its last) and counts the arrival with one acquire-release
 // atomic; the last contributor sums every contributor's partial in warp order,
 // rounds once to fp16, stores y and resets the counter.
-template <int NT>
-__device__ __noinline__ void publish_partial(const GemvArgs& p, int64_t w, int slot, int64_t rb,
+template <int NT, bool GT>
+__device__ __noinline__ void publish_partial(const GemvArgs& p, const GatedArgs& ga, int64_t w, int slot, int64_t rb,
                                              const float (&acc)[NT][4], int gid, int t4, int lane) {
     store_partial<NT>(p, w, slot, acc, gid, t4);
     __syncwarp();  // the lanes' stores happen before lane 0's release
@@ -382,15 +440,24 @@ __device__ __noinline__ void publish_partial(const GemvArgs& p, int64_t w, int s
                 if (m < p.M) sum[t][i] += __ldcg(src + m * kRows + gid + 8 * (i >> 1));
             }
     }
-    store_y<NT>(p, rb, sum, gid, t4);
     if (lane == 0) p.counter[rb] = 0;
+    finish_row_block<NT, GT>(p, ga, (int)rb, sum, gid, t4, lane);
 }
+
+// The tensor maps of one launch (kernel parameters): weights and scales, and
+// for a gated pair the up projection's as well.
+struct MapPtrs {
+    const CUtensorMap* w;
+    const CUtensorMap* s;
+    const CUtensorMap* w2;
+    const CUtensorMap* s2;
+};
 
 // The producer warp: lane c streams compute warp c's units into that warp's
 // ring, refilling a slot as soon as the warp releases it. The lanes issue
 // their copies side by side, so no compute warp waits behind another.
-template <int G, bool TS>
-__device__ __forceinline__ void produce(const CUtensorMap* tmap_w, const CUtensorMap* tmap_s, const GemvArgs& p,
+template <int G, bool TS, bool GT>
+__device__ __forceinline__ void produce(const MapPtrs& maps, const GemvArgs& p,
                                         Bars* bars, uint8_t* ring, volatile int* abort, int lane) {
     constexpr int SLOT = kSlotBytes<G, TS>;
     const int KU = (int)p.KU;
@@ -402,18 +469,28 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmap_w, const CUtenso
     // first group of the box holding unit ku's groups (a multiple of 8: 16-byte aligned)
     auto scale_x = [](int ku) { return (ku * (kUnitK / G)) / kScaleBox<G> * kScaleBox<G>; };
     auto issue = [&](int sl, int u) {
-        const int rb = u / KU, ku = u % KU;
+        const int vrb = u / KU, ku = u % KU;
+        int rb = vrb;
+        const CUtensorMap* mw = maps.w;
+        const CUtensorMap* ms = maps.s;
+        if constexpr (GT) {
+            rb = vrb >> 1;
+            if (vrb & 1) {
+                mw = maps.w2;
+                ms = maps.s2;
+            }
+        }
         uint64_t* bar = &bars->full[c][sl];
         uint8_t* dst = ring + (c * kSlots + sl) * SLOT;
         ptx::mbar_arrive_expect_tx(bar, SLOT);
         if (p.w3d) {
-            ptx::tma_load_3d(dst, tmap_w, bar, 0, rb * kRows, ku * kUnitSteps);
+            ptx::tma_load_3d(dst, mw, bar, 0, rb * kRows, ku * kUnitSteps);
         } else {
 #pragma unroll
             for (int step = 0; step < kUnitSteps; ++step)
-                ptx::tma_load_2d(dst + step * (kRows * 64), tmap_w, bar, (ku * kUnitSteps + step) * 64, rb * kRows);
+                ptx::tma_load_2d(dst + step * (kRows * 64), mw, bar, (ku * kUnitSteps + step) * 64, rb * kRows);
         }
-        if (TS) ptx::tma_load_2d(dst + kWBytes, tmap_s, bar, scale_x(ku), rb * kRows);
+        if (TS) ptx::tma_load_2d(dst + kWBytes, ms, bar, scale_x(ku), rb * kRows);
     };
 
     // Every input, the weights included, may come from the kernel before this
@@ -457,10 +534,8 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmap_w, const CUtenso
         ptx::mbar_wait(&bars->full[c][q % kSlots], (uint32_t)((q / kSlots) & 1), &never, kWaitLimitNs);
 }
 
-template <int G, int NT, bool XS, bool TS>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
-                const GemvArgs p) {
+template <int G, int NT, bool XS, bool TS, bool GT>
+__device__ __forceinline__ void gemv_body(const MapPtrs& maps, const GemvArgs& p, const GatedArgs& ga) {
     constexpr int SLOT = kSlotBytes<G, TS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -479,14 +554,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         bars->abort = 0;
         ptx::fence_mbar_init();
-        ptx::prefetch_tensormap(&tmap_w);
-        if (TS) ptx::prefetch_tensormap(&tmap_s);
+        ptx::prefetch_tensormap(maps.w);
+        if (TS) ptx::prefetch_tensormap(maps.s);
+        if constexpr (GT) {
+            ptx::prefetch_tensormap(maps.w2);
+            if (TS) ptx::prefetch_tensormap(maps.s2);
+        }
     }
     if (threadIdx.x < 64) reinterpret_cast<uint4*>(bars->zero)[threadIdx.x] = make_uint4(0, 0, 0, 0);
     __syncthreads();
 
     if (warp == kProducer) {
-        produce<G, TS>(&tmap_w, &tmap_s, p, bars, ring, abort, lane);
+        produce<G, TS, GT>(maps, p, bars, ring, abort, lane);
         return;
     }
 
@@ -498,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int rb = u_begin / (int)p.KU, ku = u_begin % (int)p.KU;
     ptx::grid_dependency_wait();
     // the first unit's scales (global path) and x go out at once
-    ScaleRows sr = scale_rows(p, rb, gid);
+    ScaleRows sr = scale_rows<GT>(p, ga, rb, gid);
     UnitScales<G> sc;
     if (!TS && n_units > 0) load_scales<G>(sc, p, sr, ku);
     if (XS) {
@@ -566,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (TS) {
             load_scales_smem<G>(sc, slot + kWBytes, ku, gid);
         } else {
-            if (nku == 0) nsr = scale_rows(p, nrb, gid);
+            if (nku == 0) nsr = scale_rows<GT>(p, ga, nrb, gid);
             if (r + 1 < n_units) load_scales<G>(sc_next, p, nsr, nku);
         }
         uint32_t xlane[NT];
@@ -584,9 +663,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (seg_end) {
             if (r == n_units - 1) ptx::launch_dependents();  // only the epilogue of this warp remains
             if (seg_ku0 == 0 && ku == KU - 1)
-                store_y<NT>(p, rb, acc, gid, t4);  // whole row-block in this warp
+                finish_row_block<NT, GT>(p, ga, rb, acc, gid, t4, lane);  // whole row-block in this warp
             else  // partial: published now, so its latency overlaps the units that follow
-                publish_partial<NT>(p, w, rb == first_rb ? 0 : 1, rb, acc, gid, t4, lane);
+                publish_partial<NT, GT>(p, ga, w, rb == first_rb ? 0 : 1, rb, acc, gid, t4, lane);
 #pragma unroll
             for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
         }
@@ -598,6 +677,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             phase ^= 1u;
         }
     }
+}
+
+template <int G, int NT, bool XS, bool TS>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
+                const GemvArgs p) {
+    const MapPtrs maps{&tmap_w, &tmap_s, &tmap_w, &tmap_s};
+    const GatedArgs none{nullptr, nullptr, nullptr};
+    gemv_body<G, NT, XS, TS, false>(maps, p, none);
+}
+
+template <int G, int NT, bool XS, bool TS>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_gated_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
+                      const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_s2,
+                      const GemvArgs p, const GatedArgs ga) {
+    const MapPtrs maps{&tmap_w, &tmap_s, &tmap_w2, &tmap_s2};
+    gemv_body<G, NT, XS, TS, true>(maps, p, ga);
 }
 
 int64_t max_warps(const DeviceInfo& dev) { return (int64_t)dev.sms * kConsumers; }
@@ -626,14 +723,16 @@ size_t smem_bytes(size_t slot_bytes, bool xs, int64_t M, int64_t steps) {
     return b;
 }
 
-template <int G, int NT, bool XS, bool TS>
-w4a16_status launch_one(const DeviceInfo& dev, const CUtensorMap (&map)[2], const GemvArgs& a, unsigned blocks,
-                        size_t smem, cudaStream_t st) {
+template <int G, int NT, bool XS, bool TS, bool GT>
+w4a16_status launch_one(const DeviceInfo& dev, const CUtensorMap (&map)[4], const GemvArgs& a, const GatedArgs& ga,
+                        unsigned blocks, size_t smem, cudaStream_t st) {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [&dev] {  // the device's opt-in maximum; each launch checks its own size
-        attr = cudaFuncSetAttribute(gemv_kernel<G, NT, XS, TS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)dev.smem_optin);
+        attr = GT ? cudaFuncSetAttribute(gemv_gated_kernel<G, NT, XS, TS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dev.smem_optin)
+                  : cudaFuncSetAttribute(gemv_kernel<G, NT, XS, TS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)dev.smem_optin);
     });
     if (attr != cudaSuccess) return cuda_status(attr, "gemv: cudaFuncSetAttribute");
     cudaLaunchConfig_t cfg = {};
@@ -646,17 +745,26 @@ w4a16_status launch_one(const DeviceInfo& dev, const CUtensorMap (&map)[2], cons
     attrs[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = 1;
-    return cuda_status(cudaLaunchKernelEx(&cfg, gemv_kernel<G, NT, XS, TS>, map[0], map[1], a),
-                       "gemv: kernel launch");
+    const cudaError_t e = GT ? cudaLaunchKernelEx(&cfg, gemv_gated_kernel<G, NT, XS, TS>, map[0], map[1], map[2],
+                                                  map[3], a, ga)
+                             : cudaLaunchKernelEx(&cfg, gemv_kernel<G, NT, XS, TS>, map[0], map[1], a);
+    return cuda_status(e, "gemv: kernel launch");
+}
+
+template <int G, int NT, bool GT>
+w4a16_status launch_xt(const DeviceInfo& dev, const CUtensorMap (&map)[4], const GemvArgs& a, const GatedArgs& ga,
+                       unsigned blocks, bool xs, bool ts, size_t smem, cudaStream_t st) {
+    if (xs) return ts ? launch_one<G, NT, true, true, GT>(dev, map, a, ga, blocks, smem, st)
+                      : launch_one<G, NT, true, false, GT>(dev, map, a, ga, blocks, smem, st);
+    return ts ? launch_one<G, NT, false, true, GT>(dev, map, a, ga, blocks, smem, st)
+              : launch_one<G, NT, false, false, GT>(dev, map, a, ga, blocks, smem, st);
 }
 
 template <int G, int NT>
-w4a16_status launch_group(const DeviceInfo& dev, const CUtensorMap (&map)[2], const GemvArgs& a, unsigned blocks,
-                          bool xs, bool ts, size_t smem, cudaStream_t st) {
-    if (xs) return ts ? launch_one<G, NT, true, true>(dev, map, a, blocks, smem, st)
-                      : launch_one<G, NT, true, false>(dev, map, a, blocks, smem, st);
-    return ts ? launch_one<G, NT, false, true>(dev, map, a, blocks, smem, st)
-              : launch_one<G, NT, false, false>(dev, map, a, blocks, smem, st);
+w4a16_status launch_group(const DeviceInfo& dev, const CUtensorMap (&map)[4], const GemvArgs& a, const GatedArgs& ga,
+                          unsigned blocks, bool xs, bool ts, bool gated, size_t smem, cudaStream_t st) {
+    return gated ? launch_xt<G, NT, true>(dev, map, a, ga, blocks, xs, ts, smem, st)
+                 : launch_xt<G, NT, false>(dev, map, a, ga, blocks, xs, ts, smem, st);
 }
 
 bool encode(CUtensorMap* map, CUtensorMapDataType type, const void* base, cuuint32_t rank, const cuuint64_t* dims,
@@ -677,48 +785,70 @@ size_t partial_region_bytes(const DeviceInfo& dev) {
     return align256((size_t)max_warps(dev) * 2 * kRows * kMaxM * sizeof(float));
 }
 
-size_t gemv_workspace_bytes(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K) {
+// Gated layout after the counters: [pair counters, one per row-block][gate and
+// up fp32 results, [2][M][N]].
+size_t gemv_workspace_bytes(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, bool gated) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
     const int64_t RB = (N + kRows - 1) / kRows;
-    return partial_region_bytes(dev) + align256((size_t)RB * sizeof(int));
+    size_t b = partial_region_bytes(dev) + align256((size_t)RB * (gated ? 2 : 1) * sizeof(int));
+    if (gated) b += align256((size_t)RB * sizeof(int)) + align256((size_t)2 * M * N * sizeof(float));
+    return b;
 }
 
-w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s,
-                         uint16_t* y, int64_t M, int64_t N, int64_t K, int group, void* workspace,
-                         size_t workspace_bytes, cudaStream_t st) {
-    const size_t need = gemv_workspace_bytes(dev, M, N, K);
+namespace {
+
+bool encode_weights(CUtensorMap (&map)[4], int slot, const uint8_t* qw, const uint16_t* s, int64_t N, int64_t K,
+                    int group, bool ts, bool* w3d) {
+    const int64_t gpr = K / group;
+    // the ring's weight boxes: one 3-D box per unit ([step][row][64 B] in shared
+    // memory) when every 64-byte step piece lies inside its row, else four 2-D
+    // boxes of 16 rows x 64 B; then the scales' 16-row boxes
+    *w3d = false;
+    if ((K / 2) % 64 == 0) {
+        const cuuint64_t dims[3] = {64, (cuuint64_t)N, (cuuint64_t)(K / 128)};
+        const cuuint64_t strides[2] = {(cuuint64_t)(K / 2), 64};
+        const cuuint32_t box[3] = {64, (cuuint32_t)kRows, (cuuint32_t)kUnitSteps};
+        *w3d = encode(&map[slot], CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, 3, dims, strides, box);
+    }
+    if (!*w3d) {
+        const cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+        const cuuint32_t box[2] = {64, (cuuint32_t)kRows};
+        if (!encode(&map[slot], CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, 2, dims, strides, box)) return false;
+    }
+    if (ts) {
+        const cuuint64_t dims[2] = {(cuuint64_t)gpr, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)(gpr * 2)};
+        const cuuint32_t box[2] = {(cuuint32_t)scale_box(group), (cuuint32_t)kRows};
+        if (!encode(&map[slot + 1], CU_TENSOR_MAP_DATA_TYPE_UINT16, s, 2, dims, strides, box)) return false;
+    }
+    return true;
+}
+
+w4a16_status gemv_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s,
+                      const uint8_t* qw2, const uint16_t* s2, uint16_t* y, int64_t M, int64_t N, int64_t K, int group,
+                      void* workspace, size_t workspace_bytes, cudaStream_t st) {
+    const bool gated = qw2 != nullptr;
+    const size_t need = gemv_workspace_bytes(dev, M, N, K, gated);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return W4A16_ERR_WORKSPACE;
     if (((uintptr_t)workspace & 255) != 0) return W4A16_ERR_MISALIGNED;
     if (M > kMaxM || N > 0x7fffffffLL || K / 2 > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
     if (!encode_fn()) return cuda_status(cudaErrorNotSupported, "gemv: cuTensorMapEncodeTiled entry point");
     const int64_t gpr = K / group;
     const bool ts = (gpr * 2) % 16 == 0;  // scale rows can be TMA boxes
-    // [0] the ring's weight boxes: one 3-D box per unit ([step][row][64 B] in
-    //     shared memory) when every 64-byte step piece lies inside its row,
-    //     else four 2-D boxes of 16 rows x 64 B; [1] the scales' 16-row boxes
-    CUtensorMap map[2];
+    // [0, 1] weights and scales; [2, 3] the up projection's (gated), else a copy of [0, 1]
+    CUtensorMap map[4];
     memset(map, 0, sizeof(map));
-    bool w3d = false;
-    if ((K / 2) % 64 == 0) {
-        const cuuint64_t dims[3] = {64, (cuuint64_t)N, (cuuint64_t)(K / 128)};
-        const cuuint64_t strides[2] = {(cuuint64_t)(K / 2), 64};
-        const cuuint32_t box[3] = {64, (cuuint32_t)kRows, (cuuint32_t)kUnitSteps};
-        w3d = encode(&map[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, 3, dims, strides, box);
+    bool w3d = false, w3d2 = false;
+    if (!encode_weights(map, 0, qw, s, N, K, group, ts, &w3d) ||
+        (gated && !encode_weights(map, 2, qw2, s2, N, K, group, ts, &w3d2)))
+        return cuda_status(cudaErrorInvalidValue, "gemv: cuTensorMapEncodeTiled");
+    if (!gated) {
+        map[2] = map[0];
+        map[3] = map[1];
+        w3d2 = w3d;
     }
-    {
-        const cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
-        const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-        const cuuint32_t box[2] = {64, (cuuint32_t)kRows};
-        if (!w3d && !encode(&map[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, 2, dims, strides, box))
-            return cuda_status(cudaErrorInvalidValue, "gemv: cuTensorMapEncodeTiled (weights)");
-    }
-    if (ts) {
-        const cuuint64_t dims[2] = {(cuuint64_t)gpr, (cuuint64_t)N};
-        const cuuint64_t strides[1] = {(cuuint64_t)(gpr * 2)};
-        const cuuint32_t box[2] = {(cuuint32_t)scale_box(group), (cuuint32_t)kRows};
-        if (!encode(&map[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, s, 2, dims, strides, box))
-            return cuda_status(cudaErrorInvalidValue, "gemv: cuTensorMapEncodeTiled (scales)");
-    }
+    if (w3d != w3d2) return W4A16_ERR_UNSUPPORTED;  // same shape, so the same choice
     GemvArgs a;
     a.x = x;
     a.s = s;
@@ -729,17 +859,24 @@ w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     a.KS = (K + kStepK - 1) / kStepK;
     a.KU = (K + kUnitK - 1) / kUnitK;
     const int64_t RB = (N + kRows - 1) / kRows;
-    a.U = RB * a.KU;
+    a.U = RB * (gated ? 2 : 1) * a.KU;
     if (a.U > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
     int64_t blocks = (a.U + kConsumers - 1) / kConsumers;
     if (blocks > dev.sms) blocks = dev.sms;
     a.P = blocks * kConsumers < a.U ? blocks * kConsumers : a.U;
-    a.partial = reinterpret_cast<float*>(workspace);
-    a.counter = reinterpret_cast<int*>(reinterpret_cast<char*>(workspace) + partial_region_bytes(dev));
+    char* ws = reinterpret_cast<char*>(workspace);
+    a.partial = reinterpret_cast<float*>(ws);
+    a.counter = reinterpret_cast<int*>(ws + partial_region_bytes(dev));
     a.err = dev.error_word;
     a.gpr = (int)gpr;
     a.svec = gpr % 8 == 0;
     a.w3d = w3d;
+    GatedArgs ga{s2, nullptr, nullptr};
+    if (gated) {
+        char* after = ws + partial_region_bytes(dev) + align256((size_t)RB * 2 * sizeof(int));
+        ga.pair = reinterpret_cast<int*>(after);
+        ga.gres = reinterpret_cast<float*>(after + align256((size_t)RB * sizeof(int)));
+    }
     const size_t slot = (size_t)kWBytes + (ts ? (size_t)kRows * scale_box(group) * 2 : 0);
     const int64_t xsteps = a.KU * kUnitSteps;
     const size_t xbytes = (size_t)M * (size_t)(xsteps * kStepK * 2 + 64);
@@ -748,13 +885,29 @@ w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     if (smem > dev.smem_optin) return W4A16_ERR_UNSUPPORTED;
     const unsigned nb = (unsigned)blocks;
     if (M <= 8) {
-        if (group == 128) return launch_group<128, 1>(dev, map, a, nb, xs, ts, smem, st);
-        if (group == 64) return launch_group<64, 1>(dev, map, a, nb, xs, ts, smem, st);
-        return launch_group<32, 1>(dev, map, a, nb, xs, ts, smem, st);
+        if (group == 128) return launch_group<128, 1>(dev, map, a, ga, nb, xs, ts, gated, smem, st);
+        if (group == 64) return launch_group<64, 1>(dev, map, a, ga, nb, xs, ts, gated, smem, st);
+        return launch_group<32, 1>(dev, map, a, ga, nb, xs, ts, gated, smem, st);
     }
-    if (group == 128) return launch_group<128, 2>(dev, map, a, nb, xs, ts, smem, st);
-    if (group == 64) return launch_group<64, 2>(dev, map, a, nb, xs, ts, smem, st);
-    return launch_group<32, 2>(dev, map, a, nb, xs, ts, smem, st);
+    if (group == 128) return launch_group<128, 2>(dev, map, a, ga, nb, xs, ts, gated, smem, st);
+    if (group == 64) return launch_group<64, 2>(dev, map, a, ga, nb, xs, ts, gated, smem, st);
+    return launch_group<32, 2>(dev, map, a, ga, nb, xs, ts, gated, smem, st);
+}
+
+}  // namespace
+
+w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s,
+                         uint16_t* y, int64_t M, int64_t N, int64_t K, int group, void* workspace,
+                         size_t workspace_bytes, cudaStream_t st) {
+    return gemv_run(dev, x, qw, s, nullptr, nullptr, y, M, N, K, group, workspace, workspace_bytes, st);
+}
+
+w4a16_status gemv_gated_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw_gate,
+                               const uint16_t* s_gate, const uint8_t* qw_up, const uint16_t* s_up, uint16_t* y,
+                               int64_t M, int64_t N, int64_t K, int group, void* workspace, size_t workspace_bytes,
+                               cudaStream_t st) {
+    if (qw_up == nullptr || s_up == nullptr) return W4A16_ERR_INVALID_ARG;
+    return gemv_run(dev, x, qw_gate, s_gate, qw_up, s_up, y, M, N, K, group, workspace, workspace_bytes, st);
 }
 
 }  // namespace w4a16

@@ -84,12 +84,16 @@ struct DeviceInfo {
 const DeviceInfo* device_info();
 
 // GEMV (decode, M <= 16).
-size_t gemv_workspace_bytes(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K);
+size_t gemv_workspace_bytes(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, bool gated = false);
 // Offset of the arrival counters inside a GEMV workspace (they follow the partials).
 size_t partial_region_bytes(const DeviceInfo& dev);
 w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw,
                          const uint16_t* s, uint16_t* y, int64_t M, int64_t N, int64_t K,
                          int group, void* workspace, size_t workspace_bytes, cudaStream_t st);
+w4a16_status gemv_gated_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw_gate,
+                               const uint16_t* s_gate, const uint8_t* qw_up, const uint16_t* s_up, uint16_t* y,
+                               int64_t M, int64_t N, int64_t K, int group, void* workspace, size_t workspace_bytes,
+                               cudaStream_t st);
 
 // Quantizer / unpack.
 w4a16_status pack_launch(const float* w, int64_t N, int64_t K, int group, uint8_t* qw,

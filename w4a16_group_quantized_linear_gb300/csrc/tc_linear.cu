@@ -86,6 +86,12 @@ struct Cfg {
 // stages amortise the MMA thread's per-stage waits and commits over 16 MMAs.
 template <int G>
 using PrefillCfg = Cfg<G, 128, 256, 4, 2, 4, 8>;
+// Small batches (dense M <= 64): narrower token tiles waste fewer MMA columns;
+// four epilogue warps cover the tile.
+template <int G>
+using Narrow64Cfg = Cfg<G, 64, 256, 4, 2, 4, 4>;
+template <int G>
+using Narrow32Cfg = Cfg<G, 32, 256, 4, 2, 4, 4>;
 
 struct Args {
     const uint16_t* s;
@@ -558,12 +564,18 @@ w4a16_status gemm_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
                          int64_t M, int64_t N, int64_t K, int group, const int32_t* expert_offsets, int E,
                          cudaStream_t st) {
     if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
-    switch (group) {
-        case 32: return gemm_g<PrefillCfg<32>>(dev, x, qw, s, y, M, N, K, expert_offsets, E, st);
-        case 64: return gemm_g<PrefillCfg<64>>(dev, x, qw, s, y, M, N, K, expert_offsets, E, st);
-        case 128: return gemm_g<PrefillCfg<128>>(dev, x, qw, s, y, M, N, K, expert_offsets, E, st);
-        default: return W4A16_ERR_UNSUPPORTED;
+    const int bn = (expert_offsets != nullptr || M > 64) ? 128 : (M > 32 ? 64 : 32);
+#define W4A16_GEMM(CFG)                                                                              \
+    switch (group) {                                                                                 \
+        case 32: return gemm_g<CFG<32>>(dev, x, qw, s, y, M, N, K, expert_offsets, E, st);           \
+        case 64: return gemm_g<CFG<64>>(dev, x, qw, s, y, M, N, K, expert_offsets, E, st);           \
+        case 128: return gemm_g<CFG<128>>(dev, x, qw, s, y, M, N, K, expert_offsets, E, st);         \
+        default: return W4A16_ERR_UNSUPPORTED;                                                       \
     }
+    if (bn == 32) W4A16_GEMM(Narrow32Cfg)
+    if (bn == 64) W4A16_GEMM(Narrow64Cfg)
+    W4A16_GEMM(PrefillCfg)
+#undef W4A16_GEMM
 }
 
 }  // namespace w4a16
