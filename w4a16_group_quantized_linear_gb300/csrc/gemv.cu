@@ -80,8 +80,7 @@ struct GemvArgs {
     const uint16_t* s;
     uint16_t* y;
     int M;
-    int64_t N, K;
-    int64_t KS;  // 128-k steps per row: ceil(K / 128)
+    int N, K;
     int64_t KU;  // 512-k units per row: ceil(K / 512)
     int64_t U;   // units: ceil(N / 16) * KU
     int64_t P;   // consumer warps taking part (each owns >= 1 unit)
@@ -832,7 +831,7 @@ w4a16_status gemv_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t* q
     const size_t need = gemv_workspace_bytes(dev, M, N, K, gated);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return W4A16_ERR_WORKSPACE;
     if (((uintptr_t)workspace & 255) != 0) return W4A16_ERR_MISALIGNED;
-    if (M > kMaxM || N > 0x7fffffffLL || K / 2 > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
+    if (M > kMaxM || N > 0x7fffffffLL || K > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
     if (!encode_fn()) return cuda_status(cudaErrorNotSupported, "gemv: cuTensorMapEncodeTiled entry point");
     const int64_t gpr = K / group;
     const bool ts = (gpr * 2) % 16 == 0;  // scale rows can be TMA boxes
@@ -854,9 +853,8 @@ w4a16_status gemv_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t* q
     a.s = s;
     a.y = y;
     a.M = (int)M;
-    a.N = N;
-    a.K = K;
-    a.KS = (K + kStepK - 1) / kStepK;
+    a.N = (int)N;
+    a.K = (int)K;
     a.KU = (K + kUnitK - 1) / kUnitK;
     const int64_t RB = (N + kRows - 1) / kRows;
     a.U = RB * (gated ? 2 : 1) * a.KU;
