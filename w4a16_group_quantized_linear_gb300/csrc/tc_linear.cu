@@ -34,6 +34,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "internal.cuh"
 #include "sm100_ptx.cuh"
@@ -45,7 +46,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s
 constexpr int kRowsPerTile = 128;
 
-template <int G_, int BN_, int KSTAGE_, int PSTAGES_, int XSTAGES_, int DEQW_, int EPIW_>
+template <int G_, int BN_, int KSTAGE_, int PSTAGES_, int XSTAGES_, int DEQW_, int EPIW_, bool SRUNS_ = false>
 struct Cfg {
     static constexpr int G = G_;              // scale group
     static constexpr int BN = BN_;            // tokens per tile (MMA N)
@@ -54,6 +55,7 @@ struct Cfg {
     static constexpr int XSTAGES = XSTAGES_;  // x ring depth = TMEM A ring depth
     static constexpr int DEQW = DEQW_;        // dequant warps (multiple of 4)
     static constexpr int EPIW = EPIW_;        // epilogue warps (multiple of 4)
+    static constexpr bool SRUNS = SRUNS_;     // scales in 16-byte runs, 16-24 groups ahead
 
     static constexpr int THREADS = (2 + DEQW + EPIW) * 32;
     static constexpr int PBYTES = kRowsPerTile * KSTAGE / 2;  // packed weights per stage
@@ -92,6 +94,10 @@ template <int G>
 using Narrow64Cfg = Cfg<G, 64, 256, 4, 2, 4, 4>;
 template <int G>
 using Narrow32Cfg = Cfg<G, 32, 256, 4, 2, 4, 4>;
+// Routed experts: the prefill tile, with the scales fetched further ahead. At group 32 a
+// stage holds 8 groups, so scalar loads a few groups ahead leave the epilogue waiting on HBM.
+template <int G>
+using MoeCfg = Cfg<G, 128, 256, 4, 2, 4, 8, true>;
 
 struct Args {
     const uint16_t* s;
@@ -406,15 +412,41 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         float acc[C::BNP];
 #pragma unroll
         for (int j = 0; j < C::BNP; ++j) acc[j] = 0.0f;
-        // scales are streamed from HBM once: keep SB..2 SB groups of them in flight
-        constexpr int SB = C::BNP > 32 ? 4 : 8;
-        float scA[SB], scB[SB];
-        auto load_scales = [&](float (&dst)[SB], int gb) {
+        // Scales are streamed from HBM once. Dense tiles keep SB..2 SB groups of them in flight
+        // (scalar loads); with SRUNS they come in runs of 8 groups (one 16-byte load when a
+        // scale row is a multiple of 16 bytes), three runs in flight, 16 to 24 groups ahead.
+        constexpr int SB = C::SRUNS ? 8 : (C::BNP > 32 ? 4 : 8);
+        using Run = std::conditional_t<C::SRUNS, uint4, float[SB]>;
+        const bool svec = (gk % 8) == 0;
+        Run run0, run1, run2;
+        auto load_run = [&](Run& dst, int gb) {
+            if constexpr (C::SRUNS) {
+                dst = make_uint4(0u, 0u, 0u, 0u);
+                if (!n_ok || gb >= gk) return;
+                if (svec) {
+                    dst = __ldg(reinterpret_cast<const uint4*>(srow + gb));
+                } else {
+                    uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int i = 0; i < SB; ++i)
-                dst[i] = (n_ok && gb + i < gk) ? __half2float(__ushort_as_half(__ldg(srow + gb + i))) : 0.0f;
+                    for (int i = 0; i < SB; ++i)
+                        if (gb + i < gk) w[i >> 1] |= (uint32_t)__ldg(srow + gb + i) << (16 * (i & 1));
+                    dst = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < SB; ++i)
+                    dst[i] = (n_ok && gb + i < gk) ? __half2float(__ushort_as_half(__ldg(srow + gb + i))) : 0.0f;
+            }
         };
-        auto run_groups = [&](const float (&sc)[SB], int gb) {
+        auto scale_of = [&](const Run& run, int i) -> float {
+            if constexpr (C::SRUNS) {
+                const uint32_t w = i < 2 ? run.x : i < 4 ? run.y : i < 6 ? run.z : run.w;
+                return __half2float(__ushort_as_half((unsigned short)(w >> (16 * (i & 1)))));
+            } else {
+                return run[i];
+            }
+        };
+        auto run_groups = [&](const Run& run, int gb) {
 #pragma unroll
             for (int i = 0; i < SB; ++i) {
                 if (gb + i >= gk || !ok) break;
@@ -426,7 +458,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
                 ptx::tc_fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * C::BN + cp * C::BNP);
-                const float sv = sc[i];
+                const float sv = scale_of(run, i);
                 if constexpr (C::BNP == 16) {
                     uint32_t v[16];
                     ptx::tmem_ld_32x32b_x16(taddr, v);
@@ -448,13 +480,25 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 ++grp;
             }
         };
-        load_scales(scA, 0);
-        load_scales(scB, SB);
-        for (int gb = 0; ok && gb < gk; gb += 2 * SB) {
-            run_groups(scA, gb);
-            load_scales(scA, gb + 2 * SB);
-            if (ok) run_groups(scB, gb + SB);
-            load_scales(scB, gb + 3 * SB);
+        load_run(run0, 0);
+        load_run(run1, SB);
+        if constexpr (C::SRUNS) {
+            load_run(run2, 2 * SB);
+            for (int gb = 0; ok && gb < gk; gb += 3 * SB) {
+                run_groups(run0, gb);
+                load_run(run0, gb + 3 * SB);
+                if (ok) run_groups(run1, gb + SB);
+                load_run(run1, gb + 4 * SB);
+                if (ok) run_groups(run2, gb + 2 * SB);
+                load_run(run2, gb + 5 * SB);
+            }
+        } else {
+            for (int gb = 0; ok && gb < gk; gb += 2 * SB) {
+                run_groups(run0, gb);
+                load_run(run0, gb + 2 * SB);
+                if (ok) run_groups(run1, gb + SB);
+                load_run(run1, gb + 3 * SB);
+            }
         }
         if (ok && n_ok) {
             const int m0 = row0 + cp * C::BNP;  // first token of this thread's share
@@ -564,7 +608,7 @@ w4a16_status gemm_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
                          int64_t M, int64_t N, int64_t K, int group, const int32_t* expert_offsets, int E,
                          cudaStream_t st) {
     if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
-    const int bn = (expert_offsets != nullptr || M > 64) ? 128 : (M > 32 ? 64 : 32);
+    const int bn = expert_offsets != nullptr ? 0 : (M > 64 ? 128 : (M > 32 ? 64 : 32));
 #define W4A16_GEMM(CFG)                                                                              \
     switch (group) {                                                                                 \
         case 32: return gemm_g<CFG<32>>(dev, x, qw, s, y, M, N, K, expert_offsets, E, st);           \
@@ -572,6 +616,7 @@ w4a16_status gemm_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
         case 128: return gemm_g<CFG<128>>(dev, x, qw, s, y, M, N, K, expert_offsets, E, st);         \
         default: return W4A16_ERR_UNSUPPORTED;                                                       \
     }
+    if (bn == 0) W4A16_GEMM(MoeCfg)
     if (bn == 32) W4A16_GEMM(Narrow32Cfg)
     if (bn == 64) W4A16_GEMM(Narrow64Cfg)
     W4A16_GEMM(PrefillCfg)
