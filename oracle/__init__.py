@@ -10,6 +10,11 @@ activations)", group 32 for the MoE models) and its Repository layout section
 (s = fp16(max|w|/7), q = clamp(rint(w/s), -8, 7), nibble q+8, even k in the
 low nibble) is the workload specification's reading of "int4 sym".
 
+The routed-MoE functions (``moe_route``, ``moe_dispatch``, ``moe_gather``,
+``moe_combine``) are numpy fp64: the softmax top-k router the infr README's
+model table names, the expert-major permutation, and the router-weighted sum
+of the selected experts' outputs.
+
 Every function here is pinned by ``tests/test_oracle.py`` against closed
 forms, exact rational arithmetic, numpy's own binary16 conversion and the
 hand-worked fixtures in ``tests/golden/``.
@@ -230,3 +235,87 @@ def gated_tolerance(g, u, absdot_g, absdot_u):
     y = silu(g) * u
     return 1.1 * eg * np.abs(u) + np.abs(silu(g)) * eu + 1.1 * eg * eu + np.ldexp(np.abs(y), -9)
 
+
+
+# ----------------------------------------------------------------------------
+# Routed-MoE dispatch around the grouped layer. The pages name the router
+# ("softmax router, top-k experts" for Qwen3 MoE and "8-of-128 routed" for the
+# Gemma 4 MoE in the infr README's model table) and run the experts "MoE
+# resident" at group 32 (LLM170 page, benchmark table). The permutation and the
+# weighted combine are the plain reading of a routed layer: each token's output
+# is the router-weighted sum of its selected experts' outputs.
+
+
+def moe_route(logits, top_k: int, renormalize: bool = True):
+    """Softmax router: for each token the top_k experts by logit (ties go to the
+    lower expert index) and their softmax probabilities as weights, divided by
+    their sum when ``renormalize``. The selection compares the fp32 logits
+    themselves; the probabilities are fp64. Returns (ids int32 [T, top_k],
+    weights fp64 [T, top_k], max_shift fp64 [T]) where max_shift is the largest
+    |l - max l| over the row (it enters the error bound of an fp32 softmax)."""
+    lf = np.asarray(logits, dtype=np.float32)
+    T, E = lf.shape
+    if not 1 <= top_k <= E:
+        raise ValueError("need 1 <= top_k <= E")
+    l64 = lf.astype(np.float64)
+    ids = np.argsort(-l64, axis=1, kind="stable")[:, :top_k].astype(np.int32)
+    shifted = l64 - l64.max(axis=1, keepdims=True)
+    p = np.exp(shifted)
+    p /= p.sum(axis=1, keepdims=True)
+    w = np.take_along_axis(p, ids.astype(np.int64), axis=1)
+    if renormalize:
+        w = w / w.sum(axis=1, keepdims=True)
+    return ids, w, np.abs(shifted).max(axis=1)
+
+
+def moe_dispatch(ids, E: int):
+    """Expert-major order of the (token t, slot j) pairs: rows sorted by
+    (expert, t, j). Returns (expert_offsets int32 [E+1], row_of int32 [T, k]
+    (the row of pair (t, j)), token_of_row int32 [R]) with R = T k."""
+    ids = np.asarray(ids)
+    T, k = ids.shape
+    flat = ids.reshape(-1).astype(np.int64)
+    if flat.size and (flat.min() < 0 or flat.max() >= E):
+        raise ValueError("expert id out of range")
+    order = np.argsort(flat, kind="stable")          # pair index t*k + j, stable within an expert
+    offsets = np.zeros(E + 1, np.int64)
+    offsets[1:] = np.cumsum(np.bincount(flat, minlength=E))
+    row_of = np.empty(T * k, np.int64)
+    row_of[order] = np.arange(T * k)
+    return offsets.astype(np.int32), row_of.reshape(T, k).astype(np.int32), (order // k).astype(np.int32)
+
+
+def moe_gather(x, token_of_row):
+    """x_sorted[r] = x[token_of_row[r]] (a row copy)."""
+    return np.asarray(x)[np.asarray(token_of_row, dtype=np.int64)]
+
+
+def moe_combine(y_sorted, row_of, weights):
+    """y[t] = sum_j weights[t, j] * y_sorted[row_of[t, j]] in fp64, y_sorted fp16.
+    Returns (y, absdot) with absdot = sum_j |weights[t, j] * y_sorted[row_of[t, j]]|."""
+    ys = half_to_double(half_bits(y_sorted))
+    row_of = np.asarray(row_of, dtype=np.int64)
+    w = np.asarray(weights, dtype=np.float64)
+    T, k = row_of.shape
+    y = np.zeros((T, ys.shape[1]), np.float64)
+    a = np.zeros_like(y)
+    for j in range(k):
+        term = w[:, j:j + 1] * ys[row_of[:, j]]
+        y += term
+        a += np.abs(term)
+    return y, a
+
+
+def route_tolerance(w_ref, max_shift, E: int, top_k: int):
+    """Bound on |w - w_ref| for weights computed in fp32: each exp(l - max) with
+    its argument rounded (relative error <= 2^-24 |l - max|) and a few ulp of
+    exp, an E-term fp32 sum, and up to three fp32 divisions."""
+    eps = 2.0 ** -24
+    return np.abs(w_ref) * eps * (np.asarray(max_shift)[:, None] + 2 * E + 2 * top_k + 16)
+
+
+def combine_tolerance(y_ref, absdot, top_k: int):
+    """Bound on |y - y_ref| for an fp32 weighted sum of top_k fp16 rows rounded
+    once to fp16: the fp16 rounding (2^-11 relative, 2^-25 absolute below the
+    normal range, doubled) and (top_k + 1) fp32 roundings of the running sum."""
+    return np.ldexp(np.abs(y_ref), -10) + (top_k + 1) * 2.0 ** -23 * absdot + 2.0 ** -24

@@ -369,3 +369,175 @@ def test_gated_tolerance_covers_linear_errors():
         for su_ in (-1, 1):
             yp = oracle.silu(g + sg_ * eg) * (u + su_ * eu)
             assert np.all(np.abs(yp - y) <= bound)
+
+
+# ------------------------------------------------------------------ routed-MoE dispatch
+
+def test_moe_route_hand_worked():
+    """logits (0, ln 2, ln 2, ln 4): softmax = (1, 2, 2, 4)/9. Top-2 picks expert 3, then
+    the tie between experts 1 and 2 goes to 1; weights 4/9 and 2/9, renormalized 2/3 and
+    1/3. Equal logits over E = 4: top-2 is (0, 1) with 1/4 each, renormalized 1/2."""
+    l = np.array([[0.0, np.log(2.0), np.log(2.0), np.log(4.0)], [0.5, 0.5, 0.5, 0.5]], np.float32)
+    ids, w, _ = oracle.moe_route(l, 2, renormalize=False)
+    assert ids.tolist() == [[3, 1], [0, 1]]
+    # the fp32 logits are ln 2 and ln 4 rounded, so the weights hold to fp32 accuracy
+    assert np.allclose(w, [[4 / 9, 2 / 9], [0.25, 0.25]], rtol=1e-6, atol=0)
+    ids, w, _ = oracle.moe_route(l, 2)
+    assert ids.tolist() == [[3, 1], [0, 1]]
+    assert np.allclose(w, [[2 / 3, 1 / 3], [0.5, 0.5]], rtol=1e-6, atol=0)
+
+
+def test_moe_route_brute_force():
+    """Selection by repeated first-maximum scans and weights from math.exp / math.fsum,
+    on small-integer logits with many ties."""
+    import math
+
+    r = np.random.default_rng(11)
+    T, E, k = 40, 9, 3
+    l = r.integers(-3, 4, size=(T, E)).astype(np.float32)
+    for renorm in (False, True):
+        ids, w, _ = oracle.moe_route(l, k, renormalize=renorm)
+        for t in range(T):
+            row = [float(v) for v in l[t]]
+            taken, pick = set(), []
+            for _ in range(k):
+                best = None
+                for e in range(E):
+                    if e not in taken and (best is None or row[e] > row[best]):
+                        best = e
+                taken.add(best)
+                pick.append(best)
+            assert ids[t].tolist() == pick
+            den = math.fsum(math.exp(v) for v in row)
+            ref = [math.exp(row[e]) / den for e in pick]
+            if renorm:
+                sref = math.fsum(ref)
+                ref = [v / sref for v in ref]
+            assert np.allclose(w[t], ref, rtol=1e-13, atol=0)
+
+
+def test_moe_route_invariants():
+    r = np.random.default_rng(12)
+    l = r.integers(-20, 20, size=(16, 32)).astype(np.float32) / 4  # exact in fp32
+    ids, w, ms = oracle.moe_route(l, 32, renormalize=False)
+    for t in range(16):
+        assert sorted(ids[t].tolist()) == list(range(32))           # k = E: a permutation
+        assert np.all(np.diff(l[t][ids[t]]) <= 0)                   # by falling logit
+    assert np.allclose(w.sum(1), 1.0, rtol=1e-14)                    # the whole softmax
+    ids2, w2, _ = oracle.moe_route(l + np.float32(3.0), 32, renormalize=False)  # shift invariance
+    assert np.array_equal(ids, ids2) and np.allclose(w, w2, rtol=1e-13)
+    ids, w, _ = oracle.moe_route(l, 5)
+    assert np.allclose(w.sum(1), 1.0, rtol=1e-14) and np.all(w > 0)
+    assert np.allclose(ms, (l.max(1) - l.min(1)).astype(np.float64))
+
+
+def test_moe_route_tolerance_covers_fp32_softmax():
+    """A plain fp32 evaluation (max, exp of the shifted logit, E-term sum, divisions)
+    stays inside route_tolerance."""
+    r = np.random.default_rng(13)
+    T, E, k = 2000, 128, 8
+    l = (r.normal(0, 3, size=(T, E))).astype(np.float32)
+    for renorm in (False, True):
+        ids, w_ref, ms = oracle.moe_route(l, k, renormalize=renorm)
+        m = l.max(1, keepdims=True)
+        e32 = np.exp((l - m).astype(np.float32)).astype(np.float32)
+        den = np.zeros((T, 1), np.float32)
+        for e in range(E):
+            den = (den + e32[:, e:e + 1]).astype(np.float32)
+        w32 = (np.take_along_axis(e32, ids.astype(np.int64), 1) / den).astype(np.float32)
+        if renorm:
+            s = np.zeros((T, 1), np.float32)
+            for j in range(k):
+                s = (s + w32[:, j:j + 1]).astype(np.float32)
+            w32 = (w32 / s).astype(np.float32)
+        err = np.abs(w32.astype(np.float64) - w_ref)
+        assert np.all(err <= oracle.route_tolerance(w_ref, ms, E, k))
+
+
+def test_moe_dispatch_hand_worked():
+    """ids (1, 0), (0, 2), (1, 2): expert 0 holds pairs (0,1), (1,0); expert 1 holds
+    (0,0), (2,0); expert 2 holds (1,1), (2,1)."""
+    off, row_of, tok = oracle.moe_dispatch(np.array([[1, 0], [0, 2], [1, 2]]), 3)
+    assert off.tolist() == [0, 2, 4, 6]
+    assert row_of.tolist() == [[2, 0], [1, 4], [3, 5]]
+    assert tok.tolist() == [0, 1, 0, 2, 1, 2]
+
+
+def test_moe_dispatch_brute_force():
+    """Rows appended expert by expert, token by token, slot by slot (repeats of an
+    expert within a token and empty experts included)."""
+    r = np.random.default_rng(14)
+    for T, k, E in ((50, 4, 7), (1, 1, 1), (9, 3, 40), (0, 2, 3)):
+        ids = r.integers(0, E, size=(T, k))
+        off, row_of, tok = oracle.moe_dispatch(ids, E)
+        rows, offs = [], [0]
+        for e in range(E):
+            for t in range(T):
+                for j in range(k):
+                    if ids[t, j] == e:
+                        rows.append((t, j))
+            offs.append(len(rows))
+        assert off.tolist() == offs
+        assert tok.tolist() == [t for t, _ in rows]
+        for rr, (t, j) in enumerate(rows):
+            assert row_of[t, j] == rr
+    with pytest.raises(ValueError):
+        oracle.moe_dispatch(np.array([[0, 3]]), 3)
+
+
+def test_moe_combine_exact():
+    """fp16 rows and dyadic weights make every product and sum exact in fp64: compare
+    with Fraction arithmetic; one-hot weights pick single rows."""
+    from fractions import Fraction
+
+    r = np.random.default_rng(15)
+    T, k, N, R = 6, 3, 5, 18
+    ys = r.normal(0, 4, size=(R, N)).astype(np.float16)
+    row_of = r.permutation(R)[: T * k].reshape(T, k)
+    w = r.integers(-64, 64, size=(T, k)) / 64.0
+    y, a = oracle.moe_combine(ys, row_of, w)
+    for t in range(T):
+        for n in range(N):
+            ex = sum(Fraction(float(w[t, j])) * Fraction(float(ys[row_of[t, j], n])) for j in range(k))
+            ab = sum(abs(Fraction(float(w[t, j])) * Fraction(float(ys[row_of[t, j], n]))) for j in range(k))
+            assert Fraction(y[t, n]) == ex and Fraction(a[t, n]) == ab
+    onehot = np.zeros((T, k))
+    onehot[:, 1] = 1.0
+    y1, _ = oracle.moe_combine(ys, row_of, onehot)
+    assert np.array_equal(y1, ys[row_of[:, 1]].astype(np.float64))
+
+
+def test_moe_combine_tolerance_covers_fp32_sum():
+    r = np.random.default_rng(16)
+    T, k, N = 300, 8, 256
+    ys = r.normal(0, 2, size=(T * k, N)).astype(np.float16)
+    row_of = r.permutation(T * k).reshape(T, k)
+    w = r.random((T, k)).astype(np.float32)
+    y_ref, a = oracle.moe_combine(ys, row_of, w)
+    acc = np.zeros((T, N), np.float32)
+    for j in range(k):
+        acc = (acc + w[:, j:j + 1] * ys[row_of[:, j]].astype(np.float32)).astype(np.float32)
+    y16 = acc.astype(np.float16).astype(np.float64)
+    assert np.all(np.abs(y16 - y_ref) <= oracle.combine_tolerance(y_ref, a, k))
+
+
+def test_moe_chain_equals_direct_per_token():
+    """route -> dispatch -> gather -> grouped_linear -> combine equals, token by token,
+    sum_j w_j * (x_t W_{e_j}^T) computed with the dense oracle on each expert's weights."""
+    r = np.random.default_rng(17)
+    T, E, k, K, N, g = 10, 5, 2, 64, 12, 32
+    x = r.normal(0, 1, size=(T, K)).astype(np.float16)
+    qw = r.integers(0, 256, size=(E, N, K // 2), dtype=np.uint8)
+    s = (np.abs(r.normal(0, 0.02, size=(E, N, K // g))) / 7).astype(np.float16)
+    logits = r.normal(0, 1, size=(T, E)).astype(np.float32)
+    ids, w, _ = oracle.moe_route(logits, k)
+    off, row_of, tok = oracle.moe_dispatch(ids, E)
+    ys, _ = oracle.grouped_linear(oracle.moe_gather(x, tok), qw, s, off, g)
+    y16 = oracle.float_to_half_bits(ys).view(np.float16)
+    y, _ = oracle.moe_combine(y16, row_of, w)
+    for t in range(T):
+        direct = np.zeros(N)
+        for j in range(k):
+            yt, _ = oracle.linear(x[t:t + 1], qw[ids[t, j]], s[ids[t, j]], g)
+            direct += w[t, j] * oracle.half_to_double(oracle.float_to_half_bits(yt))[0]
+        assert np.allclose(y[t], direct, rtol=1e-12, atol=1e-15)
