@@ -367,6 +367,32 @@ def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):
         w4.device_status()
     except w4.W4A16Error as e:
         out["moe"] = {"unavailable": str(e)}
+    # routed-MoE dispatch around the grouped layer at the same workload: router
+    # (softmax top-8 of 128), permutation + gather of x (K = 2048), weighted combine (N = 2048)
+    try:
+        T, E, k, Kh = workloads.MOE["tokens"], workloads.MOE["E"], workloads.MOE["top_k"], workloads.MOE["hidden"]
+        gr = workloads.rng(7)
+        logits = torch.from_numpy(workloads.router_logits(gr, T, E)).to(dev)
+        xt = torch.from_numpy(workloads.activations(gr, T, Kh)).to(dev)
+        ids, wts = w4.moe_route(logits, k)
+        off, row_of, tok, xs = w4.moe_dispatch(ids, E, xt)
+        ys = torch.from_numpy(workloads.activations(gr, T * k, Kh)).to(dev)
+        P = T * k
+        cases = {
+            "moe_route": (lambda i: w4.moe_route(logits, k), T * E * 4 + P * 8),
+            "moe_dispatch": (lambda i: w4.moe_dispatch(ids, E, xt), P * 4 * 2 + P * 8 + T * Kh * 2 + P * Kh * 2),
+            "moe_combine": (lambda i: w4.moe_combine(ys, row_of, wts), P * Kh * 2 + T * Kh * 2 + P * 8),
+        }
+        for name, (f, b) in cases.items():
+            for i in range(3):
+                f(i)
+            ms = statistics.median(_time_launches(torch, f, 30))
+            out[name] = {"T": T, "E": E, "top_k": k, "K": Kh, "us": ms * 1e3, "GB/s": b / (ms * 1e-3) / 1e9,
+                         "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm_peak}
+        w4.device_status()
+        del logits, xt, ys, xs
+    except w4.W4A16Error as e:
+        out["moe_dispatch"] = {"unavailable": str(e)}
     return out
 
 

@@ -66,7 +66,9 @@ typedef enum {
     W4A16_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
     W4A16_ERR_TIMEOUT = 5,       /* device: a bounded wait gave up (kernel returned early) */
     W4A16_ERR_BAD_OFFSETS = 6,   /* device: expert_offsets not 0 = o[0] <= ... <= o[E] = R */
-    W4A16_ERR_WORKSPACE = 7      /* workspace missing or smaller than w4a16_workspace_bytes */
+    W4A16_ERR_WORKSPACE = 7,     /* workspace missing or smaller than w4a16_workspace_bytes */
+    W4A16_ERR_BAD_ROUTING = 8    /* device: a top-k expert id outside [0, E), or a combine row
+                                    outside [0, R) */
 } w4a16_status;
 
 /*
@@ -171,6 +173,58 @@ W4A16_API size_t w4a16_linear_gated_workspace_bytes(int64_t M, int64_t N, int64_
 W4A16_API w4a16_status w4a16_linear_noalloc(const uint16_t* x, const uint8_t* qweight, const uint16_t* scales,
                                             uint16_t* y, int64_t M, int64_t N, int64_t K, int32_t group,
                                             void* stream);
+
+/*
+ * Routed-MoE dispatch around w4a16_grouped_linear. The pages name the router
+ * (infr README, model table: "softmax router, top-k experts" for the Qwen3 MoE,
+ * "8-of-128 routed" for the Gemma 4 MoE) and run the routed experts at group 32
+ * (LLM170 page, benchmark table: "g32, MoE resident"). A routed layer is
+ *   route -> dispatch -> w4a16_grouped_linear (one or more) -> combine.
+ * All three calls are deterministic and never synchronize.
+ *
+ * w4a16_moe_route: softmax router. For each token t of logits fp32 [T, E]
+ * (device), the top_k experts with the largest logits, compared as fp32 values;
+ * equal logits go to the lower expert index. topk_ids int32 [T, top_k] lists
+ * them by falling logit; topk_weights fp32 [T, top_k] holds their softmax
+ * probabilities exp(l - max l) / sum_e exp(l_e - max l) (fp32, expf), divided
+ * by their sum when renormalize != 0. Requires 1 <= top_k <= min(E, 32) and
+ * E <= 1024 (else UNSUPPORTED). NaN logits are not supported.
+ */
+W4A16_API w4a16_status w4a16_moe_route(const float* logits, int64_t T, int32_t E, int32_t top_k,
+                                       int32_t renormalize, int32_t* topk_ids, float* topk_weights,
+                                       void* stream);
+
+/*
+ * w4a16_moe_dispatch: expert-major order of the T * top_k (token, slot) pairs,
+ * rows sorted by (expert, token, slot) (a stable counting sort):
+ *   expert_offsets int32 [E+1]: rows of expert e are [offsets[e], offsets[e+1]);
+ *   row_of int32 [T, top_k]:    the row of pair (t, j);
+ *   token_of_row int32 [T*top_k]: the token of row r;
+ *   x_sorted fp16 [T*top_k, K]:  x_sorted[r] = x[token_of_row[r]] (x fp16 [T, K]).
+ * These are the inputs w4a16_grouped_linear takes (x_sorted, expert_offsets).
+ * K = 0 skips the gather (x and x_sorted may then be NULL); otherwise K % 8 == 0
+ * and x, x_sorted 16-byte aligned. E <= 4096, T * top_k < 2^31.
+ * An id outside [0, E) sets W4A16_ERR_BAD_ROUTING in the device word; that pair
+ * gets row -1 and no row, so offsets[E] < T * top_k.
+ * workspace: w4a16_moe_dispatch_workspace_bytes(T, top_k, E) bytes (no
+ * initialisation needed; NULL when that is 0).
+ */
+W4A16_API size_t w4a16_moe_dispatch_workspace_bytes(int64_t T, int32_t top_k, int32_t E);
+W4A16_API w4a16_status w4a16_moe_dispatch(const int32_t* topk_ids, int64_t T, int32_t top_k, int32_t E,
+                                          const uint16_t* x, int64_t K, int32_t* expert_offsets,
+                                          int32_t* row_of, int32_t* token_of_row, uint16_t* x_sorted,
+                                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * w4a16_moe_combine: y[t, n] = sum_j topk_weights[t, j] * y_sorted[row_of[t, j], n]
+ * for y_sorted fp16 [R, N] (the grouped layer's output in dispatch order) and
+ * y fp16 [T, N]: fp32 products and sum in slot order j = 0, 1, ..., rounded
+ * once to fp16. A row of -1 adds nothing; a row outside [0, R) sets
+ * W4A16_ERR_BAD_ROUTING and adds nothing.
+ */
+W4A16_API w4a16_status w4a16_moe_combine(const uint16_t* y_sorted, int64_t R, const int32_t* row_of,
+                                         const float* topk_weights, int64_t T, int32_t top_k, int64_t N,
+                                         uint16_t* y, void* stream);
 
 /* Bytes of workspace w4a16_linear (E = 1) or w4a16_grouped_linear (E experts,
  * M = R rows) needs for this problem on the current device; 0 if none. */

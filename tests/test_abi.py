@@ -87,3 +87,30 @@ def test_grouped_and_pack_validation(lib):
     assert lib.w4a16_pack(p, 4, 100, 32, p, p, None) == 1
     assert lib.w4a16_pack(p, 4, 128, 48, p, p, None) == 2
     assert lib.w4a16_unpack(p, 4, 7, p, None) == 1
+
+
+def test_moe_validation(lib):
+    p, q = _fake(1 << 20), _fake((1 << 20) + 8)
+    # router: 1 <= top_k <= E, E <= 1024, top_k <= 32
+    assert lib.w4a16_moe_route(p, 4, 16, 17, 1, p, p, None) == 1
+    assert lib.w4a16_moe_route(p, 4, 0, 1, 1, p, p, None) == 1
+    assert lib.w4a16_moe_route(p, 4, 2048, 8, 1, p, p, None) == 2
+    assert lib.w4a16_moe_route(p, 4, 64, 33, 1, p, p, None) == 2
+    assert lib.w4a16_moe_route(None, 4, 64, 8, 1, p, p, None) == 1
+    assert lib.w4a16_moe_route(None, 0, 64, 8, 1, None, None, None) == 0
+    # dispatch: one int per (chunk of 1024 pairs, expert) of workspace
+    assert lib.w4a16_moe_dispatch_workspace_bytes(4096, 8, 128) == 32 * 128 * 4
+    assert lib.w4a16_moe_dispatch_workspace_bytes(4, 8, 5000) == 0
+    big = 1 << 20
+    assert lib.w4a16_moe_dispatch(p, 4, 2, 0, p, 64, p, p, p, p, p, big, None) == 1
+    assert lib.w4a16_moe_dispatch(p, 4, 2, 5000, p, 64, p, p, p, p, p, big, None) == 2
+    assert lib.w4a16_moe_dispatch(p, 4, 2, 8, p, 60, p, p, p, p, p, big, None) == 2
+    assert lib.w4a16_moe_dispatch(p, 4, 2, 8, q, 64, p, p, p, p, p, big, None) == 3
+    assert lib.w4a16_moe_dispatch(p, 4, 2, 8, p, 64, p, p, p, p, None, 0, None) == 7
+    assert lib.w4a16_moe_dispatch(p, 4, 2, 8, p, 64, None, p, p, p, p, big, None) == 1
+    assert lib.w4a16_moe_dispatch(p, 4, 2, 8, None, 64, p, p, p, p, p, big, None) == 1
+    # combine
+    assert lib.w4a16_moe_combine(p, 8, p, p, 4, 0, 16, p, None) == 1
+    assert lib.w4a16_moe_combine(p, 8, p, p, 0, 2, 16, p, None) == 0
+    assert lib.w4a16_moe_combine(p, 8, None, p, 4, 2, 16, p, None) == 1
+    assert lib.w4a16_moe_combine(p, -1, p, p, 4, 2, 16, p, None) == 1

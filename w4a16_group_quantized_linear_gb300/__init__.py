@@ -20,13 +20,15 @@ import threading
 
 import torch
 
-__all__ = ["pack", "unpack", "linear", "linear_gated", "grouped_linear", "workspace_bytes", "device_status",
+__all__ = ["pack", "unpack", "linear", "linear_gated", "grouped_linear", "moe_route", "moe_dispatch", "moe_combine",
+           "workspace_bytes", "device_status",
            "W4A16Error", "lib", "LIB_PATH", "EXPORTS", "STATUS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libw4a16.so")
 
 STATUS = {0: "W4A16_OK", 1: "W4A16_ERR_INVALID_ARG", 2: "W4A16_ERR_UNSUPPORTED", 3: "W4A16_ERR_MISALIGNED",
-          4: "W4A16_ERR_CUDA", 5: "W4A16_ERR_TIMEOUT", 6: "W4A16_ERR_BAD_OFFSETS", 7: "W4A16_ERR_WORKSPACE"}
+          4: "W4A16_ERR_CUDA", 5: "W4A16_ERR_TIMEOUT", 6: "W4A16_ERR_BAD_OFFSETS", 7: "W4A16_ERR_WORKSPACE",
+          8: "W4A16_ERR_BAD_ROUTING"}
 
 _P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
 # name -> (restype, argtypes); mirrors include/w4a16.h
@@ -38,6 +40,10 @@ EXPORTS = {
     "w4a16_linear_gated": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
     "w4a16_linear_gated_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
     "w4a16_grouped_linear": (_I32, [_P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
+    "w4a16_moe_route": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _P]),
+    "w4a16_moe_dispatch_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
+    "w4a16_moe_dispatch": (_I32, [_P, _I64, _I32, _I32, _P, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
+    "w4a16_moe_combine": (_I32, [_P, _I64, _P, _P, _I64, _I32, _I64, _P, _P]),
     "w4a16_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32, _I32]),
     "w4a16_workspace_init": (_I32, [_P, _SZ, _P]),
     "w4a16_device_status": (_I32, [_P]),
@@ -217,6 +223,65 @@ def grouped_linear(x_sorted: torch.Tensor, qweight: torch.Tensor, scales: torch.
                                       _ptr(out), E, R, N, K, group,
                                       _ptr(ws) if ws is not None else None, ws.numel() if ws is not None else 0,
                                       st), "w4a16_grouped_linear")
+    return out
+
+
+def moe_route(logits: torch.Tensor, top_k: int, renormalize: bool = True):
+    """Softmax top-k router: logits fp32 [T, E] -> (topk_ids int32 [T, top_k],
+    topk_weights fp32 [T, top_k])."""
+    _need(logits, "logits", torch.float32, 2)
+    T, E = logits.shape
+    ids = torch.empty((T, top_k), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, top_k), dtype=torch.float32, device=logits.device)
+    _check(lib().w4a16_moe_route(_ptr(logits), T, E, top_k, 1 if renormalize else 0, _ptr(ids), _ptr(w),
+                                 _stream(logits.device)), "w4a16_moe_route")
+    return ids, w
+
+
+def moe_dispatch(topk_ids: torch.Tensor, E: int, x: torch.Tensor | None = None):
+    """Expert-major order of the (token, slot) pairs: returns (expert_offsets int32
+    [E+1], row_of int32 [T, top_k], token_of_row int32 [T*top_k], x_sorted fp16
+    [T*top_k, K] or None when x is None)."""
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    row_of = torch.empty((T, k), dtype=torch.int32, device=dev)
+    token_of_row = torch.empty(T * k, dtype=torch.int32, device=dev)
+    x_sorted, K = None, 0
+    if x is not None:
+        _need(x, "x", torch.float16, 2)
+        if x.shape[0] != T:
+            raise ValueError("x must have one row per token")
+        K = x.shape[1]
+        x_sorted = torch.empty((T * k, K), dtype=torch.float16, device=dev)
+    nb = int(lib().w4a16_moe_dispatch_workspace_bytes(T, k, E))
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
+    _check(lib().w4a16_moe_dispatch(_ptr(topk_ids), T, k, E, _ptr(x) if x is not None else None, K,
+                                    _ptr(offsets), _ptr(row_of), _ptr(token_of_row),
+                                    _ptr(x_sorted) if x_sorted is not None else None,
+                                    _ptr(ws) if ws is not None else None, nb, _stream(dev)), "w4a16_moe_dispatch")
+    return offsets, row_of, token_of_row, x_sorted
+
+
+def moe_combine(y_sorted: torch.Tensor, row_of: torch.Tensor, topk_weights: torch.Tensor,
+                out: torch.Tensor | None = None) -> torch.Tensor:
+    """y[t] = sum_j topk_weights[t, j] * y_sorted[row_of[t, j]] (fp32 sum, fp16 result)."""
+    _need(y_sorted, "y_sorted", torch.float16, 2)
+    _need(row_of, "row_of", torch.int32, 2)
+    _need(topk_weights, "topk_weights", torch.float32, 2)
+    if tuple(topk_weights.shape) != tuple(row_of.shape):
+        raise ValueError("row_of and topk_weights must both be [T, top_k]")
+    T, k = row_of.shape
+    R, N = y_sorted.shape
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.float16, device=y_sorted.device)
+    else:
+        _need(out, "out", torch.float16, 2)
+        if tuple(out.shape) != (T, N):
+            raise ValueError("out must be [T, N]")
+    _check(lib().w4a16_moe_combine(_ptr(y_sorted), R, _ptr(row_of), _ptr(topk_weights), T, k, N, _ptr(out),
+                                   _stream(y_sorted.device)), "w4a16_moe_combine")
     return out
 
 

@@ -98,6 +98,7 @@ const char* w4a16_status_string(w4a16_status status) {
         case W4A16_ERR_TIMEOUT: return "W4A16_ERR_TIMEOUT: a device wait gave up";
         case W4A16_ERR_BAD_OFFSETS: return "W4A16_ERR_BAD_OFFSETS: expert offsets are not a partition of the rows";
         case W4A16_ERR_WORKSPACE: return "W4A16_ERR_WORKSPACE: workspace missing or too small";
+        case W4A16_ERR_BAD_ROUTING: return "W4A16_ERR_BAD_ROUTING: an expert id or a combine row is out of range";
     }
     return "W4A16: unknown status";
 }
@@ -188,6 +189,64 @@ w4a16_status w4a16_grouped_linear(const uint16_t* x_sorted, const uint8_t* qweig
     cudaStream_t st = (cudaStream_t)stream;
     if (K == 0) return cuda_status(cudaMemsetAsync(y_sorted, 0, (size_t)(R * N) * sizeof(uint16_t), st));
     return gemm_launch(*dev, x_sorted, qweight, scales, y_sorted, R, N, K, group, expert_offsets, E, st);
+}
+
+namespace {
+// The current device, if it is the sm_103 part the kernels are built for.
+w4a16_status current_device(const DeviceInfo** dev) {
+    *dev = device_info();
+    if (!*dev) return W4A16_ERR_CUDA;
+    if ((*dev)->cc_major != 10 || (*dev)->cc_minor != 3) return W4A16_ERR_UNSUPPORTED;
+    return W4A16_OK;
+}
+}  // namespace
+
+w4a16_status w4a16_moe_route(const float* logits, int64_t T, int32_t E, int32_t top_k, int32_t renormalize,
+                             int32_t* topk_ids, float* topk_weights, void* stream) {
+    if (T < 0 || E < 1 || top_k < 1 || top_k > E) return W4A16_ERR_INVALID_ARG;
+    if (E > 1024 || top_k > 32) return W4A16_ERR_UNSUPPORTED;
+    if (T == 0) return W4A16_OK;
+    if (!logits || !topk_ids || !topk_weights) return W4A16_ERR_INVALID_ARG;
+    const DeviceInfo* dev = nullptr;
+    const w4a16_status d = current_device(&dev);
+    if (d != W4A16_OK) return d;
+    return moe_route_launch(logits, T, E, top_k, renormalize != 0, topk_ids, topk_weights, (cudaStream_t)stream);
+}
+
+size_t w4a16_moe_dispatch_workspace_bytes(int64_t T, int32_t top_k, int32_t E) {
+    if (T < 0 || top_k < 1 || E < 1 || E > moe_max_experts() || T > 0x7fffffffLL / top_k) return 0;
+    return moe_dispatch_workspace_bytes(T * top_k, E);
+}
+
+w4a16_status w4a16_moe_dispatch(const int32_t* topk_ids, int64_t T, int32_t top_k, int32_t E, const uint16_t* x,
+                                int64_t K, int32_t* expert_offsets, int32_t* row_of, int32_t* token_of_row,
+                                uint16_t* x_sorted, void* workspace, size_t workspace_bytes, void* stream) {
+    if (T < 0 || top_k < 1 || E < 1 || K < 0 || !expert_offsets) return W4A16_ERR_INVALID_ARG;
+    if (E > moe_max_experts() || T > 0x7fffffffLL / top_k) return W4A16_ERR_UNSUPPORTED;
+    if (T > 0 && (!topk_ids || !row_of || !token_of_row)) return W4A16_ERR_INVALID_ARG;
+    if (T > 0 && K > 0) {
+        if (!x || !x_sorted) return W4A16_ERR_INVALID_ARG;
+        if (K % 8 != 0) return W4A16_ERR_UNSUPPORTED;
+        if (!aligned16(x) || !aligned16(x_sorted)) return W4A16_ERR_MISALIGNED;
+    }
+    const size_t need = moe_dispatch_workspace_bytes(T * top_k, E);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return W4A16_ERR_WORKSPACE;
+    const DeviceInfo* dev = nullptr;
+    const w4a16_status d = current_device(&dev);
+    if (d != W4A16_OK) return d;
+    return moe_dispatch_launch(*dev, topk_ids, T, top_k, E, x, T > 0 ? K : 0, expert_offsets, row_of, token_of_row,
+                               x_sorted, workspace, (cudaStream_t)stream);
+}
+
+w4a16_status w4a16_moe_combine(const uint16_t* y_sorted, int64_t R, const int32_t* row_of, const float* topk_weights,
+                               int64_t T, int32_t top_k, int64_t N, uint16_t* y, void* stream) {
+    if (R < 0 || T < 0 || top_k < 1 || N < 0) return W4A16_ERR_INVALID_ARG;
+    if (T == 0 || N == 0) return W4A16_OK;
+    if (!row_of || !topk_weights || !y || (R > 0 && !y_sorted)) return W4A16_ERR_INVALID_ARG;
+    const DeviceInfo* dev = nullptr;
+    const w4a16_status d = current_device(&dev);
+    if (d != W4A16_OK) return d;
+    return moe_combine_launch(*dev, y_sorted, R, row_of, topk_weights, T, top_k, N, y, (cudaStream_t)stream);
 }
 
 w4a16_status w4a16_device_status(void* stream) {

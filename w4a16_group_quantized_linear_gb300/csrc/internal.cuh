@@ -105,6 +105,17 @@ w4a16_status gemm_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
                          const uint16_t* s, uint16_t* y, int64_t M, int64_t N, int64_t K,
                          int group, const int32_t* expert_offsets, int E, cudaStream_t st);
 
+// Routed-MoE router, dispatch (permutation + gather) and combine.
+w4a16_status moe_route_launch(const float* logits, int64_t T, int E, int top_k, bool renormalize, int32_t* ids,
+                              float* weights, cudaStream_t st);
+size_t moe_dispatch_workspace_bytes(int64_t P, int E);
+int moe_max_experts();
+w4a16_status moe_dispatch_launch(const DeviceInfo& dev, const int32_t* ids, int64_t T, int k, int E,
+                                 const uint16_t* x, int64_t K, int32_t* offsets, int32_t* row_of,
+                                 int32_t* token_of_row, uint16_t* x_sorted, void* workspace, cudaStream_t st);
+w4a16_status moe_combine_launch(const DeviceInfo& dev, const uint16_t* y_sorted, int64_t R, const int32_t* row_of,
+                                const float* weights, int64_t T, int k, int64_t N, uint16_t* y, cudaStream_t st);
+
 // Records a failed CUDA runtime call for w4a16_last_cuda_error (per host thread).
 void note_cuda_error(cudaError_t e, const char* where);
 

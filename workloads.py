@@ -78,6 +78,11 @@ def routing(g: np.random.Generator, tokens: int, E: int, top_k: int) -> Routing:
     return Routing(offsets.astype(np.int32), tok[order], exp[order])
 
 
+def router_logits(g: np.random.Generator, tokens: int, E: int, std: float = 1.0) -> np.ndarray:
+    """Router logits fp32 [tokens, E] ~ N(0, std); the pages give no distribution."""
+    return g.normal(0.0, std, size=(tokens, E)).astype(np.float32)
+
+
 def config0(seed: int = 0):
     """M=1, K=1024, N=256, group 128: W ~ N(0, 0.02) fp32, x ~ N(0, 1) fp16."""
     g = rng(seed)
