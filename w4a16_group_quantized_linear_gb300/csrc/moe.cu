@@ -11,12 +11,21 @@
 #include <climits>
 
 #include "internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace w4a16 {
 namespace {
 
 constexpr int kChunk = 1024;  // pairs per counting-sort chunk
 constexpr int kMaxE = 4096;   // experts (one int per expert in shared memory)
+
+// Every kernel here may start while the kernel before it on the stream is still
+// running (programmatic dependent launch): it reads nothing before the wait,
+// which returns once that kernel has completed and its writes are visible.
+__device__ __forceinline__ void after_previous_kernel() {
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
+}
 
 // ------------------------------------------------------------------ router --
 
@@ -28,6 +37,7 @@ template <int NPL>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int64_t T, int E, int top_k,
                                                     int renormalize, int32_t* __restrict__ ids,
                                                     float* __restrict__ weights) {
+    after_previous_kernel();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -101,6 +111,7 @@ __global__ void __launch_bounds__(256) count_kernel(const int32_t* __restrict__ 
                                                     int32_t* __restrict__ hist, int32_t* __restrict__ row_of,
                                                     unsigned int* err) {
     extern __shared__ int32_t cnt[];
+    after_previous_kernel();
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
     const int64_t p0 = (int64_t)blockIdx.x * kChunk;
@@ -122,21 +133,34 @@ __global__ void __launch_bounds__(256) count_kernel(const int32_t* __restrict__ 
 
 // Pass 2 (one block of 1024 threads): expert_offsets from the column sums of
 // hist, then hist[c][e] becomes the first row of chunk c's pairs of expert e.
+// Threads own experts (coalesced over e) and read 8 chunks per batch, so the
+// loads of a column overlap instead of waiting one by one.
 __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, int C, int E,
                                                     int32_t* __restrict__ offsets) {
+    __shared__ int32_t first[kMaxE];  // column sums, then the first row of each expert
     __shared__ int32_t warp_sum[32];
-    constexpr int kPer = kMaxE / 1024;  // experts per thread
+    after_previous_kernel();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int32_t sum = 0;
+        int c = 0;
+        for (; c + 8 <= C; c += 8) {
+            int32_t v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = hist[(int64_t)(c + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) sum += v[u];
+        }
+        for (; c < C; ++c) sum += hist[(int64_t)c * E + e];
+        first[e] = sum;
+    }
+    __syncthreads();
+    // exclusive scan over e: thread i owns experts [kPer i, kPer i + kPer)
+    constexpr int kPer = kMaxE / 1024;
     const int e0 = threadIdx.x * kPer;
-    int32_t tot[kPer];
     int32_t mine = 0;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-        tot[i] = 0;
-        if (e0 + i < E)
-            for (int c = 0; c < C; ++c) tot[i] += hist[(int64_t)c * E + e0 + i];
-        mine += tot[i];
-    }
-    // exclusive scan of the per-thread sums over the block
+    for (int i = 0; i < kPer; ++i)
+        if (e0 + i < E) mine += first[e0 + i];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int32_t incl = mine;
 #pragma unroll
@@ -147,7 +171,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, 
     if (lane == 31) warp_sum[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int32_t w = warp_sum[lane], wi = w;
+        const int32_t w = warp_sum[lane];
+        int32_t wi = w;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
             const int32_t o = __shfl_up_sync(0xffffffffu, wi, d);
@@ -162,15 +187,30 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, 
     for (int i = 0; i < kPer; ++i) {
         const int e = e0 + i;
         if (e >= E) break;
-        int32_t run = base;
-        for (int c = 0; c < C; ++c) {
-            int32_t* h = hist + (int64_t)c * E + e;
-            const int32_t n = *h;
-            *h = run;
+        const int32_t n = first[e];
+        first[e] = base;
+        base += n;
+        offsets[e + 1] = base;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int32_t run = first[e];
+        int c = 0;
+        for (; c + 8 <= C; c += 8) {
+            int32_t v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = hist[(int64_t)(c + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                hist[(int64_t)(c + u) * E + e] = run;
+                run += v[u];
+            }
+        }
+        for (; c < C; ++c) {
+            const int32_t n = hist[(int64_t)c * E + e];
+            hist[(int64_t)c * E + e] = run;
             run += n;
         }
-        base += tot[i];
-        offsets[e + 1] = base;
     }
 }
 
@@ -181,19 +221,24 @@ __global__ void __launch_bounds__(32) scatter_kernel(const int32_t* __restrict__
                                                      const int32_t* __restrict__ hist, int32_t* __restrict__ row_of,
                                                      int32_t* __restrict__ token_of_row) {
     extern __shared__ int32_t next[];
+    after_previous_kernel();
     const int lane = threadIdx.x;
+    const int64_t p0 = (int64_t)blockIdx.x * kChunk;
+    int key[kChunk / 32];  // the chunk's expert ids, all loads in flight at once
+#pragma unroll
+    for (int i = 0; i < kChunk / 32; ++i) {
+        const int64_t p = p0 + i * 32 + lane;
+        key[i] = p < P ? __ldg(ids + p) : -2;  // -2: no pair
+    }
     const int32_t* h = hist + (int64_t)blockIdx.x * E;
     for (int e = lane; e < E; e += 32) next[e] = h[e];
     __syncwarp();
-    const int64_t p0 = (int64_t)blockIdx.x * kChunk;
     const uint32_t lt = (1u << lane) - 1u;
-    for (int i = 0; i < kChunk; i += 32) {
-        const int64_t p = p0 + i + lane;
-        int e = -2;  // no pair
-        if (p < P) {
-            e = __ldg(ids + p);
-            if (e < 0 || e >= E) e = -1;  // reported and marked by pass 1
-        }
+#pragma unroll
+    for (int i = 0; i < kChunk / 32; ++i) {
+        const int64_t p = p0 + i * 32 + lane;
+        int e = key[i];
+        if (e != -2 && (e < 0 || e >= E)) e = -1;  // reported and marked by pass 1
         const uint32_t peers = __match_any_sync(0xffffffffu, e);
         int32_t pos = 0;
         if (e >= 0) pos = next[e] + __popc(peers & lt);
@@ -213,6 +258,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
                                                      const int32_t* __restrict__ token_of_row,
                                                      const int32_t* __restrict__ offsets, int E,
                                                      uint16_t* __restrict__ x_sorted) {
+    after_previous_kernel();
     const int64_t rows = __ldg(offsets + E);
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -221,7 +267,15 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
         const int64_t t = __ldg(token_of_row + r);
         const uint4* src = reinterpret_cast<const uint4*>(x + t * K);
         uint4* dst = reinterpret_cast<uint4*>(x_sorted + r * K);
-        for (int64_t i = lane; i < vec; i += 32) dst[i] = __ldg(src + i);
+        int64_t i = lane;
+        for (; i + 7 * 32 < vec; i += 8 * 32) {  // eight loads in flight per lane
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldg(src + i + u * 32);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) dst[i + u * 32] = v[u];
+        }
+        for (; i < vec; i += 32) dst[i] = __ldg(src + i);
     }
 }
 
@@ -235,6 +289,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       const int32_t* __restrict__ row_of,
                                                       const float* __restrict__ weights, int k, int64_t N,
                                                       uint16_t* __restrict__ y, unsigned int* err) {
+    after_previous_kernel();
     const int64_t t = blockIdx.x;
     const int64_t n0 = ((int64_t)blockIdx.y * blockDim.x + threadIdx.x) * 8;
     if (n0 >= N) return;
@@ -272,6 +327,7 @@ __global__ void __launch_bounds__(256) combine_scalar_kernel(const uint16_t* __r
                                                              const int32_t* __restrict__ row_of,
                                                              const float* __restrict__ weights, int k, int64_t N,
                                                              uint16_t* __restrict__ y, unsigned int* err) {
+    after_previous_kernel();
     const int64_t t = blockIdx.x;
     const int64_t n = (int64_t)blockIdx.y * blockDim.x + threadIdx.x;
     if (n >= N) return;
@@ -293,24 +349,35 @@ __global__ void __launch_bounds__(256) combine_scalar_kernel(const uint16_t* __r
 
 // ------------------------------------------------------------------- host --
 
+template <typename... KArgs, typename... Args>
+w4a16_status launch(const char* what, void (*kernel)(KArgs...), dim3 grid, unsigned block, size_t smem,
+                    cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...), what);
+}
+
 w4a16_status moe_route_launch(const float* logits, int64_t T, int E, int top_k, bool renormalize, int32_t* ids,
                               float* weights, cudaStream_t st) {
     const int64_t blocks = (T + 7) / 8;
     if (blocks > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
     const int npl = (E + 31) / 32;
-#define W4A16_ROUTE(N)                                                                                       \
-    route_kernel<N><<<(unsigned)blocks, 256, 0, st>>>(logits, T, E, top_k, renormalize ? 1 : 0, ids, weights); \
-    break;
-    switch (npl <= 1 ? 1 : npl <= 2 ? 2 : npl <= 4 ? 4 : npl <= 8 ? 8 : npl <= 16 ? 16 : 32) {
-        case 1: W4A16_ROUTE(1)
-        case 2: W4A16_ROUTE(2)
-        case 4: W4A16_ROUTE(4)
-        case 8: W4A16_ROUTE(8)
-        case 16: W4A16_ROUTE(16)
-        default: W4A16_ROUTE(32)
-    }
-#undef W4A16_ROUTE
-    return cuda_status(cudaGetLastError(), "moe_route: kernel launch");
+    const dim3 g((unsigned)blocks);
+    const int rn = renormalize ? 1 : 0;
+    if (npl <= 1) return launch("moe_route", route_kernel<1>, g, 256, 0, st, logits, T, E, top_k, rn, ids, weights);
+    if (npl <= 2) return launch("moe_route", route_kernel<2>, g, 256, 0, st, logits, T, E, top_k, rn, ids, weights);
+    if (npl <= 4) return launch("moe_route", route_kernel<4>, g, 256, 0, st, logits, T, E, top_k, rn, ids, weights);
+    if (npl <= 8) return launch("moe_route", route_kernel<8>, g, 256, 0, st, logits, T, E, top_k, rn, ids, weights);
+    if (npl <= 16) return launch("moe_route", route_kernel<16>, g, 256, 0, st, logits, T, E, top_k, rn, ids, weights);
+    return launch("moe_route", route_kernel<32>, g, 256, 0, st, logits, T, E, top_k, rn, ids, weights);
 }
 
 size_t moe_dispatch_workspace_bytes(int64_t P, int E) {
@@ -328,23 +395,23 @@ w4a16_status moe_dispatch_launch(const DeviceInfo& dev, const int32_t* ids, int6
     if (C > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
     int32_t* hist = static_cast<int32_t*>(workspace);
     const size_t smem = (size_t)E * sizeof(int32_t);
+    w4a16_status s = W4A16_OK;
     if (C > 0) {
-        count_kernel<<<(unsigned)C, 256, smem, st>>>(ids, P, E, hist, row_of, dev.error_word);
-        w4a16_status s = cuda_status(cudaGetLastError(), "moe_dispatch: count launch");
+        s = launch("moe_dispatch: count", count_kernel, dim3((unsigned)C), 256, smem, st, ids, P, E, hist, row_of,
+                   dev.error_word);
         if (s != W4A16_OK) return s;
     }
-    scan_kernel<<<1, 1024, 0, st>>>(hist, (int)C, E, offsets);
-    w4a16_status s = cuda_status(cudaGetLastError(), "moe_dispatch: scan launch");
+    s = launch("moe_dispatch: scan", scan_kernel, dim3(1), 1024, 0, st, hist, (int)C, E, offsets);
     if (s != W4A16_OK || C == 0) return s;
-    scatter_kernel<<<(unsigned)C, 32, smem, st>>>(ids, P, k, E, hist, row_of, token_of_row);
-    s = cuda_status(cudaGetLastError(), "moe_dispatch: scatter launch");
+    s = launch("moe_dispatch: scatter", scatter_kernel, dim3((unsigned)C), 32, smem, st, ids, P, k, E,
+               (const int32_t*)hist, row_of, token_of_row);
     if (s != W4A16_OK || K == 0) return s;
     const int64_t rows_per_block = 8;
     int64_t blocks = (P + rows_per_block - 1) / rows_per_block;
     const int64_t cap = (int64_t)dev.sms * 16;
     if (blocks > cap) blocks = cap;
-    gather_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, K, token_of_row, offsets, E, x_sorted);
-    return cuda_status(cudaGetLastError(), "moe_dispatch: gather launch");
+    return launch("moe_dispatch: gather", gather_kernel, dim3((unsigned)blocks), 256, 0, st, x, K,
+                  (const int32_t*)token_of_row, (const int32_t*)offsets, E, x_sorted);
 }
 
 w4a16_status moe_combine_launch(const DeviceInfo& dev, const uint16_t* y_sorted, int64_t R, const int32_t* row_of,
@@ -356,10 +423,10 @@ w4a16_status moe_combine_launch(const DeviceInfo& dev, const uint16_t* y_sorted,
     if (gy > 65535) return W4A16_ERR_UNSUPPORTED;
     const dim3 grid((unsigned)T, (unsigned)gy);
     if (vec)
-        combine_kernel<<<grid, 256, 0, st>>>(y_sorted, R, row_of, weights, k, N, y, dev.error_word);
-    else
-        combine_scalar_kernel<<<grid, 256, 0, st>>>(y_sorted, R, row_of, weights, k, N, y, dev.error_word);
-    return cuda_status(cudaGetLastError(), "moe_combine: kernel launch");
+        return launch("moe_combine", combine_kernel, grid, 256, 0, st, y_sorted, R, row_of, weights, k, N, y,
+                      dev.error_word);
+    return launch("moe_combine", combine_scalar_kernel, grid, 256, 0, st, y_sorted, R, row_of, weights, k, N, y,
+                  dev.error_word);
 }
 
 }  // namespace w4a16

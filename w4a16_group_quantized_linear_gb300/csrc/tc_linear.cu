@@ -105,6 +105,7 @@ struct Args {
     const int32_t* offsets;  // routed experts; nullptr: dense
     int64_t M, N, K;
     int E;
+    int n_fast;  // 1: blockIdx.x is the weight-row tile and blockIdx.y the token tile
     unsigned int* err;
 };
 
@@ -130,8 +131,7 @@ __device__ __forceinline__ void fail(const Args& a, Smem* sm, unsigned code) {
 
 // Routed experts: the CTA's token tile from the device offsets. One warp.
 template <int BN>
-__device__ void find_tile(const Args& a, Smem* sm, int lane) {
-    const int t = blockIdx.x;
+__device__ void find_tile(const Args& a, Smem* sm, int lane, int t) {
     int base = 0;
     bool ok = true;
     int found = -1, f_row0 = 0, f_end = 0;
@@ -190,15 +190,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint8_t* xring = base + C::XOFF;      // x stages
     Smem* sm = reinterpret_cast<Smem*>(xring + C::XSTAGES * C::XBYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n_tile = blockIdx.y;
+    const int64_t n_tile = a.n_fast ? blockIdx.x : blockIdx.y;
+    const int m_tile = (int)(a.n_fast ? blockIdx.y : blockIdx.x);
     const int64_t nst = (a.K + C::KSTAGE - 1) / C::KSTAGE;  // stages over K
 
     if (warp == 0) {
         if (a.offsets != nullptr) {
-            find_tile<C::BN>(a, sm, lane);
+            find_tile<C::BN>(a, sm, lane, m_tile);
         } else if (lane == 0) {
             sm->expert = 0;
-            sm->row0 = (int)(blockIdx.x * C::BN);
+            sm->row0 = m_tile * C::BN;
             sm->row_end = (int)a.M;
             sm->valid = 1;
         }
@@ -599,6 +600,13 @@ w4a16_status gemm_g(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw,
     const int64_t mt = offsets ? (M + C::BN - 1) / C::BN + E : (M + C::BN - 1) / C::BN;
     const int64_t nt = (N + kRowsPerTile - 1) / kRowsPerTile;
     if (mt > 0x7fffffffLL || nt > 65535) return W4A16_ERR_UNSUPPORTED;
+    // Routed experts: the weight-row tiles of one token tile run side by side, so
+    // they share that x tile in L2 instead of streaming x from HBM once per
+    // weight-row tile (x_sorted is larger than L2 at the routed workloads).
+    if (offsets && mt <= 65535) {
+        a.n_fast = 1;
+        return launch<C>(mx, mw, a, dim3((unsigned)nt, (unsigned)mt), st);
+    }
     return launch<C>(mx, mw, a, dim3((unsigned)mt, (unsigned)nt), st);
 }
 
