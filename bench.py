@@ -448,7 +448,8 @@ def cpu_baseline_sample(budget_s=12.0):
 
 # ----------------------------------------------------------------- profile --
 
-PROFILE_CASES = ("decode", "decode_down", "decode_m4", "prefill", "prefill_m512", "moe_gate_up", "moe_down")
+PROFILE_CASES = ("decode", "decode_down", "decode_m4", "decode_gated", "prefill", "prefill_m512", "moe_gate_up",
+                 "moe_down", "moe_dispatch")
 
 
 def run_profile(case: str, launches: int):
@@ -461,7 +462,25 @@ def run_profile(case: str, launches: int):
     torch.cuda.set_device(dev)
     w4.lib()
     g = workloads.rng(0)
-    if case.startswith("moe"):
+    if case == "moe_dispatch":
+        # router, dispatch (with the gather of x) and combine at the routed-expert workload
+        T, E, k, Kh = workloads.MOE["tokens"], workloads.MOE["E"], workloads.MOE["top_k"], workloads.MOE["hidden"]
+        logits = torch.from_numpy(workloads.router_logits(g, T, E)).to(dev)
+        xt = torch.from_numpy(workloads.activations(g, T, Kh)).to(dev)
+        ys = torch.from_numpy(workloads.activations(g, T * k, Kh)).to(dev)
+        for _ in range(launches):
+            ids, wts = w4.moe_route(logits, k)
+            off, row_of, tok, xs = w4.moe_dispatch(ids, E, xt)
+            w4.moe_combine(ys, row_of, wts)
+    elif case == "decode_gated":
+        K, N = DECODE[0]
+        mats = [w4.pack(torch.from_numpy(workloads.weights(g, N, K)).to(dev), GROUP) for _ in range(8)]
+        x = torch.from_numpy(workloads.activations(g, 1, K)).to(dev)
+        y = torch.empty((1, N), dtype=torch.float16, device=dev)
+        for i in range(launches):  # four gate/up pairs in turn: successive launches miss in L2
+            j = 2 * (i % 4)
+            w4.linear_gated(x, *mats[j], *mats[j + 1], GROUP, out=y)
+    elif case.startswith("moe"):
         Km, Nm = (2048, 512) if case == "moe_gate_up" else (512, 2048)
         W, xs, rt = workloads.moe(Km, Nm)
         E = W.shape[0]
