@@ -18,6 +18,7 @@ namespace {
 
 constexpr int kChunk = 1024;  // pairs per counting-sort chunk
 constexpr int kMaxE = 4096;   // experts (one int per expert in shared memory)
+constexpr int kBlockRankMaxE = 256;  // experts up to which a whole block ranks a chunk at once
 
 // Every kernel here may start while the kernel before it on the stream is still
 // running (programmatic dependent launch): it reads nothing before the wait,
@@ -252,6 +253,47 @@ __global__ void __launch_bounds__(32) scatter_kernel(const int32_t* __restrict__
     }
 }
 
+// Pass 3 for E <= 256: a block of 32 warps ranks a whole chunk at once. Warp w
+// takes pairs [32 w, 32 w + 32) of the chunk and ranks its lanes by expert
+// (match_any); per-warp expert counts in shared memory, scanned over the warps,
+// give each warp's first row per expert. The order is the pair order, as in
+// scatter_kernel.
+__global__ void __launch_bounds__(kChunk) scatter_block_kernel(const int32_t* __restrict__ ids, int64_t P, int k,
+                                                               int E, const int32_t* __restrict__ hist,
+                                                               int32_t* __restrict__ row_of,
+                                                               int32_t* __restrict__ token_of_row) {
+    extern __shared__ int32_t wcnt[];  // [32 warps][E]
+    after_previous_kernel();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int e = lane; e < E; e += 32) wcnt[warp * E + e] = 0;
+    const int64_t p = (int64_t)blockIdx.x * kChunk + threadIdx.x;
+    int e = -2;  // no pair
+    if (p < P) {
+        e = __ldg(ids + p);
+        if (e < 0 || e >= E) e = -1;  // reported and marked by pass 1
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const uint32_t lt = (1u << lane) - 1u;
+    __syncwarp();
+    if (e >= 0 && (peers & lt) == 0) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    const int32_t* h = hist + (int64_t)blockIdx.x * E;
+    for (int x = threadIdx.x; x < E; x += blockDim.x) {
+        int32_t run = h[x];
+        for (int w = 0; w < kChunk / 32; ++w) {
+            const int32_t n = wcnt[w * E + x];
+            wcnt[w * E + x] = run;
+            run += n;
+        }
+    }
+    __syncthreads();
+    if (e >= 0) {
+        const int32_t pos = wcnt[warp * E + e] + __popc(peers & lt);
+        row_of[p] = pos;
+        token_of_row[pos] = (int32_t)(p / k);
+    }
+}
+
 // x_sorted[r] = x[token_of_row[r]] for r < offsets[E]: one warp per row,
 // 16-byte copies.
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int64_t K,
@@ -403,8 +445,13 @@ w4a16_status moe_dispatch_launch(const DeviceInfo& dev, const int32_t* ids, int6
     }
     s = launch("moe_dispatch: scan", scan_kernel, dim3(1), 1024, 0, st, hist, (int)C, E, offsets);
     if (s != W4A16_OK || C == 0) return s;
-    s = launch("moe_dispatch: scatter", scatter_kernel, dim3((unsigned)C), 32, smem, st, ids, P, k, E,
-               (const int32_t*)hist, row_of, token_of_row);
+    if (E <= kBlockRankMaxE)
+        s = launch("moe_dispatch: scatter", scatter_block_kernel, dim3((unsigned)C), kChunk,
+                   (size_t)(kChunk / 32) * E * sizeof(int32_t), st, ids, P, k, E, (const int32_t*)hist, row_of,
+                   token_of_row);
+    else
+        s = launch("moe_dispatch: scatter", scatter_kernel, dim3((unsigned)C), 32, smem, st, ids, P, k, E,
+                   (const int32_t*)hist, row_of, token_of_row);
     if (s != W4A16_OK || K == 0) return s;
     const int64_t rows_per_block = 8;
     int64_t blocks = (P + rows_per_block - 1) / rows_per_block;
