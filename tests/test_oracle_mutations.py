@@ -62,3 +62,57 @@ def test_pins_catch_planted_mistake(name, monkeypatch):
             except AssertionError:
                 failed.append(fn.__name__)
         assert failed, f"no pin caught: {name}"
+
+
+# ---------------------------------------------------------------- routed-MoE dispatch
+# The MoE functions are numpy in oracle/__init__.py: each mutant is that module's
+# source with one planted mistake, executed into a fresh namespace whose MoE
+# functions replace the real ones while the MoE pins run.
+
+PY_SRC = open(oracle.__file__).read()
+
+PY_MUTANTS = {
+    "router ties go to the higher index": (
+        'ids = np.argsort(-l64, axis=1, kind="stable")[:, :top_k].astype(np.int32)',
+        'ids = (E - 1 - np.argsort(-l64[:, ::-1], axis=1, kind="stable"))[:, :top_k].astype(np.int32)'),
+    "router ignores renormalize": ("    if renormalize:\n        w = w / w.sum", "    if False:\n        w = w / w.sum"),
+    "softmax over the selected experts only": (
+        "    p /= p.sum(axis=1, keepdims=True)\n",
+        "    p /= np.take_along_axis(p, ids.astype(np.int64), axis=1).sum(axis=1, keepdims=True)\n"),
+    "dispatch orders by (expert, slot, token)": (
+        'order = np.argsort(flat, kind="stable")',
+        "order = np.lexsort((np.arange(T * k) // k, np.arange(T * k) % k, flat))"),
+    "dispatch offsets shifted by one expert": ("    offsets[1:] = np.cumsum(", "    offsets[:-1] = np.cumsum("),
+    "combine drops the last slot": ("    for j in range(k):\n        term", "    for j in range(k - 1):\n        term"),
+    "combine reads the pair index, not its row": (
+        "term = w[:, j:j + 1] * ys[row_of[:, j]]", "term = w[:, j:j + 1] * ys[np.arange(T) * k + j]"),
+}
+
+MOE_FUNCS = ("moe_route", "moe_dispatch", "moe_gather", "moe_combine", "route_tolerance", "combine_tolerance")
+
+
+def _moe_pins():
+    yield pins.test_moe_route_hand_worked
+    yield pins.test_moe_route_brute_force
+    yield pins.test_moe_route_invariants
+    yield pins.test_moe_dispatch_hand_worked
+    yield pins.test_moe_dispatch_brute_force
+    yield pins.test_moe_combine_exact
+    yield pins.test_moe_chain_equals_direct_per_token
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_moe_pins_catch_planted_mistake(name, monkeypatch):
+    old, new = PY_MUTANTS[name]
+    assert PY_SRC.count(old) == 1, f"mutation anchor not found once: {old!r}"
+    ns = {"__name__": "oracle_mutant", "__file__": oracle.__file__}
+    exec(compile(PY_SRC.replace(old, new), "oracle_mutant", "exec"), ns)
+    for f in MOE_FUNCS:
+        monkeypatch.setattr(oracle, f, ns[f])
+    failed = []
+    for fn in _moe_pins():
+        try:
+            fn()
+        except (AssertionError, ValueError, IndexError):
+            failed.append(fn.__name__)
+    assert failed, f"no pin caught: {name}"
