@@ -608,7 +608,8 @@ def main():
     line = {
         "metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16 in, fp32 accumulate, int4 weights", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f16", "accumulate": "f32", "weights": "int4, fp16 group scales",
+        "data": "synthetic",
         "config": config,
         "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["hbm_peak"], "unit": "GB/s",
                      "frac": r["achieved"] / r["hbm_peak"],
