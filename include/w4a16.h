@@ -188,7 +188,8 @@ W4A16_API w4a16_status w4a16_linear_noalloc(const uint16_t* x, const uint8_t* qw
  * them by falling logit; topk_weights fp32 [T, top_k] holds their softmax
  * probabilities exp(l - max l) / sum_e exp(l_e - max l) (fp32, expf), divided
  * by their sum when renormalize != 0. Requires 1 <= top_k <= min(E, 32) and
- * E <= 1024 (else UNSUPPORTED). NaN logits are not supported.
+ * E <= 1024 (else UNSUPPORTED). NaN logits are not supported, and each token
+ * needs at least one finite logit (-inf marks an expert that must get weight 0).
  */
 W4A16_API w4a16_status w4a16_moe_route(const float* logits, int64_t T, int32_t E, int32_t top_k,
                                        int32_t renormalize, int32_t* topk_ids, float* topk_weights,
