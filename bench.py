@@ -12,6 +12,11 @@ Side measurements in the same JSON line: the batched decode (M=4), the
 prefill GEMM (M=4096, K=5120, N=17408; TFLOP/s) and the routed-expert layer
 (E=128, 4096 tokens, top-8, group 32), when the library provides them.
 
+The decode weights are declared static (W4A16_STATIC_WEIGHTS: nothing
+pending on the stream writes them, as in any decode loop), so each GEMV
+streams its weights while the one before it finishes; the same step without
+the flag is reported beside it.
+
 --impl reference times the CPU oracle (fp64, single thread) on the same
 workload and metric. With --gpus N > 1 (torchrun), every rank runs an
 independent replica (the layer needs no collective), timing is the max over
@@ -20,8 +25,10 @@ ranks and the value is the sum over ranks (weak scaling).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -112,6 +119,52 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------- host records --
+
+def host_info():
+    """CPU model and logical core count of the machine the bench runs on."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"cpu_model": model or platform.processor() or platform.machine(), "nproc": os.cpu_count(),
+            "arch": platform.machine()}
+
+
+def source_info():
+    """The git commit when the tree has one, and a hash of the sources that run."""
+    rev = None
+    try:
+        r = subprocess.run(["git", "-C", ROOT, "rev-parse", "HEAD"], capture_output=True, text=True, timeout=10)
+        rev = r.stdout.strip() or None if r.returncode == 0 else None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "w4a16_group_quantized_linear_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)) + ["../../include/w4a16.h", "../../bench.py"]:
+        try:
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+        except OSError:
+            pass
+    return {"git": rev, "sources_sha256": h.hexdigest()[:16]}
+
+
+def gpu_software(torch):
+    drv = None
+    try:
+        drv = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=10).stdout.strip().splitlines()[0]
+    except (OSError, subprocess.SubprocessError, IndexError):
+        pass
+    return {"driver": drv, "cuda": torch.version.cuda, "torch": torch.__version__}
+
+
 # ------------------------------------------------------------------ GPU arm --
 
 def _peaks():
@@ -186,10 +239,10 @@ def run_gpu(args, rank, world):
     h = torch.empty((M, DECODE[0][1]), dtype=torch.float16, device=dev)
     out = torch.empty((M, DECODE[1][1]), dtype=torch.float16, device=dev)
 
-    def step(i):
+    def step(i, static=True):
         (qa, sa), (qb, sb) = rot[i % copies]
-        w4.linear(x, qa, sa, GROUP, out=h)
-        w4.linear(h, qb, sb, GROUP, out=out)
+        w4.linear(x, qa, sa, GROUP, out=h, static_weights=static)
+        w4.linear(h, qb, sb, GROUP, out=out, static_weights=static)
 
     for i in range(args.warmup):
         step(i)
@@ -217,6 +270,31 @@ def run_gpu(args, rank, world):
     per_launch_bytes = step_bytes / 2  # both GEMVs move the same algorithmic bytes
     achieved = per_launch_bytes / (kernel_ms * 1e-3) / 1e9
     value = job_throughput(step_bytes * args.steps, world, ms_total) / 1e9
+
+    # ---- spread per call: 10 back-to-back regions of 20 steps each (CUDA events at the
+    # two ends of every region); median and p95 of the per-GEMV mean, both modes
+    def per_call(static):
+        samples = []
+        for rep_ in range(10):
+            torch.cuda.synchronize()
+            torch.cuda._sleep(int(2e6))
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            for i in range(20):
+                step(rep_ * 20 + i, static)
+            b.record()
+            torch.cuda.synchronize()
+            samples.append(a.elapsed_time(b) * 1e3 / 40)
+        samples.sort()
+        return {"median_us": statistics.median(samples), "p95_us": samples[int(0.95 * (len(samples) - 1) + 0.5)],
+                "samples": len(samples), "how": "10 regions x 20 back-to-back steps (40 GEMVs), mean per GEMV each"}
+
+    spread = per_call(True)
+    default_mode = per_call(False)
+    default_mode["GB/s"] = per_launch_bytes / (default_mode["median_us"] * 1e-6) / 1e9
+    default_mode["frac_hbm"] = default_mode["GB/s"] / hbm_peak
+    w4.device_status()
 
     # ---- end to end through the public API: pinned host x in, host result out.
     # A decode loop replays its step as a CUDA graph: the step (x copied in, the
@@ -273,6 +351,7 @@ def run_gpu(args, rank, world):
 
     cs = clocks.summary()
     return dict(
+        spread=spread, default_mode=default_mode, software=gpu_software(torch),
         value=value, ms_per_step=ms_total / args.steps, kernel_ms=kernel_ms, achieved=achieved,
         hbm_peak=hbm_peak, tc_peak=tc_peak, peak_kind=peak_kind, copies=copies,
         e2e=dict(value=step_bytes * args.steps * world / (e2e_ms * 1e-3) / 1e9, unit="GB/s",
@@ -310,7 +389,7 @@ def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):
     rot = [(qw.clone(), s.clone()) for _ in range(copies)]
     x4 = torch.from_numpy(workloads.activations(g, 4, K)).to(dev)
     y4 = torch.empty((4, N), dtype=torch.float16, device=dev)
-    f = lambda i: w4.linear(x4, rot[i % copies][0], rot[i % copies][1], GROUP, out=y4)  # noqa: E731
+    f = lambda i: w4.linear(x4, rot[i % copies][0], rot[i % copies][1], GROUP, out=y4, static_weights=True)  # noqa: E731
     for i in range(5):
         f(i)
     ms = statistics.median(_time_launches(torch, f, 100))
@@ -321,7 +400,8 @@ def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):
     for Ms in (8, 16, 32, 64):
         xs_ = torch.from_numpy(workloads.activations(g, Ms, K)).to(dev)
         ys_ = torch.empty((Ms, N), dtype=torch.float16, device=dev)
-        f = lambda i: w4.linear(xs_, rot[i % copies][0], rot[i % copies][1], GROUP, out=ys_)  # noqa: E731
+        f = lambda i: w4.linear(xs_, rot[i % copies][0], rot[i % copies][1], GROUP, out=ys_,  # noqa: E731
+                                static_weights=True)
         for i in range(5):
             f(i)
         ms = statistics.median(_time_launches(torch, f, 100))
@@ -337,7 +417,7 @@ def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):
         pairs = [(rot[i][0], rot[i][1], qw2.clone(), s2.clone()) for i in range(copies)]
         x1 = torch.from_numpy(workloads.activations(g, 1, K)).to(dev)
         y1 = torch.empty((1, N), dtype=torch.float16, device=dev)
-        f = lambda i: w4.linear_gated(x1, *pairs[i % copies], GROUP, out=y1)  # noqa: E731
+        f = lambda i: w4.linear_gated(x1, *pairs[i % copies], GROUP, out=y1, static_weights=True)  # noqa: E731
         for i in range(5):
             f(i)
         ms = statistics.median(_time_launches(torch, f, 100))
@@ -427,41 +507,60 @@ def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):
 
 # ------------------------------------------------------------ reference arm --
 
-def run_reference(args):
-    """The CPU oracle (fp64, one thread) on the same decode step and metric."""
-    import oracle
-
-    oracle.build()
-    g = workloads.rng(0)
-    mats = []
-    for K, N in DECODE:
-        W = workloads.weights(g, N, K)
-        mats.append(oracle.quantize(W, GROUP))
-    x = workloads.activations(g, 1, DECODE[0][0])
-
-    def step():
-        y1, _ = oracle.linear(x, *mats[0], GROUP)
-        h = y1.astype(np.float16)
-        y2, _ = oracle.linear(h, *mats[1], GROUP)
-        return y2
-
-    for _ in range(min(args.warmup, 1)):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = time.perf_counter() - t0
-    return dt
-
-
-def cpu_baseline_sample(budget_s=12.0):
-    """Oracle decode steps on one host core until about `budget_s` seconds pass."""
+def _oracle_decode_setup():
     import oracle
 
     oracle.build()
     g = workloads.rng(0)
     mats = [oracle.quantize(workloads.weights(g, N, K), GROUP) for K, N in DECODE]
     x = workloads.activations(g, 1, DECODE[0][0])
+    # the second layer's input (one untimed pass): a step that covers only part of
+    # the first layer's outputs still feeds the second layer a full activation row
+    h = oracle.linear(x, *mats[0], GROUP)[0].astype(np.float16)
+    return oracle, mats, x, h
+
+
+def _sample_bytes(rows):
+    """Algorithmic bytes of a decode step that computes rows[i] outputs of layer i."""
+    total = 0
+    for (K, N), n in zip(DECODE, rows):
+        total += n * K // 2 + n * (K // GROUP) * 2 + K * 2 + n * 2
+    return total
+
+
+def run_reference(steps: int, warmup: int, budget_s: float = 150.0):
+    """The CPU oracle (fp64, one thread) on the decode step. A full step takes
+    about a second on one core; when steps + warmup full steps would exceed
+    about `budget_s`, every step computes the same leading fraction of both
+    layers' outputs (a bounded sample of the same workload; the metric is
+    bytes per second either way)."""
+    oracle, mats, x, h = _oracle_decode_setup()
+    t0 = time.perf_counter()
+    oracle.linear(x, mats[0][0][:256], mats[0][1][:256], GROUP)  # probe: seconds per output row
+    per_row = (time.perf_counter() - t0) / 256
+    full_s = per_row * sum(N * K / DECODE[0][0] for K, N in DECODE)
+    frac = min(1.0, budget_s / max(1e-9, (steps + warmup) * full_s))
+    rows = [max(16, int(N * frac)) for _, N in DECODE]
+
+    def step():
+        oracle.linear(x, mats[0][0][:rows[0]], mats[0][1][:rows[0]], GROUP)
+        oracle.linear(h, mats[1][0][:rows[1]], mats[1][1][:rows[1]], GROUP)
+
+    for _ in range(warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = time.perf_counter() - t0
+    sample = (f"{steps} timed steps after {warmup} warm-up steps; each step = the decode step (M=1, "
+              f"5120->17408->5120, group 128) on the first {rows[0]} and {rows[1]} output rows of the two "
+              f"layers ({100 * frac:.1f} %), fp64, one thread")
+    return _sample_bytes(rows) * steps / dt / 1e9, dt, sample
+
+
+def cpu_baseline_sample(budget_s=12.0):
+    """Oracle decode steps on one host core until about `budget_s` seconds pass."""
+    oracle, mats, x, _ = _oracle_decode_setup()
     n, t0 = 0, time.perf_counter()
     while True:
         y1, _ = oracle.linear(x, *mats[0], GROUP)
@@ -470,9 +569,58 @@ def cpu_baseline_sample(budget_s=12.0):
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return {"value": decode_bytes(1) * n / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} full decode steps (M=1, 5120->17408->5120, group 128), fp64, one thread, "
-                      f"{dt:.1f} s"}
+    host = host_info()
+    out = {"value": decode_bytes(1) * n / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": f"{n} full decode steps (M=1, 5120->17408->5120, group 128), fp64, one thread, {dt:.1f} s",
+           "host": host}
+    # the same oracle threaded over the output columns on every host core
+    threads = max(1, host["nproc"] or 1)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        y1, _ = oracle.linear(x, *mats[0], GROUP, threads=threads)
+        oracle.linear(y1.astype(np.float16), *mats[1], GROUP, threads=threads)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s / 4:
+            break
+    dt = time.perf_counter() - t0
+    out["threaded"] = {"value": decode_bytes(1) * n / dt / 1e9, "unit": "GB/s", "cores": threads,
+                       "sample": f"{n} full decode steps, the oracle split over output columns on {threads} "
+                                 f"threads, {dt:.1f} s"}
+    out["extrapolated"] = oracle_other_configs(oracle)
+    return out
+
+
+def oracle_other_configs(oracle):
+    """The oracle (one thread) on bounded samples of the prefill and routed-expert
+    workloads, extrapolated linearly in the number of multiply-adds to the full
+    problems. Labelled 'extrapolated': the full problems would take hours."""
+    res = {}
+    g = workloads.rng(11)
+    # prefill: 64 token rows x the first 2048 output columns of K=5120 -> N=17408
+    K, N, rows, cols = 5120, 17408, 64, 2048
+    qw, s = oracle.quantize(workloads.weights(g, cols, K), GROUP)
+    x = workloads.activations(g, rows, K, outlier_frac=0.01)
+    t0 = time.perf_counter()
+    oracle.linear(x, qw, s, GROUP)
+    dt = time.perf_counter() - t0
+    per_mac = dt / (rows * cols * K)
+    for M in (512, 4096):
+        t = per_mac * M * N * K
+        res[f"prefill_m{M}"] = {"s": t, "TFLOP/s": 2.0 * M * N * K / t / 1e12,
+                                "sample": f"{rows} rows x {cols} columns timed ({dt:.2f} s), extrapolated"}
+    # routed experts: the rows of 2 experts (about 512 of 32768) at each projection's shape
+    for name, (Km, Nm) in (("moe_gate_up", (2048, 512)), ("moe_down", (512, 2048))):
+        rows = 512
+        qw, s = oracle.quantize(workloads.weights(g, Nm, Km), 32)
+        x = workloads.activations(g, rows, Km)
+        t0 = time.perf_counter()
+        oracle.linear(x, qw, s, 32)
+        dt = time.perf_counter() - t0
+        R = workloads.MOE["tokens"] * workloads.MOE["top_k"]
+        t = dt * R / rows
+        res[name] = {"s": t, "TFLOP/s": 2.0 * R * Nm * Km / t / 1e12,
+                     "sample": f"{rows} rows of one expert's weights timed ({dt:.2f} s), extrapolated to R={R}"}
+    return res
 
 
 # ----------------------------------------------------------------- profile --
@@ -508,7 +656,7 @@ def run_profile(case: str, launches: int):
         y = torch.empty((1, N), dtype=torch.float16, device=dev)
         for i in range(launches):  # four gate/up pairs in turn: successive launches miss in L2
             j = 2 * (i % 4)
-            w4.linear_gated(x, *mats[j], *mats[j + 1], GROUP, out=y)
+            w4.linear_gated(x, *mats[j], *mats[j + 1], GROUP, out=y, static_weights=True)
     elif case.startswith("moe"):
         Km, Nm = (2048, 512) if case == "moe_gate_up" else (512, 2048)
         W, xs, rt = workloads.moe(Km, Nm)
@@ -528,7 +676,7 @@ def run_profile(case: str, launches: int):
         x = torch.from_numpy(workloads.activations(g, M, K, outlier_frac=0.01 if M > 16 else 0.0)).to(dev)
         y = torch.empty((M, N), dtype=torch.float16, device=dev)
         for i in range(launches):
-            w4.linear(x, *copies[i % 4], GROUP, out=y)
+            w4.linear(x, *copies[i % 4], GROUP, out=y, static_weights=True)
     torch.cuda.synchronize()
     w4.device_status()
     print(f"profile {case}: {launches} launches done")
@@ -586,15 +734,13 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        steps = max(1, min(args.steps, 20))
-        dt = run_reference(argparse.Namespace(steps=steps, warmup=args.warmup))
-        value = decode_bytes(1) * steps / dt / 1e9
+        value, dt, sample = run_reference(args.steps, args.warmup)
         print(json.dumps({
-            "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": steps,
-            "warmup": 1, "ms_per_step": dt * 1e3 / steps, "higher_is_better": True, "scaling": "weak",
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{steps} full decode steps, fp64, one thread"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                             "host": host_info()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return
 
@@ -614,9 +760,11 @@ def main():
         "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["hbm_peak"], "unit": "GB/s",
                      "frac": r["achieved"] / r["hbm_peak"],
                      "traffic": measured_traffic("gemv.cu", "gemv_decode_m1.md"),
-                     "kernel": "gemv_kernel<group 128, M<=8>", "peak_kind": r["peak_kind"],
+                     "kernel": "gemv_kernel<group 128, M<=8>, static weights", "peak_kind": r["peak_kind"],
                      "kernel_us": r["kernel_ms"] * 1e3, "algorithmic_bytes_per_launch": r["per_launch_bytes"]},
+        "per_call": r["spread"], "default_mode": r["default_mode"],
         "e2e": r["e2e"], "gpu_launches": r["launches"], "clocks": r["clocks"], "gpu": r["gpu"], "sms": r["sms"],
+        "software": r["software"], "source": source_info(), "host": host_info(),
         "side": r["extra"],
     }
     if not args.no_cpu_baseline:

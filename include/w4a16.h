@@ -116,7 +116,9 @@ W4A16_API w4a16_status w4a16_linear(const uint16_t* x, const uint8_t* qweight, c
  * expert_offsets lives in device memory and is read only by the device, so
  * no host synchronization happens; an invalid partition sets
  * W4A16_ERR_BAD_OFFSETS in the device word and leaves y_sorted unspecified.
- * Empty experts are allowed. workspace: w4a16_workspace_bytes(R, N, K, group, E).
+ * Empty experts are allowed. The grouped GEMM needs no scratch memory:
+ * w4a16_workspace_bytes(R, N, K, group, E) is 0 and workspace /
+ * workspace_bytes are ignored (NULL and 0 are fine).
  */
 W4A16_API w4a16_status w4a16_grouped_linear(const uint16_t* x_sorted, const uint8_t* qweight,
                                   const uint16_t* scales, const int32_t* expert_offsets,
@@ -144,6 +146,36 @@ W4A16_API w4a16_status w4a16_linear_gated(const uint16_t* x, const uint8_t* qwei
                                           const uint16_t* scales_up, uint16_t* y, int64_t M, int64_t N,
                                           int64_t K, int32_t group, void* workspace, size_t workspace_bytes,
                                           void* stream);
+
+/*
+ * Flags of w4a16_linear_ex and w4a16_linear_gated_ex (0 gives exactly
+ * w4a16_linear / w4a16_linear_gated; unknown bits return
+ * W4A16_ERR_INVALID_ARG).
+ *
+ * W4A16_STATIC_WEIGHTS: the caller promises that the weights (qweight and
+ * scales) were written by work that completed before this call was enqueued
+ * (packed or copied in, then synchronized), and that nothing still pending
+ * on `stream` writes them: the usual case for the weights of a decode loop.
+ * The decode GEMV (M <= 16) may then stream them into shared memory while
+ * the kernel before it on the stream is still running, and waits for that
+ * kernel only before it reads x. Without the flag the GEMV reads nothing
+ * before the previous kernel on the stream has completed. The flag changes
+ * no result bit; if the promise is broken the results are undefined. The
+ * tensor-core path (M > 16) ignores it.
+ */
+#define W4A16_STATIC_WEIGHTS 1u
+
+/* w4a16_linear with flags (see above); otherwise the same contract. */
+W4A16_API w4a16_status w4a16_linear_ex(const uint16_t* x, const uint8_t* qweight, const uint16_t* scales,
+                                       uint16_t* y, int64_t M, int64_t N, int64_t K, int32_t group, uint32_t flags,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* w4a16_linear_gated with flags (see above); otherwise the same contract. */
+W4A16_API w4a16_status w4a16_linear_gated_ex(const uint16_t* x, const uint8_t* qweight_gate,
+                                             const uint16_t* scales_gate, const uint8_t* qweight_up,
+                                             const uint16_t* scales_up, uint16_t* y, int64_t M, int64_t N, int64_t K,
+                                             int32_t group, uint32_t flags, void* workspace, size_t workspace_bytes,
+                                             void* stream);
 
 /* Bytes of workspace w4a16_linear_gated needs on the current device; 0 if the
  * problem is not one it runs. */
@@ -237,7 +269,10 @@ W4A16_API size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t 
 W4A16_API w4a16_status w4a16_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronizes `stream`, then reads and clears the current device's sticky
- * error word: W4A16_OK, W4A16_ERR_TIMEOUT or W4A16_ERR_BAD_OFFSETS. */
+ * error word: W4A16_OK, W4A16_ERR_TIMEOUT (a bounded wait in the GEMV or the
+ * GEMM gave up), W4A16_ERR_BAD_OFFSETS (w4a16_grouped_linear) or
+ * W4A16_ERR_BAD_ROUTING (w4a16_moe_dispatch, w4a16_moe_combine). The word
+ * keeps the first error raised since it was last cleared. */
 W4A16_API w4a16_status w4a16_device_status(void* stream);
 
 /* Static, human-readable name of a status code. */

@@ -93,3 +93,18 @@ def test_gated_decode_full_size(w4, cuda_device, M):
     x = workloads.activations(workloads.rng(2), M, K)
     y = _run(w4, cuda_device, x, qg, sg, qu, su, g)
     _check(y, x, qg, sg, qu, su, g, f"gated decode M={M}", threads=8)
+
+
+def test_gated_static_weights_same_bits(w4, cuda_device):
+    """W4A16_STATIC_WEIGHTS changes no result bit of the fused pair."""
+    r = workloads.rng(61)
+    M, N, K, g = 2, 1000, 2048, 128
+    qg, sg = _scaled(r, N, K, g, 8.0)
+    qu, su = workloads.raw_packed(r, N, K, g)
+    x = workloads.activations(r, M, K)
+    args = [to_dev(x, cuda_device), to_dev(qg, cuda_device), to_dev(sg.view(np.float16), cuda_device),
+            to_dev(qu, cuda_device), to_dev(su.view(np.float16), cuda_device)]
+    y0 = w4.linear_gated(*args, g).cpu().numpy()
+    y1 = w4.linear_gated(*args, g, static_weights=True).cpu().numpy()
+    assert np.array_equal(y0.view(np.uint16), y1.view(np.uint16))
+    _check(y1, x, qg, sg, qu, su, g, "gated static weights")

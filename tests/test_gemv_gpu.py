@@ -153,3 +153,52 @@ def test_weights_written_by_previous_kernel(w4, cuda_device):
         qh, sh = oracle.quantize(W, g)
         y_ref, a = oracle.linear(x, qh, sh, g)
         assert_within_bound(y, y_ref, a, f"pack then GEMV, round {i}")
+
+
+@pytest.mark.parametrize("M,N,K,g", [(1, 4099, 384, 128), (4, 1000, 2080, 32), (9, 203, 1536, 64),
+                                     (16, 300, 4096, 128), (1, 17408, 5120, 128), (2, 31, 8192, 64)])
+def test_static_weights_same_bits(w4, cuda_device, M, N, K, g):
+    """W4A16_STATIC_WEIGHTS only lets the weights stream before the previous
+    kernel completes: the result bits are those of the default mode."""
+    r = workloads.rng(M + N + K + g)
+    qw, s = workloads.raw_packed(r, N, K, g)
+    x = workloads.activations(r, M, K)
+    xd, qd, sd = to_dev(x, cuda_device), to_dev(qw, cuda_device), to_dev(s, cuda_device)
+    y0 = w4.linear(xd, qd, sd, g).cpu().numpy()
+    y1 = w4.linear(xd, qd, sd, g, static_weights=True).cpu().numpy()
+    assert np.array_equal(y0.view(np.uint16), y1.view(np.uint16))
+    y_ref, a = oracle.linear(x, qw, s, g)
+    assert_within_bound(y1, y_ref, a, "static weights")
+
+
+def test_static_weights_chain_reads_x_after_the_previous_kernel(w4, cuda_device):
+    """A decode-like chain queued back to back: x_i -> layer 1 -> h -> layer 2
+    -> o_i, with one h buffer for every step. Layer 2 streams its weights
+    early but must read h only after layer 1 of the same step has written it;
+    reading early would give the previous step's h."""
+    import torch
+
+    g, K1, N1 = 128, 1024, 1536
+    r = workloads.rng(26)
+    q1, s1 = workloads.raw_packed(r, N1, K1, g)
+    q2, s2 = workloads.raw_packed(r, K1, N1, g)
+    xs = [workloads.activations(r, 1, K1) * np.float16(1 + i) for i in range(8)]
+    dq1, ds1, dq2, ds2 = (to_dev(t, cuda_device) for t in (q1, s1, q2, s2))
+    dxs = [to_dev(x, cuda_device) for x in xs]
+    torch.cuda.synchronize()
+    h = torch.empty((1, N1), dtype=torch.float16, device=cuda_device)
+    outs = [torch.empty((1, K1), dtype=torch.float16, device=cuda_device) for _ in xs]
+    for x, o in zip(dxs, outs):
+        w4.linear(x, dq1, ds1, g, out=h, static_weights=True)
+        w4.linear(h, dq2, ds2, g, out=o, static_weights=True)
+    got = [o.cpu().numpy() for o in outs]
+    w4.device_status()
+    for i, (x, y) in enumerate(zip(xs, got)):
+        hh = w4.linear(dxs[i], dq1, ds1, g)
+        want = w4.linear(hh, dq2, ds2, g).cpu().numpy()
+        assert np.array_equal(y.view(np.uint16), want.view(np.uint16)), f"step {i}"
+        y1_ref, a1 = oracle.linear(x, q1, s1, g)
+        hh_h = hh.cpu().numpy()
+        assert_within_bound(hh_h, y1_ref, a1, f"step {i} layer 1")
+        y2_ref, a2 = oracle.linear(hh_h, q2, s2, g)
+        assert_within_bound(y, y2_ref, a2, f"step {i} layer 2")

@@ -277,6 +277,30 @@ def test_grouped_equals_loop_of_dense_calls():
     assert np.array_equal(y1, oracle.linear(x, qw[0], s[0], g)[0])
 
 
+def test_tolerance_hand_worked():
+    """The per-element bound of the workload specification,
+    |y - y_ref| <= 2^-9 |y_ref| + 1e-4 sum_k |x_k W^_nk|, on values worked out
+    by hand: each term alone, a negative y_ref (its magnitude counts), and the
+    two terms together. Every GPU parity check compares against this bound."""
+    cases = [
+        # y_ref, sum_k |x W^|, bound
+        (1.0, 0.0, 0.001953125),            # 2^-9 alone
+        (0.0, 1.0, 0.0001),                 # 1e-4 alone
+        (-3.0, 2.0, 0.005859375 + 0.0002),  # 3 * 2^-9 + 2 * 1e-4: |y_ref|, not y_ref
+        (512.0, 0.0, 1.0),                  # 512 * 2^-9
+        (-0.25, 10000.0, 1.00048828125),    # 2^-11 + 1
+        (0.0, 0.0, 0.0),
+    ]
+    y = np.array([c[0] for c in cases])
+    a = np.array([c[1] for c in cases])
+    want = np.array([c[2] for c in cases])
+    got = oracle.tolerance(y, a)
+    assert got.shape == want.shape
+    assert np.allclose(got, want, rtol=1e-14, atol=0.0), (got, want)
+    # the bound grows with both arguments, and only with |y_ref|
+    assert np.array_equal(oracle.tolerance(-y, a), got)
+
+
 def test_threaded_linear_equals_single_thread():
     x, qw, s = _raw(20, 3, 101, 256, 128)
     y1, a1 = oracle.linear(x, qw, s, 128)

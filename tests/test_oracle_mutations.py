@@ -116,3 +116,27 @@ def test_moe_pins_catch_planted_mistake(name, monkeypatch):
         except (AssertionError, ValueError, IndexError):
             failed.append(fn.__name__)
     assert failed, f"no pin caught: {name}"
+
+
+# ------------------------------------------------------------ the error bound
+# tolerance() is the bound every GPU parity check applies; a mutant with a
+# looser or wrong bound must fail its hand-worked pin.
+
+TOL_LINE = "    return np.ldexp(np.abs(y_ref), -9) + 1e-4 * absdot\n"
+TOL_MUTANTS = {
+    "relative term 2^-8": "    return np.ldexp(np.abs(y_ref), -8) + 1e-4 * absdot\n",
+    "absolute term 1e-3": "    return np.ldexp(np.abs(y_ref), -9) + 1e-3 * absdot\n",
+    "signed y_ref": "    return np.ldexp(y_ref, -9) + 1e-4 * absdot\n",
+    "absolute term dropped": "    return np.ldexp(np.abs(y_ref), -9)\n",
+    "terms multiplied": "    return np.ldexp(np.abs(y_ref), -9) * (1 + 1e-4 * absdot)\n",
+}
+
+
+@pytest.mark.parametrize("name", sorted(TOL_MUTANTS))
+def test_tolerance_pin_catches_planted_mistake(name, monkeypatch):
+    assert PY_SRC.count(TOL_LINE) == 1, "mutation anchor not found once"
+    ns = {"__name__": "oracle_mutant", "__file__": oracle.__file__}
+    exec(compile(PY_SRC.replace(TOL_LINE, TOL_MUTANTS[name]), "oracle_mutant", "exec"), ns)
+    monkeypatch.setattr(oracle, "tolerance", ns["tolerance"])
+    with pytest.raises(AssertionError):
+        pins.test_tolerance_hand_worked()

@@ -21,7 +21,7 @@ import threading
 import torch
 
 __all__ = ["pack", "unpack", "linear", "linear_gated", "grouped_linear", "moe_route", "moe_dispatch", "moe_combine",
-           "workspace_bytes", "device_status",
+           "workspace_bytes", "device_status", "STATIC_WEIGHTS",
            "W4A16Error", "lib", "LIB_PATH", "EXPORTS", "STATUS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libw4a16.so")
@@ -36,8 +36,11 @@ EXPORTS = {
     "w4a16_pack": (_I32, [_P, _I64, _I64, _I32, _P, _P, _P]),
     "w4a16_unpack": (_I32, [_P, _I64, _I64, _P, _P]),
     "w4a16_linear": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
+    "w4a16_linear_ex": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, ctypes.c_uint32, _P, _SZ, _P]),
     "w4a16_linear_noalloc": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]),
     "w4a16_linear_gated": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
+    "w4a16_linear_gated_ex": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, ctypes.c_uint32, _P, _SZ,
+                                     _P]),
     "w4a16_linear_gated_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
     "w4a16_grouped_linear": (_I32, [_P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
     "w4a16_moe_route": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _P]),
@@ -51,6 +54,10 @@ EXPORTS = {
     "w4a16_version": (_I32, []),
     "w4a16_last_cuda_error": (ctypes.c_char_p, []),
 }
+
+
+# flags of w4a16_linear_ex / w4a16_linear_gated_ex (include/w4a16.h)
+STATIC_WEIGHTS = 1
 
 
 class W4A16Error(RuntimeError):
@@ -144,8 +151,13 @@ def unpack(qw: torch.Tensor, K: int) -> torch.Tensor:
 
 
 def linear(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, group: int = 128,
-           out: torch.Tensor | None = None) -> torch.Tensor:
-    """y = x W^T for x fp16 [M, K], qweight uint8 [N, K/2], scales fp16 [N, K/group]."""
+           out: torch.Tensor | None = None, static_weights: bool = False) -> torch.Tensor:
+    """y = x W^T for x fp16 [M, K], qweight uint8 [N, K/2], scales fp16 [N, K/group].
+
+    ``static_weights=True`` passes W4A16_STATIC_WEIGHTS: the caller promises
+    that no work still pending on the stream writes qweight or scales (the
+    weights of a decode loop), so the decode GEMV may stream them before the
+    previous kernel on the stream completes. Results are identical."""
     _need(x, "x", torch.float16, 2)
     _need(qweight, "qweight", torch.uint8, 2)
     _need(scales, "scales", torch.float16, 2)
@@ -162,17 +174,19 @@ def linear(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, group: 
     st = _stream(x.device)
     nb = workspace_bytes(M, N, K, group, 1)
     ws = _workspace(x.device, st, nb)
-    _check(lib().w4a16_linear(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(out), M, N, K, group,
-                              _ptr(ws) if ws is not None else None, ws.numel() if ws is not None else 0, st),
+    _check(lib().w4a16_linear_ex(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(out), M, N, K, group,
+                                 STATIC_WEIGHTS if static_weights else 0,
+                                 _ptr(ws) if ws is not None else None, ws.numel() if ws is not None else 0, st),
            "w4a16_linear")
     return out
 
 
 def linear_gated(x: torch.Tensor, qweight_gate: torch.Tensor, scales_gate: torch.Tensor,
                  qweight_up: torch.Tensor, scales_up: torch.Tensor, group: int = 128,
-                 out: torch.Tensor | None = None) -> torch.Tensor:
+                 out: torch.Tensor | None = None, static_weights: bool = False) -> torch.Tensor:
     """y = silu(x Wg^T) * (x Wu^T) in one decode pass (M <= 16); both weight
-    matrices uint8 [N, K/2] with fp16 scales [N, K/group]."""
+    matrices uint8 [N, K/2] with fp16 scales [N, K/group]. ``static_weights``
+    as in :func:`linear`."""
     _need(x, "x", torch.float16, 2)
     for t, name in ((qweight_gate, "qweight_gate"), (qweight_up, "qweight_up")):
         _need(t, name, torch.uint8, 2)
@@ -192,10 +206,11 @@ def linear_gated(x: torch.Tensor, qweight_gate: torch.Tensor, scales_gate: torch
     st = _stream(x.device)
     nb = int(lib().w4a16_linear_gated_workspace_bytes(M, N, K, group))
     ws = _workspace(x.device, st, nb)
-    _check(lib().w4a16_linear_gated(_ptr(x), _ptr(qweight_gate), _ptr(scales_gate), _ptr(qweight_up),
-                                    _ptr(scales_up), _ptr(out), M, N, K, group,
-                                    _ptr(ws) if ws is not None else None, ws.numel() if ws is not None else 0, st),
-           "w4a16_linear_gated")
+    _check(lib().w4a16_linear_gated_ex(_ptr(x), _ptr(qweight_gate), _ptr(scales_gate), _ptr(qweight_up),
+                                       _ptr(scales_up), _ptr(out), M, N, K, group,
+                                       STATIC_WEIGHTS if static_weights else 0,
+                                       _ptr(ws) if ws is not None else None, ws.numel() if ws is not None else 0,
+                                       st), "w4a16_linear_gated")
     return out
 
 

@@ -21,7 +21,6 @@ void note_cuda_error(cudaError_t e, const char* where) {
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 constexpr int64_t kGemvMaxM = 16;
 
 std::mutex g_info_mutex;
@@ -60,9 +59,7 @@ const DeviceInfo* device_info() {
     return &g_info[dev];
 }
 
-namespace {
-
-// Common validation of w4a16_linear / w4a16_grouped_linear.
+// Common validation of w4a16_linear / w4a16_grouped_linear / w4a16_linear_noalloc.
 w4a16_status check_linear(const void* x, const void* qw, const void* s, const void* y, int64_t M, int64_t N,
                           int64_t K, int32_t group, const DeviceInfo** dev) {
     if (M < 0 || N < 0 || K < 0) return W4A16_ERR_INVALID_ARG;
@@ -75,6 +72,48 @@ w4a16_status check_linear(const void* x, const void* qw, const void* s, const vo
     if (!*dev) return W4A16_ERR_CUDA;
     if ((*dev)->cc_major != 10 || (*dev)->cc_minor != 3) return W4A16_ERR_UNSUPPORTED;
     return W4A16_OK;
+}
+
+namespace {
+
+constexpr uint32_t kKnownFlags = W4A16_STATIC_WEIGHTS;
+
+GemvOptions gemv_options(uint32_t flags) {
+    GemvOptions o;
+    o.static_weights = (flags & W4A16_STATIC_WEIGHTS) != 0;
+    return o;
+}
+
+w4a16_status linear_impl(const uint16_t* x, const uint8_t* qweight, const uint16_t* scales, uint16_t* y, int64_t M,
+                         int64_t N, int64_t K, int32_t group, uint32_t flags, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    if (flags & ~kKnownFlags) return W4A16_ERR_INVALID_ARG;
+    const DeviceInfo* dev = nullptr;
+    const w4a16_status v = check_linear(x, qweight, scales, y, M, N, K, group, &dev);
+    if (v != W4A16_OK || M == 0 || N == 0) return v;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(uint16_t), st));
+    if (M <= kGemvMaxM)
+        return gemv_launch(*dev, x, qweight, scales, y, M, N, K, group, workspace, workspace_bytes,
+                           gemv_options(flags), st);
+    return gemm_launch(*dev, x, qweight, scales, y, M, N, K, group, nullptr, 1, st);
+}
+
+w4a16_status linear_gated_impl(const uint16_t* x, const uint8_t* qweight_gate, const uint16_t* scales_gate,
+                               const uint8_t* qweight_up, const uint16_t* scales_up, uint16_t* y, int64_t M,
+                               int64_t N, int64_t K, int32_t group, uint32_t flags, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    if (flags & ~kKnownFlags) return W4A16_ERR_INVALID_ARG;
+    const DeviceInfo* dev = nullptr;
+    w4a16_status v = check_linear(x, qweight_gate, scales_gate, y, M, N, K, group, &dev);
+    if (v != W4A16_OK || M == 0 || N == 0) return v;
+    if (K > 0 && (!qweight_up || !scales_up)) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(qweight_up) || !aligned16(scales_up)) return W4A16_ERR_MISALIGNED;
+    if (M > kGemvMaxM) return W4A16_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(uint16_t), st));  // silu(0) * 0
+    return gemv_gated_launch(*dev, x, qweight_gate, scales_gate, qweight_up, scales_up, y, M, N, K, group, workspace,
+                             workspace_bytes, gemv_options(flags), st);
 }
 
 }  // namespace
@@ -143,30 +182,29 @@ w4a16_status w4a16_workspace_init(void* workspace, size_t workspace_bytes, void*
 w4a16_status w4a16_linear(const uint16_t* x, const uint8_t* qweight, const uint16_t* scales, uint16_t* y,
                           int64_t M, int64_t N, int64_t K, int32_t group, void* workspace, size_t workspace_bytes,
                           void* stream) {
-    const DeviceInfo* dev = nullptr;
-    const w4a16_status v = check_linear(x, qweight, scales, y, M, N, K, group, &dev);
-    if (v != W4A16_OK || M == 0 || N == 0) return v;
-    cudaStream_t st = (cudaStream_t)stream;
-    if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(uint16_t), st));
-    if (M <= kGemvMaxM)
-        return gemv_launch(*dev, x, qweight, scales, y, M, N, K, group, workspace, workspace_bytes, st);
-    return gemm_launch(*dev, x, qweight, scales, y, M, N, K, group, nullptr, 1, st);
+    return linear_impl(x, qweight, scales, y, M, N, K, group, 0u, workspace, workspace_bytes, stream);
+}
+
+w4a16_status w4a16_linear_ex(const uint16_t* x, const uint8_t* qweight, const uint16_t* scales, uint16_t* y,
+                             int64_t M, int64_t N, int64_t K, int32_t group, uint32_t flags, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    return linear_impl(x, qweight, scales, y, M, N, K, group, flags, workspace, workspace_bytes, stream);
 }
 
 w4a16_status w4a16_linear_gated(const uint16_t* x, const uint8_t* qweight_gate, const uint16_t* scales_gate,
                                 const uint8_t* qweight_up, const uint16_t* scales_up, uint16_t* y, int64_t M,
                                 int64_t N, int64_t K, int32_t group, void* workspace, size_t workspace_bytes,
                                 void* stream) {
-    const DeviceInfo* dev = nullptr;
-    w4a16_status v = check_linear(x, qweight_gate, scales_gate, y, M, N, K, group, &dev);
-    if (v != W4A16_OK || M == 0 || N == 0) return v;
-    if (K > 0 && (!qweight_up || !scales_up)) return W4A16_ERR_INVALID_ARG;
-    if (!aligned16(qweight_up) || !aligned16(scales_up)) return W4A16_ERR_MISALIGNED;
-    if (M > kGemvMaxM) return W4A16_ERR_UNSUPPORTED;
-    cudaStream_t st = (cudaStream_t)stream;
-    if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(uint16_t), st));  // silu(0) * 0
-    return gemv_gated_launch(*dev, x, qweight_gate, scales_gate, qweight_up, scales_up, y, M, N, K, group, workspace,
-                             workspace_bytes, st);
+    return linear_gated_impl(x, qweight_gate, scales_gate, qweight_up, scales_up, y, M, N, K, group, 0u, workspace,
+                             workspace_bytes, stream);
+}
+
+w4a16_status w4a16_linear_gated_ex(const uint16_t* x, const uint8_t* qweight_gate, const uint16_t* scales_gate,
+                                   const uint8_t* qweight_up, const uint16_t* scales_up, uint16_t* y, int64_t M,
+                                   int64_t N, int64_t K, int32_t group, uint32_t flags, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+    return linear_gated_impl(x, qweight_gate, scales_gate, qweight_up, scales_up, y, M, N, K, group, flags,
+                             workspace, workspace_bytes, stream);
 }
 
 size_t w4a16_linear_gated_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t group) {
@@ -248,6 +286,26 @@ w4a16_status w4a16_moe_combine(const uint16_t* y_sorted, int64_t R, const int32_
     if (d != W4A16_OK) return d;
     return moe_combine_launch(*dev, y_sorted, R, row_of, topk_weights, T, top_k, N, y, (cudaStream_t)stream);
 }
+
+#ifdef W4A16_TEST_HOOKS
+// Test-only build: set the wait limit and the producers' issue limit of the
+// GEMV and the GEMM (synchronous), and read the GEMM's TMEM counters.
+W4A16_API w4a16_status w4a16_test_set_hooks(uint64_t wait_limit_ns, int32_t issue_limit) {
+    const TestHooks h{(unsigned long long)wait_limit_ns, (int)issue_limit};
+    const w4a16_status a = cuda_status(gemv_set_test_hooks(h), "test hooks (gemv)");
+    if (a != W4A16_OK) return a;
+    return cuda_status(gemm_set_test_hooks(h), "test hooks (gemm)");
+}
+
+W4A16_API w4a16_status w4a16_test_tmem_counters(uint64_t* allocs, uint64_t* frees) {
+    TestCounters c{};
+    const w4a16_status a = cuda_status(gemm_get_test_counters(&c), "test counters");
+    if (a != W4A16_OK) return a;
+    *allocs = c.tmem_allocs;
+    *frees = c.tmem_frees;
+    return W4A16_OK;
+}
+#endif
 
 w4a16_status w4a16_device_status(void* stream) {
     const DeviceInfo* dev = device_info();

@@ -35,9 +35,15 @@
 //   warp order (deterministic), rounds once to fp16 and resets the counter.
 //   A warp publishes each partial as soon as its segment ends, with one
 //   acquire-release atomic on the counter.
-// * Programmatic dependent launch: the block starts while the kernel before it
-//   is still finishing, and reads nothing (weights included, which that kernel
-//   may have written) before griddepcontrol.wait returns.
+// * Programmatic dependent launch: every block lets the next kernel on the
+//   stream launch as soon as it has set up, so that kernel's blocks take each
+//   SM the moment this one's block leaves it. A block may start while the
+//   kernel before it is still finishing. By default it reads nothing (weights
+//   included, which that kernel may have written) before griddepcontrol.wait
+//   returns. With static weights (the caller's promise that no pending work
+//   writes them) the producer fills every ring with weights and scales first
+//   and only x waits for the previous kernel, so the HBM stream of one GEMV
+//   runs on into the tail of the one before it.
 //
 // Every wait is bounded in time; one that gives up records W4A16_ERR_TIMEOUT in
 // the device error word, and the block leaves only after the copies it issued
@@ -75,6 +81,19 @@ constexpr size_t kXSmemMax = 84 * 1024;  // x staged in shared memory up to this
 constexpr int kXLoads = (int)((kXSmemMax / 16 + kConsumerThreads - 1) / kConsumerThreads);  // x loads per thread
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+#ifdef W4A16_TEST_HOOKS
+__device__ TestHooks g_hooks = {kWaitLimitNs, -1};
+__device__ __forceinline__ uint64_t wait_limit() { return g_hooks.wait_limit_ns; }
+__device__ __forceinline__ bool may_issue(int issued) { return g_hooks.issue_limit < 0 || issued < g_hooks.issue_limit; }
+#else
+__device__ __forceinline__ constexpr uint64_t wait_limit() { return kWaitLimitNs; }
+__device__ __forceinline__ constexpr bool may_issue(int) { return true; }
+#endif
+
+// GemvArgs::mode bits
+constexpr int kMode3d = 1;      // the weight map is 3-D: one TMA box per unit
+constexpr int kModeStatic = 2;  // weights and scales may be read before the dependency wait
+
 struct GemvArgs {
     const uint16_t* x;
     const uint16_t* s;
@@ -89,7 +108,7 @@ struct GemvArgs {
     unsigned int* err;
     int gpr;         // scale groups per row: K / G
     int svec;        // scale rows start 16-byte aligned (gpr % 8 == 0): whole units load as vectors
-    int w3d;         // the weight map is 3-D: one TMA box per unit
+    int mode;        // kMode3d | kModeStatic
 };
 
 // Gated pair (gate and up projections of one MLP, fused; a parameter of the
@@ -371,6 +390,7 @@ __device__ __forceinline__ void finish_row_block(const GemvArgs& p, const GatedA
     if (lane == 0) old = ptx::atom_add_acq_rel_gpu(ga.pair + rb, 1);
     old = __shfl_sync(0xffffffffu, old, 0);
     if (old == 0) return;  // the other half finishes the pair
+    __syncwarp();  // every lane's loads below come after lane 0's acquire
     const float* other = ga.gres + (mat ^ 1) * half;
 #pragma unroll
     for (int t = 0; t < NT; ++t)
@@ -422,6 +442,7 @@ __device__ __noinline__ void publish_partial(const GemvArgs& p, const GatedArgs&
     const int64_t wa = warp_of_unit(rb * p.KU, p);
     const int64_t wb = warp_of_unit(rb * p.KU + p.KU - 1, p);
     if ((int64_t)old != wb - wa) return;  // another warp finishes this row-block
+    __syncwarp();  // every lane's loads of the other partials come after lane 0's acquire
     const int64_t slot_elems = (int64_t)kRows * p.M;
     float sum[NT][4];
 #pragma unroll
@@ -482,7 +503,7 @@ __device__ __forceinline__ void produce(const MapPtrs& maps, const GemvArgs& p,
         uint64_t* bar = &bars->full[c][sl];
         uint8_t* dst = ring + (c * kSlots + sl) * SLOT;
         ptx::mbar_arrive_expect_tx(bar, SLOT);
-        if (p.w3d) {
+        if (p.mode & kMode3d) {
             ptx::tma_load_3d(dst, mw, bar, 0, rb * kRows, ku * kUnitSteps);
         } else {
 #pragma unroll
@@ -492,18 +513,20 @@ __device__ __forceinline__ void produce(const MapPtrs& maps, const GemvArgs& p,
         if (TS) ptx::tma_load_2d(dst + kWBytes, ms, bar, scale_x(ku), rb * kRows);
     };
 
-    // Every input, the weights included, may come from the kernel before this
-    // one on the stream, which may still be running: nothing is read before
-    // griddepcontrol.wait returns. (Prefetching the first units into L2 before
-    // the wait is safe, but measured slower: the extra traffic delays the
-    // previous kernel's completion and this kernel's x loads.)
-    ptx::grid_dependency_wait();
-    for (; ri < kSlots && ri < n; ++ri) issue(ri, ub + ri);
+    // By default every input, the weights included, may come from the kernel
+    // before this one on the stream, which may still be running: nothing is
+    // read before griddepcontrol.wait returns. (Prefetching the first units
+    // into L2 before the wait is safe, but measured slower: the extra traffic
+    // delays the previous kernel's completion and this kernel's x loads.) With
+    // static weights the producer reads only what no pending kernel writes, so
+    // it fills the rings at once and never waits.
+    if (!(p.mode & kModeStatic)) ptx::grid_dependency_wait();
+    for (; ri < kSlots && ri < n && may_issue(ri); ++ri) issue(ri, ub + ri);
     uint64_t idle_since = 0;
     bool failed = false;
     while (__any_sync(0xffffffffu, ri < n && !failed)) {
         bool moved = false;
-        if (ri < n && !failed) {
+        if (ri < n && !failed && may_issue(ri)) {
             const int sl = ri % kSlots;
             // the slot's previous unit (ri - kSlots) completed phase ri / kSlots - 1
             if (ptx::mbar_try_wait(&bars->empty[c][sl], (uint32_t)((ri / kSlots + 1) & 1))) {
@@ -518,7 +541,7 @@ __device__ __forceinline__ void produce(const MapPtrs& maps, const GemvArgs& p,
         }
         const uint64_t now = ptx::globaltimer_ns();
         if (idle_since == 0) idle_since = now;
-        if (*abort || now - idle_since > kWaitLimitNs) {
+        if (*abort || now - idle_since > wait_limit()) {
             if (lane == 0 && !*abort) {
                 raise_device_error(p.err, W4A16_ERR_TIMEOUT);
                 *abort = 1;
@@ -562,6 +585,10 @@ __device__ __forceinline__ void gemv_body(const MapPtrs& maps, const GemvArgs& p
     }
     if (threadIdx.x < 64) reinterpret_cast<uint4*>(bars->zero)[threadIdx.x] = make_uint4(0, 0, 0, 0);
     __syncthreads();
+    // the next kernel on the stream may launch now: its blocks take each SM as
+    // this kernel's block there leaves, and wait for this grid's completion
+    // before they read anything it writes
+    ptx::launch_dependents();
 
     if (warp == kProducer) {
         produce<G, TS, GT>(maps, p, bars, ring, abort, lane);
@@ -628,7 +655,7 @@ __device__ __forceinline__ void gemv_body(const MapPtrs& maps, const GemvArgs& p
     int sl = 0;
     uint32_t phase = 0;
     for (int r = 0; r < n_units; ++r) {
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bars->full[cw][sl], phase, abort, kWaitLimitNs))) {
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bars->full[cw][sl], phase, abort, wait_limit()))) {
             if (!*abort) raise_device_error(p.err, W4A16_ERR_TIMEOUT);
             *abort = 1;  // the producer stops and waits for the loads it issued
             return;
@@ -660,7 +687,6 @@ __device__ __forceinline__ void gemv_body(const MapPtrs& maps, const GemvArgs& p
 
         const bool seg_end = (ku == KU - 1) || (r == n_units - 1);
         if (seg_end) {
-            if (r == n_units - 1) ptx::launch_dependents();  // only the epilogue of this warp remains
             if (seg_ku0 == 0 && ku == KU - 1)
                 finish_row_block<NT, GT>(p, ga, rb, acc, gid, t4, lane);  // whole row-block in this warp
             else  // partial: published now, so its latency overlaps the units that follow
@@ -725,11 +751,10 @@ size_t smem_bytes(size_t slot_bytes, bool xs, int64_t M, int64_t steps) {
 template <int G, int NT, bool XS, bool TS, bool GT>
 w4a16_status launch_one(const DeviceInfo& dev, const CUtensorMap (&map)[4], const GemvArgs& a, const GatedArgs& ga,
                         unsigned blocks, size_t smem, cudaStream_t st) {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [&dev] {  // the device's opt-in maximum; each launch checks its own size
-        attr = GT ? cudaFuncSetAttribute(gemv_gated_kernel<G, NT, XS, TS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dev.smem_optin)
+    static PerDeviceOnce once;
+    const cudaError_t attr = once.run(dev.device, [&dev] {  // the device's opt-in maximum; each launch checks its own size
+        return GT ? cudaFuncSetAttribute(gemv_gated_kernel<G, NT, XS, TS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)dev.smem_optin)
                   : cudaFuncSetAttribute(gemv_kernel<G, NT, XS, TS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)dev.smem_optin);
     });
@@ -826,7 +851,7 @@ bool encode_weights(CUtensorMap (&map)[4], int slot, const uint8_t* qw, const ui
 
 w4a16_status gemv_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s,
                       const uint8_t* qw2, const uint16_t* s2, uint16_t* y, int64_t M, int64_t N, int64_t K, int group,
-                      void* workspace, size_t workspace_bytes, cudaStream_t st) {
+                      void* workspace, size_t workspace_bytes, const GemvOptions& opt, cudaStream_t st) {
     const bool gated = qw2 != nullptr;
     const size_t need = gemv_workspace_bytes(dev, M, N, K, gated);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return W4A16_ERR_WORKSPACE;
@@ -868,7 +893,7 @@ w4a16_status gemv_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t* q
     a.err = dev.error_word;
     a.gpr = (int)gpr;
     a.svec = gpr % 8 == 0;
-    a.w3d = w3d;
+    a.mode = (w3d ? kMode3d : 0) | (opt.static_weights ? kModeStatic : 0);
     GatedArgs ga{s2, nullptr, nullptr};
     if (gated) {
         char* after = ws + partial_region_bytes(dev) + align256((size_t)RB * 2 * sizeof(int));
@@ -896,16 +921,20 @@ w4a16_status gemv_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t* q
 
 w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s,
                          uint16_t* y, int64_t M, int64_t N, int64_t K, int group, void* workspace,
-                         size_t workspace_bytes, cudaStream_t st) {
-    return gemv_run(dev, x, qw, s, nullptr, nullptr, y, M, N, K, group, workspace, workspace_bytes, st);
+                         size_t workspace_bytes, const GemvOptions& opt, cudaStream_t st) {
+    return gemv_run(dev, x, qw, s, nullptr, nullptr, y, M, N, K, group, workspace, workspace_bytes, opt, st);
 }
 
 w4a16_status gemv_gated_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw_gate,
                                const uint16_t* s_gate, const uint8_t* qw_up, const uint16_t* s_up, uint16_t* y,
                                int64_t M, int64_t N, int64_t K, int group, void* workspace, size_t workspace_bytes,
-                               cudaStream_t st) {
+                               const GemvOptions& opt, cudaStream_t st) {
     if (qw_up == nullptr || s_up == nullptr) return W4A16_ERR_INVALID_ARG;
-    return gemv_run(dev, x, qw_gate, s_gate, qw_up, s_up, y, M, N, K, group, workspace, workspace_bytes, st);
+    return gemv_run(dev, x, qw_gate, s_gate, qw_up, s_up, y, M, N, K, group, workspace, workspace_bytes, opt, st);
 }
+
+#ifdef W4A16_TEST_HOOKS
+cudaError_t gemv_set_test_hooks(const TestHooks& h) { return cudaMemcpyToSymbol(g_hooks, &h, sizeof(h)); }
+#endif
 
 }  // namespace w4a16

@@ -5,9 +5,13 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "w4a16.h"
 
 namespace w4a16 {
+
+constexpr int kMaxDevices = 64;  // device ordinals the library serves
 
 // ----------------------------------------------------------------- device --
 
@@ -83,17 +87,44 @@ struct DeviceInfo {
 // Cached per-device properties of the current device (nullptr on failure).
 const DeviceInfo* device_info();
 
+// One-time set-up per device for one call site: kernel attributes such as the
+// dynamic shared-memory limit belong to each device's context, so they are set
+// once on every device that launches the kernel.
+struct PerDeviceOnce {
+    std::once_flag flag[kMaxDevices];
+    cudaError_t err[kMaxDevices] = {};
+
+    template <class F>
+    cudaError_t run(int device, F&& setup) {
+        std::call_once(flag[device], [&] { err[device] = setup(); });
+        return err[device];
+    }
+};
+
+// Host validation shared by w4a16_linear, w4a16_linear_ex and the
+// allocation-free entry point: sizes, group, null pointers, 16-byte
+// alignment and the device (sm_103). On W4A16_OK with M, N > 0, *dev is the
+// current device's properties.
+w4a16_status check_linear(const void* x, const void* qw, const void* s, const void* y, int64_t M, int64_t N,
+                          int64_t K, int32_t group, const DeviceInfo** dev);
+
+// Launch options of the decode GEMV (flags of the _ex entry points).
+struct GemvOptions {
+    bool static_weights = false;  // weights may be streamed before the previous kernel completes
+};
+
 // GEMV (decode, M <= 16).
 size_t gemv_workspace_bytes(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, bool gated = false);
 // Offset of the arrival counters inside a GEMV workspace (they follow the partials).
 size_t partial_region_bytes(const DeviceInfo& dev);
 w4a16_status gemv_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw,
                          const uint16_t* s, uint16_t* y, int64_t M, int64_t N, int64_t K,
-                         int group, void* workspace, size_t workspace_bytes, cudaStream_t st);
+                         int group, void* workspace, size_t workspace_bytes, const GemvOptions& opt,
+                         cudaStream_t st);
 w4a16_status gemv_gated_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw_gate,
                                const uint16_t* s_gate, const uint8_t* qw_up, const uint16_t* s_up, uint16_t* y,
                                int64_t M, int64_t N, int64_t K, int group, void* workspace, size_t workspace_bytes,
-                               cudaStream_t st);
+                               const GemvOptions& opt, cudaStream_t st);
 
 // Quantizer / unpack.
 w4a16_status pack_launch(const float* w, int64_t N, int64_t K, int group, uint8_t* qw,
@@ -115,6 +146,25 @@ w4a16_status moe_dispatch_launch(const DeviceInfo& dev, const int32_t* ids, int6
                                  int32_t* token_of_row, uint16_t* x_sorted, void* workspace, cudaStream_t st);
 w4a16_status moe_combine_launch(const DeviceInfo& dev, const uint16_t* y_sorted, int64_t R, const int32_t* row_of,
                                 const float* weights, int64_t T, int k, int64_t N, uint16_t* y, cudaStream_t st);
+
+#ifdef W4A16_TEST_HOOKS
+// Test-only build (compiled with -DW4A16_TEST_HOOKS into a separate library):
+// the bounded waits give up after a limit the test chooses, and the TMA
+// producers stop after a given number of copies, so a test can make a wait
+// run out and check the error status and the unwind, with nothing faulting or
+// hanging. The production library has none of this.
+struct TestHooks {
+    unsigned long long wait_limit_ns;  // limit of every bounded wait
+    int issue_limit;                   // copies a producer may issue (per ring); < 0: no limit
+};
+// Counters the GEMM keeps in the test build: TMEM allocations and frees.
+struct TestCounters {
+    unsigned long long tmem_allocs, tmem_frees;
+};
+cudaError_t gemv_set_test_hooks(const TestHooks& h);
+cudaError_t gemm_set_test_hooks(const TestHooks& h);
+cudaError_t gemm_get_test_counters(TestCounters* c);
+#endif
 
 // Records a failed CUDA runtime call for w4a16_last_cuda_error (per host thread).
 void note_cuda_error(cudaError_t e, const char* where);

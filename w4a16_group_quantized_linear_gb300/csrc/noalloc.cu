@@ -9,7 +9,6 @@ namespace w4a16 {
 namespace {
 
 constexpr size_t kScratchBytes = W4A16_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 // One copy per device, resident while the library is loaded.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
@@ -39,15 +38,19 @@ using namespace w4a16;
 extern "C" w4a16_status w4a16_linear_noalloc(const uint16_t* x, const uint8_t* qweight, const uint16_t* scales,
                                              uint16_t* y, int64_t M, int64_t N, int64_t K, int32_t group,
                                              void* stream) {
-    // 0 for invalid arguments (w4a16_linear then reports them) and for the
-    // tensor-core path, which needs no scratch
+    // the same host checks as w4a16_linear, before the shared array is touched,
+    // so an invalid call neither clears it nor reports anything but its own error
+    const DeviceInfo* dev = nullptr;
+    const w4a16_status v = check_linear(x, qweight, scales, y, M, N, K, group, &dev);
+    if (v != W4A16_OK || M == 0 || N == 0 || K == 0)
+        return v != W4A16_OK ? v : w4a16_linear(x, qweight, scales, y, M, N, K, group, nullptr, 0, stream);
+    // 0 for the tensor-core path, which needs no scratch
     const size_t need = w4a16_workspace_bytes(M, N, K, group, 1);
     if (need > kScratchBytes) return W4A16_ERR_WORKSPACE;
     void* scratch = nullptr;
     if (need > 0) {
-        const DeviceInfo* dev = device_info();
         scratch = scratch_address();
-        if (dev == nullptr || scratch == nullptr) return W4A16_ERR_CUDA;
+        if (scratch == nullptr) return W4A16_ERR_CUDA;
         // the arrival counters must start at zero; the partial sums need no clearing
         const size_t counters = partial_region_bytes(*dev);
         if (cudaMemsetAsync(static_cast<char*>(scratch) + counters, 0, need - counters, (cudaStream_t)stream) !=

@@ -46,6 +46,21 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s
 constexpr int kRowsPerTile = 128;
 
+#ifdef W4A16_TEST_HOOKS
+__device__ TestHooks g_hooks = {kWaitLimitNs, -1};
+__device__ TestCounters g_counters = {0ull, 0ull};
+__device__ __forceinline__ uint64_t wait_limit() { return g_hooks.wait_limit_ns; }
+__device__ __forceinline__ bool may_issue(int64_t issued) {
+    return g_hooks.issue_limit < 0 || issued < g_hooks.issue_limit;
+}
+__device__ __forceinline__ void count_tmem(unsigned long long* c) { atomicAdd(c, 1ull); }
+#define W4A16_COUNT_TMEM(field) count_tmem(&g_counters.field)
+#else
+__device__ __forceinline__ constexpr uint64_t wait_limit() { return kWaitLimitNs; }
+__device__ __forceinline__ constexpr bool may_issue(int64_t) { return true; }
+#define W4A16_COUNT_TMEM(field) ((void)0)
+#endif
+
 template <int G_, int BN_, int KSTAGE_, int PSTAGES_, int XSTAGES_, int DEQW_, int EPIW_, bool SRUNS_ = false>
 struct Cfg {
     static constexpr int G = G_;              // scale group
@@ -229,6 +244,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (warp == 1) {
         ptx::tmem_alloc(&sm->tmem_base, C::TMEM_COLS);
         ptx::tmem_relinquish();
+        if (lane == 0) W4A16_COUNT_TMEM(tmem_allocs);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -247,7 +263,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             uint64_t idle_since = 0;
             while (ip < nst || ix < nst) {
                 bool moved = false;
-                if (ix < nst) {
+                if (ix < nst && may_issue(ip + ix)) {
                     const int st = (int)(ix % C::XSTAGES);
                     const int64_t round = ix / C::XSTAGES;
                     if (round == 0 || ptx::mbar_try_wait(&sm->xempty[st], (uint32_t)((round - 1) & 1))) {
@@ -261,7 +277,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         moved = true;
                     }
                 }
-                if (ip < nst) {
+                if (ip < nst && may_issue(ip + ix)) {
                     const int st = (int)(ip % C::PSTAGES);
                     const int64_t round = ip / C::PSTAGES;
                     if (round == 0 || ptx::mbar_try_wait(&sm->pempty[st], (uint32_t)((round - 1) & 1))) {
@@ -281,7 +297,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
                 const uint64_t now = ptx::globaltimer_ns();
                 if (idle_since == 0) idle_since = now;
-                if (*abort || now - idle_since > kWaitLimitNs) {
+                if (*abort || now - idle_since > wait_limit()) {
                     ok = false;
                     break;
                 }
@@ -306,8 +322,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int64_t c = 0; ok && c < nst; ++c) {
                 const int xs = (int)(c % C::XSTAGES);
                 const uint32_t par = (uint32_t)((c / C::XSTAGES) & 1);
-                if (!ptx::mbar_wait(&sm->xfull[xs], par, abort, kWaitLimitNs) ||
-                    !ptx::mbar_wait(&sm->afull[xs], par, abort, kWaitLimitNs)) {
+                if (!ptx::mbar_wait(&sm->xfull[xs], par, abort, wait_limit()) ||
+                    !ptx::mbar_wait(&sm->afull[xs], par, abort, wait_limit())) {
                     ok = false;
                     break;
                 }
@@ -328,7 +344,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         cur_b = (int)(grp & 1);
                         if (grp >= 2) {
                             if (!ptx::mbar_wait(&sm->dempty[cur_b], (uint32_t)(((grp >> 1) - 1) & 1), abort,
-                                                kWaitLimitNs)) {
+                                                wait_limit())) {
                                 ok = false;
                                 break;
                             }
@@ -362,9 +378,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         for (int64_t c = 0; c < nst; ++c) {
             const int ps = (int)(c % C::PSTAGES), xs = (int)(c % C::XSTAGES);
             const int64_t around = c / C::XSTAGES;
-            if (!ptx::mbar_wait(&sm->pfull[ps], (uint32_t)((c / C::PSTAGES) & 1), abort, kWaitLimitNs) ||
-                (around > 0 &&
-                 !ptx::mbar_wait(&sm->xempty[xs], (uint32_t)((around - 1) & 1), abort, kWaitLimitNs))) {
+            // warp-uniform outcome: the TMEM stores below are .sync.aligned
+            const bool got = ptx::mbar_wait(&sm->pfull[ps], (uint32_t)((c / C::PSTAGES) & 1), abort, wait_limit()) &&
+                             (around == 0 ||
+                              ptx::mbar_wait(&sm->xempty[xs], (uint32_t)((around - 1) & 1), abort, wait_limit()));
+            if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
@@ -453,7 +471,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if (gb + i >= gk || !ok) break;
                 const int b = (int)(grp & 1);
                 if (!__all_sync(0xffffffffu,
-                                ptx::mbar_wait(&sm->dfull[b], (uint32_t)((grp >> 1) & 1), abort, kWaitLimitNs))) {
+                                ptx::mbar_wait(&sm->dfull[b], (uint32_t)((grp >> 1) & 1), abort, wait_limit()))) {
                     ok = false;
                     break;
                 }
@@ -513,7 +531,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (warp == 1) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+    if (warp == 1) {
+        ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+        if (lane == 0) W4A16_COUNT_TMEM(tmem_frees);
+    }
 }
 
 // ------------------------------------------------------------------- host --
@@ -570,11 +591,10 @@ w4a16_status make_maps(const uint16_t* x, const uint8_t* qw, int64_t M, int64_t 
 }
 
 template <class C>
-w4a16_status launch(const CUtensorMap& mx, const CUtensorMap& mw, const Args& a, dim3 grid, cudaStream_t st) {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+w4a16_status launch(int dev, const CUtensorMap& mx, const CUtensorMap& mw, const Args& a, dim3 grid, cudaStream_t st) {
+    static PerDeviceOnce once;
+    const cudaError_t attr_err = once.run(dev, [] {
+        return cudaFuncSetAttribute(tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     });
     if (attr_err != cudaSuccess) return cuda_status(attr_err, "gemm: cudaFuncSetAttribute");
     tc_kernel<C><<<grid, C::THREADS, C::SMEM, st>>>(mx, mw, a);
@@ -605,9 +625,9 @@ w4a16_status gemm_g(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw,
     // weight-row tile (x_sorted is larger than L2 at the routed workloads).
     if (offsets && mt <= 65535) {
         a.n_fast = 1;
-        return launch<C>(mx, mw, a, dim3((unsigned)nt, (unsigned)mt), st);
+        return launch<C>(dev.device, mx, mw, a, dim3((unsigned)nt, (unsigned)mt), st);
     }
-    return launch<C>(mx, mw, a, dim3((unsigned)mt, (unsigned)nt), st);
+    return launch<C>(dev.device, mx, mw, a, dim3((unsigned)mt, (unsigned)nt), st);
 }
 
 }  // namespace
@@ -630,5 +650,10 @@ w4a16_status gemm_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     W4A16_GEMM(PrefillCfg)
 #undef W4A16_GEMM
 }
+
+#ifdef W4A16_TEST_HOOKS
+cudaError_t gemm_set_test_hooks(const TestHooks& h) { return cudaMemcpyToSymbol(g_hooks, &h, sizeof(h)); }
+cudaError_t gemm_get_test_counters(TestCounters* c) { return cudaMemcpyFromSymbol(c, g_counters, sizeof(*c)); }
+#endif
 
 }  // namespace w4a16
