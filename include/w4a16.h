@@ -101,7 +101,10 @@ W4A16_API w4a16_status w4a16_unpack(const uint8_t* qweight, int64_t N, int64_t K
  * partial sums live in `workspace`; larger M runs the tensor-core GEMM.
  * workspace: device buffer of at least w4a16_workspace_bytes(M, N, K, group, 1)
  * bytes, zero-filled once before its first use (w4a16_workspace_init); every
- * call returns it to that state. May be NULL when that size is 0.
+ * call leaves it ready for the next (the counters it keeps there are back at
+ * zero; the partial sums it parks there are always written before they are
+ * read). One workspace may serve w4a16_linear and w4a16_linear_gated calls of
+ * any shape in turn. May be NULL when that size is 0.
  */
 W4A16_API w4a16_status w4a16_linear(const uint16_t* x, const uint8_t* qweight, const uint16_t* scales,
                           uint16_t* y, int64_t M, int64_t N, int64_t K, int32_t group,
@@ -137,9 +140,10 @@ W4A16_API w4a16_status w4a16_grouped_linear(const uint16_t* x_sorted, const uint
  * in fp32; silu and the product are fp32; y is rounded once to fp16.
  * Decode only: 1 <= M <= 16, else W4A16_ERR_UNSUPPORTED. Same alignment rules
  * as w4a16_linear. workspace: w4a16_linear_gated_workspace_bytes(M, N, K,
- * group) bytes, zero-filled once (w4a16_workspace_init); every call returns
- * it to that state. One launch streams both weight matrices once and never
- * writes g or u to y's buffer.
+ * group) bytes, zero-filled once (w4a16_workspace_init); every call leaves it
+ * ready for the next, as for w4a16_linear (its fp32 g and u parking area is
+ * zero again when the call ends). One launch streams both weight matrices
+ * once and never writes g or u to y's buffer.
  */
 W4A16_API w4a16_status w4a16_linear_gated(const uint16_t* x, const uint8_t* qweight_gate,
                                           const uint16_t* scales_gate, const uint8_t* qweight_up,

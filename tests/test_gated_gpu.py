@@ -108,3 +108,35 @@ def test_gated_static_weights_same_bits(w4, cuda_device):
     y1 = w4.linear_gated(*args, g, static_weights=True).cpu().numpy()
     assert np.array_equal(y0.view(np.uint16), y1.view(np.uint16))
     _check(y1, x, qg, sg, qu, su, g, "gated static weights")
+
+
+def test_gated_then_plain_share_one_workspace(w4, cuda_device):
+    """A fused gate+up call and a plain GEMV may share one workspace: every
+    call leaves it ready for the next, including the fp32 gate/up parking
+    area, whose bytes lie where a wide plain GEMV keeps its arrival counters."""
+    import torch
+
+    lib = w4.lib()
+    r = workloads.rng(62)
+    M, N, K, g = 2, 4096, 1024, 128
+    qg, sg = _scaled(r, N, K, g, 8.0)
+    qu, su = workloads.raw_packed(r, N, K, g)
+    x = workloads.activations(r, M, K)
+    Np, Kp = 17408, 1024                      # 1088 row-blocks of counters
+    qp, sp = workloads.raw_packed(r, Np, Kp, g)
+    xp = workloads.activations(r, 1, Kp)
+    nb = max(lib.w4a16_linear_gated_workspace_bytes(M, N, K, g), lib.w4a16_workspace_bytes(1, Np, Kp, g, 1))
+    ws = torch.empty(nb, dtype=torch.uint8, device=cuda_device)
+    st = w4._stream(cuda_device)
+    assert lib.w4a16_workspace_init(w4._ptr(ws), nb, st) == 0
+    d = [to_dev(t, cuda_device) for t in (x, qg, sg.view(np.float16), qu, su.view(np.float16))]
+    y = torch.empty((M, N), dtype=torch.float16, device=cuda_device)
+    assert lib.w4a16_linear_gated(*(w4._ptr(t) for t in d), w4._ptr(y), M, N, K, g, w4._ptr(ws), nb, st) == 0
+    dp = [to_dev(t, cuda_device) for t in (xp, qp, sp)]
+    yp = torch.empty((1, Np), dtype=torch.float16, device=cuda_device)
+    assert lib.w4a16_linear(*(w4._ptr(t) for t in dp), w4._ptr(yp), 1, Np, Kp, g, w4._ptr(ws), nb, st) == 0
+    w4.device_status()
+    _check(y.cpu().numpy(), x, qg, sg, qu, su, g, "gated on a shared workspace")
+    y_ref, a = oracle.linear(xp, qp, sp, g, threads=8)
+    from helpers import assert_within_bound
+    assert_within_bound(yp.cpu().numpy(), y_ref, a, "plain GEMV after the gated call")

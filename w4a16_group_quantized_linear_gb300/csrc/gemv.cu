@@ -148,23 +148,13 @@ __device__ __forceinline__ uint2 ld_l2_v2(const void* p) {
     asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
     return v;
 }
-// Shared-memory loads by 32-bit shared address (the offsets fold into the
-// instruction); volatile keeps them after the barrier wait that guards them.
-__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ uint2 lds_v2(uint32_t a) {
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-    return v;
-}
+// Shared-memory loads as plain C++ loads: the compiler may schedule them
+// freely between the barriers that order them (the slot's "full" wait before,
+// the warp sync and the slot release after, both compiler memory barriers),
+// so the loads of one step overlap the MMAs of the previous one.
+__device__ __forceinline__ uint4 lds_v4(const uint8_t* a) { return *reinterpret_cast<const uint4*>(a); }
+__device__ __forceinline__ uint2 lds_v2(const uint8_t* a) { return *reinterpret_cast<const uint2*>(a); }
+__device__ __forceinline__ uint32_t lds_u32(const uint8_t* a) { return *reinterpret_cast<const uint32_t*>(a); }
 __device__ __forceinline__ uint32_t ld_l2_u16(const uint16_t* p) {
     unsigned short v;
     asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p));
@@ -256,10 +246,10 @@ __device__ __forceinline__ void load_scales(UnitScales<G>& sc, const GemvArgs& p
 // Scales from the unit's TMA box in its slot (rows and groups outside the
 // tensor were filled with zeros by the copy).
 template <int G>
-__device__ __forceinline__ void load_scales_smem(UnitScales<G>& sc, uint32_t box, int ku, int gid) {
+__device__ __forceinline__ void load_scales_smem(UnitScales<G>& sc, const uint8_t* box, int ku, int gid) {
     constexpr int GPU = kUnitK / G;
-    const uint32_t r0 = box + gid * (kScaleBox<G> * 2) + ((ku * GPU) % kScaleBox<G>) * 2;
-    const uint32_t r1 = r0 + 8 * (kScaleBox<G> * 2);
+    const uint8_t* r0 = box + gid * (kScaleBox<G> * 2) + ((ku * GPU) % kScaleBox<G>) * 2;
+    const uint8_t* r1 = r0 + 8 * (kScaleBox<G> * 2);
     if constexpr (GPU == 4) {
         const uint2 a = lds_v2(r0), b = lds_v2(r1);
         sc.lo[0] = a.x; sc.lo[1] = a.y;
@@ -279,14 +269,14 @@ __device__ __forceinline__ float half_bits(uint32_t w, int h) {
 }
 
 // One unit from its ring slot: for every 128-k step and scale group, the
-// quad's share of rows gid and gid+8. `wlane` is the shared address of this
-// lane's first weight bytes in the slot (row gid, its quad's offset). XS: x
-// comes from shared memory at xlane[t] (this lane's 16-byte chunk of the
-// unit's x for token 8t+gid, or of the zero block for lanes without a token),
-// so no load is predicated and every offset below is a constant.
+// quad's share of rows gid and gid+8. `wlane` points at this lane's first
+// weight bytes in the slot (row gid, its quad's offset). XS: x comes from
+// shared memory at xlane[t] (this lane's 16-byte chunk of the unit's x for
+// token 8t+gid, or of the zero block for lanes without a token), so no load
+// is predicated and every offset below is a constant.
 template <int G, int NT, bool XS>
-__device__ __forceinline__ void compute_unit(uint32_t wlane, const UnitScales<G>& sc, const GemvArgs& p,
-                                             const uint32_t (&xlane)[NT], int ku, int gid, int t4,
+__device__ __forceinline__ void compute_unit(const uint8_t* wlane, const UnitScales<G>& sc, const GemvArgs& p,
+                                             const uint8_t* const (&xlane)[NT], int ku, int gid, int t4,
                                              float (&acc)[NT][4]) {
     constexpr int WPP = G / 32;      // words per thread per row per group
     constexpr int GPS = kStepK / G;  // groups per step
@@ -295,8 +285,8 @@ __device__ __forceinline__ void compute_unit(uint32_t wlane, const UnitScales<G>
 #pragma unroll
         for (int j = 0; j < GPS; ++j) {
             uint32_t wa[WPP], wb[WPP];
-            const uint32_t ra = wlane + step * (kRows * 64) + j * (G / 2);
-            const uint32_t rbp = ra + 8 * 64;
+            const uint8_t* ra = wlane + step * (kRows * 64) + j * (G / 2);
+            const uint8_t* rbp = ra + 8 * 64;
             if constexpr (WPP == 4) {
                 const uint4 a = lds_v4(ra), b = lds_v4(rbp);
                 wa[0] = a.x; wa[1] = a.y; wa[2] = a.z; wa[3] = a.w;
@@ -391,7 +381,7 @@ __device__ __forceinline__ void finish_row_block(const GemvArgs& p, const GatedA
     old = __shfl_sync(0xffffffffu, old, 0);
     if (old == 0) return;  // the other half finishes the pair
     __syncwarp();  // every lane's loads below come after lane 0's acquire
-    const float* other = ga.gres + (mat ^ 1) * half;
+    float* other = ga.gres + (mat ^ 1) * half;
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -403,6 +393,10 @@ __device__ __forceinline__ void finish_row_block(const GemvArgs& p, const GatedA
                 const float g = mat == 0 ? v[t][i] : o, u = mat == 0 ? o : v[t][i];
                 const float silu = g / (1.0f + expf(-g));
                 p.y[(int64_t)m * p.N + n] = __half_as_ushort(__float2half_rn(silu * u));
+                // both halves are consumed: return the parking area to zero, so the
+                // workspace is all zero between calls (a plain GEMV may reuse it)
+                __stcg(mine + (int64_t)m * p.N + n, 0.0f);
+                __stcg(other + (int64_t)m * p.N + n, 0.0f);
             }
         }
     if (lane == 0) ga.pair[rb] = 0;
@@ -560,7 +554,8 @@ template <int G, int NT, bool XS, bool TS, bool GT>
 __device__ __forceinline__ void gemv_body(const MapPtrs& maps, const GemvArgs& p, const GatedArgs& ga) {
     constexpr int SLOT = kSlotBytes<G, TS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned start, by pointer arithmetic so the pointers stay shared-space
+    uint8_t* ring = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     Bars* bars = reinterpret_cast<Bars*>(ring + kConsumers * kSlots * SLOT);
     uint8_t* xs = reinterpret_cast<uint8_t*>(bars) + ((sizeof(Bars) + 127) & ~(size_t)127);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
@@ -642,15 +637,16 @@ __device__ __forceinline__ void gemv_body(const MapPtrs& maps, const GemvArgs& p
     for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
     // shared address of this lane's x chunk in unit 0 (the zero block for lanes
     // without a token) and its stride per unit
-    uint32_t xlane0[NT], xunit[NT];
+    const uint8_t* xlane0[NT];
+    int xunit[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         const bool has = 8 * t + gid < p.M;
-        xlane0[t] = (has ? ptx::smem_u32(xs) + (8 * t + gid) * (uint32_t)xstride : ptx::smem_u32(bars->zero)) + t4 * 16;
+        xlane0[t] = (has ? xs + (8 * t + gid) * xstride : bars->zero) + t4 * 16;
         xunit[t] = has ? kUnitSteps * kStepK * 2 : 0;
     }
-    const uint32_t slot0 = ptx::smem_u32(ring) + cw * (kSlots * SLOT);
-    const uint32_t wlane = gid * 64 + t4 * (G / 8);
+    const uint8_t* slot0 = ring + cw * (kSlots * SLOT);
+    const int wlane = gid * 64 + t4 * (G / 8);
 
     int sl = 0;
     uint32_t phase = 0;
@@ -665,7 +661,7 @@ __device__ __forceinline__ void gemv_body(const MapPtrs& maps, const GemvArgs& p
             nku = 0;
             ++nrb;
         }
-        const uint32_t slot = slot0 + sl * SLOT;
+        const uint8_t* slot = slot0 + sl * SLOT;
         UnitScales<G> sc_next;
         ScaleRows nsr = sr;
         if (TS) {
@@ -674,7 +670,7 @@ __device__ __forceinline__ void gemv_body(const MapPtrs& maps, const GemvArgs& p
             if (nku == 0) nsr = scale_rows<GT>(p, ga, nrb, gid);
             if (r + 1 < n_units) load_scales<G>(sc_next, p, nsr, nku);
         }
-        uint32_t xlane[NT];
+        const uint8_t* xlane[NT];
 #pragma unroll
         for (int t = 0; t < NT; ++t) xlane[t] = xlane0[t] + ku * xunit[t];
         compute_unit<G, NT, XS>(slot + wlane, sc, p, xlane, ku, gid, t4, acc);
@@ -752,11 +748,17 @@ template <int G, int NT, bool XS, bool TS, bool GT>
 w4a16_status launch_one(const DeviceInfo& dev, const CUtensorMap (&map)[4], const GemvArgs& a, const GatedArgs& ga,
                         unsigned blocks, size_t smem, cudaStream_t st) {
     static PerDeviceOnce once;
-    const cudaError_t attr = once.run(dev.device, [&dev] {  // the device's opt-in maximum; each launch checks its own size
-        return GT ? cudaFuncSetAttribute(gemv_gated_kernel<G, NT, XS, TS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)dev.smem_optin)
-                  : cudaFuncSetAttribute(gemv_kernel<G, NT, XS, TS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)dev.smem_optin);
+    const cudaError_t attr = once.run(dev.device, [&dev] {
+        const void* fn = GT ? reinterpret_cast<const void*>(gemv_gated_kernel<G, NT, XS, TS>)
+                            : reinterpret_cast<const void*>(gemv_kernel<G, NT, XS, TS>);
+        // the device's opt-in maximum (each launch checks its own size), and the
+        // largest shared-memory carveout for every GEMV: consecutive GEMVs of any
+        // shape then need no reconfiguration of an SM between them, so the next
+        // launch's block can take an SM the moment the previous one leaves it
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dev.smem_optin);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+        return e;
     });
     if (attr != cudaSuccess) return cuda_status(attr, "gemv: cudaFuncSetAttribute");
     cudaLaunchConfig_t cfg = {};

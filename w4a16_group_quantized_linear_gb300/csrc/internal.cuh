@@ -48,10 +48,11 @@ __device__ __forceinline__ void nibbles_to_half2(uint32_t v, uint32_t& h04, uint
     h37 = *reinterpret_cast<uint32_t*>(&r3);
 }
 
-// D = A * B + C, m16n8k16, fp16 inputs, fp32 accumulators (register operands).
+// D = A * B + C, m16n8k16, fp16 inputs, fp32 accumulators (register operands;
+// not volatile: a pure function of its operands, free to be scheduled).
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -62,7 +63,7 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 __device__ __forceinline__ void mma_16816_zero(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
     const float z = 0.0f;
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -80,7 +81,7 @@ struct DeviceInfo {
     int device;
     int sms;
     int cc_major, cc_minor;
-    size_t smem_optin;
+    size_t smem_optin;                // largest dynamic shared memory a block may opt in to
     unsigned int* error_word;  // device address of the sticky error word
 };
 
