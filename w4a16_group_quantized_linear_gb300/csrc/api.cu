@@ -292,17 +292,19 @@ w4a16_status w4a16_moe_combine(const uint16_t* y_sorted, int64_t R, const int32_
 // GEMV and the GEMM (synchronous), and read the GEMM's TMEM counters.
 W4A16_API w4a16_status w4a16_test_set_hooks(uint64_t wait_limit_ns, int32_t issue_limit) {
     const TestHooks h{(unsigned long long)wait_limit_ns, (int)issue_limit};
-    const w4a16_status a = cuda_status(gemv_set_test_hooks(h), "test hooks (gemv)");
-    if (a != W4A16_OK) return a;
-    return cuda_status(gemm_set_test_hooks(h), "test hooks (gemm)");
+    w4a16_status a = cuda_status(gemv_set_test_hooks(h), "test hooks (gemv)");
+    if (a == W4A16_OK) a = cuda_status(gemm_set_test_hooks(h), "test hooks (gemm)");
+    if (a == W4A16_OK) a = cuda_status(split_set_test_hooks(h), "test hooks (gemm g32)");
+    return a;
 }
 
 W4A16_API w4a16_status w4a16_test_tmem_counters(uint64_t* allocs, uint64_t* frees) {
-    TestCounters c{};
-    const w4a16_status a = cuda_status(gemm_get_test_counters(&c), "test counters");
+    TestCounters c{}, d{};
+    w4a16_status a = cuda_status(gemm_get_test_counters(&c), "test counters");
+    if (a == W4A16_OK) a = cuda_status(split_get_test_counters(&d), "test counters (gemm g32)");
     if (a != W4A16_OK) return a;
-    *allocs = c.tmem_allocs;
-    *frees = c.tmem_frees;
+    *allocs = c.tmem_allocs + d.tmem_allocs;
+    *frees = c.tmem_frees + d.tmem_frees;
     return W4A16_OK;
 }
 #endif

@@ -137,6 +137,12 @@ w4a16_status gemm_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
                          const uint16_t* s, uint16_t* y, int64_t M, int64_t N, int64_t K,
                          int group, const int32_t* expert_offsets, int E, cudaStream_t st);
 
+// Tensor-core GEMM for group 32 with the scale split exactly into the A operand
+// (routed experts and dense layers): supported for E <= 4096 experts.
+bool split_supports(int group, int E);
+w4a16_status split_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s, uint16_t* y,
+                          int64_t M, int64_t N, int64_t K, const int32_t* expert_offsets, int E, cudaStream_t st);
+
 // Routed-MoE router, dispatch (permutation + gather) and combine.
 w4a16_status moe_route_launch(const float* logits, int64_t T, int E, int top_k, bool renormalize, int32_t* ids,
                               float* weights, cudaStream_t st);
@@ -165,6 +171,8 @@ struct TestCounters {
 cudaError_t gemv_set_test_hooks(const TestHooks& h);
 cudaError_t gemm_set_test_hooks(const TestHooks& h);
 cudaError_t gemm_get_test_counters(TestCounters* c);
+cudaError_t split_set_test_hooks(const TestHooks& h);
+cudaError_t split_get_test_counters(TestCounters* c);
 #endif
 
 // Records a failed CUDA runtime call for w4a16_last_cuda_error (per host thread).

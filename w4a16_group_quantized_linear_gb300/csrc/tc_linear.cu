@@ -636,6 +636,11 @@ w4a16_status gemm_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
                          int64_t M, int64_t N, int64_t K, int group, const int32_t* expert_offsets, int E,
                          cudaStream_t st) {
     if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
+    // group 32 (routed experts, and dense tiles of 128 tokens): the scale goes
+    // into the A operand as an exact fp16 pair (tc_split.cu), with no per-group
+    // epilogue round trip
+    if (split_supports(group, expert_offsets != nullptr ? E : 1) && (expert_offsets != nullptr || M > 64))
+        return split_launch(dev, x, qw, s, y, M, N, K, expert_offsets, E, st);
     const int bn = expert_offsets != nullptr ? 0 : (M > 64 ? 128 : (M > 32 ? 64 : 32));
 #define W4A16_GEMM(CFG)                                                                              \
     switch (group) {                                                                                 \
