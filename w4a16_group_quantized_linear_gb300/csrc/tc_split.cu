@@ -24,24 +24,29 @@
 // while they stay normal fp16 numbers) and its result multiplied by 2^e.
 //
 // Formulation ("swap AB", as in tc_linear.cu): D[n, m] = sum_k W^[n, k] x[m, k].
-// Persistent: one CTA per SM walks the tiles (expert, 128-token tile, 128-row
+// Persistent: one CTA per SM walks the tiles (expert, token tile, 128-row
 // weight tile) t = blockIdx.x, blockIdx.x + gridDim.x, ... with the weight-row
-// tile fastest (the tiles that share an x tile run side by side). TMEM is
-// allocated once; two accumulators let tile i's epilogue overlap tile i+1's
-// MMAs; the producer and the dequant warps run ahead across tile boundaries.
-// The last token tile of an expert issues MMAs only as wide as its rows
-// (rounded up to 16).
+// tile fastest (the tiles that share an x tile run side by side). A token tile
+// holds up to 256 tokens: the MMA issue rate, not the tensor math, bounds
+// narrow MMAs, so each expert's rows are split evenly over as few tiles as
+// possible (260 rows: 144 + 116, not 256 + 4) and each tile's MMAs are only as
+// wide as its rows (rounded up to 16). TMEM is allocated once; the producer
+// and the dequant warps run ahead across tile boundaries; the epilogue reads
+// the accumulator into registers and releases it before it stores, so the
+// next tile's MMAs start at once.
 //
 //   warp 0      TMA producer: the packed weights of each 128-k stage
 //               (128 rows x 64 B, 64-byte swizzle) into a 4-deep ring, and
-//               the stage's x (two boxes of 128 tokens x 64 k, 128-byte
+//               the stage's x (two boxes of 256 tokens x 64 k, 128-byte
 //               swizzle) into a 2-deep ring.
 //   warp 1      TMEM allocation and the MMA issuer (one lane).
 //   warps 2-5   dequant: thread = TMEM lane = weight row; turns each 32-k
 //               group into hi and lo and writes them to the stage's TMEM A
-//               columns (tcgen05.st).
-//   warps 6-9   epilogue: per tile, tcgen05.ld of the accumulator, times 2^e,
-//               rounded once to fp16, stored.
+//               columns (tcgen05.st); the scales of the next stage are loaded
+//               one stage ahead.
+//   warps 6-13  epilogue: two threads per weight row (= TMEM lane), each
+//               reading half of the tile's tokens from the accumulator,
+//               times 2^e, rounded once to fp16, stored.
 // Every mbarrier wait is bounded in time; a wait that gives up records
 // W4A16_ERR_TIMEOUT and the CTA unwinds (drains its copies and MMAs, frees TMEM).
 #include <cudaTypedefs.h>
@@ -56,22 +61,26 @@ namespace {
 
 constexpr int kG = 32;                               // scale group of this kernel
 constexpr int kRows = 128;                           // weight rows per tile: MMA M, TMEM lanes
-constexpr int kBN = 128;                             // tokens per tile: MMA N at most
+constexpr int kBN = 256;                             // tokens per tile: MMA N at most
 constexpr int kKS = 128;                             // k per pipeline stage
 constexpr int kGroupsPerStage = kKS / kG;            // 4
 constexpr int kPStages = 4;                          // packed-weight ring
-constexpr int kXStages = 2;                          // x ring = TMEM A stages
+constexpr int kXStages = 2;                          // x ring (shared memory)
+constexpr int kAStages = 2;                          // TMEM A stages
 constexpr int kPBytes = kRows * kKS / 2;             // 8 KB
-constexpr int kXBoxBytes = kBN * 128;                // 64 k x 128 tokens, 128-byte swizzle
+constexpr int kXBoxBytes = kBN * 128;                // 64 k x 256 tokens, 128-byte swizzle
 constexpr int kXBytes = (kKS / 64) * kXBoxBytes;     // 32 KB
 constexpr int kMaxE = 4096;                          // experts (two ints each in shared memory)
-constexpr int kDeqWarps = 4;
-constexpr int kEpiWarps = 4;
+constexpr int kDeqWarps = 4;                         // one thread per weight row
+constexpr int kDeqParts = kDeqWarps / 4;
+constexpr int kPartGroups = kGroupsPerStage / kDeqParts;  // groups of a stage per dequant thread
+constexpr int kEpiWarps = 8;                         // two threads per weight row
+constexpr int kEpiCols = kBN / (kEpiWarps / 4);      // accumulator columns per epilogue thread
 constexpr int kThreads = (2 + kDeqWarps + kEpiWarps) * 32;
-// TMEM columns: accumulators [0, 128) and [128, 256); A stage s at 256 + 128 s:
-// hi in its first 64 columns, lo in the next 64 (two fp16 k per column)
+// TMEM columns: the accumulator [0, 256); A stage s at 256 + 128 s: hi in its
+// first 64 columns, lo in the next 64 (two fp16 k per column)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAColBase = 2 * kBN;
+constexpr uint32_t kAColBase = kBN;
 constexpr uint32_t kAStageCols = kKS;
 constexpr uint32_t kAHalfCols = kKS / 2;
 constexpr float kMaxUnshifted = 8188.0f;             // |s| <= 8188 keeps |s q| <= 65504 for |q| <= 8
@@ -105,10 +114,11 @@ struct SplitSmem {
     uint64_t pfull[kPStages];   // a packed-weight stage landed
     uint64_t pempty[kPStages];  // the dequant warps finished reading it
     uint64_t xfull[kXStages];   // an x stage landed
-    uint64_t xempty[kXStages];  // the MMAs reading an x stage and its TMEM A stage finished
-    uint64_t afull[kXStages];   // a TMEM A stage was written
-    uint64_t dfull[2];          // accumulator b holds a finished tile
-    uint64_t dempty[2];         // the epilogue has read accumulator b
+    uint64_t xempty[kXStages];  // the MMAs reading an x stage finished
+    uint64_t afull[kAStages];   // a TMEM A stage was written
+    uint64_t aempty[kAStages];  // the MMAs reading a TMEM A stage finished
+    uint64_t dfull;             // the accumulator holds a finished tile
+    uint64_t dempty;            // the epilogue has read the accumulator
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort;
@@ -126,6 +136,12 @@ __device__ __forceinline__ void fail(const SplitArgs& a, SplitSmem* sm, unsigned
     *reinterpret_cast<volatile int*>(&sm->abort) = 1;
 }
 
+// An expert's token tiles: as few as hold its rows (at most kBN each), all of
+// one size, a multiple of 16 (the last one takes what remains).
+__device__ __forceinline__ int tile_tokens(int rows, int tiles) {
+    return ((rows + tiles - 1) / tiles + 15) & ~15;
+}
+
 // Tile t: token tile t / ntn (over the experts in order), weight-row tile t % ntn.
 __device__ __forceinline__ Tile decode_tile(const SplitSmem* sm, int t, int ntn, int E) {
     const int tt = t / ntn;
@@ -135,10 +151,12 @@ __device__ __forceinline__ Tile decode_tile(const SplitSmem* sm, int t, int ntn,
         if (sm->first_tile[mid] <= tt) lo = mid;
         else hi = mid - 1;
     }
+    const int rows_e = sm->row_start[lo + 1] - sm->row_start[lo];
+    const int size = tile_tokens(rows_e, sm->first_tile[lo + 1] - sm->first_tile[lo]);
     Tile r;
     r.e = lo;
-    r.row0 = sm->row_start[lo] + (tt - sm->first_tile[lo]) * kBN;
-    r.rows = min(kBN, sm->row_start[lo + 1] - r.row0);
+    r.row0 = sm->row_start[lo] + (tt - sm->first_tile[lo]) * size;
+    r.rows = min(size, sm->row_start[lo + 1] - r.row0);
     r.n0 = (t % ntn) * kRows;
     return r;
 }
@@ -162,7 +180,7 @@ __device__ void plan_tiles(const SplitArgs& a, SplitSmem* sm, int lane) {
                 hi = (int)a.M;
             }
             if (hi < lo || lo < 0 || (int64_t)hi > a.M) ok = false;
-            tiles = hi > lo ? (hi - lo + kBN - 1) / kBN : 0;
+            tiles = hi > lo ? (hi - lo + kBN - 1) / kBN : 0;  // as few as hold its rows
         }
         int incl = tiles;
 #pragma unroll
@@ -233,12 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < kXStages; ++i) {
                 ptx::mbar_init(&sm->xfull[i], 1);
                 ptx::mbar_init(&sm->xempty[i], 1);
+            }
+            for (int i = 0; i < kAStages; ++i) {
                 ptx::mbar_init(&sm->afull[i], kDeqWarps * 32);
+                ptx::mbar_init(&sm->aempty[i], 1);
             }
-            for (int b = 0; b < 2; ++b) {
-                ptx::mbar_init(&sm->dfull[b], 1);
-                ptx::mbar_init(&sm->dempty[b], kEpiWarps * 32);
-            }
+            ptx::mbar_init(&sm->dfull, 1);
+            ptx::mbar_init(&sm->dempty, kEpiWarps * 32);
             ptx::mbar_init(&sm->mma_done, 1);
             sm->abort = 0;
             ptx::fence_mbar_init();
@@ -339,19 +358,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             int64_t c = 0;
             for (int j = 0; ok && j < my_tiles; ++j) {
                 const Tile tl = decode_tile(sm, (int)blockIdx.x + j * (int)gridDim.x, ntn, a.E);
-                const int b = j & 1;
-                if (j >= 2 && !ptx::mbar_wait(&sm->dempty[b], (uint32_t)(((j >> 1) - 1) & 1), abort, wait_limit())) {
+                if (j >= 1 && !ptx::mbar_wait(&sm->dempty, (uint32_t)((j - 1) & 1), abort, wait_limit())) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t idesc = ptx::idesc_f16_f32(kRows, (tl.rows + 15) & ~15);
-                const uint32_t d = tmem + (uint32_t)(b * kBN);
+                const uint32_t d = tmem;
                 for (int s = 0; s < nst; ++s, ++c) {
-                    const int xs = (int)(c % kXStages);
-                    const uint32_t par = (uint32_t)((c / kXStages) & 1);
-                    if (!ptx::mbar_wait(&sm->xfull[xs], par, abort, wait_limit()) ||
-                        !ptx::mbar_wait(&sm->afull[xs], par, abort, wait_limit())) {
+                    const int xs = (int)(c % kXStages), as = (int)(c % kAStages);
+                    if (!ptx::mbar_wait(&sm->xfull[xs], (uint32_t)((c / kXStages) & 1), abort, wait_limit()) ||
+                        !ptx::mbar_wait(&sm->afull[as], (uint32_t)((c / kAStages) & 1), abort, wait_limit())) {
                         ok = false;
                         break;
                     }
@@ -359,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int64_t kc = (int64_t)s * kKS;
                     const int nk = (int)((a.K - kc < kKS ? a.K - kc : kKS) >> 4);
                     const uint64_t bdesc0 = ptx::smem_desc_sw128(ptx::smem_u32(xring + xs * kXBytes));
-                    const uint32_t a_hi = tmem + kAColBase + (uint32_t)xs * kAStageCols;
+                    const uint32_t a_hi = tmem + kAColBase + (uint32_t)as * kAStageCols;
                     const uint32_t a_lo = a_hi + kAHalfCols;
 #pragma unroll
                     for (int kk = 0; kk < kKS / 16; ++kk) {
@@ -368,10 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::mma_f16_ts(d, a_hi + (uint32_t)(kk * 8), bdesc, idesc, (s | kk) ? 1u : 0u);
                         ptx::mma_f16_ts(d, a_lo + (uint32_t)(kk * 8), bdesc, idesc, 1u);
                     }
-                    ptx::mma_commit(&sm->xempty[xs]);  // x slot and TMEM A stage are free again
+                    ptx::mma_commit(&sm->xempty[xs]);  // the x slot is free again
+                    ptx::mma_commit(&sm->aempty[as]);  // and the TMEM A stage
                 }
                 if (!ok) break;
-                ptx::mma_commit(&sm->dfull[b]);  // the tile's accumulator is complete
+                ptx::mma_commit(&sm->dfull);  // the tile's accumulator is complete
             }
             if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
             ptx::mma_commit(&sm->mma_done);
@@ -380,8 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < 2 + kDeqWarps) {
         // -------------------------------------------------------------- dequant
-        const int quad = warp & 3;      // TMEM lane quadrant of this warp
-        const int r = quad * 32 + lane; // weight row in the tile = TMEM lane
+        const int quad = warp & 3;                // TMEM lane quadrant of this warp
+        const int part = (warp - 2) >> 2;         // which groups of each stage
+        const int r = quad * 32 + lane;           // weight row in the tile = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         bool ok = true;
         int64_t c = 0;
@@ -391,32 +410,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool n_ok = n < a.N;
             const uint16_t* srow = a.s + ((int64_t)tl.e * a.N + (n_ok ? n : 0)) * gk;
             const float f = row_shift(srow, gk, n_ok);
-            for (int s = 0; s < nst; ++s, ++c) {
-                const int ps = (int)(c % kPStages), xs = (int)(c % kXStages);
-                // this stage's scales go out before the waits
-                const int g0 = s * kGroupsPerStage;
-                const int ng = min(kGroupsPerStage, gk - g0);
-                float sc[kGroupsPerStage];
+            // this thread's scales of a stage (0 past the row), one stage ahead
+            auto load_scales = [&](int s_, uint32_t (&dst)[kPartGroups]) {
 #pragma unroll
-                for (int gi = 0; gi < kGroupsPerStage; ++gi)
-                    sc[gi] = gi < ng ? __half2float(__ushort_as_half(__ldg(srow + g0 + gi))) * f : 0.0f;
+                for (int i = 0; i < kPartGroups; ++i) {
+                    const int g = s_ * kGroupsPerStage + part * kPartGroups + i;
+                    dst[i] = (s_ < nst && g < gk) ? (uint32_t)__ldg(srow + g) : 0u;
+                }
+            };
+            uint32_t sc[kPartGroups], sc_next[kPartGroups];
+            load_scales(0, sc);
+            for (int s = 0; s < nst; ++s, ++c) {
+                const int ps = (int)(c % kPStages), as = (int)(c % kAStages);
+                load_scales(s + 1, sc_next);
+                const int g0 = s * kGroupsPerStage + part * kPartGroups;
+                const int ng = min(kPartGroups, gk - g0);  // this thread's groups in the stage
                 const bool got =
                     ptx::mbar_wait(&sm->pfull[ps], (uint32_t)((c / kPStages) & 1), abort, wait_limit()) &&
-                    (c < kXStages ||
-                     ptx::mbar_wait(&sm->xempty[xs], (uint32_t)((c / kXStages - 1) & 1), abort, wait_limit()));
+                    (c < kAStages ||
+                     ptx::mbar_wait(&sm->aempty[as], (uint32_t)((c / kAStages - 1) & 1), abort, wait_limit()));
                 if (!__all_sync(0xffffffffu, got)) {  // warp-uniform: the TMEM stores are .sync.aligned
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint8_t* prow = pring + ps * kPBytes;
-                const uint32_t acol = lane_base + kAColBase + (uint32_t)xs * kAStageCols;
+                const uint32_t acol = lane_base + kAColBase + (uint32_t)as * kAStageCols;
 #pragma unroll
-                for (int gi = 0; gi < kGroupsPerStage; ++gi) {
-                    if (gi >= ng) break;  // uniform: every lane has the same groups
+                for (int i = 0; i < kPartGroups; ++i) {
+                    if (i >= ng) break;  // uniform: every lane has the same groups
+                    const int gi = part * kPartGroups + i;  // group within the stage
                     const uint4 pk = *reinterpret_cast<const uint4*>(prow + packed_offset(r, gi));
                     const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
-                    const __half2 s2 = __float2half2_rn(sc[gi]);  // exact: a (shifted) fp16 scale
+                    // exact: a (shifted) fp16 scale
+                    const __half2 s2 = __float2half2_rn(__half2float(__ushort_as_half((unsigned short)sc[i])) * f);
                     uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {  // word w holds k = 8w .. 8w+7 of the group
@@ -425,12 +452,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t q[4] = {__byte_perm(h04, h15, 0x5410), __byte_perm(h26, h37, 0x5410),
                                                __byte_perm(h04, h15, 0x7632), __byte_perm(h26, h37, 0x7632)};
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const __half2 qh = *reinterpret_cast<const __half2*>(&q[i]);
+                        for (int k2 = 0; k2 < 4; ++k2) {
+                            const __half2 qh = *reinterpret_cast<const __half2*>(&q[k2]);
                             const __half2 h = __hmul2(s2, qh);                 // fp16_rn(s q)
                             const __half2 l = __hfma2(s2, qh, __hneg2(h));     // s q - hi, exact
-                            hi[4 * w + i] = *reinterpret_cast<const uint32_t*>(&h);
-                            lo[4 * w + i] = *reinterpret_cast<const uint32_t*>(&l);
+                            hi[4 * w + k2] = *reinterpret_cast<const uint32_t*>(&h);
+                            lo[4 * w + k2] = *reinterpret_cast<const uint32_t*>(&l);
                         }
                     }
                     ptx::tmem_st_32x32b_x16(acol + (uint32_t)(gi * 16), hi);
@@ -439,45 +466,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mbar_arrive(&sm->pempty[ps]);  // this thread has read its packed bytes
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(&sm->afull[xs]);
+                ptx::mbar_arrive(&sm->afull[as]);
+#pragma unroll
+                for (int i = 0; i < kPartGroups; ++i) sc[i] = sc_next[i];
             }
         }
         if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
     } else {
         // ------------------------------------------------------------- epilogue
         const int quad = warp & 3;
-        const int r = quad * 32 + lane;  // weight row in the tile = TMEM lane
-        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const int half = (warp - 2 - kDeqWarps) >> 2;  // which tokens of the tile
+        const int r = quad * 32 + lane;                // weight row in the tile = TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * kEpiCols);
         bool ok = true;
         for (int j = 0; ok && j < my_tiles; ++j) {
             const Tile tl = decode_tile(sm, (int)blockIdx.x + j * (int)gridDim.x, ntn, a.E);
-            const int b = j & 1;
             const int64_t n = (int64_t)tl.n0 + r;
             const bool n_ok = n < a.N;
+            const int m0 = half * kEpiCols;                          // first token of this thread's share
+            const int mine = max(0, min(kEpiCols, tl.rows - m0));    // tokens of the tile in that share
             // the row's 2^e, found while the tile's MMAs run
             const float mult = 1.0f / row_shift(a.s + ((int64_t)tl.e * a.N + (n_ok ? n : 0)) * gk, gk, n_ok);
-            if (!__all_sync(0xffffffffu,
-                            ptx::mbar_wait(&sm->dfull[b], (uint32_t)((j >> 1) & 1), abort, wait_limit()))) {
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sm->dfull, (uint32_t)(j & 1), abort, wait_limit()))) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            const uint32_t dcol = lane_base + (uint32_t)(b * kBN);
-            uint16_t* yrow = a.y + (int64_t)tl.row0 * a.N + n;
-            for (int ch = 0; ch * 32 < tl.rows; ++ch) {  // uniform: same tile in every lane
-                uint32_t v[32];
-                ptx::tmem_ld_32x32b_x32(dcol + (uint32_t)(ch * 32), v);
-                ptx::tmem_ld_wait();
-                if (n_ok) {
+            // read the accumulator (rounded to fp16 pairs), then release it for the next tile
+            uint32_t packed[kEpiCols / 2];
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj)
-                        if (ch * 32 + jj < tl.rows)
-                            yrow[(int64_t)(ch * 32 + jj) * a.N] =
-                                __half_as_ushort(__float2half_rn(__uint_as_float(v[jj]) * mult));
+            for (int ch = 0; ch < kEpiCols / 32; ++ch) {
+                if (ch * 32 < mine) {  // uniform: same tile in every lane
+                    uint32_t v[32];
+                    ptx::tmem_ld_32x32b_x32(lane_base + (uint32_t)(ch * 32), v);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const __half2 h = __floats2half2_rn(__uint_as_float(v[2 * i]) * mult,
+                                                            __uint_as_float(v[2 * i + 1]) * mult);
+                        packed[ch * 16 + i] = *reinterpret_cast<const uint32_t*>(&h);
+                    }
                 }
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&sm->dempty[b]);
+            ptx::mbar_arrive(&sm->dempty);
+            if (n_ok) {
+                uint16_t* yrow = a.y + ((int64_t)tl.row0 + m0) * a.N + n;
+#pragma unroll
+                for (int i = 0; i < kEpiCols; ++i)
+                    if (i < mine) yrow[(int64_t)i * a.N] = (uint16_t)(packed[i >> 1] >> (16 * (i & 1)));
+            }
         }
         if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
     }
