@@ -502,6 +502,49 @@ def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):
         del logits, xt, ys, xs
     except w4.W4A16Error as e:
         out["moe_dispatch"] = {"unavailable": str(e)}
+    # the whole routed layer (4096 tokens, top-8 of 128 experts, hidden 2048, expert
+    # width 512, group 32): route -> dispatch -> gate/up GEMM -> down GEMM -> combine,
+    # with the token gather as a separate copy (dispatch writes x_sorted) or fused into
+    # the gate/up GEMM's activation loads
+    try:
+        T, E, k, Kh, Ni = (workloads.MOE[key] for key in ("tokens", "E", "top_k", "hidden", "inter"))
+        gr = workloads.rng(8)
+        logits = torch.from_numpy(workloads.router_logits(gr, T, E)).to(dev)
+        xt = torch.from_numpy(workloads.activations(gr, T, Kh)).to(dev)
+        w_gu = torch.from_numpy(workloads.weights(gr, E * Ni, Kh)).to(dev)
+        q_gu, s_gu = w4.pack(w_gu, 32)
+        del w_gu
+        w_dn = torch.from_numpy(workloads.weights(gr, E * Kh, Ni)).to(dev)
+        q_dn, s_dn = w4.pack(w_dn, 32)
+        del w_dn
+        q_gu, s_gu = q_gu.view(E, Ni, Kh // 2), s_gu.view(E, Ni, Kh // 32)
+        q_dn, s_dn = q_dn.view(E, Kh, Ni // 2), s_dn.view(E, Kh, Ni // 32)
+        h = torch.empty((T * k, Ni), dtype=torch.float16, device=dev)
+        ys = torch.empty((T * k, Kh), dtype=torch.float16, device=dev)
+
+        def layer(fused):
+            ids, wts = w4.moe_route(logits, k)
+            if fused:
+                off, row_of, tok, _ = w4.moe_dispatch(ids, E)
+                w4.grouped_linear_gather(xt, tok, q_gu, s_gu, off, 32, out=h)
+            else:
+                off, row_of, tok, xs = w4.moe_dispatch(ids, E, xt)
+                w4.grouped_linear(xs, q_gu, s_gu, off, 32, out=h)
+            w4.grouped_linear(h, q_dn, s_dn, off, 32, out=ys)
+            return w4.moe_combine(ys, row_of, wts)
+
+        for name, fused in (("moe_layer_unfused", False), ("moe_layer_fused_gather", True)):
+            for i in range(3):
+                layer(fused)
+            ms = statistics.median(_time_launches(torch, lambda i: layer(fused), 20))
+            out[name] = {"T": T, "E": E, "top_k": k, "hidden": Kh, "inter": Ni, "us": ms * 1e3,
+                         "TFLOP/s": 2 * 2.0 * T * k * Kh * Ni / (ms * 1e-3) / 1e12,
+                         "steps": "route, dispatch" + ("" if fused else " with x gather") +
+                                  ", gate/up GEMM" + (" gathering x" if fused else "") + ", down GEMM, combine"}
+        w4.device_status()
+        del q_gu, s_gu, q_dn, s_dn, h, ys, xt, logits
+    except w4.W4A16Error as e:
+        out["moe_layer"] = {"unavailable": str(e)}
     return out
 
 
@@ -626,7 +669,7 @@ def oracle_other_configs(oracle):
 # ----------------------------------------------------------------- profile --
 
 PROFILE_CASES = ("decode", "decode_down", "decode_m4", "decode_gated", "prefill", "prefill_m512", "moe_gate_up",
-                 "moe_down", "moe_dispatch")
+                 "moe_down", "moe_dispatch", "moe_gate_up_gather")
 
 
 def run_profile(case: str, launches: int):
@@ -657,6 +700,17 @@ def run_profile(case: str, launches: int):
         for i in range(launches):  # four gate/up pairs in turn: successive launches miss in L2
             j = 2 * (i % 4)
             w4.linear_gated(x, *mats[j], *mats[j + 1], GROUP, out=y, static_weights=True)
+    elif case == "moe_gate_up_gather":
+        # the gate/up projection reading its rows straight from the token-major x
+        T, E, k, Kh, Ni = (workloads.MOE[key] for key in ("tokens", "E", "top_k", "hidden", "inter"))
+        logits = torch.from_numpy(workloads.router_logits(g, T, E)).to(dev)
+        xt = torch.from_numpy(workloads.activations(g, T, Kh)).to(dev)
+        qm, sm = w4.pack(torch.from_numpy(workloads.weights(g, E * Ni, Kh)).to(dev), 32)
+        qm, sm = qm.view(E, Ni, Kh // 2), sm.view(E, Ni, Kh // 32)
+        ids, _ = w4.moe_route(logits, k)
+        off, row_of, tok, _ = w4.moe_dispatch(ids, E)
+        for _ in range(launches):
+            w4.grouped_linear_gather(xt, tok, qm, sm, off, 32)
     elif case.startswith("moe"):
         Km, Nm = (2048, 512) if case == "moe_gate_up" else (512, 2048)
         W, xs, rt = workloads.moe(Km, Nm)

@@ -130,6 +130,23 @@ W4A16_API w4a16_status w4a16_grouped_linear(const uint16_t* x_sorted, const uint
                                   size_t workspace_bytes, void* stream);
 
 /*
+ * w4a16_grouped_linear with the token gather fused into the activation loads:
+ * row r of the expert-sorted activations is x[token_of_row[r]], read straight
+ * from the token-major x fp16 [T, K] (device) as the GEMM needs it, so no
+ * expert-sorted copy of x is written or read back. token_of_row int32 [R]
+ * (device) is what w4a16_moe_dispatch returns (it may then skip its own
+ * gather, K = 0). Otherwise the contract of w4a16_grouped_linear, with the
+ * same results bit for bit. Group 32 only (the routed-expert group; else
+ * W4A16_ERR_UNSUPPORTED), E <= 4096. A token id outside [0, T) sets
+ * W4A16_ERR_BAD_ROUTING in the device word and that row reads zeros.
+ * x must be 16-byte aligned; no workspace.
+ */
+W4A16_API w4a16_status w4a16_grouped_linear_gather(const uint16_t* x, int64_t T, const int32_t* token_of_row,
+                                                   const uint8_t* qweight, const uint16_t* scales,
+                                                   const int32_t* expert_offsets, uint16_t* y_sorted, int32_t E,
+                                                   int64_t R, int64_t N, int64_t K, int32_t group, void* stream);
+
+/*
  * Gate and up projections of a gated (SwiGLU) MLP fused into one decode pass:
  *   g = x * Wg^T,  u = x * Wu^T,  y[m, n] = silu(g[m, n]) * u[m, n],
  *   silu(v) = v / (1 + exp(-v)),

@@ -114,3 +114,16 @@ def test_moe_validation(lib):
     assert lib.w4a16_moe_combine(p, 8, p, p, 0, 2, 16, p, None) == 0
     assert lib.w4a16_moe_combine(p, 8, None, p, 4, 2, 16, p, None) == 1
     assert lib.w4a16_moe_combine(p, -1, p, p, 4, 2, 16, p, None) == 1
+
+
+def test_grouped_gather_validation(lib):
+    p, q = _fake(1 << 20), _fake((1 << 20) + 8)
+    # E < 1, no offsets, negative T
+    assert lib.w4a16_grouped_linear_gather(p, 64, p, p, p, p, p, 0, 16, 8, 128, 32, None) == 1
+    assert lib.w4a16_grouped_linear_gather(p, 64, p, p, p, None, p, 4, 16, 8, 128, 32, None) == 1
+    assert lib.w4a16_grouped_linear_gather(p, -1, p, p, p, p, p, 4, 16, 8, 128, 32, None) == 1
+    # misaligned x; K not a multiple of the group
+    assert lib.w4a16_grouped_linear_gather(q, 64, p, p, p, p, p, 4, 16, 8, 128, 32, None) == 3
+    assert lib.w4a16_grouped_linear_gather(p, 64, p, p, p, p, p, 4, 16, 8, 100, 32, None) == 1
+    # nothing to do
+    assert lib.w4a16_grouped_linear_gather(p, 64, p, p, p, p, p, 4, 0, 8, 128, 32, None) == 0

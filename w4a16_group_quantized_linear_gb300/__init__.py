@@ -20,7 +20,8 @@ import threading
 
 import torch
 
-__all__ = ["pack", "unpack", "linear", "linear_gated", "grouped_linear", "moe_route", "moe_dispatch", "moe_combine",
+__all__ = ["pack", "unpack", "linear", "linear_gated", "grouped_linear", "grouped_linear_gather", "moe_route",
+           "moe_dispatch", "moe_combine",
            "workspace_bytes", "device_status", "STATIC_WEIGHTS",
            "W4A16Error", "lib", "LIB_PATH", "EXPORTS", "STATUS"]
 
@@ -43,6 +44,7 @@ EXPORTS = {
                                      _P]),
     "w4a16_linear_gated_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
     "w4a16_grouped_linear": (_I32, [_P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
+    "w4a16_grouped_linear_gather": (_I32, [_P, _I64, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I32, _P]),
     "w4a16_moe_route": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "w4a16_moe_dispatch_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
     "w4a16_moe_dispatch": (_I32, [_P, _I64, _I32, _I32, _P, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -238,6 +240,36 @@ def grouped_linear(x_sorted: torch.Tensor, qweight: torch.Tensor, scales: torch.
                                       _ptr(out), E, R, N, K, group,
                                       _ptr(ws) if ws is not None else None, ws.numel() if ws is not None else 0,
                                       st), "w4a16_grouped_linear")
+    return out
+
+
+def grouped_linear_gather(x: torch.Tensor, token_of_row: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
+                          expert_offsets: torch.Tensor, group: int = 32,
+                          out: torch.Tensor | None = None) -> torch.Tensor:
+    """Routed experts reading their rows straight from the token-major x:
+    y_sorted[r] = x[token_of_row[r]] W_e^T for the expert e of row r. x fp16
+    [T, K]; token_of_row int32 [R] (from moe_dispatch); qweight uint8
+    [E, N, K/2]; scales fp16 [E, N, K/group] (group 32); expert_offsets int32
+    [E+1]. The same bits as grouped_linear on the gathered rows."""
+    _need(x, "x", torch.float16, 2)
+    _need(token_of_row, "token_of_row", torch.int32, 1)
+    _need(qweight, "qweight", torch.uint8, 3)
+    _need(scales, "scales", torch.float16, 3)
+    _need(expert_offsets, "expert_offsets", torch.int32, 1)
+    T, K = x.shape
+    R = token_of_row.shape[0]
+    E, N = qweight.shape[0], qweight.shape[1]
+    if qweight.shape[2] * 2 != K or tuple(scales.shape) != (E, N, K // group) or expert_offsets.numel() != E + 1:
+        raise ValueError("shape mismatch between x, qweight, scales and expert_offsets")
+    if out is None:
+        out = torch.empty((R, N), dtype=torch.float16, device=x.device)
+    else:
+        _need(out, "out", torch.float16, 2)
+        if tuple(out.shape) != (R, N):
+            raise ValueError("out must be [R, N]")
+    _check(lib().w4a16_grouped_linear_gather(_ptr(x), T, _ptr(token_of_row), _ptr(qweight), _ptr(scales),
+                                             _ptr(expert_offsets), _ptr(out), E, R, N, K, group,
+                                             _stream(x.device)), "w4a16_grouped_linear_gather")
     return out
 
 

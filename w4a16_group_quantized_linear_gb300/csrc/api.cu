@@ -229,6 +229,21 @@ w4a16_status w4a16_grouped_linear(const uint16_t* x_sorted, const uint8_t* qweig
     return gemm_launch(*dev, x_sorted, qweight, scales, y_sorted, R, N, K, group, expert_offsets, E, st);
 }
 
+w4a16_status w4a16_grouped_linear_gather(const uint16_t* x, int64_t T, const int32_t* token_of_row,
+                                         const uint8_t* qweight, const uint16_t* scales,
+                                         const int32_t* expert_offsets, uint16_t* y_sorted, int32_t E, int64_t R,
+                                         int64_t N, int64_t K, int32_t group, void* stream) {
+    if (E < 1 || T < 0 || !expert_offsets) return W4A16_ERR_INVALID_ARG;
+    const DeviceInfo* dev = nullptr;
+    const w4a16_status v = check_linear(x, qweight, scales, y_sorted, R, N, K, group, &dev);
+    if (v != W4A16_OK || R == 0 || N == 0) return v;
+    if (!split_supports(group, E)) return W4A16_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (K == 0) return cuda_status(cudaMemsetAsync(y_sorted, 0, (size_t)(R * N) * sizeof(uint16_t), st));
+    if (!token_of_row || T == 0) return W4A16_ERR_INVALID_ARG;
+    return split_launch(*dev, x, qweight, scales, y_sorted, R, N, K, expert_offsets, E, token_of_row, T, st);
+}
+
 namespace {
 // The current device, if it is the sm_103 part the kernels are built for.
 w4a16_status current_device(const DeviceInfo** dev) {

@@ -640,7 +640,7 @@ w4a16_status gemm_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     // into the A operand as an exact fp16 pair (tc_split.cu), with no per-group
     // epilogue round trip
     if (split_supports(group, expert_offsets != nullptr ? E : 1) && (expert_offsets != nullptr || M > 64))
-        return split_launch(dev, x, qw, s, y, M, N, K, expert_offsets, E, st);
+        return split_launch(dev, x, qw, s, y, M, N, K, expert_offsets, E, nullptr, 0, st);
     const int bn = expert_offsets != nullptr ? 0 : (M > 64 ? 128 : (M > 32 ? 64 : 32));
 #define W4A16_GEMM(CFG)                                                                              \
     switch (group) {                                                                                 \

@@ -35,10 +35,17 @@
 // the accumulator into registers and releases it before it stores, so the
 // next tile's MMAs start at once.
 //
-//   warp 0      TMA producer: the packed weights of each 128-k stage
-//               (128 rows x 64 B, 64-byte swizzle) into a 4-deep ring, and
-//               the stage's x (two boxes of 256 tokens x 64 k, 128-byte
-//               swizzle) into a 2-deep ring.
+// Pipeline stages of KS k (Pipe<KS>): 128 for long K (two TMEM A stages, a
+// 2-deep x ring of 64 KB stages, a 4-deep packed ring), 64 for short K, where a
+// tile has few stages and a deeper pipeline hides its fill (four A stages, a
+// 4-deep x ring of 32 KB, an 8-deep packed ring). Measured on the routed-expert
+// layer: gate/up (K = 2048) 119 us at 128-k stages against 139 us at 64;
+// down (K = 512) 177 us at 64-k stages against 205 us at 128.
+//
+//   warp 0      TMA producer: the packed weights of each stage (128 rows x
+//               KS/2 bytes, swizzled) and the stage's x (KS/64 boxes of 256
+//               tokens x 64 k, 128-byte swizzle) into their rings (x not with
+//               a row gather, below).
 //   warp 1      TMEM allocation and the MMA issuer (one lane).
 //   warps 2-5   dequant: thread = TMEM lane = weight row; turns each 32-k
 //               group into hi and lo and writes them to the stage's TMEM A
@@ -46,7 +53,14 @@
 //               one stage ahead.
 //   warps 6-13  epilogue: two threads per weight row (= TMEM lane), each
 //               reading half of the tile's tokens from the accumulator,
-//               times 2^e, rounded once to fp16, stored.
+//               times 2^e, rounded once to fp16, stored. With a row gather
+//               (routed experts read straight from the token-major x) these
+//               warps also fill the x ring while the tile's MMAs run: each
+//               copies 32 rows of a stage, x[token_of_row[r]], 16 bytes at a
+//               time into the swizzled layout a TMA box would have, and each
+//               lane's arrival on the stage's barrier fires when its copies
+//               land (nothing waits for them). The MMA thread fences them over
+//               to the async proxy before it reads them.
 // Every mbarrier wait is bounded in time; a wait that gives up records
 // W4A16_ERR_TIMEOUT and the CTA unwinds (drains its copies and MMAs, frees TMEM).
 #include <cudaTypedefs.h>
@@ -62,30 +76,43 @@ namespace {
 constexpr int kG = 32;                               // scale group of this kernel
 constexpr int kRows = 128;                           // weight rows per tile: MMA M, TMEM lanes
 constexpr int kBN = 256;                             // tokens per tile: MMA N at most
-constexpr int kKS = 128;                             // k per pipeline stage
-constexpr int kGroupsPerStage = kKS / kG;            // 4
-constexpr int kPStages = 4;                          // packed-weight ring
-constexpr int kXStages = 2;                          // x ring (shared memory)
-constexpr int kAStages = 2;                          // TMEM A stages
-constexpr int kPBytes = kRows * kKS / 2;             // 8 KB
 constexpr int kXBoxBytes = kBN * 128;                // 64 k x 256 tokens, 128-byte swizzle
-constexpr int kXBytes = (kKS / 64) * kXBoxBytes;     // 32 KB
 constexpr int kMaxE = 4096;                          // experts (two ints each in shared memory)
 constexpr int kDeqWarps = 4;                         // one thread per weight row
-constexpr int kDeqParts = kDeqWarps / 4;
-constexpr int kPartGroups = kGroupsPerStage / kDeqParts;  // groups of a stage per dequant thread
 constexpr int kEpiWarps = 8;                         // two threads per weight row
 constexpr int kEpiCols = kBN / (kEpiWarps / 4);      // accumulator columns per epilogue thread
 constexpr int kThreads = (2 + kDeqWarps + kEpiWarps) * 32;
-// TMEM columns: the accumulator [0, 256); A stage s at 256 + 128 s: hi in its
-// first 64 columns, lo in the next 64 (two fp16 k per column)
+// TMEM columns: the accumulator [0, 256), then the A stages: hi of a stage in
+// its first KS/2 columns, lo in the next KS/2 (two fp16 k per column)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAColBase = kBN;
-constexpr uint32_t kAStageCols = kKS;
-constexpr uint32_t kAHalfCols = kKS / 2;
 constexpr float kMaxUnshifted = 8188.0f;             // |s| <= 8188 keeps |s q| <= 65504 for |q| <= 8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s
 constexpr uint64_t kDrainLimitNs = 1000000000ull;    // 1 s
+
+// The rings of a pipeline of KS-k stages.
+template <int KS>
+struct Pipe {
+    static constexpr int kKS = KS;
+    static constexpr int kGroupsPerStage = KS / kG;
+    static constexpr int kPStages = KS == 128 ? 4 : 8;   // packed-weight ring
+    static constexpr int kXStages = KS == 128 ? 2 : 4;   // x ring (shared memory)
+    static constexpr int kAStages = KS == 128 ? 2 : 4;   // TMEM A stages
+    static constexpr int kPBytes = kRows * KS / 2;        // packed weights of a stage
+    static constexpr int kXBoxes = KS / 64;
+    static constexpr int kXBytes = kXBoxes * kXBoxBytes;
+    static constexpr uint32_t kAStageCols = KS;          // hi (KS fp16 = KS/2 columns), then lo
+    static constexpr uint32_t kAHalfCols = KS / 2;
+    static constexpr CUtensorMapSwizzle kPSwizzle = KS == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    static_assert(KS == 64 || KS == 128, "stage");
+    static_assert(kAColBase + kAStages * kAStageCols <= kTmemCols, "TMEM budget");
+
+    // byte offset of 16-byte chunk c of row r in a packed stage (rows of KS/2 bytes, swizzled)
+    __device__ static __forceinline__ int packed_offset(int r, int c) {
+        if constexpr (KS == 128) return r * 64 + ((c ^ ((r >> 1) & 3)) << 4);  // 64-byte swizzle
+        else return r * 32 + ((c ^ ((r >> 2) & 1)) << 4);                     // 32-byte swizzle
+    }
+};
 
 #ifdef W4A16_TEST_HOOKS
 __device__ TestHooks g_hooks = {kWaitLimitNs, -1};
@@ -105,35 +132,44 @@ struct SplitArgs {
     const uint16_t* s;
     uint16_t* y;
     const int32_t* offsets;  // routed experts; nullptr: dense, one expert of M rows
+    const int32_t* gather;   // token of each row: x rows come from xg [T, K]; nullptr: x by TMA
+    const uint16_t* xg;
+    int64_t T;
     int64_t M, N, K;
     int E;
     unsigned int* err;
 };
 
-struct SplitSmem {
-    uint64_t pfull[kPStages];   // a packed-weight stage landed
-    uint64_t pempty[kPStages];  // the dequant warps finished reading it
-    uint64_t xfull[kXStages];   // an x stage landed
-    uint64_t xempty[kXStages];  // the MMAs reading an x stage finished
-    uint64_t afull[kAStages];   // a TMEM A stage was written
-    uint64_t aempty[kAStages];  // the MMAs reading a TMEM A stage finished
-    uint64_t dfull;             // the accumulator holds a finished tile
-    uint64_t dempty;            // the epilogue has read the accumulator
-    uint64_t mma_done;
-    uint32_t tmem_base;
-    int abort;
+// The tile plan (filled once per CTA).
+struct TilePlan {
     int tiles;                        // token tiles over all experts (0: invalid offsets)
     int first_tile[kMaxE + 1];        // token tiles of the experts before e
     int row_start[kMaxE + 1];         // expert_offsets
+};
+
+template <class P>
+struct SplitSmem {
+    uint64_t pfull[P::kPStages];   // a packed-weight stage landed
+    uint64_t pempty[P::kPStages];  // the dequant warps finished reading it
+    uint64_t xfull[P::kXStages];   // an x stage landed
+    uint64_t xempty[P::kXStages];  // the MMAs reading an x stage finished
+    uint64_t afull[P::kAStages];   // a TMEM A stage was written
+    uint64_t aempty[P::kAStages];  // the MMAs reading a TMEM A stage finished
+    uint64_t dfull;                // the accumulator holds a finished tile
+    uint64_t dempty;               // the epilogue has read the accumulator
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+    TilePlan plan;
 };
 
 struct Tile {
     int e, row0, rows, n0;
 };
 
-__device__ __forceinline__ void fail(const SplitArgs& a, SplitSmem* sm, unsigned code) {
+__device__ __forceinline__ void fail(const SplitArgs& a, int* abort, unsigned code) {
     raise_device_error(a.err, code);
-    *reinterpret_cast<volatile int*>(&sm->abort) = 1;
+    *reinterpret_cast<volatile int*>(abort) = 1;
 }
 
 // An expert's token tiles: as few as hold its rows (at most kBN each), all of
@@ -143,20 +179,20 @@ __device__ __forceinline__ int tile_tokens(int rows, int tiles) {
 }
 
 // Tile t: token tile t / ntn (over the experts in order), weight-row tile t % ntn.
-__device__ __forceinline__ Tile decode_tile(const SplitSmem* sm, int t, int ntn, int E) {
+__device__ __forceinline__ Tile decode_tile(const TilePlan& pl, int t, int ntn, int E) {
     const int tt = t / ntn;
     int lo = 0, hi = E - 1;  // the last expert whose first token tile is <= tt
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (sm->first_tile[mid] <= tt) lo = mid;
+        if (pl.first_tile[mid] <= tt) lo = mid;
         else hi = mid - 1;
     }
-    const int rows_e = sm->row_start[lo + 1] - sm->row_start[lo];
-    const int size = tile_tokens(rows_e, sm->first_tile[lo + 1] - sm->first_tile[lo]);
+    const int rows_e = pl.row_start[lo + 1] - pl.row_start[lo];
+    const int size = tile_tokens(rows_e, pl.first_tile[lo + 1] - pl.first_tile[lo]);
     Tile r;
     r.e = lo;
-    r.row0 = sm->row_start[lo] + (tt - sm->first_tile[lo]) * size;
-    r.rows = min(size, sm->row_start[lo + 1] - r.row0);
+    r.row0 = pl.row_start[lo] + (tt - pl.first_tile[lo]) * size;
+    r.rows = min(size, pl.row_start[lo + 1] - r.row0);
     r.n0 = (t % ntn) * kRows;
     return r;
 }
@@ -164,7 +200,7 @@ __device__ __forceinline__ Tile decode_tile(const SplitSmem* sm, int t, int ntn,
 // Warp 0, at start: each expert's first token tile and first row, from the
 // device offsets (dense: one expert of M rows); an invalid partition is
 // reported and leaves no tile.
-__device__ void plan_tiles(const SplitArgs& a, SplitSmem* sm, int lane) {
+__device__ void plan_tiles(const SplitArgs& a, TilePlan& pl, int lane) {
     int base = 0;
     bool ok = true;
     for (int e0 = 0; e0 < a.E; e0 += 32) {
@@ -189,8 +225,8 @@ __device__ void plan_tiles(const SplitArgs& a, SplitSmem* sm, int lane) {
             if (lane >= d) incl += v;
         }
         if (e < a.E) {
-            sm->first_tile[e] = base + incl - tiles;
-            sm->row_start[e] = lo;
+            pl.first_tile[e] = base + incl - tiles;
+            pl.row_start[e] = lo;
         }
         base += __shfl_sync(0xffffffffu, incl, 31);
     }
@@ -198,9 +234,9 @@ __device__ void plan_tiles(const SplitArgs& a, SplitSmem* sm, int lane) {
     const int end = a.offsets ? __ldg(a.offsets + a.E) : (int)a.M;
     const bool ends_ok = (a.offsets ? __ldg(a.offsets) == 0 : true) && (int64_t)end == a.M;
     if (lane == 0) {
-        sm->first_tile[a.E] = base;
-        sm->row_start[a.E] = end;
-        sm->tiles = (ok && ends_ok) ? base : 0;
+        pl.first_tile[a.E] = base;
+        pl.row_start[a.E] = end;
+        pl.tiles = (ok && ends_ok) ? base : 0;
         if (!ok || !ends_ok) raise_device_error(a.err, W4A16_ERR_BAD_OFFSETS);
     }
 }
@@ -228,31 +264,31 @@ __device__ __forceinline__ float row_shift(const uint16_t* srow, int gk, bool ok
     return f;
 }
 
-// Byte offset of 16-byte chunk c of row r in a 64-byte-swizzled packed box.
-__device__ __forceinline__ int packed_offset(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
-
+template <int KS>
 __global__ void __launch_bounds__(kThreads, 1)
     split_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                  const SplitArgs a) {
+    using P = Pipe<KS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t* pring = base;                              // packed-weight stages
-    uint8_t* xring = base + kPStages * kPBytes;          // x stages
-    SplitSmem* sm = reinterpret_cast<SplitSmem*>(xring + kXStages * kXBytes);
+    uint8_t* pring = base;                                 // packed-weight stages
+    uint8_t* xring = base + P::kPStages * P::kPBytes;      // x stages (1024-byte aligned)
+    SplitSmem<P>* sm = reinterpret_cast<SplitSmem<P>*>(xring + P::kXStages * P::kXBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (warp == 0) {
-        plan_tiles(a, sm, lane);
+        plan_tiles(a, sm->plan, lane);
         if (lane == 0) {
-            for (int i = 0; i < kPStages; ++i) {
+            for (int i = 0; i < P::kPStages; ++i) {
                 ptx::mbar_init(&sm->pfull[i], 1);
                 ptx::mbar_init(&sm->pempty[i], kDeqWarps * 32);
             }
-            for (int i = 0; i < kXStages; ++i) {
-                ptx::mbar_init(&sm->xfull[i], 1);
+            for (int i = 0; i < P::kXStages; ++i) {
+                // TMA: one arrival with the byte count; row gather: every epilogue lane
+                ptx::mbar_init(&sm->xfull[i], a.gather ? kEpiWarps * 32 : 1);
                 ptx::mbar_init(&sm->xempty[i], 1);
             }
-            for (int i = 0; i < kAStages; ++i) {
+            for (int i = 0; i < P::kAStages; ++i) {
                 ptx::mbar_init(&sm->afull[i], kDeqWarps * 32);
                 ptx::mbar_init(&sm->aempty[i], 1);
             }
@@ -266,8 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
+    const TilePlan& plan = sm->plan;
     const int ntn = (int)((a.N + kRows - 1) / kRows);   // weight-row tiles
-    const int total = sm->tiles * ntn;
+    const int total = plan.tiles * ntn;
     if ((int)blockIdx.x >= total) return;                // nothing for this CTA (uniform)
     if (warp == 1) {
         ptx::tmem_alloc(&sm->tmem_base, kTmemCols);
@@ -279,77 +316,91 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = sm->tmem_base;
     volatile int* abort = &sm->abort;
-    const int nst = (int)((a.K + kKS - 1) / kKS);      // stages per tile
+    const int nst = (int)((a.K + KS - 1) / KS);         // stages per tile
     const int gk = (int)(a.K / kG);                     // scale groups per row
     const int my_tiles = (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int64_t stages = (int64_t)my_tiles * nst;
+    auto tile_of = [&](int j) { return decode_tile(plan, (int)blockIdx.x + j * (int)gridDim.x, ntn, a.E); };
 
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            const int64_t stages = (int64_t)my_tiles * nst;
-            int64_t ix = 0, ip = 0;  // stages issued on each ring
-            int jx = -1, jp = -1;    // the tile each ring is on
-            Tile tx{}, tp{};
-            bool ok = true;
-            uint64_t idle_since = 0;
-            while (ix < stages || ip < stages) {
-                bool moved = false;
-                if (ix < stages && may_issue(ix + ip)) {
-                    const int st = (int)(ix % kXStages);
-                    const int64_t round = ix / kXStages;
-                    if (round == 0 || ptx::mbar_try_wait(&sm->xempty[st], (uint32_t)((round - 1) & 1))) {
-                        const int j = (int)(ix / nst), s = (int)(ix % nst);
-                        if (j != jx) {
-                            tx = decode_tile(sm, (int)blockIdx.x + j * (int)gridDim.x, ntn, a.E);
-                            jx = j;
-                        }
-                        ptx::mbar_arrive_expect_tx(&sm->xfull[st], kXBytes);
+        // the warp polls together; lane 0 issues the copies
+        int64_t ix = a.gather ? stages : 0, ip = 0;  // stages issued on each ring (x: none with a gather)
+        int jx = -1, jp = -1;                        // the tile each ring is on
+        Tile tx{}, tp{};
+        bool ok = true;
+        uint64_t idle_since = 0;
+        while (ix < stages || ip < stages) {
+            bool moved = false;
+            if (ix < stages && may_issue(ix + ip)) {
+                const int st = (int)(ix % P::kXStages);
+                const int64_t round = ix / P::kXStages;
+                bool free = round == 0;
+                if (!free && lane == 0) free = ptx::mbar_try_wait(&sm->xempty[st], (uint32_t)((round - 1) & 1));
+                if (__shfl_sync(0xffffffffu, free, 0)) {
+                    const int j = (int)(ix / nst), s = (int)(ix % nst);
+                    if (j != jx) {
+                        tx = tile_of(j);
+                        jx = j;
+                    }
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(&sm->xfull[st], P::kXBytes);
 #pragma unroll
-                        for (int b = 0; b < kKS / 64; ++b)
-                            ptx::tma_load_2d(xring + st * kXBytes + b * kXBoxBytes, &tmap_x, &sm->xfull[st],
-                                             s * kKS + 64 * b, tx.row0);
-                        ++ix;
-                        moved = true;
+                        for (int b = 0; b < P::kXBoxes; ++b)
+                            ptx::tma_load_2d(xring + st * P::kXBytes + b * kXBoxBytes, &tmap_x, &sm->xfull[st],
+                                             s * KS + 64 * b, tx.row0);
                     }
+                    ++ix;
+                    moved = true;
                 }
-                if (ip < stages && may_issue(ix + ip)) {
-                    const int st = (int)(ip % kPStages);
-                    const int64_t round = ip / kPStages;
-                    if (round == 0 || ptx::mbar_try_wait(&sm->pempty[st], (uint32_t)((round - 1) & 1))) {
-                        const int j = (int)(ip / nst), s = (int)(ip % nst);
-                        if (j != jp) {
-                            tp = decode_tile(sm, (int)blockIdx.x + j * (int)gridDim.x, ntn, a.E);
-                            jp = j;
-                        }
-                        ptx::mbar_arrive_expect_tx(&sm->pfull[st], kPBytes);
+            }
+            if (ip < stages && may_issue(ix + ip)) {
+                const int st = (int)(ip % P::kPStages);
+                const int64_t round = ip / P::kPStages;
+                bool free = round == 0;
+                if (!free && lane == 0) free = ptx::mbar_try_wait(&sm->pempty[st], (uint32_t)((round - 1) & 1));
+                if (__shfl_sync(0xffffffffu, free, 0)) {
+                    const int j = (int)(ip / nst), s = (int)(ip % nst);
+                    if (j != jp) {
+                        tp = tile_of(j);
+                        jp = j;
+                    }
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(&sm->pfull[st], P::kPBytes);
                         if (a.offsets == nullptr)
-                            ptx::tma_load_2d(pring + st * kPBytes, &tmap_w, &sm->pfull[st], s * (kKS / 2), tp.n0);
+                            ptx::tma_load_2d(pring + st * P::kPBytes, &tmap_w, &sm->pfull[st], s * (KS / 2), tp.n0);
                         else
-                            ptx::tma_load_3d(pring + st * kPBytes, &tmap_w, &sm->pfull[st], s * (kKS / 2), tp.n0,
+                            ptx::tma_load_3d(pring + st * P::kPBytes, &tmap_w, &sm->pfull[st], s * (KS / 2), tp.n0,
                                              tp.e);
-                        ++ip;
-                        moved = true;
                     }
+                    ++ip;
+                    moved = true;
                 }
-                if (moved) {
-                    idle_since = 0;
-                    continue;
-                }
+            }
+            if (moved) {
+                idle_since = 0;
+                continue;
+            }
+            bool quit = false;
+            if (lane == 0) {
                 const uint64_t now = ptx::globaltimer_ns();
                 if (idle_since == 0) idle_since = now;
-                if (*abort || now - idle_since > wait_limit()) {
-                    ok = false;
-                    break;
-                }
+                quit = *abort || now - idle_since > wait_limit();
             }
-            if (!ok) {
-                if (!*abort) fail(a, sm, W4A16_ERR_TIMEOUT);
-                volatile int never = 0;  // let our own loads land before the CTA exits
-                for (int64_t i = ip > kPStages ? ip - kPStages : 0; i < ip; ++i)
-                    ptx::mbar_wait(&sm->pfull[i % kPStages], (uint32_t)((i / kPStages) & 1), &never, kDrainLimitNs);
-                for (int64_t i = ix > kXStages ? ix - kXStages : 0; i < ix; ++i)
-                    ptx::mbar_wait(&sm->xfull[i % kXStages], (uint32_t)((i / kXStages) & 1), &never, kDrainLimitNs);
+            if (__shfl_sync(0xffffffffu, quit, 0)) {
+                ok = false;
+                break;
             }
+        }
+        if (!ok && lane == 0) {
+            if (!*abort) fail(a, &sm->abort, W4A16_ERR_TIMEOUT);
+            volatile int never = 0;  // let our own loads land before the CTA exits
+            for (int64_t i = ip > P::kPStages ? ip - P::kPStages : 0; i < ip; ++i)
+                ptx::mbar_wait(&sm->pfull[i % P::kPStages], (uint32_t)((i / P::kPStages) & 1), &never, kDrainLimitNs);
+            if (!a.gather)
+                for (int64_t i = ix > P::kXStages ? ix - P::kXStages : 0; i < ix; ++i)
+                    ptx::mbar_wait(&sm->xfull[i % P::kXStages], (uint32_t)((i / P::kXStages) & 1), &never,
+                                   kDrainLimitNs);
         }
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA issue
@@ -357,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             int64_t c = 0;
             for (int j = 0; ok && j < my_tiles; ++j) {
-                const Tile tl = decode_tile(sm, (int)blockIdx.x + j * (int)gridDim.x, ntn, a.E);
+                const Tile tl = tile_of(j);
                 if (j >= 1 && !ptx::mbar_wait(&sm->dempty, (uint32_t)((j - 1) & 1), abort, wait_limit())) {
                     ok = false;
                     break;
@@ -366,21 +417,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t idesc = ptx::idesc_f16_f32(kRows, (tl.rows + 15) & ~15);
                 const uint32_t d = tmem;
                 for (int s = 0; s < nst; ++s, ++c) {
-                    const int xs = (int)(c % kXStages), as = (int)(c % kAStages);
-                    if (!ptx::mbar_wait(&sm->xfull[xs], (uint32_t)((c / kXStages) & 1), abort, wait_limit()) ||
-                        !ptx::mbar_wait(&sm->afull[as], (uint32_t)((c / kAStages) & 1), abort, wait_limit())) {
+                    const int xs = (int)(c % P::kXStages), as = (int)(c % P::kAStages);
+                    if (!ptx::mbar_wait(&sm->xfull[xs], (uint32_t)((c / P::kXStages) & 1), abort, wait_limit()) ||
+                        !ptx::mbar_wait(&sm->afull[as], (uint32_t)((c / P::kAStages) & 1), abort, wait_limit())) {
                         ok = false;
                         break;
                     }
+                    // gathered x was written through the generic proxy; the MMAs read it through the async one
+                    if (a.gather) ptx::fence_proxy_async_shared();
                     ptx::tc_fence_after();
-                    const int64_t kc = (int64_t)s * kKS;
-                    const int nk = (int)((a.K - kc < kKS ? a.K - kc : kKS) >> 4);
-                    const uint64_t bdesc0 = ptx::smem_desc_sw128(ptx::smem_u32(xring + xs * kXBytes));
-                    const uint32_t a_hi = tmem + kAColBase + (uint32_t)as * kAStageCols;
-                    const uint32_t a_lo = a_hi + kAHalfCols;
+                    const int64_t kc = (int64_t)s * KS;
+                    const int nk = (int)((a.K - kc < KS ? a.K - kc : KS) >> 4);
+                    const uint64_t bdesc0 = ptx::smem_desc_sw128(ptx::smem_u32(xring + xs * P::kXBytes));
+                    const uint32_t a_hi = tmem + kAColBase + (uint32_t)as * P::kAStageCols;
+                    const uint32_t a_lo = a_hi + P::kAHalfCols;
 #pragma unroll
-                    for (int kk = 0; kk < kKS / 16; ++kk) {
+                    for (int kk = 0; kk < KS / 16; ++kk) {
                         if (kk >= nk) break;
+                        // next 64-k box every 4 MMAs; 32 bytes per 16 k inside the swizzle atom
                         const uint64_t bdesc = bdesc0 + (uint64_t)((((kk >> 2) * kXBoxBytes) + (kk & 3) * 32) >> 4);
                         ptx::mma_f16_ts(d, a_hi + (uint32_t)(kk * 8), bdesc, idesc, (s | kk) ? 1u : 0u);
                         ptx::mma_f16_ts(d, a_lo + (uint32_t)(kk * 8), bdesc, idesc, 1u);
@@ -391,59 +445,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 ptx::mma_commit(&sm->dfull);  // the tile's accumulator is complete
             }
-            if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
+            if (!ok) fail(a, &sm->abort, W4A16_ERR_TIMEOUT);
             ptx::mma_commit(&sm->mma_done);
             volatile int never = 0;
             ptx::mbar_wait(&sm->mma_done, 0, &never, kDrainLimitNs);
         }
     } else if (warp < 2 + kDeqWarps) {
         // -------------------------------------------------------------- dequant
+        constexpr int GPS = P::kGroupsPerStage;
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
-        const int part = (warp - 2) >> 2;         // which groups of each stage
         const int r = quad * 32 + lane;           // weight row in the tile = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         bool ok = true;
         int64_t c = 0;
         for (int j = 0; ok && j < my_tiles; ++j) {
-            const Tile tl = decode_tile(sm, (int)blockIdx.x + j * (int)gridDim.x, ntn, a.E);
+            const Tile tl = tile_of(j);
             const int64_t n = (int64_t)tl.n0 + r;
             const bool n_ok = n < a.N;
             const uint16_t* srow = a.s + ((int64_t)tl.e * a.N + (n_ok ? n : 0)) * gk;
             const float f = row_shift(srow, gk, n_ok);
-            // this thread's scales of a stage (0 past the row), one stage ahead
-            auto load_scales = [&](int s_, uint32_t (&dst)[kPartGroups]) {
+            // this row's scales of a stage (0 past the row), one stage ahead
+            auto load_scales = [&](int s_, uint32_t (&dst)[GPS]) {
 #pragma unroll
-                for (int i = 0; i < kPartGroups; ++i) {
-                    const int g = s_ * kGroupsPerStage + part * kPartGroups + i;
+                for (int i = 0; i < GPS; ++i) {
+                    const int g = s_ * GPS + i;
                     dst[i] = (s_ < nst && g < gk) ? (uint32_t)__ldg(srow + g) : 0u;
                 }
             };
-            uint32_t sc[kPartGroups], sc_next[kPartGroups];
+            uint32_t sc[GPS], sc_next[GPS];
             load_scales(0, sc);
             for (int s = 0; s < nst; ++s, ++c) {
-                const int ps = (int)(c % kPStages), as = (int)(c % kAStages);
+                const int ps = (int)(c % P::kPStages), as = (int)(c % P::kAStages);
                 load_scales(s + 1, sc_next);
-                const int g0 = s * kGroupsPerStage + part * kPartGroups;
-                const int ng = min(kPartGroups, gk - g0);  // this thread's groups in the stage
+                const int ng = min(GPS, gk - s * GPS);  // groups in the stage
                 const bool got =
-                    ptx::mbar_wait(&sm->pfull[ps], (uint32_t)((c / kPStages) & 1), abort, wait_limit()) &&
-                    (c < kAStages ||
-                     ptx::mbar_wait(&sm->aempty[as], (uint32_t)((c / kAStages - 1) & 1), abort, wait_limit()));
+                    ptx::mbar_wait(&sm->pfull[ps], (uint32_t)((c / P::kPStages) & 1), abort, wait_limit()) &&
+                    (c < P::kAStages ||
+                     ptx::mbar_wait(&sm->aempty[as], (uint32_t)((c / P::kAStages - 1) & 1), abort, wait_limit()));
                 if (!__all_sync(0xffffffffu, got)) {  // warp-uniform: the TMEM stores are .sync.aligned
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint8_t* prow = pring + ps * kPBytes;
-                const uint32_t acol = lane_base + kAColBase + (uint32_t)as * kAStageCols;
+                const uint8_t* prow = pring + ps * P::kPBytes;
+                const uint32_t acol = lane_base + kAColBase + (uint32_t)as * P::kAStageCols;
 #pragma unroll
-                for (int i = 0; i < kPartGroups; ++i) {
-                    if (i >= ng) break;  // uniform: every lane has the same groups
-                    const int gi = part * kPartGroups + i;  // group within the stage
-                    const uint4 pk = *reinterpret_cast<const uint4*>(prow + packed_offset(r, gi));
+                for (int gi = 0; gi < GPS; ++gi) {
+                    if (gi >= ng) break;  // uniform: every lane has the same groups
+                    const uint4 pk = *reinterpret_cast<const uint4*>(prow + P::packed_offset(r, gi));
                     const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
                     // exact: a (shifted) fp16 scale
-                    const __half2 s2 = __float2half2_rn(__half2float(__ushort_as_half((unsigned short)sc[i])) * f);
+                    const __half2 s2 = __float2half2_rn(__half2float(__ushort_as_half((unsigned short)sc[gi])) * f);
                     uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {  // word w holds k = 8w .. 8w+7 of the group
@@ -461,38 +513,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     ptx::tmem_st_32x32b_x16(acol + (uint32_t)(gi * 16), hi);
-                    ptx::tmem_st_32x32b_x16(acol + kAHalfCols + (uint32_t)(gi * 16), lo);
+                    ptx::tmem_st_32x32b_x16(acol + P::kAHalfCols + (uint32_t)(gi * 16), lo);
                 }
                 ptx::mbar_arrive(&sm->pempty[ps]);  // this thread has read its packed bytes
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&sm->afull[as]);
 #pragma unroll
-                for (int i = 0; i < kPartGroups; ++i) sc[i] = sc_next[i];
+                for (int i = 0; i < GPS; ++i) sc[i] = sc_next[i];
             }
         }
-        if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
+        if (!ok) fail(a, &sm->abort, W4A16_ERR_TIMEOUT);
     } else {
         // ------------------------------------------------------------- epilogue
+        const int ew = warp - 2 - kDeqWarps;           // epilogue warp 0..7
         const int quad = warp & 3;
-        const int half = (warp - 2 - kDeqWarps) >> 2;  // which tokens of the tile
+        const int half = ew >> 2;                      // which tokens of the tile
         const int r = quad * 32 + lane;                // weight row in the tile = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * kEpiCols);
-        bool ok = true;
-        for (int j = 0; ok && j < my_tiles; ++j) {
-            const Tile tl = decode_tile(sm, (int)blockIdx.x + j * (int)gridDim.x, ntn, a.E);
+        // tile j's results: the accumulator read as fp16 pairs (times the row's
+        // 2^e), the accumulator released, then y stored
+        auto finish_tile = [&](const Tile& tl, float mult) {
             const int64_t n = (int64_t)tl.n0 + r;
-            const bool n_ok = n < a.N;
             const int m0 = half * kEpiCols;                          // first token of this thread's share
             const int mine = max(0, min(kEpiCols, tl.rows - m0));    // tokens of the tile in that share
-            // the row's 2^e, found while the tile's MMAs run
-            const float mult = 1.0f / row_shift(a.s + ((int64_t)tl.e * a.N + (n_ok ? n : 0)) * gk, gk, n_ok);
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sm->dfull, (uint32_t)(j & 1), abort, wait_limit()))) {
-                ok = false;
-                break;
-            }
             ptx::tc_fence_after();
-            // read the accumulator (rounded to fp16 pairs), then release it for the next tile
             uint32_t packed[kEpiCols / 2];
 #pragma unroll
             for (int ch = 0; ch < kEpiCols / 32; ++ch) {
@@ -510,14 +555,105 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(&sm->dempty);
-            if (n_ok) {
+            if (n < a.N) {
                 uint16_t* yrow = a.y + ((int64_t)tl.row0 + m0) * a.N + n;
 #pragma unroll
                 for (int i = 0; i < kEpiCols; ++i)
                     if (i < mine) yrow[(int64_t)i * a.N] = (uint16_t)(packed[i >> 1] >> (16 * (i & 1)));
             }
+        };
+        auto row_mult = [&](const Tile& tl) {  // the row's 2^e
+            const int64_t n = (int64_t)tl.n0 + r;
+            const bool n_ok = n < a.N;
+            return 1.0f / row_shift(a.s + ((int64_t)tl.e * a.N + (n_ok ? n : 0)) * gk, gk, n_ok);
+        };
+        bool ok = true;
+        if (!a.gather) {
+            for (int j = 0; ok && j < my_tiles; ++j) {
+                const Tile tl = tile_of(j);
+                const float mult = row_mult(tl);  // found while the tile's MMAs run
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sm->dfull, (uint32_t)(j & 1), abort, wait_limit()))) {
+                    ok = false;
+                    break;
+                }
+                finish_tile(tl, mult);
+            }
+        } else {
+            // Row gather: between tile epilogues these warps fill the x ring, each with
+            // 32 rows of every stage. Lane l copies 16-byte chunk l % CPR of rows
+            // 32 ew + l / CPR + (32 / CPR) i, written where the 128-byte swizzle of a TMA
+            // box puts it; rows past the tile, k past K and tokens outside [0, T) read
+            // zeros. Each lane's arrival fires when its copies land.
+            constexpr int CPR = KS / 8;              // 16-byte chunks of a row per stage
+            constexpr int RPI = 32 / CPR;            // rows per warp instruction
+            int64_t gx = 0;                          // x stages this warp has gathered its rows of
+            int jg = -1;
+            Tile tg{};
+            int jm = -1;
+            Tile tl{};
+            float mult = 0.0f;
+            uint64_t idle_since = 0;
+            for (int j = 0; ok && j < my_tiles;) {
+                if (jm != j) {
+                    tl = tile_of(j);
+                    mult = row_mult(tl);
+                    jm = j;
+                }
+                if (gx < stages) {
+                    const int st = (int)(gx % P::kXStages);
+                    const int64_t round = gx / P::kXStages;
+                    bool free = round == 0;
+                    if (!free && lane == 0)
+                        free = ptx::mbar_try_wait(&sm->xempty[st], (uint32_t)((round - 1) & 1));
+                    if (__shfl_sync(0xffffffffu, free, 0)) {
+                        const int jx = (int)(gx / nst), sx = (int)(gx % nst);
+                        if (jx != jg) {
+                            tg = tile_of(jx);
+                            jg = jx;
+                        }
+                        const uint32_t xdst = ptx::smem_u32(xring + st * P::kXBytes);
+                        const int c16 = lane % CPR;
+                        const int64_t k = (int64_t)sx * KS + c16 * 8;
+                        const int n_mma = (tg.rows + 15) & ~15;
+#pragma unroll
+                        for (int i = 0; i < CPR; ++i) {
+                            const int row = 32 * ew + lane / CPR + RPI * i;
+                            if (row >= n_mma) continue;
+                            int t = row < tg.rows ? __ldg(a.gather + tg.row0 + row) : -1;
+                            if (row < tg.rows && (t < 0 || (int64_t)t >= a.T)) {
+                                if (sx == 0 && c16 == 0) raise_device_error(a.err, W4A16_ERR_BAD_ROUTING);
+                                t = -1;
+                            }
+                            const bool v = t >= 0 && k < a.K;
+                            const uint32_t dst = xdst + (uint32_t)((c16 >> 3) * kXBoxBytes + row * 128 +
+                                                                   (((c16 & 7) ^ (row & 7)) << 4));
+                            ptx::cp_async_16(dst, v ? a.xg + (int64_t)t * a.K + k : a.xg, v ? 16u : 0u);
+                        }
+                        ptx::cp_async_mbar_arrive_noinc(&sm->xfull[st]);
+                        ++gx;
+                        idle_since = 0;
+                        continue;
+                    }
+                }
+                bool ready = false;
+                if (lane == 0) ready = ptx::mbar_try_wait(&sm->dfull, (uint32_t)(j & 1));
+                if (__shfl_sync(0xffffffffu, ready, 0)) {
+                    finish_tile(tl, mult);
+                    ++j;
+                    idle_since = 0;
+                    continue;
+                }
+                bool quit = false;
+                if (lane == 0) {
+                    const uint64_t now = ptx::globaltimer_ns();
+                    if (idle_since == 0) idle_since = now;
+                    quit = *abort || now - idle_since > wait_limit();
+                }
+                if (__shfl_sync(0xffffffffu, quit, 0)) ok = false;
+            }
+            ptx::cp_async_wait_all();  // this lane's copies land before the CTA exits
         }
-        if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
+        if (!ok) fail(a, &sm->abort, W4A16_ERR_TIMEOUT);
     }
 
     ptx::tc_fence_before();
@@ -531,7 +667,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------- host --
 
-constexpr size_t kSmem = 1024 + kPStages * kPBytes + kXStages * kXBytes + ((sizeof(SplitSmem) + 127) & ~(size_t)127);
+template <class P>
+constexpr size_t smem_bytes() {
+    return 1024 + P::kPStages * P::kPBytes + P::kXStages * P::kXBytes + ((sizeof(SplitSmem<P>) + 127) & ~(size_t)127);
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -547,19 +686,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-}  // namespace
-
-bool split_supports(int group, int E) { return group == kG && E >= 1 && E <= kMaxE; }
-
-w4a16_status split_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s, uint16_t* y,
-                          int64_t M, int64_t N, int64_t K, const int32_t* offsets, int E, cudaStream_t st) {
-    if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
+template <int KS>
+w4a16_status launch_split(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s,
+                          uint16_t* y, int64_t M, int64_t N, int64_t K, const int32_t* offsets, int E,
+                          const int32_t* gather, int64_t T, cudaStream_t st) {
+    using P = Pipe<KS>;
+    constexpr size_t kSmem = smem_bytes<P>();
     if (kSmem > dev.smem_optin) return W4A16_ERR_UNSUPPORTED;
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cuda_status(cudaErrorNotSupported, "gemm g32: cuTensorMapEncodeTiled entry point");
     CUtensorMap mx, mw;
-    {
-        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    {  // x [M, K] (with a row gather: x [T, K]; the map is then never loaded from)
+        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(gather ? T : M)};
         cuuint64_t strides[1] = {(cuuint64_t)K * 2};
         cuuint32_t box[2] = {64, (cuuint32_t)kBN};
         cuuint32_t es[2] = {1, 1};
@@ -571,19 +709,19 @@ w4a16_status split_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_
     if (offsets == nullptr) {
         cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
         cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-        cuuint32_t box[2] = {kKS / 2, (cuuint32_t)kRows};
+        cuuint32_t box[2] = {KS / 2, (cuuint32_t)kRows};
         cuuint32_t es[2] = {1, 1};
         if (enc(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(qw), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, P::kPSwizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cuda_status(cudaErrorInvalidValue, "gemm g32: cuTensorMapEncodeTiled (weights)");
     } else {
         cuuint64_t dims[3] = {(cuuint64_t)(K / 2), (cuuint64_t)N, (cuuint64_t)E};
         cuuint64_t strides[2] = {(cuuint64_t)(K / 2), (cuuint64_t)(N * (K / 2))};
-        cuuint32_t box[3] = {kKS / 2, (cuuint32_t)kRows, 1};
+        cuuint32_t box[3] = {KS / 2, (cuuint32_t)kRows, 1};
         cuuint32_t es[3] = {1, 1, 1};
         if (enc(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(qw), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, P::kPSwizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cuda_status(cudaErrorInvalidValue, "gemm g32: cuTensorMapEncodeTiled (weights)");
     }
@@ -591,6 +729,9 @@ w4a16_status split_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_
     a.s = s;
     a.y = y;
     a.offsets = offsets;
+    a.gather = gather;
+    a.xg = x;
+    a.T = T;
     a.M = M;
     a.N = N;
     a.K = K;
@@ -603,11 +744,24 @@ w4a16_status split_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_
     const unsigned grid = (unsigned)(tiles < dev.sms ? tiles : dev.sms);
     static PerDeviceOnce once;
     const cudaError_t attr = once.run(dev.device, [] {
-        return cudaFuncSetAttribute(split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+        return cudaFuncSetAttribute(split_kernel<KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     });
     if (attr != cudaSuccess) return cuda_status(attr, "gemm g32: cudaFuncSetAttribute");
-    split_kernel<<<grid, kThreads, kSmem, st>>>(mx, mw, a);
+    split_kernel<KS><<<grid, kThreads, kSmem, st>>>(mx, mw, a);
     return cuda_status(cudaGetLastError(), "gemm g32: kernel launch");
+}
+
+}  // namespace
+
+bool split_supports(int group, int E) { return group == kG && E >= 1 && E <= kMaxE; }
+
+w4a16_status split_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s, uint16_t* y,
+                          int64_t M, int64_t N, int64_t K, const int32_t* offsets, int E, const int32_t* gather,
+                          int64_t T, cudaStream_t st) {
+    if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL || T > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
+    // long K: 128-k stages; short K: 64-k stages and a deeper pipeline for the tile's fill
+    if (K >= 1024) return launch_split<128>(dev, x, qw, s, y, M, N, K, offsets, E, gather, T, st);
+    return launch_split<64>(dev, x, qw, s, y, M, N, K, offsets, E, gather, T, st);
 }
 
 #ifdef W4A16_TEST_HOOKS
