@@ -228,12 +228,16 @@ def gated_tolerance(g, u, absdot_g, absdot_u):
     """Per-element bound on |y - y_ref| for a kernel whose g and u each meet
     the linear bound (tolerance()) and which evaluates silu(g) * u in fp32 and
     rounds once to fp16. First-order propagation with |silu'| <= 1.1 on the
-    real line, the cross term of the two errors, and 2^-9 |y| for the fp32
-    evaluation and the final rounding."""
+    real line, the cross term of the two errors, and 2^-9 |y| + 2^-25 for the
+    fp32 evaluation and the final rounding: rounding to fp16 errs by at most
+    half a unit in the last place, 2^-11 |y| for normal values and the
+    absolute 2^-25 (half the subnormal spacing 2^-24) below 2^-14, where
+    silu(g) * u lands when g and u are both small."""
     eg = tolerance(g, absdot_g)
     eu = tolerance(u, absdot_u)
     y = silu(g) * u
-    return 1.1 * eg * np.abs(u) + np.abs(silu(g)) * eu + 1.1 * eg * eu + np.ldexp(np.abs(y), -9)
+    return (1.1 * eg * np.abs(u) + np.abs(silu(g)) * eu + 1.1 * eg * eu + np.ldexp(np.abs(y), -9)
+            + np.ldexp(1.0, -25))
 
 
 

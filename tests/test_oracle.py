@@ -395,6 +395,27 @@ def test_gated_tolerance_covers_linear_errors():
             assert np.all(np.abs(yp - y) <= bound)
 
 
+def test_gated_tolerance_covers_fp16_rounding_down_to_subnormals():
+    """The final rounding to fp16: for exact g and u (zero linear error terms
+    apart from the 2^-9 relative part) the bound still covers |fp16(y) - y|
+    for y from the largest fp16 values down through the subnormal range
+    (spacing 2^-24), where the relative part alone is far too small."""
+    r = np.random.default_rng(6)
+    y_target = np.concatenate([np.ldexp(1.0, np.arange(-34, 15)),
+                               np.exp(r.uniform(np.log(1e-10), np.log(6e4), 20000))])
+    y_target *= r.choice([-1.0, 1.0], y_target.size)
+    g = np.full_like(y_target, 40.0)          # silu(40) = 40 to 1e-16 relative
+    u = y_target / oracle.silu(g)
+    y = oracle.silu(g) * u
+    zero = np.zeros_like(g)
+    bound = oracle.gated_tolerance(g, u, zero, zero)
+    err = np.abs(y.astype(np.float16).astype(np.float64) - y)
+    assert np.all(err <= bound)
+    # the subnormal values need the absolute term: 2^-9 |y| alone does not cover them
+    sub = np.abs(y) < np.ldexp(1.0, -14)
+    assert np.any(err[sub] > np.ldexp(np.abs(y[sub]), -9) * 3)
+
+
 # ------------------------------------------------------------------ routed-MoE dispatch
 
 def test_moe_route_hand_worked():
