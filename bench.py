@@ -450,6 +450,37 @@ def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):
                                "frac_tc": fl / (ms * 1e-3) / 1e12 / tc_peak}
     except w4.W4A16Error as e:
         out["prefill"] = {"unavailable": str(e)}
+    # fused gate + up with the SiLU * up epilogue (one GEMM over both matrices)
+    # against the two projections as separate GEMMs, at M = 512 and 4096
+    try:
+        if "prefill_m512" not in out:
+            raise w4.W4A16Error("the prefill GEMM did not run")
+        W2 = torch.from_numpy(workloads.weights(workloads.rng(7), N, K)).to(dev)
+        qu, su = w4.pack(W2, GROUP)
+        del W2
+        for Mg in (512, 4096):
+            xg = xp[:Mg].contiguous()
+            yg, yu = yp[:Mg], torch.empty((Mg, N), dtype=torch.float16, device=dev)
+            fused = lambda i: w4.linear_gated(xg, qw, s, qu, su, GROUP, out=yg)  # noqa: E731
+
+            def two(i):
+                w4.linear(xg, qw, s, GROUP, out=yg)
+                w4.linear(xg, qu, su, GROUP, out=yu)
+            n = 50 if Mg == 512 else 10
+            for i in range(3):
+                fused(i)
+                two(i)
+            ms = statistics.median(_time_launches(torch, fused, n))
+            ms2 = statistics.median(_time_launches(torch, two, n))
+            fl = 2.0 * 2 * Mg * N * K
+            out[f"prefill_gated_m{Mg}"] = {"shape": [Mg, K, N], "us": ms * 1e3, "us_two_gemms": ms2 * 1e3,
+                                           "TFLOP/s": fl / (ms * 1e-3) / 1e12,
+                                           "frac_tc": fl / (ms * 1e-3) / 1e12 / tc_peak}
+            del yu
+        w4.device_status()
+        del qu, su
+    except w4.W4A16Error as e:
+        out["prefill_gated"] = {"unavailable": str(e)}
     # routed experts: E=128, 4096 tokens, top-8 (R = 32768 rows), group 32
     try:
         for name, (Km, Nm) in (("moe_gate_up", (2048, 512)), ("moe_down", (512, 2048))):
@@ -668,8 +699,8 @@ def oracle_other_configs(oracle):
 
 # ----------------------------------------------------------------- profile --
 
-PROFILE_CASES = ("decode", "decode_down", "decode_m4", "decode_gated", "prefill", "prefill_m512", "moe_gate_up",
-                 "moe_down", "moe_dispatch", "moe_gate_up_gather")
+PROFILE_CASES = ("decode", "decode_down", "decode_m4", "decode_gated", "prefill", "prefill_m512", "prefill_gated",
+                 "moe_gate_up", "moe_down", "moe_dispatch", "moe_gate_up_gather")
 
 
 def run_profile(case: str, launches: int):
@@ -700,6 +731,15 @@ def run_profile(case: str, launches: int):
         for i in range(launches):  # four gate/up pairs in turn: successive launches miss in L2
             j = 2 * (i % 4)
             w4.linear_gated(x, *mats[j], *mats[j + 1], GROUP, out=y, static_weights=True)
+    elif case == "prefill_gated":
+        # the gate/up pair at M = 512 in one GEMM with the SiLU * up epilogue
+        K, N = DECODE[0]
+        qg, sg = w4.pack(torch.from_numpy(workloads.weights(g, N, K)).to(dev), GROUP)
+        qu, su = w4.pack(torch.from_numpy(workloads.weights(g, N, K)).to(dev), GROUP)
+        x = torch.from_numpy(workloads.activations(g, 512, K, outlier_frac=0.01)).to(dev)
+        y = torch.empty((512, N), dtype=torch.float16, device=dev)
+        for _ in range(launches):
+            w4.linear_gated(x, qg, sg, qu, su, GROUP, out=y)
     elif case == "moe_gate_up_gather":
         # the gate/up projection reading its rows straight from the token-major x
         T, E, k, Kh, Ni = (workloads.MOE[key] for key in ("tokens", "E", "top_k", "hidden", "inter"))

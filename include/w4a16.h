@@ -147,7 +147,7 @@ W4A16_API w4a16_status w4a16_grouped_linear_gather(const uint16_t* x, int64_t T,
                                                    int64_t R, int64_t N, int64_t K, int32_t group, void* stream);
 
 /*
- * Gate and up projections of a gated (SwiGLU) MLP fused into one decode pass:
+ * Gate and up projections of a gated (SwiGLU) MLP fused into one pass:
  *   g = x * Wg^T,  u = x * Wu^T,  y[m, n] = silu(g[m, n]) * u[m, n],
  *   silu(v) = v / (1 + exp(-v)),
  * (rust-inference page, list of accuracy fixes, item 5: the SiLU-activated
@@ -155,12 +155,16 @@ W4A16_API w4a16_status w4a16_grouped_linear_gather(const uint16_t* x, int64_t T,
  * shape [N, K] and group, in the format of w4a16_linear; g and u are formed
  * exactly as w4a16_linear forms y (fp32 group sums, scale in fp32) and stay
  * in fp32; silu and the product are fp32; y is rounded once to fp16.
- * Decode only: 1 <= M <= 16, else W4A16_ERR_UNSUPPORTED. Same alignment rules
- * as w4a16_linear. workspace: w4a16_linear_gated_workspace_bytes(M, N, K,
- * group) bytes, zero-filled once (w4a16_workspace_init); every call leaves it
- * ready for the next, as for w4a16_linear (its fp32 g and u parking area is
- * zero again when the call ends). One launch streams both weight matrices
- * once and never writes g or u to y's buffer.
+ * M, N >= 0 and the K, group and alignment rules of w4a16_linear. Decode
+ * (M <= 16) runs a split-K GEMV over both matrices; its workspace is
+ * w4a16_linear_gated_workspace_bytes(M, N, K, group) bytes, zero-filled once
+ * (w4a16_workspace_init), and every call leaves it ready for the next, as
+ * for w4a16_linear (its fp32 g and u parking area is zero again when the
+ * call ends). Larger M runs the tensor-core GEMM with tiles of 64 rows of Wg
+ * and the same 64 rows of Wu, so one block holds g and u of the same outputs
+ * in fp32; it needs no workspace (the size is 0; NULL is fine). Either way
+ * one launch streams both weight matrices once and never writes g or u to
+ * y's buffer.
  */
 W4A16_API w4a16_status w4a16_linear_gated(const uint16_t* x, const uint8_t* qweight_gate,
                                           const uint16_t* scales_gate, const uint8_t* qweight_up,

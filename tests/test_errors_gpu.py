@@ -99,15 +99,21 @@ def test_gemv_wait_times_out_and_next_call_is_correct(hooks, cuda_device):
     assert_within_bound(y.cpu().numpy(), y_ref, a, "GEMV after a timeout")
 
 
-@pytest.mark.parametrize("grouped", [False, True])
-def test_gemm_wait_times_out_frees_tmem_and_next_call_is_correct(hooks, cuda_device, grouped):
+@pytest.mark.parametrize("kind", ["dense", "grouped", "gated"])
+def test_gemm_wait_times_out_frees_tmem_and_next_call_is_correct(hooks, cuda_device, kind):
     import torch
 
     lib = hooks
+    grouped = kind == "grouped"
     N, K, g = 512, 2048, 128 if not grouped else 32
-    r = workloads.rng(91 + grouped)
+    r = workloads.rng(91 + ["dense", "grouped", "gated"].index(kind))
     st = _stream(cuda_device)
-    if grouped:
+    if kind == "gated":   # both weight matrices; the epilogue swaps the up sums through shared memory
+        M = 256
+        qw, s = workloads.raw_packed(r, N, K, g)
+        qu, su = workloads.raw_packed(r, N, K, g)
+        qud, sud = to_dev(qu, cuda_device), to_dev(su, cuda_device)
+    elif grouped:
         counts = [100, 0, 200, 37]
         E = len(counts)
         qw = r.integers(0, 256, (E, N, K // 2), dtype=np.uint8)
@@ -125,6 +131,8 @@ def test_gemm_wait_times_out_frees_tmem_and_next_call_is_correct(hooks, cuda_dev
     def call():
         if grouped:
             return lib.w4a16_grouped_linear(_p(xd), _p(qd), _p(sd), _p(offd), _p(y), E, M, N, K, g, None, 0, st)
+        if kind == "gated":
+            return lib.w4a16_linear_gated(_p(xd), _p(qd), _p(sd), _p(qud), _p(sud), _p(y), M, N, K, g, None, 0, st)
         return lib.w4a16_linear(_p(xd), _p(qd), _p(sd), _p(y), M, N, K, g, None, 0, st)
 
     for issue_limit in (0, 3, 9):   # no copy; the first stage only; about half of K
@@ -141,6 +149,11 @@ def test_gemm_wait_times_out_frees_tmem_and_next_call_is_correct(hooks, cuda_dev
     assert lib.w4a16_device_status(st) == 0
     if grouped:
         y_ref, a = oracle.grouped_linear(x, qw, s, off, g)
+    elif kind == "gated":
+        y_ref, gg, uu, ag, au = oracle.gated_linear(x, qw, s, qu, su, g, threads=8)
+        err = np.abs(y.cpu().numpy().astype(np.float64) - y_ref)
+        assert np.all(err <= oracle.gated_tolerance(gg, uu, ag, au)), "gated GEMM after a timeout"
+        return
     else:
         y_ref, a = oracle.linear(x, qw, s, g, threads=8)
     assert_within_bound(y.cpu().numpy(), y_ref, a, "GEMM after a timeout")

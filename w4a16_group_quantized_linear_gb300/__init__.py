@@ -186,9 +186,9 @@ def linear(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, group: 
 def linear_gated(x: torch.Tensor, qweight_gate: torch.Tensor, scales_gate: torch.Tensor,
                  qweight_up: torch.Tensor, scales_up: torch.Tensor, group: int = 128,
                  out: torch.Tensor | None = None, static_weights: bool = False) -> torch.Tensor:
-    """y = silu(x Wg^T) * (x Wu^T) in one decode pass (M <= 16); both weight
-    matrices uint8 [N, K/2] with fp16 scales [N, K/group]. ``static_weights``
-    as in :func:`linear`."""
+    """y = silu(x Wg^T) * (x Wu^T) in one launch (the decode GEMV for M <= 16,
+    the tensor-core GEMM above); both weight matrices uint8 [N, K/2] with fp16
+    scales [N, K/group]. ``static_weights`` as in :func:`linear`."""
     _need(x, "x", torch.float16, 2)
     for t, name in ((qweight_gate, "qweight_gate"), (qweight_up, "qweight_up")):
         _need(t, name, torch.uint8, 2)

@@ -109,9 +109,10 @@ w4a16_status linear_gated_impl(const uint16_t* x, const uint8_t* qweight_gate, c
     if (v != W4A16_OK || M == 0 || N == 0) return v;
     if (K > 0 && (!qweight_up || !scales_up)) return W4A16_ERR_INVALID_ARG;
     if (!aligned16(qweight_up) || !aligned16(scales_up)) return W4A16_ERR_MISALIGNED;
-    if (M > kGemvMaxM) return W4A16_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
     if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(uint16_t), st));  // silu(0) * 0
+    if (M > kGemvMaxM)
+        return gemm_gated_launch(*dev, x, qweight_gate, scales_gate, qweight_up, scales_up, y, M, N, K, group, st);
     return gemv_gated_launch(*dev, x, qweight_gate, scales_gate, qweight_up, scales_up, y, M, N, K, group, workspace,
                              workspace_bytes, gemv_options(flags), st);
 }

@@ -136,6 +136,11 @@ w4a16_status unpack_launch(const uint8_t* qw, int64_t N, int64_t K, int8_t* q, c
 w4a16_status gemm_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw,
                          const uint16_t* s, uint16_t* y, int64_t M, int64_t N, int64_t K,
                          int group, const int32_t* expert_offsets, int E, cudaStream_t st);
+// y = silu(x Wg^T) * (x Wu^T) for M > 16 on the tensor-core GEMM: each tile
+// holds 64 rows of Wg and the same 64 rows of Wu.
+w4a16_status gemm_gated_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qweight_gate,
+                               const uint16_t* scales_gate, const uint8_t* qweight_up, const uint16_t* scales_up,
+                               uint16_t* y, int64_t M, int64_t N, int64_t K, int group, cudaStream_t st);
 
 // Tensor-core GEMM for group 32 with the scale split exactly into the A operand
 // (routed experts and dense layers): supported for E <= 4096 experts.

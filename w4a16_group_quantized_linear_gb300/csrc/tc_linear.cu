@@ -116,6 +116,7 @@ using MoeCfg = Cfg<G, 128, 256, 4, 2, 4, 8, true>;
 
 struct Args {
     const uint16_t* s;
+    const uint16_t* s2;      // gated: the up projection's scales (s holds the gate's)
     uint16_t* y;
     const int32_t* offsets;  // routed experts; nullptr: dense
     int64_t M, N, K;
@@ -196,9 +197,15 @@ __device__ __forceinline__ int packed_offset(int r, int c) {
     else return r * 32 + ((c ^ ((r >> 2) & 1)) << 4);                             // 32-byte swizzle
 }
 
-template <class C>
+// GATED: the tile's 128 weight rows are 64 rows of Wg (TMEM lanes 0-63) and
+// the same 64 rows of Wu (lanes 64-127), loaded as two boxes of 64 rows into
+// one packed stage (tmap_w, tmap_w2); the CTA forms y = silu(g) * u for its 64
+// outputs from the fp32 sums.
+template <class C, bool GATED>
 __global__ void __launch_bounds__(C::THREADS, 1)
-    tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w, const Args a) {
+    tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+              const __grid_constant__ CUtensorMap tmap_w2, const Args a) {
+    constexpr int kOutRows = GATED ? kRowsPerTile / 2 : kRowsPerTile;  // outputs n per tile
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* pring = base;                // packed-weight stages
@@ -237,6 +244,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             ptx::fence_mbar_init();
             ptx::prefetch_tensormap(&tmap_x);
             ptx::prefetch_tensormap(&tmap_w);
+            if (GATED) ptx::prefetch_tensormap(&tmap_w2);
         }
     }
     __syncthreads();
@@ -256,7 +264,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
-            const int n0 = (int)(n_tile * kRowsPerTile);
+            const int n0 = (int)(n_tile * kOutRows);
             int64_t ip = 0, ix = 0;  // stages issued on each ring
             // Both rings are polled, so a full ring never holds up the other one.
             bool ok = true;
@@ -283,10 +291,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     if (round == 0 || ptx::mbar_try_wait(&sm->pempty[st], (uint32_t)((round - 1) & 1))) {
                         ptx::mbar_arrive_expect_tx(&sm->pfull[st], C::PBYTES);
                         const int kc = (int)(ip * C::KSTAGE);
-                        if (a.offsets == nullptr)
+                        if (GATED) {
                             ptx::tma_load_2d(pring + st * C::PBYTES, &tmap_w, &sm->pfull[st], kc / 2, n0);
-                        else
+                            ptx::tma_load_2d(pring + st * C::PBYTES + C::PBYTES / 2, &tmap_w2, &sm->pfull[st],
+                                             kc / 2, n0);
+                        } else if (a.offsets == nullptr) {
+                            ptx::tma_load_2d(pring + st * C::PBYTES, &tmap_w, &sm->pfull[st], kc / 2, n0);
+                        } else {
                             ptx::tma_load_3d(pring + st * C::PBYTES, &tmap_w, &sm->pfull[st], kc / 2, n0, expert);
+                        }
                         ++ip;
                         moved = true;
                     }
@@ -425,9 +438,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int gk = (int)(a.K / C::G);          // groups per row
         int64_t grp = 0;
         bool ok = true;
-        const int64_t n = n_tile * kRowsPerTile + r;
+        const int64_t n = n_tile * kOutRows + (GATED ? (r & 63) : r);
         const bool n_ok = n < a.N;
-        const uint16_t* srow = a.s + ((int64_t)expert * a.N + (n_ok ? n : 0)) * gk;
+        const uint16_t* srow = (GATED && r >= 64 ? a.s2 : a.s) + ((int64_t)expert * a.N + (n_ok ? n : 0)) * gk;
         float acc[C::BNP];
 #pragma unroll
         for (int j = 0; j < C::BNP; ++j) acc[j] = 0.0f;
@@ -519,13 +532,40 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 load_run(run1, gb + 3 * SB);
             }
         }
-        if (ok && n_ok) {
-            const int m0 = row0 + cp * C::BNP;  // first token of this thread's share
+        const int m0 = row0 + cp * C::BNP;  // first token of this thread's share
+        if constexpr (GATED) {
+            // The up rows (lanes 64-127) hand their fp32 sums to the gate rows of the
+            // same n through shared memory. The x ring is idle by now: every stage's
+            // MMAs completed before the last group partial was published. Every
+            // epilogue thread reaches both barriers; a failed wait anywhere has set
+            // the abort flag before the first one.
+            if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
+            float* xch = reinterpret_cast<float*>(xring);  // [BN tokens][64 rows]
+            ptx::named_bar_sync(1, C::EPIW * 32);
+            const bool all_ok = !*abort;
+            if (all_ok && r >= 64) {
 #pragma unroll
-            for (int j = 0; j < C::BNP; ++j)
-                if (m0 + j < row_end) a.y[(int64_t)(m0 + j) * a.N + n] = __half_as_ushort(__float2half_rn(acc[j]));
+                for (int j = 0; j < C::BNP; ++j) xch[(cp * C::BNP + j) * 64 + (r - 64)] = acc[j];
+            }
+            ptx::named_bar_sync(1, C::EPIW * 32);
+            if (all_ok && r < 64 && n_ok) {
+#pragma unroll
+                for (int j = 0; j < C::BNP; ++j) {
+                    if (m0 + j < row_end) {
+                        const float g = acc[j], u = xch[(cp * C::BNP + j) * 64 + r];
+                        const float silu = g / (1.0f + expf(-g));
+                        a.y[(int64_t)(m0 + j) * a.N + n] = __half_as_ushort(__float2half_rn(silu * u));
+                    }
+                }
+            }
+        } else {
+            if (ok && n_ok) {
+#pragma unroll
+                for (int j = 0; j < C::BNP; ++j)
+                    if (m0 + j < row_end) a.y[(int64_t)(m0 + j) * a.N + n] = __half_as_ushort(__float2half_rn(acc[j]));
+            }
+            if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
         }
-        if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
     }
 
     ptx::tc_fence_before();
@@ -555,7 +595,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 template <class C>
 w4a16_status make_maps(const uint16_t* x, const uint8_t* qw, int64_t M, int64_t N, int64_t K, int E, bool grouped,
-                       CUtensorMap* mx, CUtensorMap* mw) {
+                       CUtensorMap* mx, CUtensorMap* mw, int w_rows = kRowsPerTile) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cuda_status(cudaErrorNotSupported, "gemm: cuTensorMapEncodeTiled entry point");
     {
@@ -571,7 +611,7 @@ w4a16_status make_maps(const uint16_t* x, const uint8_t* qw, int64_t M, int64_t 
     if (!grouped) {
         cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
         cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-        cuuint32_t box[2] = {(cuuint32_t)(C::KSTAGE / 2), (cuuint32_t)kRowsPerTile};
+        cuuint32_t box[2] = {(cuuint32_t)(C::KSTAGE / 2), (cuuint32_t)w_rows};
         cuuint32_t es[2] = {1, 1};
         if (enc(mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(qw), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, C::PSWIZZLE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -590,14 +630,15 @@ w4a16_status make_maps(const uint16_t* x, const uint8_t* qw, int64_t M, int64_t 
     return W4A16_OK;
 }
 
-template <class C>
-w4a16_status launch(int dev, const CUtensorMap& mx, const CUtensorMap& mw, const Args& a, dim3 grid, cudaStream_t st) {
+template <class C, bool GATED = false>
+w4a16_status launch(int dev, const CUtensorMap& mx, const CUtensorMap& mw, const CUtensorMap& mw2, const Args& a,
+                    dim3 grid, cudaStream_t st) {
     static PerDeviceOnce once;
     const cudaError_t attr_err = once.run(dev, [] {
-        return cudaFuncSetAttribute(tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        return cudaFuncSetAttribute(tc_kernel<C, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     });
     if (attr_err != cudaSuccess) return cuda_status(attr_err, "gemm: cudaFuncSetAttribute");
-    tc_kernel<C><<<grid, C::THREADS, C::SMEM, st>>>(mx, mw, a);
+    tc_kernel<C, GATED><<<grid, C::THREADS, C::SMEM, st>>>(mx, mw, mw2, a);
     return cuda_status(cudaGetLastError(), "gemm: kernel launch");
 }
 
@@ -625,9 +666,34 @@ w4a16_status gemm_g(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw,
     // weight-row tile (x_sorted is larger than L2 at the routed workloads).
     if (offsets && mt <= 65535) {
         a.n_fast = 1;
-        return launch<C>(dev.device, mx, mw, a, dim3((unsigned)nt, (unsigned)mt), st);
+        return launch<C>(dev.device, mx, mw, mw, a, dim3((unsigned)nt, (unsigned)mt), st);
     }
-    return launch<C>(dev.device, mx, mw, a, dim3((unsigned)mt, (unsigned)nt), st);
+    return launch<C>(dev.device, mx, mw, mw, a, dim3((unsigned)mt, (unsigned)nt), st);
+}
+
+// Gated pair: each CTA covers 64 outputs n with the 64 matching rows of Wg and Wu.
+template <class C>
+w4a16_status gemm_gated_g(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qg, const uint16_t* sg,
+                          const uint8_t* qu, const uint16_t* su, uint16_t* y, int64_t M, int64_t N, int64_t K,
+                          cudaStream_t st) {
+    if ((size_t)C::SMEM > dev.smem_optin) return W4A16_ERR_UNSUPPORTED;
+    CUtensorMap mx, mg, mu, unused;
+    w4a16_status ms = make_maps<C>(x, qg, M, N, K, 1, false, &mx, &mg, kRowsPerTile / 2);
+    if (ms == W4A16_OK) ms = make_maps<C>(x, qu, M, N, K, 1, false, &unused, &mu, kRowsPerTile / 2);
+    if (ms != W4A16_OK) return ms;
+    Args a{};
+    a.s = sg;
+    a.s2 = su;
+    a.y = y;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.E = 1;
+    a.err = dev.error_word;
+    const int64_t mt = (M + C::BN - 1) / C::BN;
+    const int64_t nt = (N + kRowsPerTile / 2 - 1) / (kRowsPerTile / 2);
+    if (mt > 0x7fffffffLL || nt > 65535) return W4A16_ERR_UNSUPPORTED;
+    return launch<C, true>(dev.device, mx, mg, mu, a, dim3((unsigned)mt, (unsigned)nt), st);
 }
 
 }  // namespace
@@ -650,6 +716,27 @@ w4a16_status gemm_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
         default: return W4A16_ERR_UNSUPPORTED;                                                       \
     }
     if (bn == 0) W4A16_GEMM(MoeCfg)
+    if (bn == 32) W4A16_GEMM(Narrow32Cfg)
+    if (bn == 64) W4A16_GEMM(Narrow64Cfg)
+    W4A16_GEMM(PrefillCfg)
+#undef W4A16_GEMM
+}
+
+w4a16_status gemm_gated_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qweight_gate,
+                               const uint16_t* scales_gate, const uint8_t* qweight_up, const uint16_t* scales_up,
+                               uint16_t* y, int64_t M, int64_t N, int64_t K, int group, cudaStream_t st) {
+    if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
+    const int bn = M > 64 ? 128 : (M > 32 ? 64 : 32);
+#define W4A16_GEMM(CFG)                                                                                    \
+    switch (group) {                                                                                       \
+        case 32: return gemm_gated_g<CFG<32>>(dev, x, qweight_gate, scales_gate, qweight_up, scales_up, y, \
+                                              M, N, K, st);                                                \
+        case 64: return gemm_gated_g<CFG<64>>(dev, x, qweight_gate, scales_gate, qweight_up, scales_up, y, \
+                                              M, N, K, st);                                                \
+        case 128: return gemm_gated_g<CFG<128>>(dev, x, qweight_gate, scales_gate, qweight_up, scales_up,  \
+                                                y, M, N, K, st);                                           \
+        default: return W4A16_ERR_UNSUPPORTED;                                                             \
+    }
     if (bn == 32) W4A16_GEMM(Narrow32Cfg)
     if (bn == 64) W4A16_GEMM(Narrow64Cfg)
     W4A16_GEMM(PrefillCfg)
