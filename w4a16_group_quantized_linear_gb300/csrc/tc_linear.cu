@@ -14,8 +14,9 @@
 //                TMEM A stage frees up.
 //   warp 1       TMEM allocation and the MMA issuer: one lane issues
 //                tcgen05.mma.kind::f16 with A (the dequantized weights) read
-//                from TMEM and B (x) from shared memory; one commit per stage
-//                releases both the x slot and the TMEM A stage.
+//                from TMEM and B (x) from shared memory; per stage one commit
+//                releases the x slot and one the TMEM A stage (the two rings
+//                may differ in depth).
 //   DEQW warps   dequant: thread = TMEM lane = weight row; expands its row's
 //                nibbles of the stage into the exact fp16 integers q (natural
 //                k order) and writes them into the TMEM A stage (tcgen05.st).
@@ -61,13 +62,15 @@ __device__ __forceinline__ constexpr bool may_issue(int64_t) { return true; }
 #define W4A16_COUNT_TMEM(field) ((void)0)
 #endif
 
-template <int G_, int BN_, int KSTAGE_, int PSTAGES_, int XSTAGES_, int DEQW_, int EPIW_, bool SRUNS_ = false>
+template <int G_, int BN_, int KSTAGE_, int PSTAGES_, int XSTAGES_, int DEQW_, int EPIW_, bool SRUNS_ = false,
+          int ASTAGES_ = XSTAGES_>
 struct Cfg {
     static constexpr int G = G_;              // scale group
     static constexpr int BN = BN_;            // tokens per tile (MMA N)
     static constexpr int KSTAGE = KSTAGE_;    // k per pipeline stage
     static constexpr int PSTAGES = PSTAGES_;  // packed-weight ring depth
-    static constexpr int XSTAGES = XSTAGES_;  // x ring depth = TMEM A ring depth
+    static constexpr int XSTAGES = XSTAGES_;  // x ring depth
+    static constexpr int ASTAGES = ASTAGES_;  // TMEM A ring depth
     static constexpr int DEQW = DEQW_;        // dequant warps (multiple of 4)
     static constexpr int EPIW = EPIW_;        // epilogue warps (multiple of 4)
     static constexpr bool SRUNS = SRUNS_;     // scales in 16-byte runs, 16-24 groups ahead
@@ -91,10 +94,10 @@ struct Cfg {
         KSTAGE == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : (KSTAGE == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
 
     static_assert(KSTAGE % 64 == 0 && KSTAGE <= 256, "stage shape");
-    static_assert(DCOLS + XSTAGES * ACOLS <= TMEM_COLS, "TMEM budget");
+    static_assert(DCOLS + ASTAGES * ACOLS <= TMEM_COLS, "TMEM budget");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
     static_assert(PART_K % 64 == 0 && BNP % 16 == 0, "per-thread shares");
-    static_assert(PSTAGES <= 8 && XSTAGES <= 4 && PSTAGES > XSTAGES, "ring depths");
+    static_assert(PSTAGES <= 8 && XSTAGES <= 8 && ASTAGES <= 4 && PSTAGES >= ASTAGES, "ring depths");
     static_assert(PBYTES % 1024 == 0 && XBYTES % 1024 == 0, "1024-byte aligned stages");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
@@ -128,9 +131,10 @@ struct Args {
 struct Smem {
     uint64_t pfull[8];   // a packed-weight stage landed
     uint64_t pempty[8];  // the dequant warps finished reading a packed stage
-    uint64_t xfull[4];   // an x stage landed
-    uint64_t xempty[4];  // the MMAs reading an x stage and its TMEM A stage finished
+    uint64_t xfull[8];   // an x stage landed
+    uint64_t xempty[8];  // the MMAs reading an x stage finished
     uint64_t afull[4];   // a TMEM A stage was written
+    uint64_t aempty[4];  // the MMAs reading a TMEM A stage finished
     uint64_t dfull[2];   // group partial ready in TMEM buffer b
     uint64_t dempty[2];  // epilogue done reading TMEM buffer b
     uint64_t mma_done;
@@ -197,10 +201,16 @@ __device__ __forceinline__ int packed_offset(int r, int c) {
     else return r * 32 + ((c ^ ((r >> 2) & 1)) << 4);                             // 32-byte swizzle
 }
 
-// GATED: the tile's 128 weight rows are 64 rows of Wg (TMEM lanes 0-63) and
-// the same 64 rows of Wu (lanes 64-127), loaded as two boxes of 64 rows into
-// one packed stage (tmap_w, tmap_w2); the CTA forms y = silu(g) * u for its 64
-// outputs from the fp32 sums.
+// GATED: the tile's 128 weight rows are 64 rows of Wg and the same 64 rows of
+// Wu, loaded as two boxes of 64 rows into one packed stage (tmap_w, tmap_w2;
+// shared-memory rows 0-63 and 64-127); the CTA forms y = silu(g) * u for its
+// 64 outputs from the fp32 sums. TMEM lane r holds output o = 8 (r / 16) +
+// r % 8 of the gate (bit 3 of r clear) or of the up projection (bit 3 set), so
+// the g and u of one output sit in lanes r and r ^ 8 of the same warp and meet
+// through one shuffle; each run of 8 lanes reads 8 distinct swizzle rows.
+__device__ __forceinline__ int gated_out_row(int r) { return ((r >> 4) << 3) | (r & 7); }
+__device__ __forceinline__ int gated_smem_row(int r) { return ((r >> 3) & 1) * 64 + gated_out_row(r); }
+
 template <class C, bool GATED>
 __global__ void __launch_bounds__(C::THREADS, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
@@ -233,7 +243,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int i = 0; i < C::XSTAGES; ++i) {
                 ptx::mbar_init(&sm->xfull[i], 1);
                 ptx::mbar_init(&sm->xempty[i], 1);
+            }
+            for (int i = 0; i < C::ASTAGES; ++i) {
                 ptx::mbar_init(&sm->afull[i], C::DEQW * 32);
+                ptx::mbar_init(&sm->aempty[i], 1);
             }
             for (int b = 0; b < 2; ++b) {
                 ptx::mbar_init(&sm->dfull[b], 1);
@@ -333,17 +346,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             int cur_b = 0;
             bool ok = true;
             for (int64_t c = 0; ok && c < nst; ++c) {
-                const int xs = (int)(c % C::XSTAGES);
-                const uint32_t par = (uint32_t)((c / C::XSTAGES) & 1);
-                if (!ptx::mbar_wait(&sm->xfull[xs], par, abort, wait_limit()) ||
-                    !ptx::mbar_wait(&sm->afull[xs], par, abort, wait_limit())) {
+                const int xs = (int)(c % C::XSTAGES), as = (int)(c % C::ASTAGES);
+                if (!ptx::mbar_wait(&sm->xfull[xs], (uint32_t)((c / C::XSTAGES) & 1), abort, wait_limit()) ||
+                    !ptx::mbar_wait(&sm->afull[as], (uint32_t)((c / C::ASTAGES) & 1), abort, wait_limit())) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const int64_t kc = c * C::KSTAGE;
                 const uint64_t bdesc0 = ptx::smem_desc_sw128(ptx::smem_u32(xring + xs * C::XBYTES));
-                const uint32_t a_col = tmem + (uint32_t)(C::DCOLS + xs * C::ACOLS);
+                const uint32_t a_col = tmem + (uint32_t)(C::DCOLS + as * C::ACOLS);
                 const int nk = (int)((a.K - kc < C::KSTAGE ? a.K - kc : C::KSTAGE) >> 4);
                 const bool stage_opens = C::KSTAGE >= C::G || (kc % C::G) == 0;
                 const bool stage_closes = C::KSTAGE >= C::G || ((kc + C::KSTAGE) % C::G) == 0;
@@ -373,7 +385,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                ptx::mma_commit(&sm->xempty[xs]);  // x slot and TMEM A stage are free again
+                ptx::mma_commit(&sm->xempty[xs]);  // the x slot is free again
+                ptx::mma_commit(&sm->aempty[as]);  // and so is the TMEM A stage
             }
             if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
             ptx::mma_commit(&sm->mma_done);
@@ -389,27 +402,28 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         constexpr int CH = C::PART_K / 32;         // 16-byte packed chunks (32 k each) per thread
         bool ok = true;
         for (int64_t c = 0; c < nst; ++c) {
-            const int ps = (int)(c % C::PSTAGES), xs = (int)(c % C::XSTAGES);
-            const int64_t around = c / C::XSTAGES;
+            const int ps = (int)(c % C::PSTAGES), as = (int)(c % C::ASTAGES);
+            const int64_t around = c / C::ASTAGES;
             // warp-uniform outcome: the TMEM stores below are .sync.aligned
             const bool got = ptx::mbar_wait(&sm->pfull[ps], (uint32_t)((c / C::PSTAGES) & 1), abort, wait_limit()) &&
                              (around == 0 ||
-                              ptx::mbar_wait(&sm->xempty[xs], (uint32_t)((around - 1) & 1), abort, wait_limit()));
+                              ptx::mbar_wait(&sm->aempty[as], (uint32_t)((around - 1) & 1), abort, wait_limit()));
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
             const uint8_t* prow = pring + ps * C::PBYTES;
+            const int prow_r = GATED ? gated_smem_row(r) : r;  // shared-memory row of this TMEM lane
             const uint32_t tcol = tmem + ((uint32_t)(quad * 32) << 16) +
-                                  (uint32_t)(C::DCOLS + xs * C::ACOLS + part * (C::PART_K / 2));
+                                  (uint32_t)(C::DCOLS + as * C::ACOLS + part * (C::PART_K / 2));
 #pragma unroll
             for (int h = 0; h < CH; h += 2) {  // two chunks = 64 k = 32 columns per store
                 uint32_t v[32];
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const uint4 p =
-                        *reinterpret_cast<const uint4*>(prow + packed_offset<C::KSTAGE>(r, part * CH + h + q));
+                        *reinterpret_cast<const uint4*>(prow + packed_offset<C::KSTAGE>(prow_r, part * CH + h + q));
                     const uint32_t words[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {  // word j holds k = 8j .. 8j+7 of this chunk
@@ -426,7 +440,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             ptx::mbar_arrive(&sm->pempty[ps]);  // this thread has read its packed bytes
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&sm->afull[xs]);
+            ptx::mbar_arrive(&sm->afull[as]);
         }
         if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
     } else {
@@ -438,9 +452,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int gk = (int)(a.K / C::G);          // groups per row
         int64_t grp = 0;
         bool ok = true;
-        const int64_t n = n_tile * kOutRows + (GATED ? (r & 63) : r);
+        const bool up_row = GATED && ((r >> 3) & 1);
+        const int64_t n = n_tile * kOutRows + (GATED ? gated_out_row(r) : r);
         const bool n_ok = n < a.N;
-        const uint16_t* srow = (GATED && r >= 64 ? a.s2 : a.s) + ((int64_t)expert * a.N + (n_ok ? n : 0)) * gk;
+        const uint16_t* srow = (up_row ? a.s2 : a.s) + ((int64_t)expert * a.N + (n_ok ? n : 0)) * gk;
         float acc[C::BNP];
 #pragma unroll
         for (int j = 0; j < C::BNP; ++j) acc[j] = 0.0f;
@@ -534,30 +549,25 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         const int m0 = row0 + cp * C::BNP;  // first token of this thread's share
         if constexpr (GATED) {
-            // The up rows (lanes 64-127) hand their fp32 sums to the gate rows of the
-            // same n through shared memory. The x ring is idle by now: every stage's
-            // MMAs completed before the last group partial was published. Every
-            // epilogue thread reaches both barriers; a failed wait anywhere has set
-            // the abort flag before the first one.
-            if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
-            float* xch = reinterpret_cast<float*>(xring);  // [BN tokens][64 rows]
-            ptx::named_bar_sync(1, C::EPIW * 32);
-            const bool all_ok = !*abort;
-            if (all_ok && r >= 64) {
+            // Lanes r and r ^ 8 hold g and u of output n: the gate lane finishes the even
+            // tokens of each pair and the up lane the odd ones, each handing the other
+            // the operand it lacks. The shuffles need the whole warp, so ok is reduced
+            // over the warp first (a time-out can strike its lanes apart).
+            const bool warp_ok = __all_sync(0xffffffffu, ok);
+            if (warp_ok) {
 #pragma unroll
-                for (int j = 0; j < C::BNP; ++j) xch[(cp * C::BNP + j) * 64 + (r - 64)] = acc[j];
-            }
-            ptx::named_bar_sync(1, C::EPIW * 32);
-            if (all_ok && r < 64 && n_ok) {
-#pragma unroll
-                for (int j = 0; j < C::BNP; ++j) {
-                    if (m0 + j < row_end) {
-                        const float g = acc[j], u = xch[(cp * C::BNP + j) * 64 + r];
-                        const float silu = g / (1.0f + expf(-g));
-                        a.y[(int64_t)(m0 + j) * a.N + n] = __half_as_ushort(__float2half_rn(silu * u));
+                for (int j = 0; j < C::BNP; j += 2) {
+                    const float mine = up_row ? acc[j] : acc[j + 1];
+                    const float other = __shfl_xor_sync(0xffffffffu, mine, 8);
+                    const float g = up_row ? other : acc[j], u = up_row ? acc[j + 1] : other;
+                    const int m = m0 + j + (up_row ? 1 : 0);
+                    if (n_ok && m < row_end) {
+                        const float silu = __fdividef(g, 1.0f + __expf(-g));
+                        a.y[(int64_t)m * a.N + n] = __half_as_ushort(__float2half_rn(silu * u));
                     }
                 }
             }
+            if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
         } else {
             if (ok && n_ok) {
 #pragma unroll
