@@ -123,8 +123,9 @@ struct Args {
     uint16_t* y;
     const int32_t* offsets;  // routed experts; nullptr: dense
     int64_t M, N, K;
+    int64_t mt, tiles;  // dense: token tiles, and tiles in all (token tile fastest)
     int E;
-    int n_fast;  // 1: blockIdx.x is the weight-row tile and blockIdx.y the token tile
+    int n_fast;  // routed experts: 1 if blockIdx.x is the weight-row tile and blockIdx.y the token tile
     unsigned int* err;
 };
 
@@ -222,16 +223,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint8_t* xring = base + C::XOFF;      // x stages
     Smem* sm = reinterpret_cast<Smem*>(xring + C::XSTAGES * C::XBYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n_tile = a.n_fast ? blockIdx.x : blockIdx.y;
-    const int m_tile = (int)(a.n_fast ? blockIdx.y : blockIdx.x);
-    const int64_t nst = (a.K + C::KSTAGE - 1) / C::KSTAGE;  // stages over K
+    const int64_t nst = (a.K + C::KSTAGE - 1) / C::KSTAGE;  // stages over K per tile
+    // Dense: a persistent grid; this CTA takes tiles blockIdx.x, + gridDim.x, ...
+    // and its rings, TMEM and group counters run on from one tile into the next,
+    // so a tile's epilogue overlaps the next tile's loads and MMAs. Routed
+    // experts: one tile per CTA, found from the device offsets.
+    const bool dense = a.offsets == nullptr;
+    const int64_t my_tiles = dense ? (a.tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 1;
+    const int64_t my_stages = my_tiles * nst;
 
     if (warp == 0) {
-        if (a.offsets != nullptr) {
-            find_tile<C::BN>(a, sm, lane, m_tile);
+        if (!dense) {
+            find_tile<C::BN>(a, sm, lane, (int)(a.n_fast ? blockIdx.y : blockIdx.x));
         } else if (lane == 0) {
             sm->expert = 0;
-            sm->row0 = m_tile * C::BN;
+            sm->row0 = 0;
             sm->row_end = (int)a.M;
             sm->valid = 1;
         }
@@ -271,25 +277,32 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = sm->tmem_base;
-    const int expert = sm->expert, row0 = sm->row0, row_end = sm->row_end;
+    const int expert = sm->expert, row_end = sm->row_end;
     volatile int* abort = &sm->abort;
+    // tile j of this CTA: its first token and its weight-row tile
+    auto tile_row0 = [&](int64_t j) -> int {
+        return dense ? (int)(((int64_t)blockIdx.x + j * gridDim.x) % a.mt * C::BN) : sm->row0;
+    };
+    auto tile_n = [&](int64_t j) -> int64_t {
+        return dense ? ((int64_t)blockIdx.x + j * gridDim.x) / a.mt : (a.n_fast ? blockIdx.x : blockIdx.y);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
-            const int n0 = (int)(n_tile * kOutRows);
             int64_t ip = 0, ix = 0;  // stages issued on each ring
             // Both rings are polled, so a full ring never holds up the other one.
             bool ok = true;
             uint64_t idle_since = 0;
-            while (ip < nst || ix < nst) {
+            while (ip < my_stages || ix < my_stages) {
                 bool moved = false;
-                if (ix < nst && may_issue(ip + ix)) {
+                if (ix < my_stages && may_issue(ip + ix)) {
                     const int st = (int)(ix % C::XSTAGES);
                     const int64_t round = ix / C::XSTAGES;
                     if (round == 0 || ptx::mbar_try_wait(&sm->xempty[st], (uint32_t)((round - 1) & 1))) {
                         ptx::mbar_arrive_expect_tx(&sm->xfull[st], C::XBYTES);
-                        const int kc = (int)(ix * C::KSTAGE);
+                        const int kc = (int)(ix % nst * C::KSTAGE);
+                        const int row0 = tile_row0(ix / nst);
 #pragma unroll
                         for (int b = 0; b < C::XBOXES; ++b)
                             ptx::tma_load_2d(xring + st * C::XBYTES + b * C::XBOX_BYTES, &tmap_x, &sm->xfull[st],
@@ -298,12 +311,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         moved = true;
                     }
                 }
-                if (ip < nst && may_issue(ip + ix)) {
+                if (ip < my_stages && may_issue(ip + ix)) {
                     const int st = (int)(ip % C::PSTAGES);
                     const int64_t round = ip / C::PSTAGES;
                     if (round == 0 || ptx::mbar_try_wait(&sm->pempty[st], (uint32_t)((round - 1) & 1))) {
                         ptx::mbar_arrive_expect_tx(&sm->pfull[st], C::PBYTES);
-                        const int kc = (int)(ip * C::KSTAGE);
+                        const int kc = (int)(ip % nst * C::KSTAGE);
+                        const int n0 = (int)(tile_n(ip / nst) * kOutRows);
                         if (GATED) {
                             ptx::tma_load_2d(pring + st * C::PBYTES, &tmap_w, &sm->pfull[st], kc / 2, n0);
                             ptx::tma_load_2d(pring + st * C::PBYTES + C::PBYTES / 2, &tmap_w2, &sm->pfull[st],
@@ -345,7 +359,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             int64_t grp = 0;
             int cur_b = 0;
             bool ok = true;
-            for (int64_t c = 0; ok && c < nst; ++c) {
+            for (int64_t c = 0; ok && c < my_stages; ++c) {
                 const int xs = (int)(c % C::XSTAGES), as = (int)(c % C::ASTAGES);
                 if (!ptx::mbar_wait(&sm->xfull[xs], (uint32_t)((c / C::XSTAGES) & 1), abort, wait_limit()) ||
                     !ptx::mbar_wait(&sm->afull[as], (uint32_t)((c / C::ASTAGES) & 1), abort, wait_limit())) {
@@ -353,7 +367,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                const int64_t kc = c * C::KSTAGE;
+                const int64_t kc = c % nst * C::KSTAGE;
                 const uint64_t bdesc0 = ptx::smem_desc_sw128(ptx::smem_u32(xring + xs * C::XBYTES));
                 const uint32_t a_col = tmem + (uint32_t)(C::DCOLS + as * C::ACOLS);
                 const int nk = (int)((a.K - kc < C::KSTAGE ? a.K - kc : C::KSTAGE) >> 4);
@@ -401,7 +415,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int r = quad * 32 + lane;            // weight row in the tile = TMEM lane
         constexpr int CH = C::PART_K / 32;         // 16-byte packed chunks (32 k each) per thread
         bool ok = true;
-        for (int64_t c = 0; c < nst; ++c) {
+        for (int64_t c = 0; c < my_stages; ++c) {
             const int ps = (int)(c % C::PSTAGES), as = (int)(c % C::ASTAGES);
             const int64_t around = c / C::ASTAGES;
             // warp-uniform outcome: the TMEM stores below are .sync.aligned
@@ -451,14 +465,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int r = quad * 32 + lane;            // weight row in the tile
         const int gk = (int)(a.K / C::G);          // groups per row
         int64_t grp = 0;
-        bool ok = true;
+        bool ok = true;  // warp-uniform: every failed wait below is agreed on by the whole warp
         const bool up_row = GATED && ((r >> 3) & 1);
-        const int64_t n = n_tile * kOutRows + (GATED ? gated_out_row(r) : r);
-        const bool n_ok = n < a.N;
-        const uint16_t* srow = (up_row ? a.s2 : a.s) + ((int64_t)expert * a.N + (n_ok ? n : 0)) * gk;
+        int64_t n = 0;                  // this thread's output row in the current tile
+        bool n_ok = false;
+        const uint16_t* srow = a.s;     // and its scale row
         float acc[C::BNP];
-#pragma unroll
-        for (int j = 0; j < C::BNP; ++j) acc[j] = 0.0f;
         // Scales are streamed from HBM once. Dense tiles keep SB..2 SB groups of them in flight
         // (scalar loads); with SRUNS they come in runs of 8 groups (one 16-byte load when a
         // scale row is a multiple of 16 bytes), three runs in flight, 16 to 24 groups ahead.
@@ -527,6 +539,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 ++grp;
             }
         };
+        for (int64_t jt = 0; ok && jt < my_tiles; ++jt) {
+        n = tile_n(jt) * kOutRows + (GATED ? gated_out_row(r) : r);
+        n_ok = n < a.N;
+        srow = (up_row ? a.s2 : a.s) + ((int64_t)expert * a.N + (n_ok ? n : 0)) * gk;
+#pragma unroll
+        for (int j = 0; j < C::BNP; ++j) acc[j] = 0.0f;
         load_run(run0, 0);
         load_run(run1, SB);
         if constexpr (C::SRUNS) {
@@ -547,14 +565,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 load_run(run1, gb + 3 * SB);
             }
         }
-        const int m0 = row0 + cp * C::BNP;  // first token of this thread's share
+        if (!ok) break;
+        const int m0 = tile_row0(jt) + cp * C::BNP;  // first token of this thread's share
         if constexpr (GATED) {
             // Lanes r and r ^ 8 hold g and u of output n: the gate lane finishes the even
             // tokens of each pair and the up lane the odd ones, each handing the other
-            // the operand it lacks. The shuffles need the whole warp, so ok is reduced
-            // over the warp first (a time-out can strike its lanes apart).
-            const bool warp_ok = __all_sync(0xffffffffu, ok);
-            if (warp_ok) {
+            // the operand it lacks (the whole warp is here: ok is warp-uniform).
+            {
 #pragma unroll
                 for (int j = 0; j < C::BNP; j += 2) {
                     const float mine = up_row ? acc[j] : acc[j + 1];
@@ -567,15 +584,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                 }
             }
-            if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
         } else {
-            if (ok && n_ok) {
+            if (n_ok) {
 #pragma unroll
                 for (int j = 0; j < C::BNP; ++j)
                     if (m0 + j < row_end) a.y[(int64_t)(m0 + j) * a.N + n] = __half_as_ushort(__float2half_rn(acc[j]));
             }
-            if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
         }
+        }
+        if (!ok) fail(a, sm, W4A16_ERR_TIMEOUT);
     }
 
     ptx::tc_fence_before();
@@ -640,15 +657,26 @@ w4a16_status make_maps(const uint16_t* x, const uint8_t* qw, int64_t M, int64_t 
     return W4A16_OK;
 }
 
+// A dense launch is a persistent grid of one CTA per SM: each CTA holds all of
+// an SM's TMEM for its lifetime, so a second CTA on the same SM would only
+// wait. Configurations whose shared memory would let two CTAs share an SM ask
+// for just over half of the SM's shared memory instead.
+template <class C>
+size_t dense_smem(const DeviceInfo& dev) {
+    const size_t half = dev.smem_optin / 2 + 1024;
+    return (size_t)C::SMEM > half ? (size_t)C::SMEM : half;
+}
+
 template <class C, bool GATED = false>
-w4a16_status launch(int dev, const CUtensorMap& mx, const CUtensorMap& mw, const CUtensorMap& mw2, const Args& a,
-                    dim3 grid, cudaStream_t st) {
+w4a16_status launch(const DeviceInfo& dev, const CUtensorMap& mx, const CUtensorMap& mw, const CUtensorMap& mw2,
+                    const Args& a, dim3 grid, size_t smem, cudaStream_t st) {
     static PerDeviceOnce once;
-    const cudaError_t attr_err = once.run(dev, [] {
-        return cudaFuncSetAttribute(tc_kernel<C, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    const cudaError_t attr_err = once.run(dev.device, [&dev] {
+        return cudaFuncSetAttribute(tc_kernel<C, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)dev.smem_optin);
     });
     if (attr_err != cudaSuccess) return cuda_status(attr_err, "gemm: cudaFuncSetAttribute");
-    tc_kernel<C, GATED><<<grid, C::THREADS, C::SMEM, st>>>(mx, mw, mw2, a);
+    tc_kernel<C, GATED><<<grid, C::THREADS, smem, st>>>(mx, mw, mw2, a);
     return cuda_status(cudaGetLastError(), "gemm: kernel launch");
 }
 
@@ -671,14 +699,20 @@ w4a16_status gemm_g(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw,
     const int64_t mt = offsets ? (M + C::BN - 1) / C::BN + E : (M + C::BN - 1) / C::BN;
     const int64_t nt = (N + kRowsPerTile - 1) / kRowsPerTile;
     if (mt > 0x7fffffffLL || nt > 65535) return W4A16_ERR_UNSUPPORTED;
+    a.mt = mt;
+    a.tiles = mt * nt;
+    if (!offsets) {  // persistent: token tiles of one weight-row tile are consecutive, sharing it in L2
+        const int64_t grid = a.tiles < dev.sms ? a.tiles : dev.sms;
+        return launch<C>(dev, mx, mw, mw, a, dim3((unsigned)grid), dense_smem<C>(dev), st);
+    }
     // Routed experts: the weight-row tiles of one token tile run side by side, so
     // they share that x tile in L2 instead of streaming x from HBM once per
     // weight-row tile (x_sorted is larger than L2 at the routed workloads).
-    if (offsets && mt <= 65535) {
+    if (mt <= 65535) {
         a.n_fast = 1;
-        return launch<C>(dev.device, mx, mw, mw, a, dim3((unsigned)nt, (unsigned)mt), st);
+        return launch<C>(dev, mx, mw, mw, a, dim3((unsigned)nt, (unsigned)mt), C::SMEM, st);
     }
-    return launch<C>(dev.device, mx, mw, mw, a, dim3((unsigned)mt, (unsigned)nt), st);
+    return launch<C>(dev, mx, mw, mw, a, dim3((unsigned)mt, (unsigned)nt), C::SMEM, st);
 }
 
 // Gated pair: each CTA covers 64 outputs n with the 64 matching rows of Wg and Wu.
@@ -702,8 +736,11 @@ w4a16_status gemm_gated_g(const DeviceInfo& dev, const uint16_t* x, const uint8_
     a.err = dev.error_word;
     const int64_t mt = (M + C::BN - 1) / C::BN;
     const int64_t nt = (N + kRowsPerTile / 2 - 1) / (kRowsPerTile / 2);
-    if (mt > 0x7fffffffLL || nt > 65535) return W4A16_ERR_UNSUPPORTED;
-    return launch<C, true>(dev.device, mx, mg, mu, a, dim3((unsigned)mt, (unsigned)nt), st);
+    if (mt > 0x7fffffffLL || nt > 0x7fffffffLL / mt) return W4A16_ERR_UNSUPPORTED;
+    a.mt = mt;
+    a.tiles = mt * nt;
+    const int64_t grid = a.tiles < dev.sms ? a.tiles : dev.sms;
+    return launch<C, true>(dev, mx, mg, mu, a, dim3((unsigned)grid), dense_smem<C>(dev), st);
 }
 
 }  // namespace
