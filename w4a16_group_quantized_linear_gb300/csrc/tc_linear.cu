@@ -224,6 +224,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     Smem* sm = reinterpret_cast<Smem*>(xring + C::XSTAGES * C::XBYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nst = (a.K + C::KSTAGE - 1) / C::KSTAGE;  // stages over K per tile
+    const int nst32 = (int)nst;                             // K < 2^31
     // Dense: a persistent grid; this CTA takes tiles blockIdx.x, + gridDim.x, ...
     // and its rings, TMEM and group counters run on from one tile into the next,
     // so a tile's epilogue overlaps the next tile's loads and MMAs. Routed
@@ -291,6 +292,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
             int64_t ip = 0, ix = 0;  // stages issued on each ring
+            // each ring's position in its current tile (kept incrementally: no 64-bit
+            // division per stage on this thread)
+            int sx = 0, sp = 0;
+            int64_t jx = 0, jp = 0;
+            int row0x = tile_row0(0);
+            int n0p = (int)(tile_n(0) * kOutRows);
             // Both rings are polled, so a full ring never holds up the other one.
             bool ok = true;
             uint64_t idle_since = 0;
@@ -301,13 +308,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const int64_t round = ix / C::XSTAGES;
                     if (round == 0 || ptx::mbar_try_wait(&sm->xempty[st], (uint32_t)((round - 1) & 1))) {
                         ptx::mbar_arrive_expect_tx(&sm->xfull[st], C::XBYTES);
-                        const int kc = (int)(ix % nst * C::KSTAGE);
-                        const int row0 = tile_row0(ix / nst);
+                        const int kc = sx * C::KSTAGE;
 #pragma unroll
                         for (int b = 0; b < C::XBOXES; ++b)
                             ptx::tma_load_2d(xring + st * C::XBYTES + b * C::XBOX_BYTES, &tmap_x, &sm->xfull[st],
-                                             kc + 64 * b, row0);
+                                             kc + 64 * b, row0x);
                         ++ix;
+                        if (++sx == nst32) {
+                            sx = 0;
+                            if (++jx < my_tiles) row0x = tile_row0(jx);
+                        }
                         moved = true;
                     }
                 }
@@ -316,8 +326,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const int64_t round = ip / C::PSTAGES;
                     if (round == 0 || ptx::mbar_try_wait(&sm->pempty[st], (uint32_t)((round - 1) & 1))) {
                         ptx::mbar_arrive_expect_tx(&sm->pfull[st], C::PBYTES);
-                        const int kc = (int)(ip % nst * C::KSTAGE);
-                        const int n0 = (int)(tile_n(ip / nst) * kOutRows);
+                        const int kc = sp * C::KSTAGE, n0 = n0p;
                         if (GATED) {
                             ptx::tma_load_2d(pring + st * C::PBYTES, &tmap_w, &sm->pfull[st], kc / 2, n0);
                             ptx::tma_load_2d(pring + st * C::PBYTES + C::PBYTES / 2, &tmap_w2, &sm->pfull[st],
@@ -328,6 +337,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             ptx::tma_load_3d(pring + st * C::PBYTES, &tmap_w, &sm->pfull[st], kc / 2, n0, expert);
                         }
                         ++ip;
+                        if (++sp == nst32) {
+                            sp = 0;
+                            if (++jp < my_tiles) n0p = (int)(tile_n(jp) * kOutRows);
+                        }
                         moved = true;
                     }
                 }
@@ -359,7 +372,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             int64_t grp = 0;
             int cur_b = 0;
             bool ok = true;
-            for (int64_t c = 0; ok && c < my_stages; ++c) {
+            int s_in = 0;  // stage within the current tile
+            for (int64_t c = 0; ok && c < my_stages; ++c, s_in = s_in + 1 == nst32 ? 0 : s_in + 1) {
                 const int xs = (int)(c % C::XSTAGES), as = (int)(c % C::ASTAGES);
                 if (!ptx::mbar_wait(&sm->xfull[xs], (uint32_t)((c / C::XSTAGES) & 1), abort, wait_limit()) ||
                     !ptx::mbar_wait(&sm->afull[as], (uint32_t)((c / C::ASTAGES) & 1), abort, wait_limit())) {
@@ -367,7 +381,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                const int64_t kc = c % nst * C::KSTAGE;
+                const int64_t kc = (int64_t)s_in * C::KSTAGE;
                 const uint64_t bdesc0 = ptx::smem_desc_sw128(ptx::smem_u32(xring + xs * C::XBYTES));
                 const uint32_t a_col = tmem + (uint32_t)(C::DCOLS + as * C::ACOLS);
                 const int nk = (int)((a.K - kc < C::KSTAGE ? a.K - kc : C::KSTAGE) >> 4);
