@@ -532,10 +532,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 ptx::tc_fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * C::BN + cp * C::BNP);
                 const float sv = scale_of(run, i);
+                // The buffer goes back to the MMA thread as soon as the partial is in
+                // registers; the multiply-adds follow.
                 if constexpr (C::BNP == 16) {
                     uint32_t v[16];
                     ptx::tmem_ld_32x32b_x16(taddr, v);
                     ptx::tmem_ld_wait();
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(&sm->dempty[b]);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) acc[j] = fmaf(sv, __uint_as_float(v[j]), acc[j]);
                 } else {
@@ -544,12 +548,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         uint32_t v[32];
                         ptx::tmem_ld_32x32b_x32(taddr + ch * 32, v);
                         ptx::tmem_ld_wait();
+                        if (ch == C::BNP / 32 - 1) {
+                            ptx::tc_fence_before();
+                            ptx::mbar_arrive(&sm->dempty[b]);
+                        }
 #pragma unroll
                         for (int j = 0; j < 32; ++j) acc[ch * 32 + j] = fmaf(sv, __uint_as_float(v[j]), acc[ch * 32 + j]);
                     }
                 }
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(&sm->dempty[b]);
                 ++grp;
             }
         };
