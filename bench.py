@@ -12,10 +12,9 @@ Side measurements in the same JSON line: the batched decode (M=4), the
 prefill GEMM (M=4096, K=5120, N=17408; TFLOP/s) and the routed-expert layer
 (E=128, 4096 tokens, top-8, group 32), when the library provides them.
 
-The decode weights are declared static (W4A16_STATIC_WEIGHTS: nothing
-pending on the stream writes them, as in any decode loop), so each GEMV
-streams its weights while the one before it finishes; the same step without
-the flag is reported beside it.
+The timed step makes the plain calls. The same step with the weights
+declared static (W4A16_STATIC_WEIGHTS: each GEMV streams its weights before
+the one ahead of it has finished) is reported beside it.
 
 --impl reference times the CPU oracle (fp64, single thread) on the same
 workload and metric. With --gpus N > 1 (torchrun), every rank runs an
@@ -239,7 +238,7 @@ def run_gpu(args, rank, world):
     h = torch.empty((M, DECODE[0][1]), dtype=torch.float16, device=dev)
     out = torch.empty((M, DECODE[1][1]), dtype=torch.float16, device=dev)
 
-    def step(i, static=True):
+    def step(i, static=False):
         (qa, sa), (qb, sb) = rot[i % copies]
         w4.linear(x, qa, sa, GROUP, out=h, static_weights=static)
         w4.linear(h, qb, sb, GROUP, out=out, static_weights=static)
@@ -290,10 +289,10 @@ def run_gpu(args, rank, world):
         return {"median_us": statistics.median(samples), "p95_us": samples[int(0.95 * (len(samples) - 1) + 0.5)],
                 "samples": len(samples), "how": "10 regions x 20 back-to-back steps (40 GEMVs), mean per GEMV each"}
 
-    spread = per_call(True)
-    default_mode = per_call(False)
-    default_mode["GB/s"] = per_launch_bytes / (default_mode["median_us"] * 1e-6) / 1e9
-    default_mode["frac_hbm"] = default_mode["GB/s"] / hbm_peak
+    spread = per_call(False)
+    static_mode = per_call(True)
+    static_mode["GB/s"] = per_launch_bytes / (static_mode["median_us"] * 1e-6) / 1e9
+    static_mode["frac_hbm"] = static_mode["GB/s"] / hbm_peak
     w4.device_status()
 
     # ---- end to end through the public API: pinned host x in, host result out.
@@ -351,7 +350,7 @@ def run_gpu(args, rank, world):
 
     cs = clocks.summary()
     return dict(
-        spread=spread, default_mode=default_mode, software=gpu_software(torch),
+        spread=spread, static_mode=static_mode, software=gpu_software(torch),
         value=value, ms_per_step=ms_total / args.steps, kernel_ms=kernel_ms, achieved=achieved,
         hbm_peak=hbm_peak, tc_peak=tc_peak, peak_kind=peak_kind, copies=copies,
         e2e=dict(value=step_bytes * args.steps * world / (e2e_ms * 1e-3) / 1e9, unit="GB/s",
@@ -389,7 +388,7 @@ def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):
     rot = [(qw.clone(), s.clone()) for _ in range(copies)]
     x4 = torch.from_numpy(workloads.activations(g, 4, K)).to(dev)
     y4 = torch.empty((4, N), dtype=torch.float16, device=dev)
-    f = lambda i: w4.linear(x4, rot[i % copies][0], rot[i % copies][1], GROUP, out=y4, static_weights=True)  # noqa: E731
+    f = lambda i: w4.linear(x4, rot[i % copies][0], rot[i % copies][1], GROUP, out=y4)  # noqa: E731
     for i in range(5):
         f(i)
     ms = statistics.median(_time_launches(torch, f, 100))
@@ -400,8 +399,7 @@ def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):
     for Ms in (8, 16, 32, 64):
         xs_ = torch.from_numpy(workloads.activations(g, Ms, K)).to(dev)
         ys_ = torch.empty((Ms, N), dtype=torch.float16, device=dev)
-        f = lambda i: w4.linear(xs_, rot[i % copies][0], rot[i % copies][1], GROUP, out=ys_,  # noqa: E731
-                                static_weights=True)
+        f = lambda i: w4.linear(xs_, rot[i % copies][0], rot[i % copies][1], GROUP, out=ys_)  # noqa: E731
         for i in range(5):
             f(i)
         ms = statistics.median(_time_launches(torch, f, 100))
@@ -417,7 +415,7 @@ def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):
         pairs = [(rot[i][0], rot[i][1], qw2.clone(), s2.clone()) for i in range(copies)]
         x1 = torch.from_numpy(workloads.activations(g, 1, K)).to(dev)
         y1 = torch.empty((1, N), dtype=torch.float16, device=dev)
-        f = lambda i: w4.linear_gated(x1, *pairs[i % copies], GROUP, out=y1, static_weights=True)  # noqa: E731
+        f = lambda i: w4.linear_gated(x1, *pairs[i % copies], GROUP, out=y1)  # noqa: E731
         for i in range(5):
             f(i)
         ms = statistics.median(_time_launches(torch, f, 100))
@@ -730,7 +728,7 @@ def run_profile(case: str, launches: int):
         y = torch.empty((1, N), dtype=torch.float16, device=dev)
         for i in range(launches):  # four gate/up pairs in turn: successive launches miss in L2
             j = 2 * (i % 4)
-            w4.linear_gated(x, *mats[j], *mats[j + 1], GROUP, out=y, static_weights=True)
+            w4.linear_gated(x, *mats[j], *mats[j + 1], GROUP, out=y)
     elif case == "prefill_gated":
         # the gate/up pair at M = 512 in one GEMM with the SiLU * up epilogue
         K, N = DECODE[0]
@@ -770,7 +768,7 @@ def run_profile(case: str, launches: int):
         x = torch.from_numpy(workloads.activations(g, M, K, outlier_frac=0.01 if M > 16 else 0.0)).to(dev)
         y = torch.empty((M, N), dtype=torch.float16, device=dev)
         for i in range(launches):
-            w4.linear(x, *copies[i % 4], GROUP, out=y, static_weights=True)
+            w4.linear(x, *copies[i % 4], GROUP, out=y)
     torch.cuda.synchronize()
     w4.device_status()
     print(f"profile {case}: {launches} launches done")
@@ -854,9 +852,9 @@ def main():
         "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["hbm_peak"], "unit": "GB/s",
                      "frac": r["achieved"] / r["hbm_peak"],
                      "traffic": measured_traffic("gemv.cu", "gemv_decode_m1.md"),
-                     "kernel": "gemv_kernel<group 128, M<=8>, static weights", "peak_kind": r["peak_kind"],
+                     "kernel": "gemv_kernel<group 128, M<=8>", "peak_kind": r["peak_kind"],
                      "kernel_us": r["kernel_ms"] * 1e3, "algorithmic_bytes_per_launch": r["per_launch_bytes"]},
-        "per_call": r["spread"], "default_mode": r["default_mode"],
+        "per_call": r["spread"], "static_weights_mode": r["static_mode"],
         "e2e": r["e2e"], "gpu_launches": r["launches"], "clocks": r["clocks"], "gpu": r["gpu"], "sms": r["sms"],
         "software": r["software"], "source": source_info(), "host": host_info(),
         "side": r["extra"],
