@@ -238,11 +238,11 @@ w4a16_status w4a16_grouped_linear_gather(const uint16_t* x, int64_t T, const int
     const DeviceInfo* dev = nullptr;
     const w4a16_status v = check_linear(x, qweight, scales, y_sorted, R, N, K, group, &dev);
     if (v != W4A16_OK || R == 0 || N == 0) return v;
-    if (!split_supports(group, E)) return W4A16_ERR_UNSUPPORTED;
+    if (group != 32 || !split_supports(group, E)) return W4A16_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
     if (K == 0) return cuda_status(cudaMemsetAsync(y_sorted, 0, (size_t)(R * N) * sizeof(uint16_t), st));
     if (!token_of_row || T == 0) return W4A16_ERR_INVALID_ARG;
-    return split_launch(*dev, x, qweight, scales, y_sorted, R, N, K, expert_offsets, E, token_of_row, T, st);
+    return split_launch(*dev, x, qweight, scales, y_sorted, R, N, K, group, expert_offsets, E, token_of_row, T, st);
 }
 
 namespace {

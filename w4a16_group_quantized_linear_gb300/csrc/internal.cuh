@@ -142,12 +142,12 @@ w4a16_status gemm_gated_launch(const DeviceInfo& dev, const uint16_t* x, const u
                                const uint16_t* scales_gate, const uint8_t* qweight_up, const uint16_t* scales_up,
                                uint16_t* y, int64_t M, int64_t N, int64_t K, int group, cudaStream_t st);
 
-// Tensor-core GEMM for group 32 with the scale split exactly into the A operand
-// (routed experts and dense layers): supported for E <= 4096 experts.
+// Tensor-core GEMM with the scale split exactly into the A operand (routed
+// experts and dense layers): groups 32, 64 and 128, E <= 4096 experts.
 bool split_supports(int group, int E);
 // gather: token of each of the M rows (x is then [T, K], token-major); nullptr: x is [M, K].
 w4a16_status split_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s, uint16_t* y,
-                          int64_t M, int64_t N, int64_t K, const int32_t* expert_offsets, int E,
+                          int64_t M, int64_t N, int64_t K, int group, const int32_t* expert_offsets, int E,
                           const int32_t* gather, int64_t T, cudaStream_t st);
 
 // Routed-MoE router, dispatch (permutation + gather) and combine.

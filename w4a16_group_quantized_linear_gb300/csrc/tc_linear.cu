@@ -63,7 +63,7 @@ __device__ __forceinline__ constexpr bool may_issue(int64_t) { return true; }
 #endif
 
 template <int G_, int BN_, int KSTAGE_, int PSTAGES_, int XSTAGES_, int DEQW_, int EPIW_, bool SRUNS_ = false,
-          int ASTAGES_ = XSTAGES_>
+          int ASTAGES_ = XSTAGES_, int MMAW_ = 1>
 struct Cfg {
     static constexpr int G = G_;              // scale group
     static constexpr int BN = BN_;            // tokens per tile (MMA N)
@@ -71,11 +71,12 @@ struct Cfg {
     static constexpr int PSTAGES = PSTAGES_;  // packed-weight ring depth
     static constexpr int XSTAGES = XSTAGES_;  // x ring depth
     static constexpr int ASTAGES = ASTAGES_;  // TMEM A ring depth
+    static constexpr int MMAW = MMAW_;        // MMA-issuing warps (2: one per partial buffer)
     static constexpr int DEQW = DEQW_;        // dequant warps (multiple of 4)
     static constexpr int EPIW = EPIW_;        // epilogue warps (multiple of 4)
     static constexpr bool SRUNS = SRUNS_;     // scales in 16-byte runs, 16-24 groups ahead
 
-    static constexpr int THREADS = (2 + DEQW + EPIW) * 32;
+    static constexpr int THREADS = (2 + DEQW + EPIW + MMAW - 1) * 32;
     static constexpr int PBYTES = kRowsPerTile * KSTAGE / 2;  // packed weights per stage
     static constexpr int XBOXES = KSTAGE / 64;                 // x boxes of 64 k per stage
     static constexpr int XBOX_BYTES = BN * 128;
@@ -98,6 +99,7 @@ struct Cfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
     static_assert(PART_K % 64 == 0 && BNP % 16 == 0, "per-thread shares");
     static_assert(PSTAGES <= 8 && XSTAGES <= 8 && ASTAGES <= 4 && PSTAGES >= ASTAGES, "ring depths");
+    static_assert(MMAW == 1 || (MMAW == 2 && KSTAGE >= G), "a second issuer takes whole groups");
     static_assert(PBYTES % 1024 == 0 && XBYTES % 1024 == 0, "1024-byte aligned stages");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
@@ -249,17 +251,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
             for (int i = 0; i < C::XSTAGES; ++i) {
                 ptx::mbar_init(&sm->xfull[i], 1);
-                ptx::mbar_init(&sm->xempty[i], 1);
+                ptx::mbar_init(&sm->xempty[i], C::MMAW);
             }
             for (int i = 0; i < C::ASTAGES; ++i) {
                 ptx::mbar_init(&sm->afull[i], C::DEQW * 32);
-                ptx::mbar_init(&sm->aempty[i], 1);
+                ptx::mbar_init(&sm->aempty[i], C::MMAW);
             }
             for (int b = 0; b < 2; ++b) {
                 ptx::mbar_init(&sm->dfull[b], 1);
                 ptx::mbar_init(&sm->dempty[b], C::EPIW * 32);
             }
-            ptx::mbar_init(&sm->mma_done, 1);
+            ptx::mbar_init(&sm->mma_done, C::MMAW);
             sm->abort = 0;
             ptx::fence_mbar_init();
             ptx::prefetch_tensormap(&tmap_x);
@@ -364,8 +366,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     ptx::mbar_wait(&sm->xfull[i % C::XSTAGES], (uint32_t)((i / C::XSTAGES) & 1), &never, kDrainLimitNs);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || (C::MMAW == 2 && warp == 2 + C::DEQW + C::EPIW)) {
         // ----------------------------------------------------------- MMA issue
+        // With two issuers, issuer mi takes the scale groups whose partial goes to
+        // TMEM buffer mi: the instruction issue of one thread is the limit.
+        const int mi = warp == 1 ? 0 : 1;
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_f16_f32(kRowsPerTile, C::BN);
             constexpr int GPS = C::G / 16;  // MMAs per scale group
@@ -393,7 +398,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const bool first = C::KSTAGE >= C::G ? (kk % GPS == 0) : (kk == 0 && stage_opens);
                     const bool last = C::KSTAGE >= C::G ? (kk % GPS == GPS - 1)
                                                         : (kk == C::KSTAGE / 16 - 1 && stage_closes);
-                    if (first) {
+                    const bool mine = C::MMAW == 1 || (int)(grp & 1) == mi;
+                    if (first && mine) {
                         cur_b = (int)(grp & 1);
                         if (grp >= 2) {
                             if (!ptx::mbar_wait(&sm->dempty[cur_b], (uint32_t)(((grp >> 1) - 1) & 1), abort,
@@ -404,13 +410,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             ptx::tc_fence_after();
                         }
                     }
-                    const uint64_t bdesc = bdesc0 + (uint64_t)((((kk >> 2) * C::XBOX_BYTES) + (kk & 3) * 32) >> 4);
-                    ptx::mma_f16_ts(tmem + (uint32_t)(cur_b * C::BN), a_col + (uint32_t)(kk * 8), bdesc, idesc,
-                                    first ? 0u : 1u);
-                    if (last) {
-                        ptx::mma_commit(&sm->dfull[cur_b]);
-                        ++grp;
+                    if (mine) {
+                        const uint64_t bdesc =
+                            bdesc0 + (uint64_t)((((kk >> 2) * C::XBOX_BYTES) + (kk & 3) * 32) >> 4);
+                        ptx::mma_f16_ts(tmem + (uint32_t)(cur_b * C::BN), a_col + (uint32_t)(kk * 8), bdesc, idesc,
+                                        first ? 0u : 1u);
+                        if (last) ptx::mma_commit(&sm->dfull[cur_b]);
                     }
+                    if (last) ++grp;
                 }
                 if (!ok) break;
                 ptx::mma_commit(&sm->xempty[xs]);  // the x slot is free again
@@ -769,11 +776,12 @@ w4a16_status gemm_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t
                          int64_t M, int64_t N, int64_t K, int group, const int32_t* expert_offsets, int E,
                          cudaStream_t st) {
     if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
-    // group 32 (routed experts, and dense tiles of 128 tokens): the scale goes
-    // into the A operand as an exact fp16 pair (tc_split.cu), with no per-group
-    // epilogue round trip
+    // routed experts, and dense layers past the narrow tiles: the scale goes into
+    // the A operand as an exact fp16 pair (tc_split.cu), with no per-group
+    // epilogue round trip and 256-token MMAs (measured at M = 4096, 5120 -> 17408:
+    // group 128 742 against 858 us on the tiles below, group 64 747 against 1066)
     if (split_supports(group, expert_offsets != nullptr ? E : 1) && (expert_offsets != nullptr || M > 64))
-        return split_launch(dev, x, qw, s, y, M, N, K, expert_offsets, E, nullptr, 0, st);
+        return split_launch(dev, x, qw, s, y, M, N, K, group, expert_offsets, E, nullptr, 0, st);
     const int bn = expert_offsets != nullptr ? 0 : (M > 64 ? 128 : (M > 32 ? 64 : 32));
 #define W4A16_GEMM(CFG)                                                                              \
     switch (group) {                                                                                 \

@@ -1,11 +1,13 @@
-// Tensor-core GEMM of the W4A16 layer for group-32 weights: the routed-expert
-// layer of the LLM170 page's "g32, MoE resident" models, and dense layers of
-// group 32 (sm_103a: TMA, tcgen05 MMA, TMEM).
+// Tensor-core GEMM of the W4A16 layer with the scale folded into the A
+// operand: the routed-expert layer (the LLM170 page's "g32, MoE resident"
+// models) and dense layers past 64 tokens, at groups 32, 64 and 128 (sm_103a:
+// TMA, tcgen05 MMA, TMEM).
 //
-// At group 32 the group-partial design of tc_linear.cu (one fp32 TMEM partial
-// per scale group, scaled by the epilogue) pays one TMEM round trip per 32 k,
-// which takes longer than the group's two MMAs. Here the scale goes into the A
-// operand instead, exactly. For a scale s (fp16) and an integer q in [-8, 7]
+// The group-partial design of tc_linear.cu (one fp32 TMEM partial per scale
+// group, scaled by the epilogue) pays one TMEM round trip and one wait for its
+// buffer per group; at group 32 that takes longer than the group's two MMAs,
+// and at any group it keeps the MMAs at 128 tokens. Here the scale goes into
+// the A operand instead, exactly. For a scale s (fp16) and an integer q in [-8, 7]
 // the product s*q has at most 15 significant bits, so it splits into two fp16
 // values with no rounding at all:
 //
@@ -48,9 +50,9 @@
 //               a row gather, below).
 //   warp 1      TMEM allocation and the MMA issuer (one lane).
 //   warps 2-5   dequant: thread = TMEM lane = weight row; turns each 32-k
-//               group into hi and lo and writes them to the stage's TMEM A
-//               columns (tcgen05.st); the scales of the next stage are loaded
-//               one stage ahead.
+//               chunk into hi and lo with the scale of its group and writes
+//               them to the stage's TMEM A columns (tcgen05.st); the scales of
+//               the next stage are loaded one stage ahead.
 //   warps 6-13  epilogue: two threads per weight row (= TMEM lane), each
 //               reading half of the tile's tokens from the accumulator,
 //               times 2^e, rounded once to fp16, stored. With a row gather
@@ -73,7 +75,7 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kG = 32;                               // scale group of this kernel
+constexpr int kChunk = 32;                           // k per dequant chunk: one scale each
 constexpr int kRows = 128;                           // weight rows per tile: MMA M, TMEM lanes
 constexpr int kBN = 256;                             // tokens per tile: MMA N at most
 constexpr int kXBoxBytes = kBN * 128;                // 64 k x 256 tokens, 128-byte swizzle
@@ -94,7 +96,7 @@ constexpr uint64_t kDrainLimitNs = 1000000000ull;    // 1 s
 template <int KS>
 struct Pipe {
     static constexpr int kKS = KS;
-    static constexpr int kGroupsPerStage = KS / kG;
+    static constexpr int kChunksPerStage = KS / kChunk;
     static constexpr int kPStages = KS == 128 ? 4 : 8;   // packed-weight ring
     static constexpr int kXStages = KS == 128 ? 2 : 4;   // x ring (shared memory)
     static constexpr int kAStages = KS == 128 ? 2 : 4;   // TMEM A stages
@@ -137,6 +139,7 @@ struct SplitArgs {
     int64_t T;
     int64_t M, N, K;
     int E;
+    int gshift;  // scale group = 32 << gshift
     unsigned int* err;
 };
 
@@ -317,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sm->tmem_base;
     volatile int* abort = &sm->abort;
     const int nst = (int)((a.K + KS - 1) / KS);         // stages per tile
-    const int gk = (int)(a.K / kG);                     // scale groups per row
+    const int gk = (int)(a.K >> (5 + a.gshift));        // scale groups per row
+    const int nck = (int)(a.K / kChunk);                // 32-k chunks per row
     const int my_tiles = (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
     const int64_t stages = (int64_t)my_tiles * nst;
     auto tile_of = [&](int j) { return decode_tile(plan, (int)blockIdx.x + j * (int)gridDim.x, ntn, a.E); };
@@ -452,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < 2 + kDeqWarps) {
         // -------------------------------------------------------------- dequant
-        constexpr int GPS = P::kGroupsPerStage;
+        constexpr int GPS = P::kChunksPerStage;
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
         const int r = quad * 32 + lane;           // weight row in the tile = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
@@ -464,12 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool n_ok = n < a.N;
             const uint16_t* srow = a.s + ((int64_t)tl.e * a.N + (n_ok ? n : 0)) * gk;
             const float f = row_shift(srow, gk, n_ok);
-            // this row's scales of a stage (0 past the row), one stage ahead
+            // the scale of each 32-k chunk of a stage (0 past the row), one stage ahead
             auto load_scales = [&](int s_, uint32_t (&dst)[GPS]) {
 #pragma unroll
                 for (int i = 0; i < GPS; ++i) {
-                    const int g = s_ * GPS + i;
-                    dst[i] = (s_ < nst && g < gk) ? (uint32_t)__ldg(srow + g) : 0u;
+                    const int ck = s_ * GPS + i;
+                    dst[i] = (s_ < nst && ck < nck) ? (uint32_t)__ldg(srow + (ck >> a.gshift)) : 0u;
                 }
             };
             uint32_t sc[GPS], sc_next[GPS];
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < nst; ++s, ++c) {
                 const int ps = (int)(c % P::kPStages), as = (int)(c % P::kAStages);
                 load_scales(s + 1, sc_next);
-                const int ng = min(GPS, gk - s * GPS);  // groups in the stage
+                const int ng = min(GPS, nck - s * GPS);  // chunks in the stage
                 const bool got =
                     ptx::mbar_wait(&sm->pfull[ps], (uint32_t)((c / P::kPStages) & 1), abort, wait_limit()) &&
                     (c < P::kAStages ||
@@ -491,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t acol = lane_base + kAColBase + (uint32_t)as * P::kAStageCols;
 #pragma unroll
                 for (int gi = 0; gi < GPS; ++gi) {
-                    if (gi >= ng) break;  // uniform: every lane has the same groups
+                    if (gi >= ng) break;  // uniform: every lane has the same chunks
                     const uint4 pk = *reinterpret_cast<const uint4*>(prow + P::packed_offset(r, gi));
                     const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
                     // exact: a (shifted) fp16 scale
@@ -688,13 +692,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 template <int KS>
 w4a16_status launch_split(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s,
-                          uint16_t* y, int64_t M, int64_t N, int64_t K, const int32_t* offsets, int E,
+                          uint16_t* y, int64_t M, int64_t N, int64_t K, int gshift, const int32_t* offsets, int E,
                           const int32_t* gather, int64_t T, cudaStream_t st) {
     using P = Pipe<KS>;
     constexpr size_t kSmem = smem_bytes<P>();
     if (kSmem > dev.smem_optin) return W4A16_ERR_UNSUPPORTED;
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (!enc) return cuda_status(cudaErrorNotSupported, "gemm g32: cuTensorMapEncodeTiled entry point");
+    if (!enc) return cuda_status(cudaErrorNotSupported, "gemm split: cuTensorMapEncodeTiled entry point");
     CUtensorMap mx, mw;
     {  // x [M, K] (with a row gather: x [T, K]; the map is then never loaded from)
         cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(gather ? T : M)};
@@ -704,7 +708,7 @@ w4a16_status launch_split(const DeviceInfo& dev, const uint16_t* x, const uint8_
         if (enc(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cuda_status(cudaErrorInvalidValue, "gemm g32: cuTensorMapEncodeTiled (x)");
+            return cuda_status(cudaErrorInvalidValue, "gemm split: cuTensorMapEncodeTiled (x)");
     }
     if (offsets == nullptr) {
         cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
@@ -714,7 +718,7 @@ w4a16_status launch_split(const DeviceInfo& dev, const uint16_t* x, const uint8_
         if (enc(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(qw), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, P::kPSwizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cuda_status(cudaErrorInvalidValue, "gemm g32: cuTensorMapEncodeTiled (weights)");
+            return cuda_status(cudaErrorInvalidValue, "gemm split: cuTensorMapEncodeTiled (weights)");
     } else {
         cuuint64_t dims[3] = {(cuuint64_t)(K / 2), (cuuint64_t)N, (cuuint64_t)E};
         cuuint64_t strides[2] = {(cuuint64_t)(K / 2), (cuuint64_t)(N * (K / 2))};
@@ -723,7 +727,7 @@ w4a16_status launch_split(const DeviceInfo& dev, const uint16_t* x, const uint8_
         if (enc(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(qw), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, P::kPSwizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cuda_status(cudaErrorInvalidValue, "gemm g32: cuTensorMapEncodeTiled (weights)");
+            return cuda_status(cudaErrorInvalidValue, "gemm split: cuTensorMapEncodeTiled (weights)");
     }
     SplitArgs a{};
     a.s = s;
@@ -736,6 +740,7 @@ w4a16_status launch_split(const DeviceInfo& dev, const uint16_t* x, const uint8_
     a.N = N;
     a.K = K;
     a.E = offsets ? E : 1;
+    a.gshift = gshift;
     a.err = dev.error_word;
     // an upper bound on the tiles (each expert adds at most one partial token tile)
     const int64_t ntn = (N + kRows - 1) / kRows;
@@ -746,22 +751,26 @@ w4a16_status launch_split(const DeviceInfo& dev, const uint16_t* x, const uint8_
     const cudaError_t attr = once.run(dev.device, [] {
         return cudaFuncSetAttribute(split_kernel<KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     });
-    if (attr != cudaSuccess) return cuda_status(attr, "gemm g32: cudaFuncSetAttribute");
+    if (attr != cudaSuccess) return cuda_status(attr, "gemm split: cudaFuncSetAttribute");
     split_kernel<KS><<<grid, kThreads, kSmem, st>>>(mx, mw, a);
-    return cuda_status(cudaGetLastError(), "gemm g32: kernel launch");
+    return cuda_status(cudaGetLastError(), "gemm split: kernel launch");
 }
 
 }  // namespace
 
-bool split_supports(int group, int E) { return group == kG && E >= 1 && E <= kMaxE; }
+bool split_supports(int group, int E) {
+    return (group == 32 || group == 64 || group == 128) && E >= 1 && E <= kMaxE;
+}
 
 w4a16_status split_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s, uint16_t* y,
-                          int64_t M, int64_t N, int64_t K, const int32_t* offsets, int E, const int32_t* gather,
-                          int64_t T, cudaStream_t st) {
+                          int64_t M, int64_t N, int64_t K, int group, const int32_t* offsets, int E,
+                          const int32_t* gather, int64_t T, cudaStream_t st) {
+    if (!split_supports(group, offsets ? E : 1)) return W4A16_ERR_UNSUPPORTED;
+    const int gshift = group == 32 ? 0 : group == 64 ? 1 : 2;
     if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL || T > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
     // long K: 128-k stages; short K: 64-k stages and a deeper pipeline for the tile's fill
-    if (K >= 1024) return launch_split<128>(dev, x, qw, s, y, M, N, K, offsets, E, gather, T, st);
-    return launch_split<64>(dev, x, qw, s, y, M, N, K, offsets, E, gather, T, st);
+    if (K >= 1024) return launch_split<128>(dev, x, qw, s, y, M, N, K, gshift, offsets, E, gather, T, st);
+    return launch_split<64>(dev, x, qw, s, y, M, N, K, gshift, offsets, E, gather, T, st);
 }
 
 #ifdef W4A16_TEST_HOOKS
