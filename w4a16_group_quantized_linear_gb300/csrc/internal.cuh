@@ -70,6 +70,15 @@ __device__ __forceinline__ void mma_16816_zero(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
 }
 
+// Fused gate + up tiles of the tensor-core GEMMs: 128 weight rows per tile are
+// 64 rows of Wg (shared-memory rows 0-63 of a packed stage) and the same 64 rows
+// of Wu (rows 64-127). TMEM lane r holds output row gated_out_row(r) of the
+// gate (bit 3 of r clear) or of the up projection (bit 3 set), read from
+// shared-memory row gated_smem_row(r): g and u of one output sit in lanes r and
+// r ^ 8 of one warp, and each run of 8 lanes reads 8 distinct swizzle rows.
+__device__ __forceinline__ int gated_out_row(int r) { return ((r >> 4) << 3) | (r & 7); }
+__device__ __forceinline__ int gated_smem_row(int r) { return ((r >> 3) & 1) * 64 + gated_out_row(r); }
+
 // Sticky device error word (one per device, in api.cu's module).
 __device__ __forceinline__ void raise_device_error(unsigned int* word, unsigned int code) {
     if (word) atomicCAS(word, 0u, code);
@@ -149,6 +158,11 @@ bool split_supports(int group, int E);
 w4a16_status split_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s, uint16_t* y,
                           int64_t M, int64_t N, int64_t K, int group, const int32_t* expert_offsets, int E,
                           const int32_t* gather, int64_t T, cudaStream_t st);
+// y = silu(x Wg^T) * (x Wu^T) on the split kernel (dense): each tile holds 64
+// rows of Wg and the same 64 rows of Wu.
+w4a16_status split_gated_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw_gate,
+                                const uint16_t* s_gate, const uint8_t* qw_up, const uint16_t* s_up, uint16_t* y,
+                                int64_t M, int64_t N, int64_t K, int group, cudaStream_t st);
 
 // Routed-MoE router, dispatch (permutation + gather) and combine.
 w4a16_status moe_route_launch(const float* logits, int64_t T, int E, int top_k, bool renormalize, int32_t* ids,

@@ -211,8 +211,6 @@ __device__ __forceinline__ int packed_offset(int r, int c) {
 // r % 8 of the gate (bit 3 of r clear) or of the up projection (bit 3 set), so
 // the g and u of one output sit in lanes r and r ^ 8 of the same warp and meet
 // through one shuffle; each run of 8 lanes reads 8 distinct swizzle rows.
-__device__ __forceinline__ int gated_out_row(int r) { return ((r >> 4) << 3) | (r & 7); }
-__device__ __forceinline__ int gated_smem_row(int r) { return ((r >> 3) & 1) * 64 + gated_out_row(r); }
 
 template <class C, bool GATED>
 __global__ void __launch_bounds__(C::THREADS, 1)
@@ -801,6 +799,9 @@ w4a16_status gemm_gated_launch(const DeviceInfo& dev, const uint16_t* x, const u
                                const uint16_t* scales_gate, const uint8_t* qweight_up, const uint16_t* scales_up,
                                uint16_t* y, int64_t M, int64_t N, int64_t K, int group, cudaStream_t st) {
     if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
+    // past the narrow tiles the pair runs on the split-scale kernel, as the plain layer does
+    if (M > 64 && split_supports(group, 1))
+        return split_gated_launch(dev, x, qweight_gate, scales_gate, qweight_up, scales_up, y, M, N, K, group, st);
     const int bn = M > 64 ? 128 : (M > 32 ? 64 : 32);
 #define W4A16_GEMM(CFG)                                                                                    \
     switch (group) {                                                                                       \

@@ -132,6 +132,7 @@ __device__ __forceinline__ constexpr bool may_issue(int64_t) { return true; }
 
 struct SplitArgs {
     const uint16_t* s;
+    const uint16_t* s2;      // gated: the up projection's scales (s holds the gate's)
     uint16_t* y;
     const int32_t* offsets;  // routed experts; nullptr: dense, one expert of M rows
     const int32_t* gather;   // token of each row: x rows come from xg [T, K]; nullptr: x by TMA
@@ -181,8 +182,9 @@ __device__ __forceinline__ int tile_tokens(int rows, int tiles) {
     return ((rows + tiles - 1) / tiles + 15) & ~15;
 }
 
-// Tile t: token tile t / ntn (over the experts in order), weight-row tile t % ntn.
-__device__ __forceinline__ Tile decode_tile(const TilePlan& pl, int t, int ntn, int E) {
+// Tile t: token tile t / ntn (over the experts in order), weight-row tile t % ntn
+// of out_rows output rows.
+__device__ __forceinline__ Tile decode_tile(const TilePlan& pl, int t, int ntn, int E, int out_rows) {
     const int tt = t / ntn;
     int lo = 0, hi = E - 1;  // the last expert whose first token tile is <= tt
     while (lo < hi) {
@@ -196,7 +198,7 @@ __device__ __forceinline__ Tile decode_tile(const TilePlan& pl, int t, int ntn, 
     r.e = lo;
     r.row0 = pl.row_start[lo] + (tt - pl.first_tile[lo]) * size;
     r.rows = min(size, pl.row_start[lo + 1] - r.row0);
-    r.n0 = (t % ntn) * kRows;
+    r.n0 = (t % ntn) * out_rows;
     return r;
 }
 
@@ -267,11 +269,15 @@ __device__ __forceinline__ float row_shift(const uint16_t* srow, int gk, bool ok
     return f;
 }
 
-template <int KS>
+// GATED (dense only): each tile's 128 weight rows are 64 rows of Wg and the same
+// 64 rows of Wu (tmap_w, tmap_w2), interleaved in TMEM as gated_out_row /
+// gated_smem_row describe; the epilogue forms y = silu(g) * u from the fp32 sums.
+template <int KS, bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
     split_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-                 const SplitArgs a) {
+                 const __grid_constant__ CUtensorMap tmap_w2, const SplitArgs a) {
     using P = Pipe<KS>;
+    constexpr int kOut = GATED ? kRows / 2 : kRows;  // output rows per tile
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* pring = base;                                 // packed-weight stages
@@ -302,11 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::fence_mbar_init();
             ptx::prefetch_tensormap(&tmap_x);
             ptx::prefetch_tensormap(&tmap_w);
+            if (GATED) ptx::prefetch_tensormap(&tmap_w2);
         }
     }
     __syncthreads();
     const TilePlan& plan = sm->plan;
-    const int ntn = (int)((a.N + kRows - 1) / kRows);   // weight-row tiles
+    const int ntn = (int)((a.N + kOut - 1) / kOut);     // weight-row tiles
     const int total = plan.tiles * ntn;
     if ((int)blockIdx.x >= total) return;                // nothing for this CTA (uniform)
     if (warp == 1) {
@@ -324,13 +331,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nck = (int)(a.K / kChunk);                // 32-k chunks per row
     const int my_tiles = (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
     const int64_t stages = (int64_t)my_tiles * nst;
-    auto tile_of = [&](int j) { return decode_tile(plan, (int)blockIdx.x + j * (int)gridDim.x, ntn, a.E); };
+    auto tile_of = [&](int j) {
+        return decode_tile(plan, (int)blockIdx.x + j * (int)gridDim.x, ntn, a.E, kOut);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
         // the warp polls together; lane 0 issues the copies
         int64_t ix = a.gather ? stages : 0, ip = 0;  // stages issued on each ring (x: none with a gather)
-        int jx = -1, jp = -1;                        // the tile each ring is on
+        int jx = 0, sx = 0, jp = 0, sp = 0;          // each ring's tile and stage in it (no division per stage)
+        int jtx = -1, jtp = -1;                      // the tile decoded for each ring
         Tile tx{}, tp{};
         bool ok = true;
         uint64_t idle_since = 0;
@@ -342,10 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool free = round == 0;
                 if (!free && lane == 0) free = ptx::mbar_try_wait(&sm->xempty[st], (uint32_t)((round - 1) & 1));
                 if (__shfl_sync(0xffffffffu, free, 0)) {
-                    const int j = (int)(ix / nst), s = (int)(ix % nst);
-                    if (j != jx) {
+                    const int j = jx, s = sx;
+                    if (++sx == nst) {
+                        sx = 0;
+                        ++jx;
+                    }
+                    if (j != jtx) {
                         tx = tile_of(j);
-                        jx = j;
+                        jtx = j;
                     }
                     if (lane == 0) {
                         ptx::mbar_arrive_expect_tx(&sm->xfull[st], P::kXBytes);
@@ -364,14 +378,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool free = round == 0;
                 if (!free && lane == 0) free = ptx::mbar_try_wait(&sm->pempty[st], (uint32_t)((round - 1) & 1));
                 if (__shfl_sync(0xffffffffu, free, 0)) {
-                    const int j = (int)(ip / nst), s = (int)(ip % nst);
-                    if (j != jp) {
+                    const int j = jp, s = sp;
+                    if (++sp == nst) {
+                        sp = 0;
+                        ++jp;
+                    }
+                    if (j != jtp) {
                         tp = tile_of(j);
-                        jp = j;
+                        jtp = j;
                     }
                     if (lane == 0) {
                         ptx::mbar_arrive_expect_tx(&sm->pfull[st], P::kPBytes);
-                        if (a.offsets == nullptr)
+                        if (GATED) {
+                            ptx::tma_load_2d(pring + st * P::kPBytes, &tmap_w, &sm->pfull[st], s * (KS / 2), tp.n0);
+                            ptx::tma_load_2d(pring + st * P::kPBytes + P::kPBytes / 2, &tmap_w2, &sm->pfull[st],
+                                             s * (KS / 2), tp.n0);
+                        } else if (a.offsets == nullptr)
                             ptx::tma_load_2d(pring + st * P::kPBytes, &tmap_w, &sm->pfull[st], s * (KS / 2), tp.n0);
                         else
                             ptx::tma_load_3d(pring + st * P::kPBytes, &tmap_w, &sm->pfull[st], s * (KS / 2), tp.n0,
@@ -460,13 +482,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
         const int r = quad * 32 + lane;           // weight row in the tile = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const bool up_row = GATED && ((r >> 3) & 1);
+        const int prow_r = GATED ? gated_smem_row(r) : r;  // shared-memory row of this TMEM lane
         bool ok = true;
         int64_t c = 0;
         for (int j = 0; ok && j < my_tiles; ++j) {
             const Tile tl = tile_of(j);
-            const int64_t n = (int64_t)tl.n0 + r;
+            const int64_t n = (int64_t)tl.n0 + (GATED ? gated_out_row(r) : r);
             const bool n_ok = n < a.N;
-            const uint16_t* srow = a.s + ((int64_t)tl.e * a.N + (n_ok ? n : 0)) * gk;
+            const uint16_t* srow = (up_row ? a.s2 : a.s) + ((int64_t)tl.e * a.N + (n_ok ? n : 0)) * gk;
             const float f = row_shift(srow, gk, n_ok);
             // the scale of each 32-k chunk of a stage (0 past the row), one stage ahead
             auto load_scales = [&](int s_, uint32_t (&dst)[GPS]) {
@@ -496,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int gi = 0; gi < GPS; ++gi) {
                     if (gi >= ng) break;  // uniform: every lane has the same chunks
-                    const uint4 pk = *reinterpret_cast<const uint4*>(prow + P::packed_offset(r, gi));
+                    const uint4 pk = *reinterpret_cast<const uint4*>(prow + P::packed_offset(prow_r, gi));
                     const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
                     // exact: a (shifted) fp16 scale
                     const __half2 s2 = __float2half2_rn(__half2float(__ushort_as_half((unsigned short)sc[gi])) * f);
@@ -535,10 +559,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = ew >> 2;                      // which tokens of the tile
         const int r = quad * 32 + lane;                // weight row in the tile = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * kEpiCols);
+        const bool up_row = GATED && ((r >> 3) & 1);
         // tile j's results: the accumulator read as fp16 pairs (times the row's
-        // 2^e), the accumulator released, then y stored
+        // 2^e), the accumulator released, then y stored. Gated: lanes r and r ^ 8
+        // hold g and u of one output; the gate lane finishes the even tokens of
+        // each pair and the up lane the odd ones, each handing the other the
+        // operand it lacks (one shuffle), and y = fp16(silu(g) * u).
         auto finish_tile = [&](const Tile& tl, float mult) {
-            const int64_t n = (int64_t)tl.n0 + r;
+            const int64_t n = (int64_t)tl.n0 + (GATED ? gated_out_row(r) : r);
             const int m0 = half * kEpiCols;                          // first token of this thread's share
             const int mine = max(0, min(kEpiCols, tl.rows - m0));    // tokens of the tile in that share
             ptx::tc_fence_after();
@@ -549,27 +577,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t v[32];
                     ptx::tmem_ld_32x32b_x32(lane_base + (uint32_t)(ch * 32), v);
                     ptx::tmem_ld_wait();
+                    if constexpr (GATED) {
+                        float yv[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const __half2 h = __floats2half2_rn(__uint_as_float(v[2 * i]) * mult,
-                                                            __uint_as_float(v[2 * i + 1]) * mult);
-                        packed[ch * 16 + i] = *reinterpret_cast<const uint32_t*>(&h);
+                        for (int i = 0; i < 16; ++i) {
+                            const float e0 = __uint_as_float(v[2 * i]) * mult, e1 = __uint_as_float(v[2 * i + 1]) * mult;
+                            const float other = __shfl_xor_sync(0xffffffffu, up_row ? e0 : e1, 8);
+                            const float g = up_row ? other : e0, u = up_row ? e1 : other;
+                            yv[i] = __fdividef(g, 1.0f + __expf(-g)) * u;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const __half2 h = __floats2half2_rn(yv[2 * i], yv[2 * i + 1]);
+                            packed[ch * 8 + i] = *reinterpret_cast<const uint32_t*>(&h);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const __half2 h = __floats2half2_rn(__uint_as_float(v[2 * i]) * mult,
+                                                                __uint_as_float(v[2 * i + 1]) * mult);
+                            packed[ch * 16 + i] = *reinterpret_cast<const uint32_t*>(&h);
+                        }
                     }
                 }
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(&sm->dempty);
             if (n < a.N) {
-                uint16_t* yrow = a.y + ((int64_t)tl.row0 + m0) * a.N + n;
+                if constexpr (GATED) {  // this lane's tokens: 2 i + (up lane)
+                    const int u0 = up_row ? 1 : 0;
+                    uint16_t* yrow = a.y + ((int64_t)tl.row0 + m0 + u0) * a.N + n;
 #pragma unroll
-                for (int i = 0; i < kEpiCols; ++i)
-                    if (i < mine) yrow[(int64_t)i * a.N] = (uint16_t)(packed[i >> 1] >> (16 * (i & 1)));
+                    for (int i = 0; i < kEpiCols / 2; ++i)
+                        if (2 * i + u0 < mine)
+                            yrow[(int64_t)(2 * i) * a.N] = (uint16_t)(packed[i >> 1] >> (16 * (i & 1)));
+                } else {
+                    uint16_t* yrow = a.y + ((int64_t)tl.row0 + m0) * a.N + n;
+#pragma unroll
+                    for (int i = 0; i < kEpiCols; ++i)
+                        if (i < mine) yrow[(int64_t)i * a.N] = (uint16_t)(packed[i >> 1] >> (16 * (i & 1)));
+                }
             }
         };
         auto row_mult = [&](const Tile& tl) {  // the row's 2^e
-            const int64_t n = (int64_t)tl.n0 + r;
+            const int64_t n = (int64_t)tl.n0 + (GATED ? gated_out_row(r) : r);
             const bool n_ok = n < a.N;
-            return 1.0f / row_shift(a.s + ((int64_t)tl.e * a.N + (n_ok ? n : 0)) * gk, gk, n_ok);
+            return 1.0f / row_shift((up_row ? a.s2 : a.s) + ((int64_t)tl.e * a.N + (n_ok ? n : 0)) * gk, gk, n_ok);
         };
         bool ok = true;
         if (!a.gather) {
@@ -690,16 +743,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <int KS>
+template <int KS, bool GATED = false>
 w4a16_status launch_split(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s,
                           uint16_t* y, int64_t M, int64_t N, int64_t K, int gshift, const int32_t* offsets, int E,
-                          const int32_t* gather, int64_t T, cudaStream_t st) {
+                          const int32_t* gather, int64_t T, cudaStream_t st, const uint8_t* qw2 = nullptr,
+                          const uint16_t* s2 = nullptr) {
+    constexpr int kOut = GATED ? kRows / 2 : kRows;
     using P = Pipe<KS>;
     constexpr size_t kSmem = smem_bytes<P>();
     if (kSmem > dev.smem_optin) return W4A16_ERR_UNSUPPORTED;
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cuda_status(cudaErrorNotSupported, "gemm split: cuTensorMapEncodeTiled entry point");
-    CUtensorMap mx, mw;
+    CUtensorMap mx, mw, mw2;
     {  // x [M, K] (with a row gather: x [T, K]; the map is then never loaded from)
         cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(gather ? T : M)};
         cuuint64_t strides[1] = {(cuuint64_t)K * 2};
@@ -710,15 +765,21 @@ w4a16_status launch_split(const DeviceInfo& dev, const uint16_t* x, const uint8_
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cuda_status(cudaErrorInvalidValue, "gemm split: cuTensorMapEncodeTiled (x)");
     }
-    if (offsets == nullptr) {
+    auto encode_w2d = [&](CUtensorMap* m, const uint8_t* w) {
         cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
         cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-        cuuint32_t box[2] = {KS / 2, (cuuint32_t)kRows};
+        cuuint32_t box[2] = {KS / 2, (cuuint32_t)kOut};  // gated: 64 rows of each matrix per stage
         cuuint32_t es[2] = {1, 1};
-        if (enc(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(qw), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, P::kPSwizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, P::kPSwizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    if (GATED && (offsets != nullptr || gather != nullptr || qw2 == nullptr || s2 == nullptr))
+        return W4A16_ERR_INVALID_ARG;
+    if (offsets == nullptr) {
+        if (!encode_w2d(&mw, qw) || (GATED && !encode_w2d(&mw2, qw2)))
             return cuda_status(cudaErrorInvalidValue, "gemm split: cuTensorMapEncodeTiled (weights)");
+        if (!GATED) mw2 = mw;
     } else {
         cuuint64_t dims[3] = {(cuuint64_t)(K / 2), (cuuint64_t)N, (cuuint64_t)E};
         cuuint64_t strides[2] = {(cuuint64_t)(K / 2), (cuuint64_t)(N * (K / 2))};
@@ -728,9 +789,11 @@ w4a16_status launch_split(const DeviceInfo& dev, const uint16_t* x, const uint8_
                 CU_TENSOR_MAP_INTERLEAVE_NONE, P::kPSwizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cuda_status(cudaErrorInvalidValue, "gemm split: cuTensorMapEncodeTiled (weights)");
+        mw2 = mw;
     }
     SplitArgs a{};
     a.s = s;
+    a.s2 = s2;
     a.y = y;
     a.offsets = offsets;
     a.gather = gather;
@@ -743,16 +806,16 @@ w4a16_status launch_split(const DeviceInfo& dev, const uint16_t* x, const uint8_
     a.gshift = gshift;
     a.err = dev.error_word;
     // an upper bound on the tiles (each expert adds at most one partial token tile)
-    const int64_t ntn = (N + kRows - 1) / kRows;
+    const int64_t ntn = (N + kOut - 1) / kOut;
     const int64_t tiles = ((M + kBN - 1) / kBN + (offsets ? E : 0)) * ntn;
     if (tiles > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
     const unsigned grid = (unsigned)(tiles < dev.sms ? tiles : dev.sms);
     static PerDeviceOnce once;
     const cudaError_t attr = once.run(dev.device, [] {
-        return cudaFuncSetAttribute(split_kernel<KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+        return cudaFuncSetAttribute(split_kernel<KS, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     });
     if (attr != cudaSuccess) return cuda_status(attr, "gemm split: cudaFuncSetAttribute");
-    split_kernel<KS><<<grid, kThreads, kSmem, st>>>(mx, mw, a);
+    split_kernel<KS, GATED><<<grid, kThreads, kSmem, st>>>(mx, mw, mw2, a);
     return cuda_status(cudaGetLastError(), "gemm split: kernel launch");
 }
 
@@ -771,6 +834,19 @@ w4a16_status split_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_
     // long K: 128-k stages; short K: 64-k stages and a deeper pipeline for the tile's fill
     if (K >= 1024) return launch_split<128>(dev, x, qw, s, y, M, N, K, gshift, offsets, E, gather, T, st);
     return launch_split<64>(dev, x, qw, s, y, M, N, K, gshift, offsets, E, gather, T, st);
+}
+
+w4a16_status split_gated_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw_gate,
+                                const uint16_t* s_gate, const uint8_t* qw_up, const uint16_t* s_up, uint16_t* y,
+                                int64_t M, int64_t N, int64_t K, int group, cudaStream_t st) {
+    if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
+    if (!split_supports(group, 1)) return W4A16_ERR_UNSUPPORTED;
+    const int gshift = group == 32 ? 0 : group == 64 ? 1 : 2;
+    if (K >= 1024)
+        return launch_split<128, true>(dev, x, qw_gate, s_gate, y, M, N, K, gshift, nullptr, 1, nullptr, 0, st,
+                                       qw_up, s_up);
+    return launch_split<64, true>(dev, x, qw_gate, s_gate, y, M, N, K, gshift, nullptr, 1, nullptr, 0, st, qw_up,
+                                  s_up);
 }
 
 #ifdef W4A16_TEST_HOOKS
