@@ -104,16 +104,19 @@ struct Cfg {
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
-// Prefill / routed experts: 128 tokens, 256-k stages, one tile per CTA. Large
-// stages amortise the MMA thread's per-stage waits and commits over 16 MMAs.
+// 128-token tiles (the fused gate+up pair and experts outside the split-scale
+// kernel's range): 256-k stages amortise the MMA thread's per-stage waits and
+// commits over 16 MMAs.
 template <int G>
 using PrefillCfg = Cfg<G, 128, 256, 4, 2, 4, 8>;
-// Small batches (dense M <= 64): narrower token tiles waste fewer MMA columns;
-// four epilogue warps cover the tile.
+// Small batches (M <= 64): narrower token tiles waste fewer MMA columns; four
+// epilogue warps cover the tile. The MMA issue rate bounds these tiles (about
+// 60 ns per instruction whatever the width), and a second issuing warp takes
+// every other scale group: M = 32 runs in 30.8 instead of 32.8 us.
 template <int G>
-using Narrow64Cfg = Cfg<G, 64, 256, 4, 2, 4, 4>;
+using Narrow64Cfg = Cfg<G, 64, 256, 4, 2, 4, 4, false, 2, 2>;
 template <int G>
-using Narrow32Cfg = Cfg<G, 32, 256, 4, 2, 4, 4>;
+using Narrow32Cfg = Cfg<G, 32, 256, 4, 2, 4, 4, false, 2, 2>;
 // Routed experts: the prefill tile, with the scales fetched further ahead. At group 32 a
 // stage holds 8 groups, so scalar loads a few groups ahead leave the epilogue waiting on HBM.
 template <int G>
