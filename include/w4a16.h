@@ -96,7 +96,10 @@ W4A16_API w4a16_status w4a16_unpack(const uint8_t* qweight, int64_t N, int64_t K
  * Dense layer y = x * W^T (see the definition at the top of this file).
  * M, N >= 0 (M = 0 or N = 0: nothing to do); K >= 0 with K % group == 0 and
  * K % 32 == 0 (K = 0 writes y = 0); group in {32, 64, 128}.
- * x, qweight, scales and y must be 16-byte aligned.
+ * x, qweight, scales and y must be 16-byte aligned. y may also point to
+ * page-locked host memory (cudaHostAlloc / cudaHostRegister) when K > 0: with
+ * unified addressing the kernels store the result into it directly, so a
+ * caller that wants the result on the host needs no separate copy.
  * Small M (decode, up to 16 rows) runs a split-K GEMV whose cross-block
  * partial sums live in `workspace`; larger M runs the tensor-core GEMM.
  * workspace: device buffer of at least w4a16_workspace_bytes(M, N, K, group, 1)

@@ -111,6 +111,26 @@ def _need(t: torch.Tensor, name: str, dtype, dim: int):
         raise ValueError(f"{name}: must be contiguous")
 
 
+def _out(out, shape, device: torch.device, K: int):
+    """The output of a dense layer: new on x's device, or the caller's tensor,
+    which may be on x's device or in pinned host memory (the kernels then store
+    to it directly through unified addressing: no separate copy)."""
+    if out is None:
+        return torch.empty(shape, dtype=torch.float16, device=device)
+    if not isinstance(out, torch.Tensor) or out.dtype != torch.float16 or out.dim() != 2:
+        raise ValueError("out: expected a 2-d torch.float16 tensor")
+    if not out.is_contiguous():
+        raise ValueError("out: must be contiguous")
+    if tuple(out.shape) != tuple(shape):
+        raise ValueError("out must be [M, N]")
+    if out.is_cuda:
+        if out.device != device:
+            raise ValueError("out must be on x's device")
+    elif not out.is_pinned() or K == 0:
+        raise ValueError("out must be a CUDA tensor, or pinned host memory (K > 0)")
+    return out
+
+
 # one zero-initialised workspace per (device, stream), grown on demand
 _ws: dict = {}
 
@@ -155,6 +175,7 @@ def unpack(qw: torch.Tensor, K: int) -> torch.Tensor:
 def linear(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, group: int = 128,
            out: torch.Tensor | None = None, static_weights: bool = False) -> torch.Tensor:
     """y = x W^T for x fp16 [M, K], qweight uint8 [N, K/2], scales fp16 [N, K/group].
+    ``out`` may be a CUDA tensor on x's device or pinned host memory (K > 0).
 
     ``static_weights=True`` passes W4A16_STATIC_WEIGHTS: the caller promises
     that no work still pending on the stream writes qweight or scales (the
@@ -167,12 +188,7 @@ def linear(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, group: 
     N = qweight.shape[0]
     if qweight.shape[1] * 2 != K or (group and tuple(scales.shape) != (N, K // group)):
         raise ValueError("shape mismatch between x, qweight and scales")
-    if out is None:
-        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
-    else:
-        _need(out, "out", torch.float16, 2)
-        if tuple(out.shape) != (M, N):
-            raise ValueError("out must be [M, N]")
+    out = _out(out, (M, N), x.device, K)
     st = _stream(x.device)
     nb = workspace_bytes(M, N, K, group, 1)
     ws = _workspace(x.device, st, nb)
@@ -199,12 +215,7 @@ def linear_gated(x: torch.Tensor, qweight_gate: torch.Tensor, scales_gate: torch
     if (qweight_gate.shape[1] * 2 != K or tuple(qweight_up.shape) != tuple(qweight_gate.shape)
             or tuple(scales_gate.shape) != (N, K // group) or tuple(scales_up.shape) != (N, K // group)):
         raise ValueError("shape mismatch between x, the weights and the scales")
-    if out is None:
-        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
-    else:
-        _need(out, "out", torch.float16, 2)
-        if tuple(out.shape) != (M, N):
-            raise ValueError("out must be [M, N]")
+    out = _out(out, (M, N), x.device, K)
     st = _stream(x.device)
     nb = int(lib().w4a16_linear_gated_workspace_bytes(M, N, K, group))
     ws = _workspace(x.device, st, nb)
