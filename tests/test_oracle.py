@@ -282,14 +282,15 @@ def test_tolerance_hand_worked():
     |y - y_ref| <= 2^-9 |y_ref| + 1e-4 sum_k |x_k W^_nk|, on values worked out
     by hand: each term alone, a negative y_ref (its magnitude counts), and the
     two terms together. Every GPU parity check compares against this bound."""
+    h = 2.0 ** -25                          # half the binary16 subnormal spacing, in every case
     cases = [
         # y_ref, sum_k |x W^|, bound
-        (1.0, 0.0, 0.001953125),            # 2^-9 alone
-        (0.0, 1.0, 0.0001),                 # 1e-4 alone
-        (-3.0, 2.0, 0.005859375 + 0.0002),  # 3 * 2^-9 + 2 * 1e-4: |y_ref|, not y_ref
-        (512.0, 0.0, 1.0),                  # 512 * 2^-9
-        (-0.25, 10000.0, 1.00048828125),    # 2^-11 + 1
-        (0.0, 0.0, 0.0),
+        (1.0, 0.0, 0.001953125 + h),            # 2^-9 alone
+        (0.0, 1.0, 0.0001 + h),                 # 1e-4 alone
+        (-3.0, 2.0, 0.005859375 + 0.0002 + h),  # 3 * 2^-9 + 2 * 1e-4: |y_ref|, not y_ref
+        (512.0, 0.0, 1.0 + h),                  # 512 * 2^-9
+        (-0.25, 10000.0, 1.00048828125 + h),    # 2^-11 + 1
+        (0.0, 0.0, h),
     ]
     y = np.array([c[0] for c in cases])
     a = np.array([c[1] for c in cases])
@@ -299,6 +300,22 @@ def test_tolerance_hand_worked():
     assert np.allclose(got, want, rtol=1e-14, atol=0.0), (got, want)
     # the bound grows with both arguments, and only with |y_ref|
     assert np.array_equal(oracle.tolerance(-y, a), got)
+
+
+def test_tolerance_admits_the_correctly_rounded_result():
+    """Whatever the size of y, its exact value rounded to fp16 (what a perfect
+    kernel returns) lies within the bound, also in the subnormal range where
+    2^-9 |y| alone is far too small; and the absolute term is no larger than
+    that rounding needs."""
+    r = np.random.default_rng(8)
+    y = np.concatenate([np.ldexp(1.0, np.arange(-34, 15)), np.exp(r.uniform(np.log(1e-10), np.log(6e4), 20000))])
+    y *= r.choice([-1.0, 1.0], y.size)
+    zero = np.zeros_like(y)
+    err = np.abs(y.astype(np.float16).astype(np.float64) - y)
+    assert np.all(err <= oracle.tolerance(y, zero))
+    sub = np.abs(y) < np.ldexp(1.0, -14)
+    assert np.any(err[sub] > np.ldexp(np.abs(y[sub]), -9))       # the relative term alone fails there
+    assert np.max(err) <= np.ldexp(1.0, -25) + np.max(np.ldexp(np.abs(y), -11))
 
 
 def test_threaded_linear_equals_single_thread():

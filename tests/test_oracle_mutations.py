@@ -122,13 +122,15 @@ def test_moe_pins_catch_planted_mistake(name, monkeypatch):
 # tolerance() is the bound every GPU parity check applies; a mutant with a
 # looser or wrong bound must fail its hand-worked pin.
 
-TOL_LINE = "    return np.ldexp(np.abs(y_ref), -9) + 1e-4 * absdot\n"
+TOL_LINE = "    return np.ldexp(np.abs(y_ref), -9) + 1e-4 * absdot + np.ldexp(1.0, -25)\n"
 TOL_MUTANTS = {
-    "relative term 2^-8": "    return np.ldexp(np.abs(y_ref), -8) + 1e-4 * absdot\n",
-    "absolute term 1e-3": "    return np.ldexp(np.abs(y_ref), -9) + 1e-3 * absdot\n",
-    "signed y_ref": "    return np.ldexp(y_ref, -9) + 1e-4 * absdot\n",
-    "absolute term dropped": "    return np.ldexp(np.abs(y_ref), -9)\n",
-    "terms multiplied": "    return np.ldexp(np.abs(y_ref), -9) * (1 + 1e-4 * absdot)\n",
+    "relative term 2^-8": "    return np.ldexp(np.abs(y_ref), -8) + 1e-4 * absdot + np.ldexp(1.0, -25)\n",
+    "absolute term 1e-3": "    return np.ldexp(np.abs(y_ref), -9) + 1e-3 * absdot + np.ldexp(1.0, -25)\n",
+    "signed y_ref": "    return np.ldexp(y_ref, -9) + 1e-4 * absdot + np.ldexp(1.0, -25)\n",
+    "absolute term dropped": "    return np.ldexp(np.abs(y_ref), -9) + np.ldexp(1.0, -25)\n",
+    "terms multiplied": "    return np.ldexp(np.abs(y_ref), -9) * (1 + 1e-4 * absdot) + np.ldexp(1.0, -25)\n",
+    "rounding term 2^-24": "    return np.ldexp(np.abs(y_ref), -9) + 1e-4 * absdot + np.ldexp(1.0, -24)\n",
+    "rounding term dropped": "    return np.ldexp(np.abs(y_ref), -9) + 1e-4 * absdot\n",
 }
 
 
