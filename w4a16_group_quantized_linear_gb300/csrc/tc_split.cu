@@ -38,11 +38,13 @@
 // next tile's MMAs start at once.
 //
 // Pipeline stages of KS k (Pipe<KS>): 128 for long K (two TMEM A stages, a
-// 2-deep x ring of 64 KB stages, a 4-deep packed ring), 64 for short K, where a
-// tile has few stages and a deeper pipeline hides its fill (four A stages, a
-// 4-deep x ring of 32 KB, an 8-deep packed ring). Measured on the routed-expert
-// layer: gate/up (K = 2048) 119 us at 128-k stages against 139 us at 64;
-// down (K = 512) 177 us at 64-k stages against 205 us at 128.
+// 3-deep x ring of 64 KB stages and a 3-deep packed ring where the tile plan
+// leaves room for them, else 2 and 4), 64 for short K, where a tile has few
+// stages and a deeper pipeline hides its fill (four A stages, a 4-deep x ring
+// of 32 KB, an 8-deep packed ring). Measured on the routed-expert layer:
+// gate/up (K = 2048) 119 us at 128-k stages against 139 us at 64, and 109
+// against 115 us with the third x stage; down (K = 512) 177 us at 64-k stages
+// against 205 us at 128.
 //
 //   warp 0      TMA producer: the packed weights of each stage (128 rows x
 //               KS/2 bytes, swizzled) and the stage's x (KS/64 boxes of 256
@@ -95,12 +97,12 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s
 constexpr uint64_t kDrainLimitNs = 1000000000ull;    // 1 s
 
 // The rings of a pipeline of KS-k stages.
-template <int KS>
+template <int KS, int XS = (KS == 128 ? 2 : 4)>
 struct Pipe {
     static constexpr int kKS = KS;
     static constexpr int kChunksPerStage = KS / kChunk;
-    static constexpr int kPStages = KS == 128 ? 4 : 8;   // packed-weight ring
-    static constexpr int kXStages = KS == 128 ? 2 : 4;   // x ring (shared memory)
+    static constexpr int kPStages = KS == 128 ? (XS >= 3 ? 3 : 4) : 8;  // packed-weight ring
+    static constexpr int kXStages = XS;                                // x ring (shared memory)
     static constexpr int kAStages = KS == 128 ? 2 : 4;   // TMEM A stages
     static constexpr int kPBytes = kRows * KS / 2;        // packed weights of a stage
     static constexpr int kXBoxes = KS / 64;
@@ -146,11 +148,11 @@ struct SplitArgs {
     unsigned int* err;
 };
 
-// The tile plan (filled once per CTA).
+// The tile plan (filled once per CTA) in shared memory, after the store
+// staging: E + 1 entries each, sized at launch.
 struct TilePlan {
-    int tiles;                        // token tiles over all experts (0: invalid offsets)
-    int first_tile[kMaxE + 1];        // token tiles of the experts before e
-    int row_start[kMaxE + 1];         // expert_offsets
+    int* first_tile;  // token tiles of the experts before e
+    int* row_start;   // expert_offsets
 };
 
 template <class P>
@@ -166,8 +168,19 @@ struct SplitSmem {
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort;
-    TilePlan plan;
+    int plan_tiles;                // token tiles over all experts (0: invalid offsets)
 };
+
+// Shared memory ahead of the rings: the store staging, the tile plan of E
+// experts and the barrier block, rounded up to the rings' 1024-byte alignment.
+// (Of the orders of these regions measured, this one ran the routed down
+// projection, K = 512, fastest: 127 us against up to 138.)
+template <class P>
+constexpr int kBarrierBytes = (int)((sizeof(SplitSmem<P>) + 127) & ~(size_t)127);
+template <class P>
+__host__ __device__ constexpr int front_bytes(int E) {
+    return (kBarrierBytes<P> + kEpiWarps * kStageBytes + 2 * (E + 1) * (int)sizeof(int) + 1023) & ~1023;
+}
 
 struct Tile {
     int e, row0, rows, n0;
@@ -207,7 +220,7 @@ __device__ __forceinline__ Tile decode_tile(const TilePlan& pl, int t, int ntn, 
 // Warp 0, at start: each expert's first token tile and first row, from the
 // device offsets (dense: one expert of M rows); an invalid partition is
 // reported and leaves no tile.
-__device__ void plan_tiles(const SplitArgs& a, TilePlan& pl, int lane) {
+__device__ void plan_tiles(const SplitArgs& a, const TilePlan& pl, int* tiles_out, int lane) {
     int base = 0;
     bool ok = true;
     for (int e0 = 0; e0 < a.E; e0 += 32) {
@@ -243,7 +256,7 @@ __device__ void plan_tiles(const SplitArgs& a, TilePlan& pl, int lane) {
     if (lane == 0) {
         pl.first_tile[a.E] = base;
         pl.row_start[a.E] = end;
-        pl.tiles = (ok && ends_ok) ? base : 0;
+        *tiles_out = (ok && ends_ok) ? base : 0;
         if (!ok || !ends_ok) raise_device_error(a.err, W4A16_ERR_BAD_OFFSETS);
     }
 }
@@ -274,23 +287,27 @@ __device__ __forceinline__ float row_shift(const uint16_t* srow, int gk, bool ok
 // GATED (dense only): each tile's 128 weight rows are 64 rows of Wg and the same
 // 64 rows of Wu (tmap_w, tmap_w2), interleaved in TMEM as gated_out_row /
 // gated_smem_row describe; the epilogue forms y = silu(g) * u from the fp32 sums.
-template <int KS, bool GATED>
+template <int KS, bool GATED, int XS>
 __global__ void __launch_bounds__(kThreads, 1)
     split_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                  const __grid_constant__ CUtensorMap tmap_w2, const SplitArgs a) {
-    using P = Pipe<KS>;
+    using P = Pipe<KS, XS>;
     constexpr int kOut = GATED ? kRows / 2 : kRows;  // output rows per tile
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t* pring = base;                                 // packed-weight stages
-    uint8_t* xring = base + P::kPStages * P::kPBytes;      // x stages (1024-byte aligned)
-    SplitSmem<P>* sm = reinterpret_cast<SplitSmem<P>*>(xring + P::kXStages * P::kXBytes);
-    // the epilogue warps' store staging, kStageBytes each, after the barrier block
-    uint8_t* ystage = reinterpret_cast<uint8_t*>(sm) + ((sizeof(SplitSmem<P>) + 127) & ~(size_t)127);
+    // the epilogue warps' store staging (kStageBytes each), the tile plan and
+    // the barrier block come first; the rings start at the next 1024 bytes
+    uint8_t* ystage = base;
+    TilePlan plan;
+    plan.first_tile = reinterpret_cast<int*>(ystage + kEpiWarps * kStageBytes);
+    plan.row_start = plan.first_tile + (a.E + 1);
+    SplitSmem<P>* sm = reinterpret_cast<SplitSmem<P>*>(plan.row_start + (a.E + 1));  // 8-byte aligned
+    uint8_t* pring = base + front_bytes<P>(a.E);           // packed-weight stages
+    uint8_t* xring = pring + P::kPStages * P::kPBytes;     // x stages (1024-byte aligned)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (warp == 0) {
-        plan_tiles(a, sm->plan, lane);
+        plan_tiles(a, plan, &sm->plan_tiles, lane);
         if (lane == 0) {
             for (int i = 0; i < P::kPStages; ++i) {
                 ptx::mbar_init(&sm->pfull[i], 1);
@@ -316,9 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-    const TilePlan& plan = sm->plan;
     const int ntn = (int)((a.N + kOut - 1) / kOut);     // weight-row tiles
-    const int total = plan.tiles * ntn;
+    const int total = sm->plan_tiles * ntn;
     if ((int)blockIdx.x >= total) return;                // nothing for this CTA (uniform)
     if (warp == 1) {
         ptx::tmem_alloc(&sm->tmem_base, kTmemCols);
@@ -757,9 +773,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------- host --
 
 template <class P>
-constexpr size_t smem_bytes() {
-    return 1024 + P::kPStages * P::kPBytes + P::kXStages * P::kXBytes + ((sizeof(SplitSmem<P>) + 127) & ~(size_t)127) +
-           kEpiWarps * kStageBytes;
+constexpr size_t smem_bytes(int E) {
+    return 1024 + front_bytes<P>(E) + P::kPStages * P::kPBytes + P::kXStages * P::kXBytes;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -782,9 +797,14 @@ w4a16_status launch_split(const DeviceInfo& dev, const uint16_t* x, const uint8_
                           const int32_t* gather, int64_t T, cudaStream_t st, const uint8_t* qw2 = nullptr,
                           const uint16_t* s2 = nullptr) {
     constexpr int kOut = GATED ? kRows / 2 : kRows;
+    // 128-k stages take a third x stage (and one packed stage less) when the
+    // tile plan leaves room for it: the MMA thread then rarely waits for x
     using P = Pipe<KS>;
-    constexpr size_t kSmem = smem_bytes<P>();
-    if (kSmem > dev.smem_optin) return W4A16_ERR_UNSUPPORTED;
+    using P3 = Pipe<KS, 3>;
+    const int ne = offsets ? E : 1;
+    const bool x3 = KS == 128 && smem_bytes<P3>(ne) <= dev.smem_optin;
+    const size_t smem = x3 ? smem_bytes<P3>(ne) : smem_bytes<P>(ne);
+    if (smem > dev.smem_optin) return W4A16_ERR_UNSUPPORTED;
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cuda_status(cudaErrorNotSupported, "gemm split: cuTensorMapEncodeTiled entry point");
     CUtensorMap mx, mw, mw2;
@@ -844,11 +864,24 @@ w4a16_status launch_split(const DeviceInfo& dev, const uint16_t* x, const uint8_
     if (tiles > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
     const unsigned grid = (unsigned)(tiles < dev.sms ? tiles : dev.sms);
     static PerDeviceOnce once;
-    const cudaError_t attr = once.run(dev.device, [] {
-        return cudaFuncSetAttribute(split_kernel<KS, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    const cudaError_t attr = once.run(dev.device, [&dev] {
+        cudaError_t e = cudaFuncSetAttribute(split_kernel<KS, GATED, P::kXStages>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dev.smem_optin);
+        if constexpr (KS == 128) {
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(split_kernel<KS, GATED, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)dev.smem_optin);
+        }
+        return e;
     });
     if (attr != cudaSuccess) return cuda_status(attr, "gemm split: cudaFuncSetAttribute");
-    split_kernel<KS, GATED><<<grid, kThreads, kSmem, st>>>(mx, mw, mw2, a);
+    if constexpr (KS == 128) {
+        if (x3) {
+            split_kernel<KS, GATED, 3><<<grid, kThreads, smem, st>>>(mx, mw, mw2, a);
+            return cuda_status(cudaGetLastError(), "gemm split: kernel launch");
+        }
+    }
+    split_kernel<KS, GATED, P::kXStages><<<grid, kThreads, smem, st>>>(mx, mw, mw2, a);
     return cuda_status(cudaGetLastError(), "gemm split: kernel launch");
 }
 
