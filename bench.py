@@ -858,7 +858,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["hbm_peak"], "unit": "GB/s",
                      "frac": r["achieved"] / r["hbm_peak"],
                      "traffic": measured_traffic("gemv.cu", "gemv_decode_m1.md"),
-                     "kernel": "gemv_kernel<group 128, M<=8>", "peak_kind": r["peak_kind"],
+                     "kernel": "gemv_decode_kernel<cluster 2|4> (group 128, M=1)", "peak_kind": r["peak_kind"],
                      "kernel_us": r["kernel_ms"] * 1e3, "algorithmic_bytes_per_launch": r["per_launch_bytes"]},
         "per_call": r["spread"], "static_weights_mode": r["static_mode"],
         "e2e": r["e2e"], "gpu_launches": r["launches"], "clocks": r["clocks"], "gpu": r["gpu"], "sms": r["sms"],

@@ -73,7 +73,10 @@ def test_gemv_wait_times_out_and_next_call_is_correct(hooks, cuda_device):
     import torch
 
     lib = hooks
-    M, N, K, g = 1, 17408, 5120, 128   # about 9 units per compute warp: a stop after 2 copies stalls every warp
+    # group 64 takes the TMA-ring kernel, whose waits are the bounded ones (the
+    # group-128 cluster kernel waits on nothing but its own cluster's barrier);
+    # about 9 units per compute warp: a stop after 2 copies stalls every warp
+    M, N, K, g = 1, 17408, 5120, 64
     r = workloads.rng(90)
     qw, s = workloads.raw_packed(r, N, K, g)
     x = workloads.activations(r, M, K)

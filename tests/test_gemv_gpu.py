@@ -52,6 +52,20 @@ def test_raw_nibbles_all_M(w4, cuda_device, M, g):
     assert_within_bound(y, y_ref, a, f"M={M} g={g}")
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 32, 65536), (2, 48, 30720), (1, 2500, 4096), (3, 16, 40960), (2, 1, 512)])
+def test_row_blocks_split_across_many_warps(w4, cuda_device, M, N, K):
+    """Group 128: row-blocks whose units are split over up to about 24 warps of
+    a cluster (their partials summed in batches), clusters left without work,
+    the two x paths (per warp for M <= 2, per block above)."""
+    r = workloads.rng(M * 31 + N + K)
+    qw, s = workloads.raw_packed(r, N, K, 128)
+    x = workloads.activations(r, M, K)
+    y = _run(w4, cuda_device, x, qw, s, 128)
+    y_ref, a = oracle.linear(x, qw, s, 128)
+    assert_within_bound(y, y_ref, a, f"M={M} N={N} K={K}")
+    assert np.array_equal(y.view(np.uint16), _run(w4, cuda_device, x, qw, s, 128).view(np.uint16))
+
+
 @pytest.mark.parametrize("N,K,g", [(1, 32, 32), (7, 96, 32), (17, 192, 64), (100, 640, 128), (1000, 2080, 32),
                                    (4099, 384, 128), (16, 128, 128), (31, 8192, 64)])
 def test_ragged_shapes(w4, cuda_device, N, K, g):

@@ -221,8 +221,8 @@ __device__ __forceinline__ ScaleRows scale_rows(const GemvArgs& p, const GatedAr
     return r;
 }
 
-template <int G>
-__device__ __forceinline__ void load_scales(UnitScales<G>& sc, const GemvArgs& p, const ScaleRows& sr, int ku) {
+template <int G, class Args>
+__device__ __forceinline__ void load_scales(UnitScales<G>& sc, const Args& p, const ScaleRows& sr, int ku) {
     constexpr int GPU = kUnitK / G;  // groups per unit: 4, 8 or 16
     const int g0 = ku * GPU;
     if (p.svec && g0 + GPU <= p.gpr) {  // whole unit from aligned rows: vector loads
@@ -452,21 +452,36 @@ __device__ __noinline__ void publish_partial(const GemvArgs& p, const GatedArgs&
     if ((int64_t)old != wb - wa) return;  // another warp finishes this row-block
     __syncwarp();  // every lane's loads of the other partials come after lane 0's acquire
     const int64_t slot_elems = (int64_t)kRows * p.M;
+    // rb is the first segment of every contributor except possibly wa
+    const bool wa_started_inside = (wa * p.U / p.P) == rb * p.KU;
     float sum[NT][4];
 #pragma unroll
     for (int t = 0; t < NT; ++t) sum[t][0] = sum[t][1] = sum[t][2] = sum[t][3] = 0.0f;
-    for (int64_t v = wa; v <= wb; ++v) {
-        // rb is the first segment of every contributor except possibly wa
-        const bool wa_started_inside = (v * p.U / p.P) == rb * p.KU;
-        const int sl = (v == wa && !wa_started_inside) ? 1 : 0;
-        const float* src = p.partial + (v * 2 + sl) * slot_elems;
+    // kBatch contributors' partials are loaded at once, then added in warp
+    // order: one L2 round trip per batch instead of one per contributor
+    constexpr int kBatch = NT == 1 ? 8 : 4;
+    for (int64_t v0 = wa; v0 <= wb; v0 += kBatch) {
+        float part[kBatch][NT][4];
 #pragma unroll
-        for (int t = 0; t < NT; ++t)
+        for (int b = 0; b < kBatch; ++b) {
+            const int64_t v = v0 + b;
+            const int sl = (v == wa && !wa_started_inside) ? 1 : 0;
+            const float* src = p.partial + (v * 2 + sl) * slot_elems;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int m = 8 * t + 2 * t4 + (i & 1);
-                if (m < p.M) sum[t][i] += __ldcg(src + m * kRows + gid + 8 * (i >> 1));
-            }
+            for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int m = 8 * t + 2 * t4 + (i & 1);
+                    part[b][t][i] = (v <= wb && m < p.M) ? __ldcg(src + m * kRows + gid + 8 * (i >> 1)) : 0.0f;
+                }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (v0 + b <= wb) sum[t][i] += part[b][t][i];
     }
     if (lane == 0) p.counter[rb] = 0;
     finish_row_block<NT, GT>(p, ga, (int)rb, sum, gid, t4, lane);
@@ -733,6 +748,542 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemv_body<G, NT, XS, TS, true>(maps, p, ga);
 }
 
+// ============================================================================
+// Cluster kernel: group 128, M <= 8, one weight matrix.
+//
+// * A cluster of C blocks (one per SM, kCWarps compute warps each) owns an
+//   equal share of whole row-blocks, and its C x kCWarps warps split the
+//   cluster's units into equal contiguous ranges (stream-K inside the
+//   cluster). Every split row-block is therefore summed inside one cluster.
+// * Each lane loads its own 16-byte pieces of a unit (rows gid and gid + 8,
+//   the k its mma fragments take) straight into registers, one unit ahead of
+//   the unit it computes: no copy engine, no ring, no wait per unit. (Against
+//   the TMA ring above, with the same arithmetic: 14.9 against 15.7 us per
+//   GEMV in the back-to-back decode step.)
+// * x: for M <= 2 each warp stages the x of its next unit in a two-slot ring
+//   of its own, so no block-wide barrier delays the first unit; larger M is
+//   staged once per block, as above.
+// * A split row-block: each contributor leaves its fp32 partial in its own
+//   block's shared memory and counts its arrival with one cluster-scope
+//   acquire-release atomic on a counter in the first contributor's block; the
+//   last to arrive sums every contributor's partial in warp order through
+//   distributed shared memory (deterministic), rounds once to fp16 and stores
+//   y. No partial crosses L2: summing split row-blocks through L2 (a partial
+//   store, a release fence and an atomic per contributor, then the last
+//   arriver's loads) cost about 4 us of each 15 us launch, almost all of it at
+//   the end of the launch, where every warp finishes its last row-block.
+// * Blocks meet on the cluster barrier at the start (the counters are zeroed
+//   before any remote atomic) and before they leave (no block's partials
+//   vanish while another may read them). Neither barrier waits on anything
+//   but the cluster's own blocks, all resident together.
+constexpr int kCWarps = 12;                    // compute warps per block
+constexpr int kCThreads = kCWarps * 32;
+
+// Shared memory of the cluster kernel for x staged per warp (MX = 1 or 2
+// tokens) or per block (MX = 8): zero x (1 KB), the partials, the counters,
+// then x. The footprint is kept small on purpose: the shared-memory carveout
+// comes out of the L1, which also holds the in-flight weight loads (a 65 KB
+// footprint against a 27 KB one measured 0.3 us slower per GEMV).
+template <int MX>
+struct CLayout {
+    static constexpr int kPart = kRows * MX;                           // floats per partial
+    static constexpr int kXTok = MX == 1 ? kUnitK * 2 : kUnitK * 2 + 64;  // a token's unit of x (+pad against bank conflicts)
+    static constexpr int kXSlot = MX * kXTok;                           // one unit of x
+    static constexpr int kFixed = 1024 + kCWarps * 2 * kPart * 4 + 128;
+    static constexpr int kXWarp = MX <= 2 ? kCWarps * 2 * kXSlot : 0;  // per-warp rings
+};
+
+static_assert(CLayout<1>::kFixed + CLayout<1>::kXWarp <= 48 * 1024, "M = 1 within the default shared memory");
+
+struct ClusterArgs {
+    const uint16_t* x;
+    const uint8_t* qw;
+    const uint16_t* s;
+    uint16_t* y;
+    int M, N, K;
+    int KU;    // 512-k units per row
+    int RB;    // row-blocks: ceil(N / 16)
+    int gpr;   // scale groups per row
+    int svec;  // scale rows start 16-byte aligned
+    int mode;  // kModeStatic
+};
+
+// A lane's share of one unit: rows gid and gid + 8, bytes 64 step + 16 t4 of
+// the unit's 256 per row ([step][row half]).
+struct Pieces {
+    uint4 w[2 * kUnitSteps];
+};
+
+// Weights: read once, through L1 without allocating there (measured 0.3 us
+// per GEMV faster than bypassing L1 with .cg). Read after griddepcontrol.wait
+// (or, with static weights, with nothing pending that writes them), so they
+// are the current contents.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+// x and scales: plain (not volatile) loads, free to be scheduled with the rest
+__device__ __forceinline__ uint4 ld_l2_v4_nv(const void* p) {
+    uint4 v;
+    asm("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ld_l2_v2_nv(const void* p) {
+    uint2 v;
+    asm("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+// EXACT (N % 16 == 0, K % 512 == 0): every piece lies inside the matrix.
+// Otherwise rows past N read row N - 1 (their sums are never stored) and
+// pieces past K are zero (K is a multiple of 32: a piece is wholly in or out).
+template <bool EXACT>
+__device__ __forceinline__ void load_pieces(Pieces& u, const ClusterArgs& p, int rb, int ku, int gid, int t4) {
+    const int64_t hk = p.K / 2;
+    int64_t r0 = (int64_t)rb * kRows + gid, r1 = r0 + 8;
+    if (!EXACT) {
+        if (r0 >= p.N) r0 = p.N - 1;
+        if (r1 >= p.N) r1 = p.N - 1;
+    }
+    const int64_t c = (int64_t)ku * (kUnitK / 2) + t4 * 16;
+    const uint8_t* a = p.qw + r0 * hk + c;
+    const uint8_t* b = p.qw + r1 * hk + c;
+#pragma unroll
+    for (int step = 0; step < kUnitSteps; ++step) {
+        const bool in = EXACT || c + step * 64 < hk;
+        u.w[2 * step] = in ? ld_stream_v4(a + step * 64) : make_uint4(0, 0, 0, 0);
+        u.w[2 * step + 1] = in ? ld_stream_v4(b + step * 64) : make_uint4(0, 0, 0, 0);
+    }
+}
+
+// The unit's four scales of rows gid and gid + 8 (EXACT: whole 16-byte aligned
+// scale rows, no row past N).
+template <bool EXACT>
+__device__ __forceinline__ void load_unit_scales(UnitScales<128>& sc, const ClusterArgs& p, const ScaleRows& sr,
+                                                 int ku) {
+    if (EXACT) {
+        const uint2 a = ld_l2_v2_nv(sr.r0 + ku * 4), b = ld_l2_v2_nv(sr.r1 + ku * 4);
+        sc.lo[0] = a.x; sc.lo[1] = a.y;
+        sc.hi[0] = b.x; sc.hi[1] = b.y;
+    } else {
+        load_scales<128>(sc, p, sr, ku);
+    }
+}
+
+__device__ __forceinline__ ScaleRows plain_scale_rows(const ClusterArgs& p, int rb, int gid) {
+    const int64_t n0 = (int64_t)rb * kRows + gid, n1 = n0 + 8;
+    ScaleRows r;
+    r.v0 = n0 < p.N;
+    r.v1 = n1 < p.N;
+    r.r0 = p.s + (r.v0 ? n0 : 0) * p.gpr;
+    r.r1 = p.s + (r.v1 ? n1 : 0) * p.gpr;
+    return r;
+}
+
+// One unit from registers (group 128: one group per 128-k step); x as in
+// compute_unit, at xl (this lane's 16-byte chunk of the unit's x).
+__device__ __forceinline__ void compute_pieces(const Pieces& u, const UnitScales<128>& sc, const uint8_t* xl,
+                                               float (&acc)[4]) {
+#pragma unroll
+    for (int step = 0; step < kUnitSteps; ++step) {
+        const uint32_t wa[4] = {u.w[2 * step].x, u.w[2 * step].y, u.w[2 * step].z, u.w[2 * step].w};
+        const uint32_t wb[4] = {u.w[2 * step + 1].x, u.w[2 * step + 1].y, u.w[2 * step + 1].z,
+                                u.w[2 * step + 1].w};
+        float c[4];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+            const uint4 xv = lds_v4(xl + step * (kStepK * 2) + wi * 64);
+            uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
+            nibbles_to_half2(wa[wi], a04, a15, a26, a37);
+            nibbles_to_half2(wb[wi], b04, b15, b26, b37);
+            if (wi == 0) mma_16816_zero(c, a04, b04, a15, b15, xv.x, xv.y);
+            else mma_16816(c, a04, b04, a15, b15, xv.x, xv.y);
+            mma_16816(c, a26, b26, a37, b37, xv.z, xv.w);
+        }
+        const float s0 = half_bits(sc.lo[step >> 1], step & 1), s1 = half_bits(sc.hi[step >> 1], step & 1);
+        acc[0] = fmaf(s0, c[0], acc[0]);
+        acc[1] = fmaf(s0, c[1], acc[1]);
+        acc[2] = fmaf(s1, c[2], acc[2]);
+        acc[3] = fmaf(s1, c[3], acc[3]);
+    }
+}
+
+__device__ __forceinline__ void store_y_cluster(const ClusterArgs& p, int rb, const float (&v)[4], int gid, int t4) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int m = 2 * t4 + (i & 1);
+        const int64_t n = (int64_t)rb * kRows + gid + 8 * (i >> 1);
+        if (m < p.M && n < p.N) p.y[(int64_t)m * p.N + n] = __half_as_ushort(__float2half_rn(v[i]));
+    }
+}
+
+// A split row-block as one contributor sees it: the cluster warps ga..gb
+// contribute, and the row-block is ga's first segment or its last.
+struct SplitSeg {
+    int ga, gb;
+    bool ga_first;
+};
+
+// MX: x staged per warp for M <= MX (1 or 2), or once per block (MX = 8);
+// C: blocks per cluster.
+template <int MX, bool EXACT, int C>
+__global__ void __launch_bounds__(kCThreads, 1) gemv_cluster_kernel(const ClusterArgs p) {
+    using L = CLayout<MX>;
+    constexpr bool XW = MX <= 2;
+    constexpr int XC = XW ? 2 * MX : 1;  // x chunks per lane per unit (per-warp staging)
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t* zero = smem_raw;                                         // 1 KB of zero x
+    float* part = reinterpret_cast<float*>(smem_raw + 1024);          // [warp][2][L::kPart]
+    int* counter = reinterpret_cast<int*>(part + kCWarps * 2 * L::kPart);  // [warp]
+    uint8_t* xs = smem_raw + L::kFixed;                               // per-warp rings, or the block's x
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
+    const int rank = (int)ptx::cluster_rank();
+    const int NC = (int)gridDim.x / C, cid = (int)blockIdx.x / C;
+    const int KU = p.KU;
+    const int rb0 = (int)((int64_t)p.RB * cid / NC), rb1 = (int)((int64_t)p.RB * (cid + 1) / NC);
+    const int64_t Tc = (int64_t)(rb1 - rb0) * KU;  // the cluster's units
+    // warps taking part: every one owns at least one unit, so the contributors
+    // to a row-block are consecutive warps
+    const int GW = (int)(Tc < C * kCWarps ? Tc : C * kCWarps), g = rank * kCWarps + warp;
+    const int q0 = g < GW ? (int)(Tc * g / GW) : 0, n = g < GW ? (int)(Tc * (g + 1) / GW) - q0 : 0;
+    // the cluster warp whose range holds the cluster's unit q
+    auto warp_of = [&](int64_t q) { return (int)(((q + 1) * GW + Tc - 1) / Tc - 1); };
+    int lrb = q0 / KU, ku = q0 % KU;  // row-block (from rb0) and unit of the next unit
+    // Only a warp's first and last row-blocks can be split with other warps:
+    // their contributors are worked out here, before the dependency wait,
+    // rather than by divisions at the end of the launch.
+    auto split_seg = [&](int lrb_) {
+        const int64_t qa = (int64_t)lrb_ * KU;
+        SplitSeg sg;
+        sg.ga = warp_of(qa);
+        sg.gb = warp_of(qa + KU - 1);
+        sg.ga_first = Tc * sg.ga / GW >= qa;
+        return sg;
+    };
+    SplitSeg seg_first = {0, 0, false}, seg_last = {0, 0, false};
+    if (n > 0) {
+        seg_first = split_seg(lrb);
+        seg_last = split_seg((q0 + n - 1) / KU);
+    }
+    const int xstride = (int)KU * (kUnitSteps * kStepK * 2) + 64;  // block-staged x: bytes per token
+
+    Pieces cur, nxt;
+    if ((p.mode & kModeStatic) && n > 0) load_pieces<EXACT>(cur, p, rb0 + lrb, ku, gid, t4);
+    if (threadIdx.x < 64) reinterpret_cast<uint4*>(zero)[threadIdx.x] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x < kCWarps) counter[threadIdx.x] = 0;
+    ptx::cluster_sync();  // the counters of every block are zero before any arrival
+    ptx::grid_dependency_wait();
+    if (!(p.mode & kModeStatic) && n > 0) load_pieces<EXACT>(cur, p, rb0 + lrb, ku, gid, t4);
+    // the first unit's scales go out before x is staged
+    ScaleRows sr = plain_scale_rows(p, rb0 + lrb, gid);
+    UnitScales<128> sc;
+    if (n > 0) load_unit_scales<EXACT>(sc, p, sr, ku);
+
+    // per-warp x: this lane's chunks c = lane + 32 i of a unit (token c / 64,
+    // 16-byte chunk c % 64 of its 1 KB), zero past K
+    uint8_t* xw = xs + warp * (2 * L::kXSlot);
+    auto load_x = [&](int ku_, uint4 (&v)[XC]) {
+#pragma unroll
+        for (int i = 0; i < XC; ++i) {
+            const int c = lane + 32 * i, m = c >> 6, j = c & 63;
+            const int64_t k = (int64_t)ku_ * kUnitK + j * 8;
+            v[i] = ((EXACT || k < p.K) && (MX == 1 || m < p.M)) ? ld_l2_v4_nv(p.x + (int64_t)m * p.K + k)
+                                                                 : make_uint4(0, 0, 0, 0);
+        }
+    };
+    auto store_x = [&](uint8_t* slot, const uint4 (&v)[XC]) {
+#pragma unroll
+        for (int i = 0; i < XC; ++i) {
+            const int c = lane + 32 * i, m = c >> 6, j = c & 63;
+            if (MX == 1 || m < p.M)
+                *reinterpret_cast<uint4*>(slot + m * L::kXTok + (j >> 4) * (kStepK * 2) + xs_pos(j & 15, 128) * 16) =
+                    permute_x8(v[i]);
+        }
+    };
+    if constexpr (XW) {
+        if (n > 0) {
+            uint4 v[XC];
+            load_x(ku, v);
+            store_x(xw, v);
+            __syncwarp();
+        }
+    } else {  // the whole x, once per block (as gemv_body does)
+        const int per_tok = KU * kUnitSteps * 16;
+        for (int c = threadIdx.x; c < p.M * per_tok; c += kCThreads) {
+            const int m = c / per_tok, cc = c % per_tok;
+            const uint4 v = cc * 8 < p.K ? ld_l2_v4(p.x + (int64_t)m * p.K + cc * 8) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(xs + m * xstride + (cc >> 4) * (kStepK * 2) + xs_pos(cc & 15, 128) * 16) =
+                permute_x8(v);
+        }
+        __syncthreads();
+    }
+
+    if (n > 0) {
+        const bool has = gid < p.M;
+        const int first_lrb = lrb;
+        int seg_ku0 = ku;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int r = 0; r < n; ++r) {
+            int nlrb = lrb, nku = ku + 1;
+            if (nku == KU) {
+                nku = 0;
+                ++nlrb;
+            }
+            UnitScales<128> sc_next = sc;
+            uint4 xv[XC];
+            if (r + 1 < n) {  // the next unit's weights, scales and x go out before this one's arithmetic
+                load_pieces<EXACT>(nxt, p, rb0 + nlrb, nku, gid, t4);
+                if (nku == 0) sr = plain_scale_rows(p, rb0 + nlrb, gid);
+                load_unit_scales<EXACT>(sc_next, p, sr, nku);
+                if constexpr (XW) load_x(nku, xv);
+            }
+            const uint8_t* xl;
+            if constexpr (XW) xl = (has ? xw + (r & 1) * L::kXSlot + gid * L::kXTok : zero) + t4 * 16;
+            else xl = (has ? xs + gid * xstride + ku * (kUnitSteps * kStepK * 2) : zero) + t4 * 16;
+            compute_pieces(cur, sc, xl, acc);
+            if constexpr (XW) {
+                if (r + 1 < n) {
+                    store_x(xw + ((r + 1) & 1) * L::kXSlot, xv);
+                    __syncwarp();  // every lane's chunks before any lane reads the slot
+                }
+            }
+            // only this warp's last sums remain: the next kernel on the stream may launch
+            if (r == n - 1) ptx::launch_dependents();
+            if (ku == KU - 1 || r == n - 1) {
+                const int rb = rb0 + lrb;
+                if (seg_ku0 == 0 && ku == KU - 1) {
+                    store_y_cluster(p, rb, acc, gid, t4);  // the whole row-block in this warp
+                } else {
+                    // the row-block's contributors: cluster warps ga..gb; this one
+                    // is at slot 0 if the row-block is its first segment
+                    const int sl = lrb == first_lrb ? 0 : 1;
+                    float* mine = part + (warp * 2 + sl) * L::kPart;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int m = 2 * t4 + (i & 1);
+                        if (m < p.M) mine[m * kRows + gid + 8 * (i >> 1)] = acc[i];
+                    }
+                    __syncwarp();  // the lanes' partials before lane 0's release
+                    const SplitSeg sg = sl == 0 ? seg_first : seg_last;
+                    const int ga = sg.ga, gb = sg.gb;
+                    int old = 0;
+                    if (lane == 0)
+                        old = ptx::atom_add_acq_rel_cluster(
+                            ptx::cluster_map(ptx::smem_u32(counter + ga % kCWarps), (uint32_t)(ga / kCWarps)), 1);
+                    old = __shfl_sync(0xffffffffu, old, 0);
+                    if (old == gb - ga) {  // the last contributor: sum them all in warp order
+                        __syncwarp();      // every lane's loads after lane 0's acquire
+                        const bool ga_first = sg.ga_first;  // the row-block is ga's first segment
+                        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+                        constexpr int kBatch = 8;  // partials loaded at once
+                        for (int v0 = ga; v0 <= gb; v0 += kBatch) {
+                            float pv[kBatch][4];
+#pragma unroll
+                            for (int b = 0; b < kBatch; ++b) {
+                                const int v = v0 + b;
+                                const int slv = (v == ga && !ga_first) ? 1 : 0;
+                                const uint32_t base = ptx::cluster_map(
+                                    ptx::smem_u32(part + ((v % kCWarps) * 2 + slv) * L::kPart),
+                                    (uint32_t)(v / kCWarps));
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int m = 2 * t4 + (i & 1);
+                                    pv[b][i] = (v <= gb && m < p.M)
+                                                   ? ptx::ld_cluster_f32(base + 4u * (m * kRows + gid + 8 * (i >> 1)))
+                                                   : 0.f;
+                                }
+                            }
+#pragma unroll
+                            for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    if (v0 + b <= gb) sum[i] += pv[b][i];
+                        }
+                        store_y_cluster(p, rb, sum, gid, t4);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+                seg_ku0 = nku;
+            }
+            lrb = nlrb;
+            ku = nku;
+            cur = nxt;
+            sc = sc_next;
+        }
+    } else {
+        ptx::launch_dependents();
+    }
+    ptx::cluster_sync();  // no block leaves while another may still read its partials
+}
+
+// The decode case of gemv_cluster_kernel, written out for it: M = 1, N % 16 ==
+// 0, K % 512 == 0, and every cluster with at least C x kCWarps units (so every
+// warp takes part). The same arithmetic in the same order, with the index
+// arithmetic of the general kernel (cluster size and warp count only known at
+// run time, rows and pieces checked against N and K, a scale-row record)
+// taken out: that costs 0.6 to 1.1 us per GEMV in the back-to-back decode
+// step, where each unit's loads and the last segment's sums are on the path.
+template <int C>
+__global__ void __launch_bounds__(kCThreads, 1) gemv_decode_kernel(const ClusterArgs p) {
+    constexpr int GW = C * kCWarps;  // the cluster's warps, all taking part
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t* zero = smem_raw;                                        // 1 KB of zero x
+    uint8_t* xr = smem_raw + 1024;                                   // [warp][2 slots][1 KB]
+    float* part = reinterpret_cast<float*>(smem_raw + 1024 + kCWarps * 2048);  // [warp][2][16]
+    int* counter = reinterpret_cast<int*>(part + kCWarps * 2 * kRows);         // [warp]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
+    const int rank = (int)ptx::cluster_rank();
+    const int cid = (int)blockIdx.x / C, NC = (int)gridDim.x / C;
+    const int KU = p.KU;
+    const int rb0 = (int)((int64_t)p.RB * cid / NC), rb1 = (int)((int64_t)p.RB * (cid + 1) / NC);
+    const int Tc = (rb1 - rb0) * KU;
+    const int g = rank * kCWarps + warp;
+    const int q0 = (int)((int64_t)Tc * g / GW), n = (int)((int64_t)Tc * (g + 1) / GW) - q0;
+    auto warp_of = [&](int q) { return (int)(((int64_t)(q + 1) * GW + Tc - 1) / Tc - 1); };
+    int lrb = q0 / KU, ku = q0 % KU;
+    const int hk = p.K / 2;
+    const uint8_t* lane_base = p.qw + (int64_t)gid * hk + t4 * 16;  // row gid of row-block 0, this lane's bytes
+    auto load_unit = [&](Pieces& u, int rb_, int ku_) {
+        const uint8_t* a = lane_base + (int64_t)rb_ * kRows * hk + ku_ * (kUnitK / 2);
+#pragma unroll
+        for (int step = 0; step < kUnitSteps; ++step) {
+            u.w[2 * step] = ld_stream_v4(a + step * 64);
+            u.w[2 * step + 1] = ld_stream_v4(a + 8 * hk + step * 64);
+        }
+    };
+    Pieces cur, nxt;
+    if ((p.mode & kModeStatic) && n > 0) load_unit(cur, rb0 + lrb, ku);
+    if (threadIdx.x < 64) reinterpret_cast<uint4*>(zero)[threadIdx.x] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x < kCWarps) counter[threadIdx.x] = 0;
+    ptx::cluster_sync();  // the counters of every block are zero before any arrival
+    ptx::grid_dependency_wait();
+    if (n > 0) {
+        if (!(p.mode & kModeStatic)) load_unit(cur, rb0 + lrb, ku);
+        // the unit's four scales of rows gid and gid + 8 (rows 16-byte aligned)
+        auto load_sc = [&](int rb_, int ku_, uint2& a, uint2& b) {
+            const uint16_t* r0 = p.s + (int64_t)(rb_ * kRows + gid) * p.gpr + ku_ * 4;
+            a = ld_l2_v2(r0);
+            b = ld_l2_v2(r0 + 8 * p.gpr);
+        };
+        // this lane's two 16-byte chunks (lane, lane + 32) of a unit's x
+        auto load_x = [&](int ku_, uint4& a, uint4& b) {
+            const uint16_t* xp = p.x + ku_ * kUnitK;
+            a = ld_l2_v4_nv(xp + lane * 8);
+            b = ld_l2_v4_nv(xp + (lane + 32) * 8);
+        };
+        uint8_t* xw = xr + warp * 2048;
+        auto store_x = [&](uint8_t* slot, uint4 a, uint4 b) {
+            const int j0 = lane, j1 = lane + 32;
+            *reinterpret_cast<uint4*>(slot + (j0 >> 4) * 256 + xs_pos(j0 & 15, 128) * 16) = permute_x8(a);
+            *reinterpret_cast<uint4*>(slot + (j1 >> 4) * 256 + xs_pos(j1 & 15, 128) * 16) = permute_x8(b);
+        };
+        uint2 sa, sb;
+        load_sc(rb0 + lrb, ku, sa, sb);
+        {
+            uint4 a, b;
+            load_x(ku, a, b);
+            store_x(xw, a, b);
+            __syncwarp();
+        }
+        const bool has = gid == 0;  // the token's lanes; the others read zero x
+        const int first_lrb = lrb;
+        int seg_ku0 = ku;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int r = 0; r < n; ++r) {
+            int nlrb = lrb, nku = ku + 1;
+            if (nku == KU) {
+                nku = 0;
+                ++nlrb;
+            }
+            uint2 na = sa, nb = sb;
+            uint4 xa, xb;
+            if (r + 1 < n) {
+                load_unit(nxt, rb0 + nlrb, nku);
+                load_sc(rb0 + nlrb, nku, na, nb);
+                load_x(nku, xa, xb);
+            }
+            UnitScales<128> sc;
+            sc.lo[0] = sa.x;
+            sc.lo[1] = sa.y;
+            sc.hi[0] = sb.x;
+            sc.hi[1] = sb.y;
+            compute_pieces(cur, sc, (has ? xw + (r & 1) * 1024 : zero) + t4 * 16, acc);
+            if (r + 1 < n) {
+                store_x(xw + ((r + 1) & 1) * 1024, xa, xb);
+                __syncwarp();  // every lane's chunks before any lane reads the slot
+            }
+            if (r == n - 1) ptx::launch_dependents();
+            const bool seg_end = (ku == KU - 1) || (r == n - 1);
+            if (seg_end) {
+                const int rb = rb0 + lrb;
+                if (seg_ku0 == 0 && ku == KU - 1) {
+                    store_y_cluster(p, rb, acc, gid, t4);  // the whole row-block in this warp
+                } else {
+                    const int sl = lrb == first_lrb ? 0 : 1;
+                    float* mine = part + (warp * 2 + sl) * kRows;
+                    if (t4 == 0) {
+                        mine[gid] = acc[0];
+                        mine[gid + 8] = acc[2];
+                    }
+                    __syncwarp();  // the lanes' partials before lane 0's release
+                    const int ga = warp_of(lrb * KU), gb = warp_of(lrb * KU + KU - 1);
+                    int old = 0;
+                    if (lane == 0)
+                        old = ptx::atom_add_acq_rel_cluster(
+                            ptx::cluster_map(ptx::smem_u32(counter + ga % kCWarps), (uint32_t)(ga / kCWarps)), 1);
+                    old = __shfl_sync(0xffffffffu, old, 0);
+                    if (old == gb - ga) {  // the last contributor: sum them all in warp order
+                        __syncwarp();      // every lane's loads after lane 0's acquire
+                        const bool ga_first = (int)((int64_t)Tc * ga / GW) >= lrb * KU;
+                        float sum0 = 0.f, sum1 = 0.f;
+                        constexpr int kBatch = 8;
+                        for (int v0 = ga; v0 <= gb; v0 += kBatch) {
+                            float pa[kBatch], pb[kBatch];
+#pragma unroll
+                            for (int b = 0; b < kBatch; ++b) {
+                                const int v = v0 + b;
+                                const int slv = (v == ga && !ga_first) ? 1 : 0;
+                                pa[b] = pb[b] = 0.f;
+                                if (v <= gb && t4 == 0) {
+                                    const uint32_t ra = ptx::cluster_map(
+                                        ptx::smem_u32(part + ((v % kCWarps) * 2 + slv) * kRows + gid),
+                                        (uint32_t)(v / kCWarps));
+                                    pa[b] = ptx::ld_cluster_f32(ra);
+                                    pb[b] = ptx::ld_cluster_f32(ra + 32);
+                                }
+                            }
+#pragma unroll
+                            for (int b = 0; b < kBatch; ++b)
+                                if (v0 + b <= gb) {
+                                    sum0 += pa[b];
+                                    sum1 += pb[b];
+                                }
+                        }
+                        const float sv[4] = {sum0, 0.f, sum1, 0.f};
+                        store_y_cluster(p, rb, sv, gid, t4);
+                    }
+                }
+                acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+            }
+            lrb = nlrb;
+            ku = nku;
+            if (seg_end) seg_ku0 = ku;
+            cur = nxt;
+            sa = na;
+            sb = nb;
+        }
+    } else {
+        ptx::launch_dependents();
+    }
+    ptx::cluster_sync();  // no block leaves while another may still read its partials
+}
+
+constexpr size_t kDecodeSmem = 1024 + kCWarps * 2048 + kCWarps * 2 * kRows * 4 + kCWarps * 4;
+
 int64_t max_warps(const DeviceInfo& dev) { return (int64_t)dev.sms * kConsumers; }
 
 size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
@@ -834,6 +1385,146 @@ size_t gemv_workspace_bytes(const DeviceInfo& dev, int64_t M, int64_t N, int64_t
 
 namespace {
 
+// Clusters of 2 and of 4 blocks that are resident at once on a device (0 when
+// none can be), found once per device; every instance of the cluster kernel
+// has the same registers and block size, so one answer serves them all.
+struct ClusterFit {
+    int count[2];
+};
+
+// The opt-in shared-memory limit, for the instances that may need more than
+// the default 48 KB (M > 1); the M = 1 instances (27 KB) keep the default.
+template <int MX>
+cudaError_t cluster_attrs(const DeviceInfo& dev) {
+    if (MX == 1) return cudaSuccess;
+    const void* fns[4] = {reinterpret_cast<const void*>(gemv_cluster_kernel<MX, true, 2>),
+                          reinterpret_cast<const void*>(gemv_cluster_kernel<MX, false, 2>),
+                          reinterpret_cast<const void*>(gemv_cluster_kernel<MX, true, 4>),
+                          reinterpret_cast<const void*>(gemv_cluster_kernel<MX, false, 4>)};
+    for (const void* fn : fns) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dev.smem_optin);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+const ClusterFit& cluster_fit(const DeviceInfo& dev, cudaError_t* err) {
+    static ClusterFit fit[kMaxDevices];
+    static PerDeviceOnce once;
+    *err = once.run(dev.device, [&dev] {
+        cudaError_t e = cluster_attrs<1>(dev);
+        if (e == cudaSuccess) e = cluster_attrs<2>(dev);
+        if (e == cudaSuccess) e = cluster_attrs<8>(dev);
+        if (e != cudaSuccess) return e;
+        for (int i = 0; i < 2; ++i) {
+            const int c = 2 << i;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(dev.sms / c * c));
+            cfg.blockDim = dim3(kCThreads);
+            cfg.dynamicSmemBytes = CLayout<1>::kFixed + CLayout<1>::kXWarp;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = (unsigned)c;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            int m = 0;
+            const cudaError_t q = c == 2 ? cudaOccupancyMaxActiveClusters(&m, gemv_cluster_kernel<1, true, 2>, &cfg)
+                                         : cudaOccupancyMaxActiveClusters(&m, gemv_cluster_kernel<1, true, 4>, &cfg);
+            if (q != cudaSuccess) {
+                (void)cudaGetLastError();  // not a sticky error: this cluster size is just not used
+                m = 0;
+            }
+            fit[dev.device].count[i] = m;
+        }
+        return cudaSuccess;
+    });
+    return fit[dev.device];
+}
+
+template <int MX>
+cudaError_t cluster_launch(const cudaLaunchConfig_t& cfg, const ClusterArgs& a, bool exact, int c) {
+    if (c == 2)
+        return exact ? cudaLaunchKernelEx(&cfg, gemv_cluster_kernel<MX, true, 2>, a)
+                     : cudaLaunchKernelEx(&cfg, gemv_cluster_kernel<MX, false, 2>, a);
+    return exact ? cudaLaunchKernelEx(&cfg, gemv_cluster_kernel<MX, true, 4>, a)
+                 : cudaLaunchKernelEx(&cfg, gemv_cluster_kernel<MX, false, 4>, a);
+}
+
+// Launches the cluster kernel when it applies (group 128, M <= 8, one matrix,
+// x within shared memory); *used is false when the caller must take the ring
+// kernel instead.
+w4a16_status cluster_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s, uint16_t* y,
+                         int64_t M, int64_t N, int64_t K, int group, bool static_weights, cudaStream_t st,
+                         bool* used) {
+    *used = false;
+    if (group != 128 || M > 8) return W4A16_OK;
+    const int64_t KU = (K + kUnitK - 1) / kUnitK, RB = (N + kRows - 1) / kRows;
+    if (RB * KU > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
+    const int mx = M == 1 ? 1 : M == 2 ? 2 : 8;
+    size_t smem = 0;
+    if (mx == 1) smem = CLayout<1>::kFixed + CLayout<1>::kXWarp;
+    else if (mx == 2) smem = CLayout<2>::kFixed + CLayout<2>::kXWarp;
+    else smem = CLayout<8>::kFixed + (size_t)M * (size_t)(KU * kUnitSteps * kStepK * 2 + 64);
+    if (smem > dev.smem_optin) return W4A16_OK;
+    cudaError_t e = cudaSuccess;
+    const ClusterFit& fit = cluster_fit(dev, &e);
+    if (e != cudaSuccess) return cuda_status(e, "gemv cluster: cudaFuncSetAttribute");
+    // the cluster size whose busiest warp has the fewest units
+    int c = 0, nc = 0;
+    int64_t best = 0;
+    for (int i = 0; i < 2; ++i) {
+        const int ci = 2 << i, ni = fit.count[i];
+        if (ni <= 0) continue;
+        const int64_t per_warp = ((RB + ni - 1) / ni * KU + ci * kCWarps - 1) / (ci * kCWarps);
+        if (c == 0 || per_warp < best) {
+            c = ci;
+            nc = ni;
+            best = per_warp;
+        }
+    }
+    if (c == 0) return W4A16_OK;
+    ClusterArgs a;
+    a.x = x;
+    a.qw = qw;
+    a.s = s;
+    a.y = y;
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.KU = (int)KU;
+    a.RB = (int)RB;
+    a.gpr = (int)(K / group);
+    a.svec = a.gpr % 8 == 0;
+    a.mode = static_weights ? kModeStatic : 0;
+    const bool exact = N % kRows == 0 && K % kUnitK == 0;  // then gpr % 4 == 0: a unit's scales are one 8-byte load
+    // the decode kernel wants every warp of every cluster busy
+    const bool decode = exact && M == 1 && (RB / nc) * KU >= (int64_t)c * kCWarps;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(nc * c));
+    cfg.blockDim = dim3(kCThreads);
+    cfg.dynamicSmemBytes = decode ? kDecodeSmem : smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = (unsigned)c;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    *used = true;
+    if (decode)
+        e = c == 2 ? cudaLaunchKernelEx(&cfg, gemv_decode_kernel<2>, a) : cudaLaunchKernelEx(&cfg, gemv_decode_kernel<4>, a);
+    else
+        e = mx == 1 ? cluster_launch<1>(cfg, a, exact, c) : mx == 2 ? cluster_launch<2>(cfg, a, exact, c)
+                                                                    : cluster_launch<8>(cfg, a, exact, c);
+    return cuda_status(e, "gemv cluster: kernel launch");
+}
+
 bool encode_weights(CUtensorMap (&map)[4], int slot, const uint8_t* qw, const uint16_t* s, int64_t N, int64_t K,
                     int group, bool ts, bool* w3d) {
     const int64_t gpr = K / group;
@@ -870,6 +1561,11 @@ w4a16_status gemv_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t* q
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return W4A16_ERR_WORKSPACE;
     if (((uintptr_t)workspace & 255) != 0) return W4A16_ERR_MISALIGNED;
     if (M > kMaxM || N > 0x7fffffffLL || K > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
+    if (!gated) {
+        bool used = false;
+        const w4a16_status r = cluster_run(dev, x, qw, s, y, M, N, K, group, opt.static_weights, st, &used);
+        if (used || r != W4A16_OK) return r;
+    }
     if (!encode_fn()) return cuda_status(cudaErrorNotSupported, "gemv: cuTensorMapEncodeTiled entry point");
     const int64_t gpr = K / group;
     const bool ts = (gpr * 2) % 16 == 0;  // scale rows can be TMA boxes
