@@ -806,6 +806,7 @@ struct ClusterArgs {
     int gpr;   // scale groups per row
     int svec;  // scale rows start 16-byte aligned
     int mode;  // kModeStatic
+    unsigned int* err;  // device error word (a summing wait that gave up)
 };
 
 // A lane's share of one unit: rows gid and gid + 8, bytes 64 step + 16 t4 of
@@ -1121,20 +1122,33 @@ __global__ void __launch_bounds__(kCThreads, 1) gemv_cluster_kernel(const Cluste
 }
 
 // The decode case of gemv_cluster_kernel, written out for it: M = 1, N % 16 ==
-// 0, K % 512 == 0, and every cluster with at least C x kCWarps units (so every
-// warp takes part). The same arithmetic in the same order, with the index
-// arithmetic of the general kernel (cluster size and warp count only known at
-// run time, rows and pieces checked against N and K, a scale-row record)
-// taken out: that costs 0.6 to 1.1 us per GEMV in the back-to-back decode
-// step, where each unit's loads and the last segment's sums are on the path.
+// 0, K % 512 == 0, every cluster with at least C x kCWarps units (so every
+// warp takes part) and at most kMail + 1 contributors to a row-block. The same
+// arithmetic in the same order, with the general kernel's index arithmetic
+// (cluster size and warp count known only at run time, rows and pieces
+// checked against N and K, a scale-row record) taken out: that cost 0.6 to
+// 1.1 us per GEMV in the back-to-back decode step.
+//
+// Split row-blocks are summed without any contributor waiting: the first
+// contributor ga of a row-block (for which it is its last segment) finishes
+// it. Every other contributor sends its 16 fp32 sums into ga's mailbox with
+// one-way st.async stores, which complete the transaction count of ga's
+// mbarrier as they land; ga arms that barrier with the bytes it expects at the
+// start of the launch, waits on it (with a time limit) after its own units,
+// and adds the sums in warp order: the same order, and the same result, as
+// the general kernel's. (A cluster-scope acquire-release atomic per
+// contributor, whose release waits for the contributor's in-flight weight
+// loads, then loads by the last arriver, cost 1.8 us of a 13.0 us launch.)
+constexpr int kMail = 8;  // contributors besides the finisher, per row-block
+
 template <int C>
 __global__ void __launch_bounds__(kCThreads, 1) gemv_decode_kernel(const ClusterArgs p) {
     constexpr int GW = C * kCWarps;  // the cluster's warps, all taking part
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    uint8_t* zero = smem_raw;                                        // 1 KB of zero x
-    uint8_t* xr = smem_raw + 1024;                                   // [warp][2 slots][1 KB]
-    float* part = reinterpret_cast<float*>(smem_raw + 1024 + kCWarps * 2048);  // [warp][2][16]
-    int* counter = reinterpret_cast<int*>(part + kCWarps * 2 * kRows);         // [warp]
+    uint8_t* zero = smem_raw;                                              // 1 KB of zero x
+    uint8_t* xr = smem_raw + 1024;                                         // [warp][2 slots][1 KB]
+    float* mail = reinterpret_cast<float*>(smem_raw + 1024 + kCWarps * 2048);  // [warp][kMail][16]
+    uint64_t* bar = reinterpret_cast<uint64_t*>(mail + kCWarps * kMail * kRows);  // [warp]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
     const int rank = (int)ptx::cluster_rank();
     const int cid = (int)blockIdx.x / C, NC = (int)gridDim.x / C;
@@ -1157,132 +1171,124 @@ __global__ void __launch_bounds__(kCThreads, 1) gemv_decode_kernel(const Cluster
     };
     Pieces cur, nxt;
     if ((p.mode & kModeStatic) && n > 0) load_unit(cur, rb0 + lrb, ku);
+    // this warp's first and last row-blocks: its only segments that may be split
+    const int lrb_first = lrb, lrb_last = (q0 + n - 1) / KU;
+    const int fa = warp_of(lrb_first * KU), fb = warp_of(lrb_first * KU + KU - 1);  // contributors, first
+    const int la = warp_of(lrb_last * KU), lb = warp_of(lrb_last * KU + KU - 1);    // contributors, last
     if (threadIdx.x < 64) reinterpret_cast<uint4*>(zero)[threadIdx.x] = make_uint4(0, 0, 0, 0);
-    if (threadIdx.x < kCWarps) counter[threadIdx.x] = 0;
-    ptx::cluster_sync();  // the counters of every block are zero before any arrival
+    if (lane == 0) {
+        ptx::mbar_init(&bar[warp], 1);
+        // the finisher of its last row-block expects the others' 64 bytes each
+        if (la == g && lb > la) ptx::mbar_arrive_expect_tx(&bar[warp], (uint32_t)(lb - la) * kRows * 4);
+        ptx::fence_mbar_init();
+    }
+    ptx::cluster_sync();  // every mailbox barrier is set up before any store lands
     ptx::grid_dependency_wait();
-    if (n > 0) {
-        if (!(p.mode & kModeStatic)) load_unit(cur, rb0 + lrb, ku);
-        // the unit's four scales of rows gid and gid + 8 (rows 16-byte aligned)
-        auto load_sc = [&](int rb_, int ku_, uint2& a, uint2& b) {
-            const uint16_t* r0 = p.s + (int64_t)(rb_ * kRows + gid) * p.gpr + ku_ * 4;
-            a = ld_l2_v2(r0);
-            b = ld_l2_v2(r0 + 8 * p.gpr);
-        };
-        // this lane's two 16-byte chunks (lane, lane + 32) of a unit's x
-        auto load_x = [&](int ku_, uint4& a, uint4& b) {
-            const uint16_t* xp = p.x + ku_ * kUnitK;
-            a = ld_l2_v4_nv(xp + lane * 8);
-            b = ld_l2_v4_nv(xp + (lane + 32) * 8);
-        };
-        uint8_t* xw = xr + warp * 2048;
-        auto store_x = [&](uint8_t* slot, uint4 a, uint4 b) {
-            const int j0 = lane, j1 = lane + 32;
-            *reinterpret_cast<uint4*>(slot + (j0 >> 4) * 256 + xs_pos(j0 & 15, 128) * 16) = permute_x8(a);
-            *reinterpret_cast<uint4*>(slot + (j1 >> 4) * 256 + xs_pos(j1 & 15, 128) * 16) = permute_x8(b);
-        };
-        uint2 sa, sb;
-        load_sc(rb0 + lrb, ku, sa, sb);
-        {
-            uint4 a, b;
-            load_x(ku, a, b);
-            store_x(xw, a, b);
-            __syncwarp();
+    if (!(p.mode & kModeStatic)) load_unit(cur, rb0 + lrb, ku);
+    // the unit's four scales of rows gid and gid + 8 (rows 16-byte aligned)
+    auto load_sc = [&](int rb_, int ku_, uint2& a, uint2& b) {
+        const uint16_t* r0 = p.s + (int64_t)(rb_ * kRows + gid) * p.gpr + ku_ * 4;
+        a = ld_l2_v2(r0);
+        b = ld_l2_v2(r0 + 8 * p.gpr);
+    };
+    // this lane's two 16-byte chunks (lane, lane + 32) of a unit's x
+    auto load_x = [&](int ku_, uint4& a, uint4& b) {
+        const uint16_t* xp = p.x + ku_ * kUnitK;
+        a = ld_l2_v4_nv(xp + lane * 8);
+        b = ld_l2_v4_nv(xp + (lane + 32) * 8);
+    };
+    uint8_t* xw = xr + warp * 2048;
+    auto store_x = [&](uint8_t* slot, uint4 a, uint4 b) {
+        const int j0 = lane, j1 = lane + 32;
+        *reinterpret_cast<uint4*>(slot + (j0 >> 4) * 256 + xs_pos(j0 & 15, 128) * 16) = permute_x8(a);
+        *reinterpret_cast<uint4*>(slot + (j1 >> 4) * 256 + xs_pos(j1 & 15, 128) * 16) = permute_x8(b);
+    };
+    uint2 sa, sb;
+    load_sc(rb0 + lrb, ku, sa, sb);
+    {
+        uint4 a, b;
+        load_x(ku, a, b);
+        store_x(xw, a, b);
+        __syncwarp();
+    }
+    const bool has = gid == 0;  // the token's lanes; the others read zero x
+    int seg_ku0 = ku;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int r = 0; r < n; ++r) {
+        int nlrb = lrb, nku = ku + 1;
+        if (nku == KU) {
+            nku = 0;
+            ++nlrb;
         }
-        const bool has = gid == 0;  // the token's lanes; the others read zero x
-        const int first_lrb = lrb;
-        int seg_ku0 = ku;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int r = 0; r < n; ++r) {
-            int nlrb = lrb, nku = ku + 1;
-            if (nku == KU) {
-                nku = 0;
-                ++nlrb;
-            }
-            uint2 na = sa, nb = sb;
-            uint4 xa, xb;
-            if (r + 1 < n) {
-                load_unit(nxt, rb0 + nlrb, nku);
-                load_sc(rb0 + nlrb, nku, na, nb);
-                load_x(nku, xa, xb);
-            }
-            UnitScales<128> sc;
-            sc.lo[0] = sa.x;
-            sc.lo[1] = sa.y;
-            sc.hi[0] = sb.x;
-            sc.hi[1] = sb.y;
-            compute_pieces(cur, sc, (has ? xw + (r & 1) * 1024 : zero) + t4 * 16, acc);
-            if (r + 1 < n) {
-                store_x(xw + ((r + 1) & 1) * 1024, xa, xb);
-                __syncwarp();  // every lane's chunks before any lane reads the slot
-            }
-            if (r == n - 1) ptx::launch_dependents();
-            const bool seg_end = (ku == KU - 1) || (r == n - 1);
-            if (seg_end) {
-                const int rb = rb0 + lrb;
-                if (seg_ku0 == 0 && ku == KU - 1) {
-                    store_y_cluster(p, rb, acc, gid, t4);  // the whole row-block in this warp
-                } else {
-                    const int sl = lrb == first_lrb ? 0 : 1;
-                    float* mine = part + (warp * 2 + sl) * kRows;
+        uint2 na = sa, nb = sb;
+        uint4 xa, xb;
+        if (r + 1 < n) {
+            load_unit(nxt, rb0 + nlrb, nku);
+            load_sc(rb0 + nlrb, nku, na, nb);
+            load_x(nku, xa, xb);
+        }
+        UnitScales<128> sc;
+        sc.lo[0] = sa.x;
+        sc.lo[1] = sa.y;
+        sc.hi[0] = sb.x;
+        sc.hi[1] = sb.y;
+        compute_pieces(cur, sc, (has ? xw + (r & 1) * 1024 : zero) + t4 * 16, acc);
+        if (r + 1 < n) {
+            store_x(xw + ((r + 1) & 1) * 1024, xa, xb);
+            __syncwarp();  // every lane's chunks before any lane reads the slot
+        }
+        if (r == n - 1) ptx::launch_dependents();
+        const bool seg_end = (ku == KU - 1) || (r == n - 1);
+        if (seg_end) {
+            const int rb = rb0 + lrb;
+            if (seg_ku0 == 0 && ku == KU - 1) {
+                store_y_cluster(p, rb, acc, gid, t4);  // the whole row-block in this warp
+            } else {
+                const bool first = lrb == lrb_first;
+                const int ga = first ? fa : la, gb = first ? fb : lb;
+                if (g != ga) {
+                    // into slot g - ga - 1 of ga's mailbox; ga's barrier counts the bytes
                     if (t4 == 0) {
-                        mine[gid] = acc[0];
-                        mine[gid + 8] = acc[2];
+                        const uint32_t rk = (uint32_t)(ga / kCWarps);
+                        const uint32_t dst = ptx::cluster_map(
+                            ptx::smem_u32(mail + ((ga % kCWarps) * kMail + (g - ga - 1)) * kRows + gid), rk);
+                        const uint32_t rbar = ptx::cluster_map(ptx::smem_u32(&bar[ga % kCWarps]), rk);
+                        ptx::st_async_cluster_f32(dst, acc[0], rbar);
+                        ptx::st_async_cluster_f32(dst + 32, acc[2], rbar);
                     }
-                    __syncwarp();  // the lanes' partials before lane 0's release
-                    const int ga = warp_of(lrb * KU), gb = warp_of(lrb * KU + KU - 1);
-                    int old = 0;
-                    if (lane == 0)
-                        old = ptx::atom_add_acq_rel_cluster(
-                            ptx::cluster_map(ptx::smem_u32(counter + ga % kCWarps), (uint32_t)(ga / kCWarps)), 1);
-                    old = __shfl_sync(0xffffffffu, old, 0);
-                    if (old == gb - ga) {  // the last contributor: sum them all in warp order
-                        __syncwarp();      // every lane's loads after lane 0's acquire
-                        const bool ga_first = (int)((int64_t)Tc * ga / GW) >= lrb * KU;
-                        float sum0 = 0.f, sum1 = 0.f;
-                        constexpr int kBatch = 8;
-                        for (int v0 = ga; v0 <= gb; v0 += kBatch) {
-                            float pa[kBatch], pb[kBatch];
-#pragma unroll
-                            for (int b = 0; b < kBatch; ++b) {
-                                const int v = v0 + b;
-                                const int slv = (v == ga && !ga_first) ? 1 : 0;
-                                pa[b] = pb[b] = 0.f;
-                                if (v <= gb && t4 == 0) {
-                                    const uint32_t ra = ptx::cluster_map(
-                                        ptx::smem_u32(part + ((v % kCWarps) * 2 + slv) * kRows + gid),
-                                        (uint32_t)(v / kCWarps));
-                                    pa[b] = ptx::ld_cluster_f32(ra);
-                                    pb[b] = ptx::ld_cluster_f32(ra + 32);
-                                }
+                } else {
+                    // this warp finishes the row-block: the others' sums, then all in warp order
+                    volatile int never = 0;
+                    const bool ok = ptx::mbar_wait(&bar[warp], 0, &never, kWaitLimitNs);
+                    if (ok) {
+                        float sum0 = 0.f + acc[0], sum1 = 0.f + acc[2];
+                        if (t4 == 0) {
+                            const float* box = mail + warp * kMail * kRows + gid;
+                            for (int v = 1; v <= gb - ga; ++v) {
+                                sum0 += box[(v - 1) * kRows];
+                                sum1 += box[(v - 1) * kRows + 8];
                             }
-#pragma unroll
-                            for (int b = 0; b < kBatch; ++b)
-                                if (v0 + b <= gb) {
-                                    sum0 += pa[b];
-                                    sum1 += pb[b];
-                                }
                         }
                         const float sv[4] = {sum0, 0.f, sum1, 0.f};
                         store_y_cluster(p, rb, sv, gid, t4);
+                    } else if (lane == 0) {
+                        raise_device_error(p.err, W4A16_ERR_TIMEOUT);
                     }
                 }
-                acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
             }
-            lrb = nlrb;
-            ku = nku;
-            if (seg_end) seg_ku0 = ku;
-            cur = nxt;
-            sa = na;
-            sb = nb;
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+            seg_ku0 = nku;
         }
-    } else {
-        ptx::launch_dependents();
+        lrb = nlrb;
+        ku = nku;
+        cur = nxt;
+        sa = na;
+        sb = nb;
     }
-    ptx::cluster_sync();  // no block leaves while another may still read its partials
+    ptx::cluster_sync();  // no block leaves while a store into its mailbox may be on the way
 }
 
-constexpr size_t kDecodeSmem = 1024 + kCWarps * 2048 + kCWarps * 2 * kRows * 4 + kCWarps * 4;
+constexpr size_t kDecodeSmem = 1024 + kCWarps * 2048 + kCWarps * kMail * kRows * 4 + kCWarps * 8;
 
 int64_t max_warps(const DeviceInfo& dev) { return (int64_t)dev.sms * kConsumers; }
 
@@ -1499,9 +1505,12 @@ w4a16_status cluster_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     a.gpr = (int)(K / group);
     a.svec = a.gpr % 8 == 0;
     a.mode = static_weights ? kModeStatic : 0;
+    a.err = dev.error_word;
     const bool exact = N % kRows == 0 && K % kUnitK == 0;  // then gpr % 4 == 0: a unit's scales are one 8-byte load
-    // the decode kernel wants every warp of every cluster busy
-    const bool decode = exact && M == 1 && (RB / nc) * KU >= (int64_t)c * kCWarps;
+    // the decode kernel wants every warp of every cluster busy, and no
+    // row-block split over more than kMail + 1 of them
+    const int64_t slice = (RB / nc) * KU / (c * kCWarps);  // the fewest units a warp gets
+    const bool decode = exact && M == 1 && slice >= 1 && (KU - 1 + slice - 1) / slice <= kMail;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nc * c));
     cfg.blockDim = dim3(kCThreads);

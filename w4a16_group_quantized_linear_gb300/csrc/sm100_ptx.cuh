@@ -250,6 +250,15 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
     return v;
 }
+// One-way 4-byte store into the shared memory of a block of the cluster;
+// when it lands it completes 4 bytes of the transaction count of the mbarrier
+// at remote_bar (in the same block). Nothing here waits for it.
+__device__ __forceinline__ void st_async_cluster_f32(uint32_t caddr, float v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(caddr),
+                 "r"(__float_as_uint(v)), "r"(remote_bar)
+                 : "memory");
+}
+
 // Every thread of every block of the cluster arrives; shared-memory writes
 // before it are visible to the whole cluster after it.
 __device__ __forceinline__ void cluster_sync() {
