@@ -100,8 +100,11 @@ W4A16_API w4a16_status w4a16_unpack(const uint8_t* qweight, int64_t N, int64_t K
  * page-locked host memory (cudaHostAlloc / cudaHostRegister) when K > 0: with
  * unified addressing the kernels store the result into it directly, so a
  * caller that wants the result on the host needs no separate copy.
- * Small M (decode, up to 16 rows) runs a split-K GEMV whose cross-block
- * partial sums live in `workspace`; larger M runs the tensor-core GEMM.
+ * Small M (decode, up to 16 rows) runs a split-K GEMV; larger M runs the
+ * tensor-core GEMM. For group 128 and M <= 8 the GEMV sums its split
+ * row-blocks inside thread-block clusters (distributed shared memory) and
+ * leaves `workspace` untouched; for the other groups and M its cross-block
+ * partial sums live in `workspace`.
  * workspace: device buffer of at least w4a16_workspace_bytes(M, N, K, group, 1)
  * bytes, zero-filled once before its first use (w4a16_workspace_init); every
  * call leaves it ready for the next (the counters it keeps there are back at
@@ -184,9 +187,9 @@ W4A16_API w4a16_status w4a16_linear_gated(const uint16_t* x, const uint8_t* qwei
  * scales) were written by work that completed before this call was enqueued
  * (packed or copied in, then synchronized), and that nothing still pending
  * on `stream` writes them: the usual case for the weights of a decode loop.
- * The decode GEMV (M <= 16) may then stream them into shared memory while
- * the kernel before it on the stream is still running, and waits for that
- * kernel only before it reads x. Without the flag the GEMV reads nothing
+ * The decode GEMV (M <= 16) may then start reading them while the kernel
+ * before it on the stream is still running, and waits for that kernel only
+ * before it reads x. Without the flag the GEMV reads nothing
  * before the previous kernel on the stream has completed. The flag changes
  * no result bit; if the promise is broken the results are undefined. The
  * tensor-core path (M > 16) ignores it.
