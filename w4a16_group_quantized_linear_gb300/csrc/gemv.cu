@@ -1248,7 +1248,8 @@ __global__ void __launch_bounds__(kCThreads, 1) gemv_decode_kernel(const Cluster
                 const int ga = first ? fa : la, gb = first ? fb : lb;
                 if (g != ga) {
                     // into slot g - ga - 1 of ga's mailbox; ga's barrier counts the bytes
-                    if (t4 == 0) {
+                    // (a test build can hold the sums back to make ga's wait run out)
+                    if (t4 == 0 && may_issue(0)) {
                         const uint32_t rk = (uint32_t)(ga / kCWarps);
                         const uint32_t dst = ptx::cluster_map(
                             ptx::smem_u32(mail + ((ga % kCWarps) * kMail + (g - ga - 1)) * kRows + gid), rk);
@@ -1259,7 +1260,7 @@ __global__ void __launch_bounds__(kCThreads, 1) gemv_decode_kernel(const Cluster
                 } else {
                     // this warp finishes the row-block: the others' sums, then all in warp order
                     volatile int never = 0;
-                    const bool ok = ptx::mbar_wait(&bar[warp], 0, &never, kWaitLimitNs);
+                    const bool ok = ptx::mbar_wait(&bar[warp], 0, &never, wait_limit());
                     if (ok) {
                         float sum0 = 0.f + acc[0], sum1 = 0.f + acc[2];
                         if (t4 == 0) {
