@@ -66,6 +66,21 @@ def test_row_blocks_split_across_many_warps(w4, cuda_device, M, N, K):
     assert np.array_equal(y.view(np.uint16), _run(w4, cuda_device, x, qw, s, 128).view(np.uint16))
 
 
+@pytest.mark.parametrize("M", [2, 5, 8])
+def test_decode_kernel_several_tokens(w4, cuda_device, M):
+    """Group 128, aligned N and K, 2 to 8 tokens: the written-out decode kernel
+    with x staged once per block and each contributor's 16 x M sums sent to
+    the row-block's finisher."""
+    r = workloads.rng(700 + M)
+    N, K = 8192, 4096
+    qw, s = workloads.raw_packed(r, N, K, 128)
+    x = workloads.activations(r, M, K)
+    y = _run(w4, cuda_device, x, qw, s, 128)
+    y_ref, a = oracle.linear(x, qw, s, 128, threads=8)
+    assert_within_bound(y, y_ref, a, f"M={M}")
+    assert np.array_equal(y.view(np.uint16), _run(w4, cuda_device, x, qw, s, 128).view(np.uint16))
+
+
 @pytest.mark.parametrize("N,K,g", [(1, 32, 32), (7, 96, 32), (17, 192, 64), (100, 640, 128), (1000, 2080, 32),
                                    (4099, 384, 128), (16, 128, 128), (31, 8192, 64)])
 def test_ragged_shapes(w4, cuda_device, N, K, g):

@@ -1291,6 +1291,196 @@ __global__ void __launch_bounds__(kCThreads, 1) gemv_decode_kernel(const Cluster
 
 constexpr size_t kDecodeSmem = 1024 + kCWarps * 2048 + kCWarps * kMail * kRows * 4 + kCWarps * 8;
 
+// The decode kernel for 2 to 8 tokens (MT = 8): the same partition and
+// mailbox sum, x staged once per block (a unit's x for 8 tokens does not fit
+// the registers of a warp that also holds two units of weights), each
+// contributor sending its 16 x M sums. (A single kernel for both token counts
+// measured 0.1 to 0.25 us slower at M = 1, so the one-token kernel above keeps
+// its own code.)
+template <int MT>
+struct DLayout {
+    static constexpr int kMail = MT == 1 ? 8 : 4;   // contributors besides the finisher, per row-block
+    static constexpr int kPart = kRows * MT;         // floats of one contributor's sums
+    static constexpr int kXr = MT == 1 ? kCWarps * 2048 : 0;  // per-warp x rings (MT = 1)
+    static constexpr int kMailOff = 1024 + kXr;
+    static constexpr int kBarOff = kMailOff + kCWarps * kMail * kPart * 4;
+    static constexpr int kFixed = (kBarOff + kCWarps * 8 + 127) & ~127;  // then the block's x (MT = 8)
+};
+
+template <int C>
+__global__ void __launch_bounds__(kCThreads, 1) gemv_decode_tokens_kernel(const ClusterArgs p) {
+    constexpr int MT = 8;
+    using L = DLayout<MT>;
+    constexpr int GW = C * kCWarps;  // the cluster's warps, all taking part
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t* zero = smem_raw;                                          // 1 KB of zero x
+    uint8_t* xr = smem_raw + 1024;                                     // MT = 1: [warp][2 slots][1 KB]
+    float* mail = reinterpret_cast<float*>(smem_raw + L::kMailOff);   // [warp][kMail][kPart]
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw + L::kBarOff);  // [warp]
+    uint8_t* xs = smem_raw + L::kFixed;                                // MT = 8: the block's x
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
+    const int rank = (int)ptx::cluster_rank();
+    const int cid = (int)blockIdx.x / C, NC = (int)gridDim.x / C;
+    const int KU = p.KU;
+    const int rb0 = (int)((int64_t)p.RB * cid / NC), rb1 = (int)((int64_t)p.RB * (cid + 1) / NC);
+    const int Tc = (rb1 - rb0) * KU;
+    const int g = rank * kCWarps + warp;
+    const int q0 = (int)((int64_t)Tc * g / GW), n = (int)((int64_t)Tc * (g + 1) / GW) - q0;
+    auto warp_of = [&](int q) { return (int)(((int64_t)(q + 1) * GW + Tc - 1) / Tc - 1); };
+    int lrb = q0 / KU, ku = q0 % KU;
+    const int hk = p.K / 2;
+    const int M = MT == 1 ? 1 : p.M;
+    const uint8_t* lane_base = p.qw + (int64_t)gid * hk + t4 * 16;  // row gid of row-block 0, this lane's bytes
+    auto load_unit = [&](Pieces& u, int rb_, int ku_) {
+        const uint8_t* a = lane_base + (int64_t)rb_ * kRows * hk + ku_ * (kUnitK / 2);
+#pragma unroll
+        for (int step = 0; step < kUnitSteps; ++step) {
+            u.w[2 * step] = ld_stream_v4(a + step * 64);
+            u.w[2 * step + 1] = ld_stream_v4(a + 8 * hk + step * 64);
+        }
+    };
+    Pieces cur, nxt;
+    if ((p.mode & kModeStatic) && n > 0) load_unit(cur, rb0 + lrb, ku);
+    // this warp's first and last row-blocks: its only segments that may be split
+    const int lrb_first = lrb, lrb_last = (q0 + n - 1) / KU;
+    const int fa = warp_of(lrb_first * KU), fb = warp_of(lrb_first * KU + KU - 1);  // contributors, first
+    const int la = warp_of(lrb_last * KU), lb = warp_of(lrb_last * KU + KU - 1);    // contributors, last
+    if (threadIdx.x < 64) reinterpret_cast<uint4*>(zero)[threadIdx.x] = make_uint4(0, 0, 0, 0);
+    if (lane == 0) {
+        ptx::mbar_init(&bar[warp], 1);
+        // the finisher of its last row-block expects the others' sums: 16 rows x M tokens each
+        if (la == g && lb > la) ptx::mbar_arrive_expect_tx(&bar[warp], (uint32_t)(lb - la) * kRows * M * 4);
+        ptx::fence_mbar_init();
+    }
+    ptx::cluster_sync();  // every mailbox barrier is set up before any store lands
+    ptx::grid_dependency_wait();
+    if (!(p.mode & kModeStatic)) load_unit(cur, rb0 + lrb, ku);
+    // the unit's four scales of rows gid and gid + 8 (rows 16-byte aligned)
+    auto load_sc = [&](int rb_, int ku_, uint2& a, uint2& b) {
+        const uint16_t* r0 = p.s + (int64_t)(rb_ * kRows + gid) * p.gpr + ku_ * 4;
+        a = ld_l2_v2(r0);
+        b = ld_l2_v2(r0 + 8 * p.gpr);
+    };
+    // MT = 1: this lane's two 16-byte chunks (lane, lane + 32) of a unit's x
+    auto load_x = [&](int ku_, uint4& a, uint4& b) {
+        const uint16_t* xp = p.x + ku_ * kUnitK;
+        a = ld_l2_v4_nv(xp + lane * 8);
+        b = ld_l2_v4_nv(xp + (lane + 32) * 8);
+    };
+    uint8_t* xw = xr + warp * 2048;
+    auto store_x = [&](uint8_t* slot, uint4 a, uint4 b) {
+        const int j0 = lane, j1 = lane + 32;
+        *reinterpret_cast<uint4*>(slot + (j0 >> 4) * 256 + xs_pos(j0 & 15, 128) * 16) = permute_x8(a);
+        *reinterpret_cast<uint4*>(slot + (j1 >> 4) * 256 + xs_pos(j1 & 15, 128) * 16) = permute_x8(b);
+    };
+    const int xstride = KU * (kUnitSteps * kStepK * 2) + 64;  // MT = 8: bytes per token of the block's x
+    uint2 sa, sb;
+    load_sc(rb0 + lrb, ku, sa, sb);
+    if constexpr (MT == 1) {
+        uint4 a, b;
+        load_x(ku, a, b);
+        store_x(xw, a, b);
+        __syncwarp();
+    } else {  // the whole x, once per block, in fragment order
+        const int per_tok = KU * kUnitSteps * 16;
+        for (int c = threadIdx.x; c < M * per_tok; c += kCThreads) {
+            const int m = c / per_tok, cc = c % per_tok;
+            const uint4 v = ld_l2_v4(p.x + (int64_t)m * p.K + cc * 8);
+            *reinterpret_cast<uint4*>(xs + m * xstride + (cc >> 4) * (kStepK * 2) + xs_pos(cc & 15, 128) * 16) =
+                permute_x8(v);
+        }
+        __syncthreads();
+    }
+    const bool has = gid < M;  // the tokens' lanes; the others read zero x
+    int seg_ku0 = ku;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int r = 0; r < n; ++r) {
+        int nlrb = lrb, nku = ku + 1;
+        if (nku == KU) {
+            nku = 0;
+            ++nlrb;
+        }
+        uint2 na = sa, nb = sb;
+        uint4 xa, xb;
+        if (r + 1 < n) {
+            load_unit(nxt, rb0 + nlrb, nku);
+            load_sc(rb0 + nlrb, nku, na, nb);
+            if constexpr (MT == 1) load_x(nku, xa, xb);
+        }
+        UnitScales<128> sc;
+        sc.lo[0] = sa.x;
+        sc.lo[1] = sa.y;
+        sc.hi[0] = sb.x;
+        sc.hi[1] = sb.y;
+        const uint8_t* xl;
+        if constexpr (MT == 1) xl = (has ? xw + (r & 1) * 1024 : zero) + t4 * 16;
+        else xl = (has ? xs + gid * xstride + ku * (kUnitSteps * kStepK * 2) : zero) + t4 * 16;
+        compute_pieces(cur, sc, xl, acc);
+        if constexpr (MT == 1) {
+            if (r + 1 < n) {
+                store_x(xw + ((r + 1) & 1) * 1024, xa, xb);
+                __syncwarp();  // every lane's chunks before any lane reads the slot
+            }
+        }
+        if (r == n - 1) ptx::launch_dependents();
+        const bool seg_end = (ku == KU - 1) || (r == n - 1);
+        if (seg_end) {
+            const int rb = rb0 + lrb;
+            if (seg_ku0 == 0 && ku == KU - 1) {
+                store_y_cluster(p, rb, acc, gid, t4);  // the whole row-block in this warp
+            } else {
+                const bool first = lrb == lrb_first;
+                const int ga = first ? fa : la, gb = first ? fb : lb;
+                if (g != ga) {
+                    // into slot g - ga - 1 of ga's mailbox ([token][row]); ga's barrier
+                    // counts the bytes (a test build can hold the sums back to make
+                    // ga's wait run out)
+                    if (may_issue(0)) {
+                        const uint32_t rk = (uint32_t)(ga / kCWarps);
+                        const uint32_t dst = ptx::cluster_map(
+                            ptx::smem_u32(mail + ((ga % kCWarps) * L::kMail + (g - ga - 1)) * L::kPart), rk);
+                        const uint32_t rbar = ptx::cluster_map(ptx::smem_u32(&bar[ga % kCWarps]), rk);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int m = 2 * t4 + (i & 1);
+                            if (m < M)
+                                ptx::st_async_cluster_f32(dst + 4u * (m * kRows + gid + 8 * (i >> 1)), acc[i], rbar);
+                        }
+                    }
+                } else {
+                    // this warp finishes the row-block: the others' sums, then all in warp order
+                    volatile int never = 0;
+                    const bool ok = ptx::mbar_wait(&bar[warp], 0, &never, wait_limit());
+                    if (ok) {
+                        float sum[4];
+                        const float* box = mail + warp * L::kMail * L::kPart;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int m = 2 * t4 + (i & 1);
+                            sum[i] = 0.f + acc[i];
+                            if (m < M)
+                                for (int v = 1; v <= gb - ga; ++v)
+                                    sum[i] += box[(v - 1) * L::kPart + m * kRows + gid + 8 * (i >> 1)];
+                        }
+                        store_y_cluster(p, rb, sum, gid, t4);
+                    } else if (lane == 0) {
+                        raise_device_error(p.err, W4A16_ERR_TIMEOUT);
+                    }
+                }
+            }
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+            seg_ku0 = nku;
+        }
+        lrb = nlrb;
+        ku = nku;
+        cur = nxt;
+        sa = na;
+        sb = nb;
+    }
+    ptx::cluster_sync();  // no block leaves while a store into its mailbox may be on the way
+}
+
+
 int64_t max_warps(const DeviceInfo& dev) { return (int64_t)dev.sms * kConsumers; }
 
 size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
@@ -1423,6 +1613,12 @@ const ClusterFit& cluster_fit(const DeviceInfo& dev, cudaError_t* err) {
         cudaError_t e = cluster_attrs<1>(dev);
         if (e == cudaSuccess) e = cluster_attrs<2>(dev);
         if (e == cudaSuccess) e = cluster_attrs<8>(dev);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemv_decode_tokens_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)dev.smem_optin);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemv_decode_tokens_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)dev.smem_optin);
         if (e != cudaSuccess) return e;
         for (int i = 0; i < 2; ++i) {
             const int c = 2 << i;
@@ -1508,14 +1704,18 @@ w4a16_status cluster_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     a.mode = static_weights ? kModeStatic : 0;
     a.err = dev.error_word;
     const bool exact = N % kRows == 0 && K % kUnitK == 0;  // then gpr % 4 == 0: a unit's scales are one 8-byte load
-    // the decode kernel wants every warp of every cluster busy, and no
-    // row-block split over more than kMail + 1 of them
+    // the decode kernel wants every warp of every cluster busy, no row-block
+    // split over more than kMail + 1 of them, and (M > 1) the block's x in
+    // shared memory
     const int64_t slice = (RB / nc) * KU / (c * kCWarps);  // the fewest units a warp gets
-    const bool decode = exact && M == 1 && slice >= 1 && (KU - 1 + slice - 1) / slice <= kMail;
+    const int mail = M == 1 ? kMail : DLayout<8>::kMail;
+    const size_t dsmem = M == 1 ? kDecodeSmem
+                                : DLayout<8>::kFixed + (size_t)M * (size_t)(KU * kUnitSteps * kStepK * 2 + 64);
+    const bool decode = exact && slice >= 1 && (KU - 1 + slice - 1) / slice <= mail && dsmem <= dev.smem_optin;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nc * c));
     cfg.blockDim = dim3(kCThreads);
-    cfg.dynamicSmemBytes = decode ? kDecodeSmem : smem;
+    cfg.dynamicSmemBytes = decode ? dsmem : smem;
     cfg.stream = st;
     cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1527,8 +1727,12 @@ w4a16_status cluster_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     cfg.attrs = at;
     cfg.numAttrs = 2;
     *used = true;
-    if (decode)
-        e = c == 2 ? cudaLaunchKernelEx(&cfg, gemv_decode_kernel<2>, a) : cudaLaunchKernelEx(&cfg, gemv_decode_kernel<4>, a);
+    if (decode && M == 1)
+        e = c == 2 ? cudaLaunchKernelEx(&cfg, gemv_decode_kernel<2>, a)
+                   : cudaLaunchKernelEx(&cfg, gemv_decode_kernel<4>, a);
+    else if (decode)
+        e = c == 2 ? cudaLaunchKernelEx(&cfg, gemv_decode_tokens_kernel<2>, a)
+                   : cudaLaunchKernelEx(&cfg, gemv_decode_tokens_kernel<4>, a);
     else
         e = mx == 1 ? cluster_launch<1>(cfg, a, exact, c) : mx == 2 ? cluster_launch<2>(cfg, a, exact, c)
                                                                     : cluster_launch<8>(cfg, a, exact, c);
