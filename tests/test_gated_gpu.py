@@ -95,6 +95,25 @@ def test_gated_decode_full_size(w4, cuda_device, M):
     _check(y, x, qg, sg, qu, su, g, f"gated decode M={M}", threads=8)
 
 
+@pytest.mark.parametrize("N,K", [(8192, 4096), (4096, 16384)])
+def test_gated_cluster_decode(w4, cuda_device, N, K):
+    """M = 1, group 128, aligned N and K: the cluster kernel for the pair (units
+    of 16 Wg rows and the same 16 Wu rows, both sums sent to a row-block's
+    finisher). Checked against the oracle, rerun bit for bit, and with
+    W4A16_STATIC_WEIGHTS."""
+    r = workloads.rng(N + K + 5)
+    qg, sg = _scaled(r, N, K, 128, 8.0)
+    qu, su = workloads.raw_packed(r, N, K, 128)
+    x = workloads.activations(r, 1, K)
+    args = [to_dev(x, cuda_device), to_dev(qg, cuda_device), to_dev(sg.view(np.float16), cuda_device),
+            to_dev(qu, cuda_device), to_dev(su.view(np.float16), cuda_device)]
+    y0 = w4.linear_gated(*args, 128).cpu().numpy()
+    _check(y0, x, qg, sg, qu, su, 128, f"gated cluster N={N} K={K}", threads=8)
+    assert np.array_equal(y0.view(np.uint16), w4.linear_gated(*args, 128).cpu().numpy().view(np.uint16))
+    y1 = w4.linear_gated(*args, 128, static_weights=True).cpu().numpy()
+    assert np.array_equal(y0.view(np.uint16), y1.view(np.uint16))
+
+
 def test_gated_static_weights_same_bits(w4, cuda_device):
     """W4A16_STATIC_WEIGHTS changes no result bit of the fused pair."""
     r = workloads.rng(61)

@@ -912,6 +912,40 @@ __device__ __forceinline__ void compute_pieces(const Pieces& u, const UnitScales
     }
 }
 
+// Two 128-k steps (one group each) from pieces base .. base + 3 ([step][row
+// half]); sl / sh hold the two groups' scales of rows gid and gid + 8.
+__device__ __forceinline__ void compute_half_pieces(const Pieces& u, int base, uint32_t sl, uint32_t sh,
+                                                    const uint8_t* xl, float (&acc)[4]) {
+#pragma unroll
+    for (int step = 0; step < kUnitSteps / 2; ++step) {
+        const uint4 A = u.w[base + 2 * step], B = u.w[base + 2 * step + 1];
+        const uint32_t wa[4] = {A.x, A.y, A.z, A.w};
+        const uint32_t wb[4] = {B.x, B.y, B.z, B.w};
+        float c[4];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+            const uint4 xv = lds_v4(xl + step * (kStepK * 2) + wi * 64);
+            uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
+            nibbles_to_half2(wa[wi], a04, a15, a26, a37);
+            nibbles_to_half2(wb[wi], b04, b15, b26, b37);
+            if (wi == 0) mma_16816_zero(c, a04, b04, a15, b15, xv.x, xv.y);
+            else mma_16816(c, a04, b04, a15, b15, xv.x, xv.y);
+            mma_16816(c, a26, b26, a37, b37, xv.z, xv.w);
+        }
+        const float s0 = half_bits(sl, step), s1 = half_bits(sh, step);
+        acc[0] = fmaf(s0, c[0], acc[0]);
+        acc[1] = fmaf(s0, c[1], acc[1]);
+        acc[2] = fmaf(s1, c[2], acc[2]);
+        acc[3] = fmaf(s1, c[3], acc[3]);
+    }
+}
+
+__device__ __forceinline__ uint32_t ld_l2_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void store_y_cluster(const ClusterArgs& p, int rb, const float (&v)[4], int gid, int t4) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -1290,6 +1324,172 @@ __global__ void __launch_bounds__(kCThreads, 1) gemv_decode_kernel(const Cluster
 }
 
 constexpr size_t kDecodeSmem = 1024 + kCWarps * 2048 + kCWarps * kMail * kRows * 4 + kCWarps * 8;
+
+// The fused gate+up decode (M = 1, group 128, N % 16 == 0, K % 512 == 0) on
+// the same design. A unit here is a pair: 16 rows of Wg and the same 16 rows
+// of Wu over 256 k (2 + 2 KB, so a lane holds what it holds in the plain
+// kernel: 8 pieces of 16 bytes). A row-block is one 16-row block of the
+// output; its units run over K / 256. A warp keeps the gate and the up sums of
+// its segment apart; a split row-block's finisher gets both from every other
+// contributor (32 fp32 values by st.async), adds them in warp order and forms
+// y = silu(g) * u in fp32, rounded once to fp16 (rust-inference README, list
+// of accuracy fixes, item 5). g and u never leave the cluster.
+struct GatedClusterArgs {
+    ClusterArgs a;        // x, Wg, sg, y, M, N, K; KU counts 256-k units
+    const uint8_t* qw2;   // Wu
+    const uint16_t* s2;   // su
+};
+
+constexpr int kGMail = 8;                 // contributors besides the finisher, per row-block
+constexpr int kGPart = 2 * kRows;         // floats of one contributor's sums: 16 g, then 16 u
+constexpr int kGMailOff = 1024 + kCWarps * 1024;  // after zero x and the per-warp x rings (2 x 512 B)
+constexpr int kGBarOff = kGMailOff + kCWarps * kGMail * kGPart * 4;
+constexpr size_t kGatedDecodeSmem = kGBarOff + kCWarps * 8;
+
+__device__ __forceinline__ float silu_times(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+template <int C>
+__global__ void __launch_bounds__(kCThreads, 1) gemv_gated_decode_kernel(const GatedClusterArgs ga_) {
+    const ClusterArgs& p = ga_.a;
+    constexpr int GW = C * kCWarps;
+    constexpr int kHalf = kUnitSteps / 2;  // 128-k steps per matrix in a pair unit
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t* zero = smem_raw;                                            // 1 KB of zero x
+    uint8_t* xr = smem_raw + 1024;                                       // [warp][2 slots][512 B]
+    float* mail = reinterpret_cast<float*>(smem_raw + kGMailOff);       // [warp][kGMail][kGPart]
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw + kGBarOff);   // [warp]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
+    const int rank = (int)ptx::cluster_rank();
+    const int cid = (int)blockIdx.x / C, NC = (int)gridDim.x / C;
+    const int KU = p.KU;  // 256-k pair units per row-block
+    const int rb0 = (int)((int64_t)p.RB * cid / NC), rb1 = (int)((int64_t)p.RB * (cid + 1) / NC);
+    const int Tc = (rb1 - rb0) * KU;
+    const int g = rank * kCWarps + warp;
+    const int q0 = (int)((int64_t)Tc * g / GW), n = (int)((int64_t)Tc * (g + 1) / GW) - q0;
+    auto warp_of = [&](int q) { return (int)(((int64_t)(q + 1) * GW + Tc - 1) / Tc - 1); };
+    int lrb = q0 / KU, ku = q0 % KU;
+    const int hk = p.K / 2;
+    const int64_t lane_off = (int64_t)gid * hk + t4 * 16;  // row gid, this lane's bytes
+    // pieces [step][row half] of Wg (0..3), then of Wu (4..7)
+    auto load_unit = [&](Pieces& u, int rb_, int ku_) {
+        const int64_t o = lane_off + (int64_t)rb_ * kRows * hk + ku_ * (kUnitK / 4);
+#pragma unroll
+        for (int step = 0; step < kHalf; ++step) {
+            u.w[2 * step] = ld_stream_v4(p.qw + o + step * 64);
+            u.w[2 * step + 1] = ld_stream_v4(p.qw + o + 8 * hk + step * 64);
+            u.w[4 + 2 * step] = ld_stream_v4(ga_.qw2 + o + step * 64);
+            u.w[4 + 2 * step + 1] = ld_stream_v4(ga_.qw2 + o + 8 * hk + step * 64);
+        }
+    };
+    Pieces cur, nxt;
+    if ((p.mode & kModeStatic) && n > 0) load_unit(cur, rb0 + lrb, ku);
+    const int lrb_first = lrb, lrb_last = (q0 + n - 1) / KU;
+    const int fa = warp_of(lrb_first * KU), fb = warp_of(lrb_first * KU + KU - 1);
+    const int la = warp_of(lrb_last * KU), lb = warp_of(lrb_last * KU + KU - 1);
+    if (threadIdx.x < 64) reinterpret_cast<uint4*>(zero)[threadIdx.x] = make_uint4(0, 0, 0, 0);
+    if (lane == 0) {
+        ptx::mbar_init(&bar[warp], 1);
+        if (la == g && lb > la) ptx::mbar_arrive_expect_tx(&bar[warp], (uint32_t)(lb - la) * kGPart * 4);
+        ptx::fence_mbar_init();
+    }
+    ptx::cluster_sync();  // every mailbox barrier is set up before any store lands
+    ptx::grid_dependency_wait();
+    if (!(p.mode & kModeStatic)) load_unit(cur, rb0 + lrb, ku);
+    // a pair unit's scales: two groups of rows gid and gid + 8, of Wg and of Wu
+    auto load_sc = [&](int rb_, int ku_, uint32_t (&sv)[4]) {
+        const int64_t o = (int64_t)(rb_ * kRows + gid) * p.gpr + ku_ * 2;
+        sv[0] = ld_l2_u32(p.s + o);
+        sv[1] = ld_l2_u32(p.s + o + 8 * p.gpr);
+        sv[2] = ld_l2_u32(ga_.s2 + o);
+        sv[3] = ld_l2_u32(ga_.s2 + o + 8 * p.gpr);
+    };
+    // this lane's 16-byte chunk of a pair unit's x (256 k = 32 chunks)
+    auto load_x = [&](int ku_) { return ld_l2_v4_nv(p.x + ku_ * (kUnitK / 2) + lane * 8); };
+    uint8_t* xw = xr + warp * 1024;
+    auto store_x = [&](uint8_t* slot, uint4 a) {
+        *reinterpret_cast<uint4*>(slot + (lane >> 4) * 256 + xs_pos(lane & 15, 128) * 16) = permute_x8(a);
+    };
+    uint32_t sv[4];
+    load_sc(rb0 + lrb, ku, sv);
+    store_x(xw, load_x(ku));
+    __syncwarp();
+    const bool has = gid == 0;
+    int seg_ku0 = ku;
+    float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int r = 0; r < n; ++r) {
+        int nlrb = lrb, nku = ku + 1;
+        if (nku == KU) {
+            nku = 0;
+            ++nlrb;
+        }
+        uint32_t nsv[4] = {sv[0], sv[1], sv[2], sv[3]};
+        uint4 xa;
+        if (r + 1 < n) {
+            load_unit(nxt, rb0 + nlrb, nku);
+            load_sc(rb0 + nlrb, nku, nsv);
+            xa = load_x(nku);
+        }
+        const uint8_t* xl = (has ? xw + (r & 1) * 512 : zero) + t4 * 16;
+        compute_half_pieces(cur, 0, sv[0], sv[1], xl, accg);
+        compute_half_pieces(cur, 4, sv[2], sv[3], xl, accu);
+        if (r + 1 < n) {
+            store_x(xw + ((r + 1) & 1) * 512, xa);
+            __syncwarp();  // every lane's chunk before any lane reads the slot
+        }
+        if (r == n - 1) ptx::launch_dependents();
+        const bool seg_end = (ku == KU - 1) || (r == n - 1);
+        if (seg_end) {
+            const int rb = rb0 + lrb;
+            if (seg_ku0 == 0 && ku == KU - 1) {
+                const float yv[4] = {silu_times(accg[0], accu[0]), 0.f, silu_times(accg[2], accu[2]), 0.f};
+                store_y_cluster(p, rb, yv, gid, t4);  // the whole row-block in this warp
+            } else {
+                const bool first = lrb == lrb_first;
+                const int ga = first ? fa : la, gb = first ? fb : lb;
+                if (g != ga) {
+                    if (t4 == 0 && may_issue(0)) {
+                        const uint32_t rk = (uint32_t)(ga / kCWarps);
+                        const uint32_t dst = ptx::cluster_map(
+                            ptx::smem_u32(mail + ((ga % kCWarps) * kGMail + (g - ga - 1)) * kGPart + gid), rk);
+                        const uint32_t rbar = ptx::cluster_map(ptx::smem_u32(&bar[ga % kCWarps]), rk);
+                        ptx::st_async_cluster_f32(dst, accg[0], rbar);
+                        ptx::st_async_cluster_f32(dst + 32, accg[2], rbar);
+                        ptx::st_async_cluster_f32(dst + 64, accu[0], rbar);
+                        ptx::st_async_cluster_f32(dst + 96, accu[2], rbar);
+                    }
+                } else {
+                    volatile int never = 0;
+                    const bool ok = ptx::mbar_wait(&bar[warp], 0, &never, wait_limit());
+                    if (ok) {
+                        float g0 = 0.f + accg[0], g1 = 0.f + accg[2], u0 = 0.f + accu[0], u1 = 0.f + accu[2];
+                        if (t4 == 0) {
+                            const float* box = mail + warp * kGMail * kGPart + gid;
+                            for (int v = 1; v <= gb - ga; ++v) {
+                                g0 += box[(v - 1) * kGPart];
+                                g1 += box[(v - 1) * kGPart + 8];
+                                u0 += box[(v - 1) * kGPart + 16];
+                                u1 += box[(v - 1) * kGPart + 24];
+                            }
+                        }
+                        const float yv[4] = {silu_times(g0, u0), 0.f, silu_times(g1, u1), 0.f};
+                        store_y_cluster(p, rb, yv, gid, t4);
+                    } else if (lane == 0) {
+                        raise_device_error(p.err, W4A16_ERR_TIMEOUT);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) accg[i] = accu[i] = 0.f;
+            seg_ku0 = nku;
+        }
+        lrb = nlrb;
+        ku = nku;
+        cur = nxt;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sv[i] = nsv[i];
+    }
+    ptx::cluster_sync();  // no block leaves while a store into its mailbox may be on the way
+}
 
 // The decode kernel for 2 to 8 tokens (MT = 8): the same partition and
 // mailbox sum, x staged once per block (a unit's x for 8 tokens does not fit
@@ -1739,6 +1939,71 @@ w4a16_status cluster_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     return cuda_status(e, "gemv cluster: kernel launch");
 }
 
+// The fused gate+up decode on clusters when it applies (group 128, M = 1,
+// N % 16 == 0, K % 512 == 0, the pair units spread so that every warp has
+// one and no row-block has more than kGMail + 1 contributors); *used is false
+// when the caller must take the ring kernel instead.
+w4a16_status gated_cluster_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t* qw, const uint16_t* s,
+                               const uint8_t* qw2, const uint16_t* s2, uint16_t* y, int64_t M, int64_t N, int64_t K,
+                               int group, bool static_weights, cudaStream_t st, bool* used) {
+    *used = false;
+    if (group != 128 || M != 1 || N % kRows != 0 || K % kUnitK != 0) return W4A16_OK;
+    const int64_t KU = K / (kUnitK / 2), RB = N / kRows;  // 256-k pair units per row-block
+    if (RB * KU > 0x7fffffffLL) return W4A16_OK;
+    cudaError_t e = cudaSuccess;
+    const ClusterFit& fit = cluster_fit(dev, &e);
+    if (e != cudaSuccess) return cuda_status(e, "gemv cluster: cudaFuncSetAttribute");
+    int c = 0, nc = 0;
+    int64_t best = 0;
+    for (int i = 0; i < 2; ++i) {
+        const int ci = 2 << i, ni = fit.count[i];
+        if (ni <= 0) continue;
+        const int64_t slice = (RB / ni) * KU / (ci * kCWarps);
+        if (slice < 1 || (KU - 1 + slice - 1) / slice > kGMail) continue;
+        const int64_t per_warp = ((RB + ni - 1) / ni * KU + ci * kCWarps - 1) / (ci * kCWarps);
+        if (c == 0 || per_warp < best) {
+            c = ci;
+            nc = ni;
+            best = per_warp;
+        }
+    }
+    if (c == 0) return W4A16_OK;
+    GatedClusterArgs g;
+    g.a.x = x;
+    g.a.qw = qw;
+    g.a.s = s;
+    g.a.y = y;
+    g.a.M = 1;
+    g.a.N = (int)N;
+    g.a.K = (int)K;
+    g.a.KU = (int)KU;
+    g.a.RB = (int)RB;
+    g.a.gpr = (int)(K / group);
+    g.a.svec = 1;
+    g.a.mode = static_weights ? kModeStatic : 0;
+    g.a.err = dev.error_word;
+    g.qw2 = qw2;
+    g.s2 = s2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(nc * c));
+    cfg.blockDim = dim3(kCThreads);
+    cfg.dynamicSmemBytes = kGatedDecodeSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = (unsigned)c;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    *used = true;
+    e = c == 2 ? cudaLaunchKernelEx(&cfg, gemv_gated_decode_kernel<2>, g)
+               : cudaLaunchKernelEx(&cfg, gemv_gated_decode_kernel<4>, g);
+    return cuda_status(e, "gemv gated cluster: kernel launch");
+}
+
 bool encode_weights(CUtensorMap (&map)[4], int slot, const uint8_t* qw, const uint16_t* s, int64_t N, int64_t K,
                     int group, bool ts, bool* w3d) {
     const int64_t gpr = K / group;
@@ -1775,9 +2040,11 @@ w4a16_status gemv_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t* q
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return W4A16_ERR_WORKSPACE;
     if (((uintptr_t)workspace & 255) != 0) return W4A16_ERR_MISALIGNED;
     if (M > kMaxM || N > 0x7fffffffLL || K > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
-    if (!gated) {
+    {
         bool used = false;
-        const w4a16_status r = cluster_run(dev, x, qw, s, y, M, N, K, group, opt.static_weights, st, &used);
+        const w4a16_status r =
+            gated ? gated_cluster_run(dev, x, qw, s, qw2, s2, y, M, N, K, group, opt.static_weights, st, &used)
+                  : cluster_run(dev, x, qw, s, y, M, N, K, group, opt.static_weights, st, &used);
         if (used || r != W4A16_OK) return r;
     }
     if (!encode_fn()) return cuda_status(cudaErrorNotSupported, "gemv: cuTensorMapEncodeTiled entry point");
