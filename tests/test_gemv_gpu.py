@@ -66,11 +66,11 @@ def test_row_blocks_split_across_many_warps(w4, cuda_device, M, N, K):
     assert np.array_equal(y.view(np.uint16), _run(w4, cuda_device, x, qw, s, 128).view(np.uint16))
 
 
-@pytest.mark.parametrize("M", [2, 5, 8])
+@pytest.mark.parametrize("M", [2, 5, 8, 9, 12, 16])
 def test_decode_kernel_several_tokens(w4, cuda_device, M):
-    """Group 128, aligned N and K, 2 to 8 tokens: the written-out decode kernel
-    with x staged once per block and each contributor's 16 x M sums sent to
-    the row-block's finisher."""
+    """Group 128, aligned N and K, 2 to 16 tokens: the written-out decode kernel
+    with x staged once per block (one or two 8-token MMA tiles) and each
+    contributor's 16 x M sums sent to the row-block's finisher."""
     r = workloads.rng(700 + M)
     N, K = 8192, 4096
     qw, s = workloads.raw_packed(r, N, K, 128)

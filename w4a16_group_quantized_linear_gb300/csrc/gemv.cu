@@ -946,10 +946,11 @@ __device__ __forceinline__ uint32_t ld_l2_u32(const void* p) {
     return v;
 }
 
-__device__ __forceinline__ void store_y_cluster(const ClusterArgs& p, int rb, const float (&v)[4], int gid, int t4) {
+__device__ __forceinline__ void store_y_cluster(const ClusterArgs& p, int rb, const float (&v)[4], int gid, int t4,
+                                                int m0 = 0) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int m = 2 * t4 + (i & 1);
+        const int m = m0 + 2 * t4 + (i & 1);
         const int64_t n = (int64_t)rb * kRows + gid + 8 * (i >> 1);
         if (m < p.M && n < p.N) p.y[(int64_t)m * p.N + n] = __half_as_ushort(__float2half_rn(v[i]));
     }
@@ -1499,25 +1500,59 @@ __global__ void __launch_bounds__(kCThreads, 1) gemv_gated_decode_kernel(const G
 // its own code.)
 template <int MT>
 struct DLayout {
-    static constexpr int kMail = MT == 1 ? 8 : 4;   // contributors besides the finisher, per row-block
-    static constexpr int kPart = kRows * MT;         // floats of one contributor's sums
-    static constexpr int kXr = MT == 1 ? kCWarps * 2048 : 0;  // per-warp x rings (MT = 1)
-    static constexpr int kMailOff = 1024 + kXr;
+    static constexpr int kMail = 4;            // contributors besides the finisher, per row-block
+    static constexpr int kPart = kRows * MT;   // floats of one contributor's sums
+    static constexpr int kMailOff = 1024;
     static constexpr int kBarOff = kMailOff + kCWarps * kMail * kPart * 4;
-    static constexpr int kFixed = (kBarOff + kCWarps * 8 + 127) & ~127;  // then the block's x (MT = 8)
+    static constexpr int kFixed = (kBarOff + kCWarps * 8 + 127) & ~127;  // then the block's x
 };
 
-template <int C>
+// One unit from registers for NT tiles of 8 tokens: each weight word is turned
+// into fp16 once and feeds NT MMAs (x of tile t at xl[t]).
+template <int NT>
+__device__ __forceinline__ void compute_pieces_nt(const Pieces& u, const UnitScales<128>& sc,
+                                                  const uint8_t* const (&xl)[NT], float (&acc)[NT][4]) {
+#pragma unroll
+    for (int step = 0; step < kUnitSteps; ++step) {
+        const uint32_t wa[4] = {u.w[2 * step].x, u.w[2 * step].y, u.w[2 * step].z, u.w[2 * step].w};
+        const uint32_t wb[4] = {u.w[2 * step + 1].x, u.w[2 * step + 1].y, u.w[2 * step + 1].z,
+                                u.w[2 * step + 1].w};
+        float c[NT][4];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+            uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
+            nibbles_to_half2(wa[wi], a04, a15, a26, a37);
+            nibbles_to_half2(wb[wi], b04, b15, b26, b37);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const uint4 xv = lds_v4(xl[t] + step * (kStepK * 2) + wi * 64);
+                if (wi == 0) mma_16816_zero(c[t], a04, b04, a15, b15, xv.x, xv.y);
+                else mma_16816(c[t], a04, b04, a15, b15, xv.x, xv.y);
+                mma_16816(c[t], a26, b26, a37, b37, xv.z, xv.w);
+            }
+        }
+        const float s0 = half_bits(sc.lo[step >> 1], step & 1), s1 = half_bits(sc.hi[step >> 1], step & 1);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            acc[t][0] = fmaf(s0, c[t][0], acc[t][0]);
+            acc[t][1] = fmaf(s0, c[t][1], acc[t][1]);
+            acc[t][2] = fmaf(s1, c[t][2], acc[t][2]);
+            acc[t][3] = fmaf(s1, c[t][3], acc[t][3]);
+        }
+    }
+}
+
+// MT tokens at most (8 or 16): NT = MT / 8 tiles of the mma's 8 columns.
+template <int C, int MT>
 __global__ void __launch_bounds__(kCThreads, 1) gemv_decode_tokens_kernel(const ClusterArgs p) {
-    constexpr int MT = 8;
     using L = DLayout<MT>;
+    constexpr int NT = MT / 8;
     constexpr int GW = C * kCWarps;  // the cluster's warps, all taking part
     extern __shared__ __align__(128) uint8_t smem_raw[];
     uint8_t* zero = smem_raw;                                          // 1 KB of zero x
-    uint8_t* xr = smem_raw + 1024;                                     // MT = 1: [warp][2 slots][1 KB]
     float* mail = reinterpret_cast<float*>(smem_raw + L::kMailOff);   // [warp][kMail][kPart]
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw + L::kBarOff);  // [warp]
-    uint8_t* xs = smem_raw + L::kFixed;                                // MT = 8: the block's x
+    uint8_t* xs = smem_raw + L::kFixed;                                // the block's x
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
     const int rank = (int)ptx::cluster_rank();
     const int cid = (int)blockIdx.x / C, NC = (int)gridDim.x / C;
@@ -1529,7 +1564,7 @@ __global__ void __launch_bounds__(kCThreads, 1) gemv_decode_tokens_kernel(const 
     auto warp_of = [&](int q) { return (int)(((int64_t)(q + 1) * GW + Tc - 1) / Tc - 1); };
     int lrb = q0 / KU, ku = q0 % KU;
     const int hk = p.K / 2;
-    const int M = MT == 1 ? 1 : p.M;
+    const int M = p.M;
     const uint8_t* lane_base = p.qw + (int64_t)gid * hk + t4 * 16;  // row gid of row-block 0, this lane's bytes
     auto load_unit = [&](Pieces& u, int rb_, int ku_) {
         const uint8_t* a = lane_base + (int64_t)rb_ * kRows * hk + ku_ * (kUnitK / 2);
@@ -1561,27 +1596,10 @@ __global__ void __launch_bounds__(kCThreads, 1) gemv_decode_tokens_kernel(const 
         a = ld_l2_v2(r0);
         b = ld_l2_v2(r0 + 8 * p.gpr);
     };
-    // MT = 1: this lane's two 16-byte chunks (lane, lane + 32) of a unit's x
-    auto load_x = [&](int ku_, uint4& a, uint4& b) {
-        const uint16_t* xp = p.x + ku_ * kUnitK;
-        a = ld_l2_v4_nv(xp + lane * 8);
-        b = ld_l2_v4_nv(xp + (lane + 32) * 8);
-    };
-    uint8_t* xw = xr + warp * 2048;
-    auto store_x = [&](uint8_t* slot, uint4 a, uint4 b) {
-        const int j0 = lane, j1 = lane + 32;
-        *reinterpret_cast<uint4*>(slot + (j0 >> 4) * 256 + xs_pos(j0 & 15, 128) * 16) = permute_x8(a);
-        *reinterpret_cast<uint4*>(slot + (j1 >> 4) * 256 + xs_pos(j1 & 15, 128) * 16) = permute_x8(b);
-    };
-    const int xstride = KU * (kUnitSteps * kStepK * 2) + 64;  // MT = 8: bytes per token of the block's x
+    const int xstride = KU * (kUnitSteps * kStepK * 2) + 64;  // bytes per token of the block's x
     uint2 sa, sb;
     load_sc(rb0 + lrb, ku, sa, sb);
-    if constexpr (MT == 1) {
-        uint4 a, b;
-        load_x(ku, a, b);
-        store_x(xw, a, b);
-        __syncwarp();
-    } else {  // the whole x, once per block, in fragment order
+    {  // the whole x, once per block, in fragment order
         const int per_tok = KU * kUnitSteps * 16;
         for (int c = threadIdx.x; c < M * per_tok; c += kCThreads) {
             const int m = c / per_tok, cc = c % per_tok;
@@ -1591,9 +1609,10 @@ __global__ void __launch_bounds__(kCThreads, 1) gemv_decode_tokens_kernel(const 
         }
         __syncthreads();
     }
-    const bool has = gid < M;  // the tokens' lanes; the others read zero x
     int seg_ku0 = ku;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
     for (int r = 0; r < n; ++r) {
         int nlrb = lrb, nku = ku + 1;
         if (nku == KU) {
@@ -1601,33 +1620,27 @@ __global__ void __launch_bounds__(kCThreads, 1) gemv_decode_tokens_kernel(const 
             ++nlrb;
         }
         uint2 na = sa, nb = sb;
-        uint4 xa, xb;
         if (r + 1 < n) {
             load_unit(nxt, rb0 + nlrb, nku);
             load_sc(rb0 + nlrb, nku, na, nb);
-            if constexpr (MT == 1) load_x(nku, xa, xb);
         }
         UnitScales<128> sc;
         sc.lo[0] = sa.x;
         sc.lo[1] = sa.y;
         sc.hi[0] = sb.x;
         sc.hi[1] = sb.y;
-        const uint8_t* xl;
-        if constexpr (MT == 1) xl = (has ? xw + (r & 1) * 1024 : zero) + t4 * 16;
-        else xl = (has ? xs + gid * xstride + ku * (kUnitSteps * kStepK * 2) : zero) + t4 * 16;
-        compute_pieces(cur, sc, xl, acc);
-        if constexpr (MT == 1) {
-            if (r + 1 < n) {
-                store_x(xw + ((r + 1) & 1) * 1024, xa, xb);
-                __syncwarp();  // every lane's chunks before any lane reads the slot
-            }
-        }
+        const uint8_t* xl[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+            xl[t] = (8 * t + gid < M ? xs + (8 * t + gid) * xstride + ku * (kUnitSteps * kStepK * 2) : zero) + t4 * 16;
+        compute_pieces_nt<NT>(cur, sc, xl, acc);
         if (r == n - 1) ptx::launch_dependents();
         const bool seg_end = (ku == KU - 1) || (r == n - 1);
         if (seg_end) {
             const int rb = rb0 + lrb;
             if (seg_ku0 == 0 && ku == KU - 1) {
-                store_y_cluster(p, rb, acc, gid, t4);  // the whole row-block in this warp
+#pragma unroll
+                for (int t = 0; t < NT; ++t) store_y_cluster(p, rb, acc[t], gid, t4, 8 * t);  // whole row-block
             } else {
                 const bool first = lrb == lrb_first;
                 const int ga = first ? fa : la, gb = first ? fb : lb;
@@ -1641,34 +1654,41 @@ __global__ void __launch_bounds__(kCThreads, 1) gemv_decode_tokens_kernel(const 
                             ptx::smem_u32(mail + ((ga % kCWarps) * L::kMail + (g - ga - 1)) * L::kPart), rk);
                         const uint32_t rbar = ptx::cluster_map(ptx::smem_u32(&bar[ga % kCWarps]), rk);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int m = 2 * t4 + (i & 1);
-                            if (m < M)
-                                ptx::st_async_cluster_f32(dst + 4u * (m * kRows + gid + 8 * (i >> 1)), acc[i], rbar);
-                        }
+                        for (int t = 0; t < NT; ++t)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int m = 8 * t + 2 * t4 + (i & 1);
+                                if (m < M)
+                                    ptx::st_async_cluster_f32(dst + 4u * (m * kRows + gid + 8 * (i >> 1)), acc[t][i],
+                                                              rbar);
+                            }
                     }
                 } else {
                     // this warp finishes the row-block: the others' sums, then all in warp order
                     volatile int never = 0;
                     const bool ok = ptx::mbar_wait(&bar[warp], 0, &never, wait_limit());
                     if (ok) {
-                        float sum[4];
                         const float* box = mail + warp * L::kMail * L::kPart;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int m = 2 * t4 + (i & 1);
-                            sum[i] = 0.f + acc[i];
-                            if (m < M)
-                                for (int v = 1; v <= gb - ga; ++v)
-                                    sum[i] += box[(v - 1) * L::kPart + m * kRows + gid + 8 * (i >> 1)];
+                        for (int t = 0; t < NT; ++t) {
+                            float sum[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int m = 8 * t + 2 * t4 + (i & 1);
+                                sum[i] = 0.f + acc[t][i];
+                                if (m < M)
+                                    for (int v = 1; v <= gb - ga; ++v)
+                                        sum[i] += box[(v - 1) * L::kPart + m * kRows + gid + 8 * (i >> 1)];
+                            }
+                            store_y_cluster(p, rb, sum, gid, t4, 8 * t);
                         }
-                        store_y_cluster(p, rb, sum, gid, t4);
                     } else if (lane == 0) {
                         raise_device_error(p.err, W4A16_ERR_TIMEOUT);
                     }
                 }
             }
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
             seg_ku0 = nku;
         }
         lrb = nlrb;
@@ -1813,12 +1833,12 @@ const ClusterFit& cluster_fit(const DeviceInfo& dev, cudaError_t* err) {
         cudaError_t e = cluster_attrs<1>(dev);
         if (e == cudaSuccess) e = cluster_attrs<2>(dev);
         if (e == cudaSuccess) e = cluster_attrs<8>(dev);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_decode_tokens_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)dev.smem_optin);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_decode_tokens_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)dev.smem_optin);
+        for (const void* fn : {reinterpret_cast<const void*>(gemv_decode_tokens_kernel<2, 8>),
+                               reinterpret_cast<const void*>(gemv_decode_tokens_kernel<4, 8>),
+                               reinterpret_cast<const void*>(gemv_decode_tokens_kernel<2, 16>),
+                               reinterpret_cast<const void*>(gemv_decode_tokens_kernel<4, 16>)})
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dev.smem_optin);
         if (e != cudaSuccess) return e;
         for (int i = 0; i < 2; ++i) {
             const int c = 2 << i;
@@ -1863,7 +1883,7 @@ w4a16_status cluster_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t
                          int64_t M, int64_t N, int64_t K, int group, bool static_weights, cudaStream_t st,
                          bool* used) {
     *used = false;
-    if (group != 128 || M > 8) return W4A16_OK;
+    if (group != 128 || M > 16) return W4A16_OK;  // 9..16 tokens: the decode kernel only
     const int64_t KU = (K + kUnitK - 1) / kUnitK, RB = (N + kRows - 1) / kRows;
     if (RB * KU > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
     const int mx = M == 1 ? 1 : M == 2 ? 2 : 8;
@@ -1871,7 +1891,7 @@ w4a16_status cluster_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     if (mx == 1) smem = CLayout<1>::kFixed + CLayout<1>::kXWarp;
     else if (mx == 2) smem = CLayout<2>::kFixed + CLayout<2>::kXWarp;
     else smem = CLayout<8>::kFixed + (size_t)M * (size_t)(KU * kUnitSteps * kStepK * 2 + 64);
-    if (smem > dev.smem_optin) return W4A16_OK;
+    if (smem > dev.smem_optin && M <= 8) return W4A16_OK;
     cudaError_t e = cudaSuccess;
     const ClusterFit& fit = cluster_fit(dev, &e);
     if (e != cudaSuccess) return cuda_status(e, "gemv cluster: cudaFuncSetAttribute");
@@ -1909,9 +1929,10 @@ w4a16_status cluster_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t
     // shared memory
     const int64_t slice = (RB / nc) * KU / (c * kCWarps);  // the fewest units a warp gets
     const int mail = M == 1 ? kMail : DLayout<8>::kMail;
-    const size_t dsmem = M == 1 ? kDecodeSmem
-                                : DLayout<8>::kFixed + (size_t)M * (size_t)(KU * kUnitSteps * kStepK * 2 + 64);
+    const size_t xblock = (size_t)M * (size_t)(KU * kUnitSteps * kStepK * 2 + 64);
+    const size_t dsmem = M == 1 ? kDecodeSmem : (M <= 8 ? DLayout<8>::kFixed : DLayout<16>::kFixed) + xblock;
     const bool decode = exact && slice >= 1 && (KU - 1 + slice - 1) / slice <= mail && dsmem <= dev.smem_optin;
+    if (M > 8 && !decode) return W4A16_OK;  // the general kernel stops at 8 tokens
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nc * c));
     cfg.blockDim = dim3(kCThreads);
@@ -1931,8 +1952,10 @@ w4a16_status cluster_run(const DeviceInfo& dev, const uint16_t* x, const uint8_t
         e = c == 2 ? cudaLaunchKernelEx(&cfg, gemv_decode_kernel<2>, a)
                    : cudaLaunchKernelEx(&cfg, gemv_decode_kernel<4>, a);
     else if (decode)
-        e = c == 2 ? cudaLaunchKernelEx(&cfg, gemv_decode_tokens_kernel<2>, a)
-                   : cudaLaunchKernelEx(&cfg, gemv_decode_tokens_kernel<4>, a);
+        e = M <= 8 ? (c == 2 ? cudaLaunchKernelEx(&cfg, gemv_decode_tokens_kernel<2, 8>, a)
+                             : cudaLaunchKernelEx(&cfg, gemv_decode_tokens_kernel<4, 8>, a))
+                   : (c == 2 ? cudaLaunchKernelEx(&cfg, gemv_decode_tokens_kernel<2, 16>, a)
+                             : cudaLaunchKernelEx(&cfg, gemv_decode_tokens_kernel<4, 16>, a));
     else
         e = mx == 1 ? cluster_launch<1>(cfg, a, exact, c) : mx == 2 ? cluster_launch<2>(cfg, a, exact, c)
                                                                     : cluster_launch<8>(cfg, a, exact, c);
