@@ -103,35 +103,48 @@ def test_gemv_wait_times_out_and_next_call_is_correct(hooks, cuda_device):
     assert_within_bound(y.cpu().numpy(), y_ref, a, "GEMV after a timeout")
 
 
-def test_cluster_gemv_mailbox_wait_times_out_and_next_call_is_correct(hooks, cuda_device):
-    """The decode GEMV's only wait is a row-block finisher's wait for the other
-    contributors' sums; with the sums held back it gives up after the limit,
-    records the timeout, stores nothing for those rows and leaves the device
-    usable."""
+@pytest.mark.parametrize("kind", ["one token", "four tokens", "gated"])
+def test_cluster_gemv_mailbox_wait_times_out_and_next_call_is_correct(hooks, cuda_device, kind):
+    """The cluster decode kernels' only wait is a row-block finisher's wait for
+    the other contributors' sums; with the sums held back it gives up after the
+    limit, records the timeout, stores nothing for those rows and leaves the
+    device usable."""
     import torch
 
     lib = hooks
-    M, N, K, g = 1, 17408, 5120, 128   # the decode kernel: every row-block split over 2-3 warps
-    r = workloads.rng(93)
+    M, N, K, g = (4 if kind == "four tokens" else 1), 17408, 5120, 128  # every row-block split over 2-3 warps
+    r = workloads.rng(93 + M)
     qw, s = workloads.raw_packed(r, N, K, g)
     x = workloads.activations(r, M, K)
     xd, qd, sd = to_dev(x, cuda_device), to_dev(qw, cuda_device), to_dev(s, cuda_device)
     y = torch.empty((M, N), dtype=torch.float16, device=cuda_device)
-    nb = lib.w4a16_workspace_bytes(M, N, K, g, 1)
+    gated = kind == "gated"
+    nb = lib.w4a16_workspace_bytes(M, N, K, g, 1) if not gated else lib.w4a16_linear_gated_workspace_bytes(M, N, K, g)
     ws = torch.empty(nb, dtype=torch.uint8, device=cuda_device)
     st = _stream(cuda_device)
+
+    def call():
+        if gated:
+            return lib.w4a16_linear_gated(_p(xd), _p(qd), _p(sd), _p(qd), _p(sd), _p(y), M, N, K, g, _p(ws), nb, st)
+        return lib.w4a16_linear(_p(xd), _p(qd), _p(sd), _p(y), M, N, K, g, _p(ws), nb, st)
+
     assert lib.w4a16_workspace_init(_p(ws), nb, st) == 0
     assert lib.w4a16_test_set_hooks(SHORT_NS, 0) == 0
-    assert lib.w4a16_linear(_p(xd), _p(qd), _p(sd), _p(y), M, N, K, g, _p(ws), nb, st) == 0
+    assert call() == 0
     status, dt = _status_after(lib, st)
     assert status == TIMEOUT, f"status {status}"
     assert dt < 1.0, f"the kernel took {dt:.3f} s to give up"
     assert lib.w4a16_device_status(st) == 0   # read and cleared
     assert lib.w4a16_test_set_hooks(NORMAL_NS, -1) == 0
-    assert lib.w4a16_linear(_p(xd), _p(qd), _p(sd), _p(y), M, N, K, g, _p(ws), nb, st) == 0
+    assert call() == 0
     assert lib.w4a16_device_status(st) == 0
-    y_ref, a = oracle.linear(x, qw, s, g, threads=8)
-    assert_within_bound(y.cpu().numpy(), y_ref, a, "cluster GEMV after a timeout")
+    if gated:
+        y_ref, gg, uu, ag, au = oracle.gated_linear(x, qw, s, qw, s, g, threads=8)
+        err = np.abs(y.cpu().numpy().astype(np.float64) - y_ref)
+        assert np.all(err <= oracle.gated_tolerance(gg, uu, ag, au)), "gated GEMV after a timeout"
+    else:
+        y_ref, a = oracle.linear(x, qw, s, g, threads=8)
+        assert_within_bound(y.cpu().numpy(), y_ref, a, f"cluster GEMV ({kind}) after a timeout")
 
 
 @pytest.mark.parametrize("kind", ["dense", "grouped", "gated"])
