@@ -40,6 +40,9 @@ def _run(w4, dev, x, qw, s, g):
     (129, 130, 96, 32),       # K % 64 == 32, ragged everything
     (256, 512, 2048, 64),
     (511, 200, 160, 32),      # K = 5 groups of 32
+    (100, 200, 544, 32),      # 128-k stages from K = 512: a last stage of 32 k
+    (300, 130, 800, 32),      # ... of 32 k, ragged N
+    (97, 264, 576, 64),       # ... of 64 k, group 64
 ])
 def test_gemm_raw_nibbles(w4, cuda_device, M, N, K, g):
     r = workloads.rng(M * 31 + N + K + g)

@@ -44,7 +44,8 @@
 // of 32 KB, an 8-deep packed ring). Measured on the routed-expert layer:
 // gate/up (K = 2048) 119 us at 128-k stages against 139 us at 64, and 109
 // against 115 us with the third x stage; down (K = 512) 177 us at 64-k stages
-// against 205 us at 128.
+// against 205 us at 128 with two x stages, but 121.4 against 126.8 us at 128
+// once the third x stage is in, so plain GEMMs take 128-k stages from K = 512.
 //
 //   warp 0      TMA producer: the packed weights of each stage (128 rows x
 //               KS/2 bytes, swizzled) and the stage's x (KS/64 boxes of 256
@@ -898,7 +899,9 @@ w4a16_status split_launch(const DeviceInfo& dev, const uint16_t* x, const uint8_
     const int gshift = group == 32 ? 0 : group == 64 ? 1 : 2;
     if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL || T > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
     // long K: 128-k stages; short K: 64-k stages and a deeper pipeline for the tile's fill
-    if (K >= 1024) return launch_split<128>(dev, x, qw, s, y, M, N, K, gshift, offsets, E, gather, T, st);
+    // 128-k stages from K = 512: with the third x stage they beat 64-k stages on
+    // the routed down projection too (K = 512: 121.4 against 126.8 us)
+    if (K >= 512) return launch_split<128>(dev, x, qw, s, y, M, N, K, gshift, offsets, E, gather, T, st);
     return launch_split<64>(dev, x, qw, s, y, M, N, K, gshift, offsets, E, gather, T, st);
 }
 
