@@ -79,6 +79,9 @@ def test_decode_kernel_several_tokens(w4, cuda_device, M):
     y_ref, a = oracle.linear(x, qw, s, 128, threads=8)
     assert_within_bound(y, y_ref, a, f"M={M}")
     assert np.array_equal(y.view(np.uint16), _run(w4, cuda_device, x, qw, s, 128).view(np.uint16))
+    ys = w4.linear(to_dev(x, cuda_device), to_dev(qw, cuda_device), to_dev(s.view(np.float16), cuda_device), 128,
+                   static_weights=True).cpu().numpy()
+    assert np.array_equal(y.view(np.uint16), ys.view(np.uint16))
 
 
 @pytest.mark.parametrize("N,K,g", [(1, 32, 32), (7, 96, 32), (17, 192, 64), (100, 640, 128), (1000, 2080, 32),

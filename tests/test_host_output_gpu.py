@@ -20,7 +20,8 @@ def w4(cuda_device):
 
 
 @pytest.mark.parametrize("M,N,K,g", [(1, 4099, 1024, 128), (4, 1000, 2080, 32), (32, 300, 512, 64),
-                                     (200, 257, 1024, 32), (512, 640, 2048, 128)])
+                                     (200, 257, 1024, 32), (512, 640, 2048, 128),
+                                     (1, 8192, 4096, 128), (4, 8192, 4096, 128)])  # the cluster decode kernels
 def test_linear_into_pinned_host_memory(w4, cuda_device, M, N, K, g):
     import torch
 
@@ -38,12 +39,11 @@ def test_linear_into_pinned_host_memory(w4, cuda_device, M, N, K, g):
     assert_within_bound(y_host.numpy(), y_ref, a, f"M={M} into host memory")
 
 
-@pytest.mark.parametrize("M", [2, 100])
-def test_gated_into_pinned_host_memory(w4, cuda_device, M):
+@pytest.mark.parametrize("M,N,K,g", [(2, 384, 1024, 64), (100, 384, 1024, 64), (1, 8192, 4096, 128)])
+def test_gated_into_pinned_host_memory(w4, cuda_device, M, N, K, g):
     import torch
 
     r = workloads.rng(300 + M)
-    N, K, g = 384, 1024, 64
     qg, sg = workloads.raw_packed(r, N, K, g)
     qu, su = workloads.raw_packed(r, N, K, g)
     x = workloads.activations(r, M, K)
