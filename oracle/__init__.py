@@ -10,6 +10,11 @@ activations)", group 32 for the MoE models) and its Repository layout section
 (s = fp16(max|w|/7), q = clamp(rint(w/s), -8, 7), nibble q+8, even k in the
 low nibble) is the workload specification's reading of "int4 sym".
 
+The block-format functions (``blocks_*``) decode the GGUF block types Q4_K
+and Q5_1 that the infr README lists among its validated formats ("Also
+validated for correctness"; footnote 3 for Q5_1 expert banks), in the ggml
+layouts the C source describes, and form y = x W^T from them in fp64.
+
 The routed-MoE functions (``moe_route``, ``moe_dispatch``, ``moe_gather``,
 ``moe_combine``) are numpy fp64: the softmax top-k router the infr README's
 model table names, the expert-major permutation, and the router-weighted sum
@@ -63,9 +68,15 @@ def _bind(path: str):
     lib.oracle_dequantize.argtypes = [P, I64, I64, I64, I32, P]
     lib.oracle_linear.argtypes = [P, P, P, I64, I64, I64, I32, P, P]
     lib.oracle_grouped_linear.argtypes = [P, P, P, P, I32, I64, I64, I64, I32, P, P]
+    lib.oracle_blocks_row_bytes.argtypes = [I32, I64]
+    lib.oracle_blocks_row_bytes.restype = I64
+    lib.oracle_blocks_decode.argtypes = [I32, P, I64, I64, P]
+    lib.oracle_blocks_decode_f32.argtypes = [I32, P, I64, I64, P]
+    lib.oracle_blocks_linear.argtypes = [I32, P, P, I64, I64, I64, P, P]
     for f in (lib.oracle_half_to_double_n, lib.oracle_float_to_half_rn_n,
               lib.oracle_quantize, lib.oracle_unpack, lib.oracle_pack_q,
-              lib.oracle_dequantize, lib.oracle_linear, lib.oracle_grouped_linear):
+              lib.oracle_dequantize, lib.oracle_linear, lib.oracle_grouped_linear,
+              lib.oracle_blocks_decode, lib.oracle_blocks_decode_f32, lib.oracle_blocks_linear):
         f.restype = None
     return lib
 
@@ -200,6 +211,76 @@ def grouped_linear(x, qw, s, offsets, group: int):
     a = np.zeros((R, N), np.float64)
     _load().oracle_grouped_linear(_p(xb), _p(qw), _p(s), _p(off), E, R, N, K, group, _p(y), _p(a))
     return y, a
+
+
+# ----------------------------------------------------------------------------
+# GGUF block formats (format codes as in oracle.c)
+
+BLOCK_FORMATS = {"q4_k": 1, "q5_1": 2}
+
+
+def _fmt(fmt) -> int:
+    return BLOCK_FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def blocks_row_bytes(fmt, K: int) -> int:
+    """Bytes of one row of K weights in a block format (-1: not whole blocks)."""
+    return int(_load().oracle_blocks_row_bytes(_fmt(fmt), K))
+
+
+def _blocks(fmt, w, K: int) -> np.ndarray:
+    w = _c(w, np.uint8)
+    rb = blocks_row_bytes(fmt, K)
+    if rb < 0 or w.ndim != 2 or w.shape[1] != rb:
+        raise ValueError(f"blocks: expected uint8 [N, {rb}] for K={K}")
+    return w
+
+
+def blocks_decode(fmt, w, K: int) -> np.ndarray:
+    """W^ fp64 [N, K] from the block bytes uint8 [N, row_bytes]."""
+    w = _blocks(fmt, w, K)
+    out = np.empty((w.shape[0], K), np.float64)
+    _load().oracle_blocks_decode(_fmt(fmt), _p(w), w.shape[0], K, _p(out))
+    return out
+
+
+def blocks_decode_f32(fmt, w, K: int) -> np.ndarray:
+    """W^ fp32 [N, K] as a CPU dequantizer forms it: a * q + b with the step a
+    and offset b in fp32, rounded once."""
+    w = _blocks(fmt, w, K)
+    out = np.empty((w.shape[0], K), np.float32)
+    _load().oracle_blocks_decode_f32(_fmt(fmt), _p(w), w.shape[0], K, _p(out))
+    return out
+
+
+def blocks_linear(fmt, x, w, threads: int = 1):
+    """y = x W^T in fp64 for block-format weights; x fp16 [M, K], w uint8
+    [N, row_bytes]. Returns (y, absterm), absterm = sum_k |x| (|a q| + |b|)
+    for W^ = a q + b: the size of what a kernel adds up, which takes the place
+    of sum_k |x W^| in tolerance(). ``threads > 1`` splits the rows n."""
+    xb = half_bits(x)
+    M, K = xb.shape
+    w = _blocks(fmt, w, K)
+    N = w.shape[0]
+    lib, f = _load(), _fmt(fmt)
+    if threads <= 1 or N < 2 * threads:
+        y = np.empty((M, N), np.float64)
+        a = np.empty((M, N), np.float64)
+        lib.oracle_blocks_linear(f, _p(xb), _p(w), M, N, K, _p(y), _p(a))
+        return y, a
+    bounds = np.linspace(0, N, threads + 1).astype(np.int64)
+
+    def part(i):
+        n0, n1 = int(bounds[i]), int(bounds[i + 1])
+        wp = np.ascontiguousarray(w[n0:n1])
+        yp = np.empty((M, n1 - n0), np.float64)
+        ap = np.empty((M, n1 - n0), np.float64)
+        lib.oracle_blocks_linear(f, _p(xb), _p(wp), M, n1 - n0, K, _p(yp), _p(ap))
+        return yp, ap
+
+    with ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(part, range(threads)))
+    return np.concatenate([p[0] for p in parts], 1), np.concatenate([p[1] for p in parts], 1)
 
 
 def tolerance(y_ref: np.ndarray, absdot: np.ndarray) -> np.ndarray:

@@ -20,6 +20,22 @@
  *   q = clamp(rint(w / s), -8, 7) in fp32, all-zero group -> s = 0, q = 0,
  *   stored as the nibble q + 8, even k in the low nibble.
  *
+ * GGUF block formats (infr README, "Also validated for correctness": Q4_K_M
+ * among the formats decoded on the GPU byte-identically to the CPU dequant;
+ * footnote 3: routed expert banks stored as Q5_1; LLM170 README, status:
+ * "q5_1 down" and "q4_K" MoE tiles). The pages name the formats but print no
+ * layout; the layouts below are the block types of the ggml tensor library
+ * that GGUF files carry (GGUF specification, ggml repository docs/gguf.md;
+ * Q4_K from the k-quants change, llama.cpp pull request 1684). A row of K
+ * weights is K/256 Q4_K blocks or K/32 Q5_1 blocks, rows one after another.
+ *
+ *   Q4_K, 256 weights in 144 bytes: fp16 d, fp16 dmin, 12 bytes holding
+ *   eight 6-bit sub-block scales sc[j] and eight 6-bit minimums mn[j] (one
+ *   pair per 32 weights), then 128 bytes of 4-bit q. Weight i has
+ *   W^ = d * sc[i/32] * q - dmin * mn[i/32].
+ *   Q5_1, 32 weights in 24 bytes: fp16 d, fp16 m, a 32-bit word of fifth
+ *   bits, 16 bytes of low nibbles. W^ = d * q + m, q in [0, 31].
+ *
  * Build: plain C99, no fast-math, -ffp-contract=off (no fused multiply-add
  * contraction), so that x86-64 and aarch64 hosts give bit-identical results.
  */
@@ -208,4 +224,152 @@ void oracle_grouped_linear(const uint16_t* x, const uint8_t* qw, const uint16_t*
         oracle_linear(x + r0 * K, qw + (int64_t)e * N * (K / 2), s + (int64_t)e * N * (K / g),
                       r1 - r0, N, K, g, y + r0 * N, absdot ? absdot + r0 * N : NULL);
     }
+}
+
+/* ------------------------------------------------------ GGUF block formats -- */
+
+#define ORACLE_Q4_K 1
+#define ORACLE_Q5_1 2
+
+/* Weights and bytes per block; 0 for an unknown format. */
+static int block_weights(int32_t fmt) { return fmt == ORACLE_Q4_K ? 256 : fmt == ORACLE_Q5_1 ? 32 : 0; }
+static int block_bytes(int32_t fmt) { return fmt == ORACLE_Q4_K ? 144 : fmt == ORACLE_Q5_1 ? 24 : 0; }
+
+/* Bytes of one row of K weights, or -1 if the format is unknown or K is not
+ * a whole number of blocks. */
+int64_t oracle_blocks_row_bytes(int32_t fmt, int64_t K)
+{
+    int bw = block_weights(fmt);
+    if (bw == 0 || K < 0 || K % bw != 0) return -1;
+    return K / bw * block_bytes(fmt);
+}
+
+static uint16_t le16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* Sub-block j of a Q4_K block: its 6-bit scale and minimum. The twelve bytes
+ * hold, for j < 4, sc[j] in the low 6 bits of byte j and mn[j] in the low 6
+ * bits of byte j + 4; for j >= 4 the low 4 bits of sc[j] and of mn[j] are the
+ * low and high nibble of byte j + 4, and their top 2 bits sit in the top 2
+ * bits of byte j - 4 (sc) and byte j (mn). */
+static void q4k_scale_min(const uint8_t* b12, int j, int* sc, int* mn)
+{
+    if (j < 4) {
+        *sc = b12[j] & 63;
+        *mn = b12[j + 4] & 63;
+    } else {
+        *sc = (b12[j + 4] & 0x0F) | ((b12[j - 4] >> 6) << 4);
+        *mn = (b12[j + 4] >> 4) | ((b12[j] >> 6) << 4);
+    }
+}
+
+/* One block as W^[i] = a[i] * q[i] + b[i]: the unsigned integer q and the
+ * fp64 step a and offset b (exact products of fp16 values and small
+ * integers). */
+static void block_terms(int32_t fmt, const uint8_t* blk, int* q, double* a, double* b)
+{
+    if (fmt == ORACLE_Q4_K) {
+        double d = oracle_half_to_double(le16(blk));
+        double dmin = oracle_half_to_double(le16(blk + 2));
+        const uint8_t* qs = blk + 16;
+        for (int i = 0; i < 256; ++i) {
+            /* 64 weights per 32 bytes: the first 32 in the low nibbles,
+             * the next 32 in the high nibbles of the same bytes */
+            int chunk = i / 64, r = i % 64;
+            uint8_t byte = qs[32 * chunk + (r % 32)];
+            int sc, mn;
+            q4k_scale_min(blk + 4, i / 32, &sc, &mn);
+            q[i] = r < 32 ? (byte & 0x0F) : (byte >> 4);
+            a[i] = d * (double)sc;
+            b[i] = -(dmin * (double)mn);
+        }
+    } else {
+        double d = oracle_half_to_double(le16(blk));
+        double m = oracle_half_to_double(le16(blk + 2));
+        uint32_t qh = (uint32_t)blk[4] | ((uint32_t)blk[5] << 8) | ((uint32_t)blk[6] << 16) |
+                      ((uint32_t)blk[7] << 24);
+        const uint8_t* qs = blk + 8;
+        for (int i = 0; i < 32; ++i) {
+            /* weight i: low nibble of byte i (i < 16) or high nibble of byte
+             * i - 16, plus bit i of qh as the fifth bit */
+            int nib = i < 16 ? (qs[i] & 0x0F) : (qs[i - 16] >> 4);
+            q[i] = nib | (int)(((qh >> i) & 1u) << 4);
+            a[i] = d;
+            b[i] = m;
+        }
+    }
+}
+
+/* W^ [N, K] in fp64 from the blocks [N, row_bytes]. */
+void oracle_blocks_decode(int32_t fmt, const uint8_t* w, int64_t N, int64_t K, double* w_hat)
+{
+    int bw = block_weights(fmt), bb = block_bytes(fmt);
+    int q[256];
+    double a[256], b[256];
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t kb = 0; kb < K / bw; ++kb) {
+            block_terms(fmt, w + (n * (K / bw) + kb) * bb, q, a, b);
+            for (int i = 0; i < bw; ++i) w_hat[n * K + kb * bw + i] = a[i] * (double)q[i] + b[i];
+        }
+}
+
+/* The same weights in fp32 as a CPU dequantizer forms them: step a and
+ * offset b in fp32 (exact), then a * q (exact) plus b, rounded once. */
+void oracle_blocks_decode_f32(int32_t fmt, const uint8_t* w, int64_t N, int64_t K, float* out)
+{
+    int bw = block_weights(fmt), bb = block_bytes(fmt);
+    int q[256];
+    double a[256], b[256];
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t kb = 0; kb < K / bw; ++kb) {
+            block_terms(fmt, w + (n * (K / bw) + kb) * bb, q, a, b);
+            for (int i = 0; i < bw; ++i) {
+                float af = (float)a[i], bf = (float)b[i];
+                float p = af * (float)q[i];
+                out[n * K + kb * bw + i] = p + bf;
+            }
+        }
+}
+
+/* y[m,n] = sum_k x[m,k] * W^[n,k] in fp64, k ascending; absterm (if not NULL)
+ * = sum_k |x[m,k]| * (|a q| + |b|), the size of the two parts a block format
+ * adds up (for a format without offset it is sum_k |x W^|).
+ * x: fp16 bits [M, K]; w: blocks [N, row_bytes]; y, absterm: fp64 [M, N]. */
+void oracle_blocks_linear(int32_t fmt, const uint16_t* x, const uint8_t* w, int64_t M, int64_t N, int64_t K,
+                          double* y, double* absterm)
+{
+    int bw = block_weights(fmt), bb = block_bytes(fmt);
+    double* xd = (double*)malloc(sizeof(double) * (size_t)(M * K + 1));
+    double* wr = (double*)malloc(sizeof(double) * (size_t)(K + 1));
+    double* ar = (double*)malloc(sizeof(double) * (size_t)(K + 1));
+    if (!xd || !wr || !ar) {
+        free(xd);
+        free(wr);
+        free(ar);
+        return;
+    }
+    int q[256];
+    double a[256], b[256];
+    for (int64_t i = 0; i < M * K; ++i) xd[i] = oracle_half_to_double(x[i]);
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t kb = 0; kb < K / bw; ++kb) {
+            block_terms(fmt, w + (n * (K / bw) + kb) * bb, q, a, b);
+            for (int i = 0; i < bw; ++i) {
+                wr[kb * bw + i] = a[i] * (double)q[i] + b[i];
+                ar[kb * bw + i] = fabs(a[i] * (double)q[i]) + fabs(b[i]);
+            }
+        }
+        for (int64_t m = 0; m < M; ++m) {
+            const double* xr = xd + m * K;
+            double acc = 0.0, aacc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                acc += xr[k] * wr[k];
+                aacc += fabs(xr[k]) * ar[k];
+            }
+            y[m * N + n] = acc;
+            if (absterm) absterm[m * N + n] = aacc;
+        }
+    }
+    free(xd);
+    free(wr);
+    free(ar);
 }

@@ -603,3 +603,155 @@ def test_moe_chain_equals_direct_per_token():
             yt, _ = oracle.linear(x[t:t + 1], qw[ids[t, j]], s[ids[t, j]], g)
             direct += w[t, j] * oracle.half_to_double(oracle.float_to_half_bits(yt))[0]
         assert np.allclose(y[t], direct, rtol=1e-12, atol=1e-15)
+
+
+# ------------------------------------------------------- GGUF block formats
+# Pins for the Q4_K and Q5_1 decoders: hand-worked blocks (tests/golden/), an
+# encoder written here in the inverse direction from the layout (fields ->
+# bytes), exact rational sums, and the special case that reduces Q5_1 to a
+# plain integer matrix product.
+
+BLOCKS = {"q4_k": (256, 144), "q5_1": (32, 24)}  # weights, bytes per block
+
+
+def _block_golden(fmt):
+    name = {"q4_k": "q4k_block.txt", "q5_1": "q5_1_block.txt"}[fmt]
+    raw, values, x, out = bytearray(), {}, {}, {}
+    for line in _golden_lines(name):
+        key, _, rest = line.partition(" ")
+        if key in ("header", "scales", "qs"):
+            raw += bytes(int(t, 16) for t in rest.split())
+        elif key == "value":
+            i, v = rest.split()
+            values[int(i)] = float(v)
+        elif key == "x":
+            x = {int(a): float(b) for a, b in (t.split(":") for t in rest.split())}
+        elif key in ("y", "absterm"):
+            out[key] = float(rest)
+    return bytes(raw), values, x, out
+
+
+def _fp16_bytes(v):
+    return np.array([v], dtype=np.float16).tobytes()  # little-endian on every host we run on
+
+
+def _enc_q4k(d, dmin, sc, mn, q):
+    """Fields -> 144 bytes: sc/mn 6-bit (0..63), q 256 nibbles (0..15)."""
+    b = bytearray(144)
+    b[0:2], b[2:4] = _fp16_bytes(d), _fp16_bytes(dmin)
+    for j in range(4):
+        b[4 + j] = sc[j] | (sc[j + 4] >> 4) << 6
+        b[8 + j] = mn[j] | (mn[j + 4] >> 4) << 6
+        b[12 + j] = (sc[j + 4] & 15) | (mn[j + 4] & 15) << 4
+    for i in range(256):
+        c, r = divmod(i, 64)
+        b[16 + 32 * c + r % 32] |= q[i] if r < 32 else q[i] << 4
+    return bytes(b)
+
+
+def _enc_q51(d, m, q):
+    """Fields -> 24 bytes: q 32 values (0..31)."""
+    b = bytearray(24)
+    b[0:2], b[2:4] = _fp16_bytes(d), _fp16_bytes(m)
+    qh = sum(((q[i] >> 4) & 1) << i for i in range(32))
+    b[4:8] = qh.to_bytes(4, "little")
+    for i in range(16):
+        b[8 + i] = (q[i] & 15) | (q[i + 16] & 15) << 4
+    return bytes(b)
+
+
+def _random_fields(fmt, g):
+    """One block's fields and its exact weights as Fractions."""
+    if fmt == "q4_k":
+        d, dmin = np.float16(g.uniform(0.5, 2.0) * 2.0 ** -10), np.float16(g.uniform(0.5, 2.0) * 2.0 ** -11)
+        sc, mn = [int(v) for v in g.integers(0, 64, 8)], [int(v) for v in g.integers(0, 64, 8)]
+        q = [int(v) for v in g.integers(0, 16, 256)]
+        w = [Fraction(float(d)) * sc[i // 32] * q[i] - Fraction(float(dmin)) * mn[i // 32] for i in range(256)]
+        return _enc_q4k(d, dmin, sc, mn, q), w
+    d, m = np.float16(g.uniform(0.5, 2.0) * 2.0 ** -9), np.float16(-g.uniform(0.5, 2.0) * 2.0 ** -5)
+    q = [int(v) for v in g.integers(0, 32, 32)]
+    return _enc_q51(d, m, q), [Fraction(float(d)) * q[i] + Fraction(float(m)) for i in range(32)]
+
+
+def _random_matrix(fmt, g, N, K):
+    bw, bb = BLOCKS[fmt]
+    rows, exact = [], []
+    for _ in range(N):
+        parts = [_random_fields(fmt, g) for _ in range(K // bw)]
+        rows.append(b"".join(p[0] for p in parts))
+        exact.append([v for p in parts for v in p[1]])
+    return np.frombuffer(b"".join(rows), np.uint8).reshape(N, K // bw * bb).copy(), exact
+
+
+@pytest.mark.parametrize("fmt", ["q4_k", "q5_1"])
+def test_blocks_golden(fmt):
+    raw, values, x, out = _block_golden(fmt)
+    bw, bb = BLOCKS[fmt]
+    assert len(raw) == bb
+    w = np.frombuffer(raw, np.uint8).reshape(1, bb)
+    dec = oracle.blocks_decode(fmt, w, bw)[0]
+    for i, v in values.items():
+        assert dec[i] == v, (fmt, i, dec[i], v)
+    xv = np.zeros((1, bw), np.float16)
+    for k, v in x.items():
+        xv[0, k] = v
+    y, a = oracle.blocks_linear(fmt, xv, w)
+    assert y[0, 0] == out["y"] and a[0, 0] == out["absterm"]
+
+
+@pytest.mark.parametrize("fmt", ["q4_k", "q5_1"])
+def test_blocks_row_bytes_closed_form(fmt):
+    bw, bb = BLOCKS[fmt]
+    for nb in (0, 1, 3, 68):
+        assert oracle.blocks_row_bytes(fmt, nb * bw) == nb * bb
+    assert oracle.blocks_row_bytes(fmt, bw + bw // 2) == -1
+    assert oracle.blocks_row_bytes(fmt, -bw) == -1
+    assert oracle.blocks_row_bytes(7, bw) == -1
+
+
+@pytest.mark.parametrize("fmt,N,K", [("q4_k", 3, 512), ("q5_1", 4, 96)])
+def test_blocks_decode_inverts_an_encoder(fmt, N, K):
+    """Random fields packed by the encoder above decode to exactly d*sc*q - dmin*mn
+    (Q4_K) or d*q + m (Q5_1), element by element, across several blocks a row."""
+    w, exact = _random_matrix(fmt, workloads.rng(11), N, K)
+    dec = oracle.blocks_decode(fmt, w, K)
+    for n in range(N):
+        for k in range(K):
+            assert Fraction(dec[n, k]) == exact[n][k], (fmt, n, k)
+
+
+@pytest.mark.parametrize("fmt,M,N,K", [("q4_k", 2, 3, 256), ("q5_1", 3, 2, 64)])
+def test_blocks_linear_exact_rational(fmt, M, N, K):
+    g = workloads.rng(12)
+    w, exact = _random_matrix(fmt, g, N, K)
+    x = workloads.activations(g, M, K)
+    y, a = oracle.blocks_linear(fmt, x, w)
+    for m in range(M):
+        for n in range(N):
+            ref = sum(Fraction(float(x[m, k])) * exact[n][k] for k in range(K))
+            assert abs(Fraction(y[m, n]) - ref) <= Fraction(K) * Fraction(2.0 ** -52) * Fraction(a[m, n])
+            assert a[m, n] >= abs(y[m, n])
+
+
+@pytest.mark.parametrize("fmt,K", [("q4_k", 512), ("q5_1", 128)])
+def test_blocks_decode_f32_is_the_rounded_exact_value(fmt, K):
+    """The fp32 decode is the exact weight rounded once to fp32 (its step and
+    offset are exact in fp32 and so is step * q: only the sum rounds)."""
+    w, exact = _random_matrix(fmt, workloads.rng(13), 5, K)
+    f32 = oracle.blocks_decode_f32(fmt, w, K)
+    for n in range(5):
+        ref = np.array([float(v) for v in exact[n]], np.float64).astype(np.float32)
+        assert np.array_equal(f32[n], ref)
+
+
+def test_blocks_q5_1_plain_nibbles_match_numpy_matmul():
+    """d = 1, m = 0, no fifth bits: W^ is the nibble matrix itself."""
+    g = workloads.rng(14)
+    N, K, M = 6, 96, 3
+    q = g.integers(0, 16, size=(N, K))
+    w = np.frombuffer(b"".join(_enc_q51(np.float16(1), np.float16(0), [int(v) for v in q[n, j:j + 32]])
+                               for n in range(N) for j in range(0, K, 32)), np.uint8).reshape(N, -1)
+    x = workloads.activations(g, M, K)
+    assert np.array_equal(oracle.blocks_decode("q5_1", w, K), q.astype(np.float64))
+    y, _ = oracle.blocks_linear("q5_1", x, w)
+    assert np.allclose(y, x.astype(np.float64) @ q.T.astype(np.float64), rtol=0, atol=1e-9)

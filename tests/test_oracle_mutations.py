@@ -23,6 +23,19 @@ MUTANTS = {
     "scale indexed by byte, not k": ("s[n * G + k / g]", "s[n * G + (k / 2) / g]"),
     "abs dropped in the bound": ("aacc += fabs(p);", "aacc += p;"),
     "subnormal exponent off by one": ("ldexp((double)f, -24)", "ldexp((double)f, -25)"),
+    "Q4_K high nibbles first": ("q[i] = r < 32 ? (byte & 0x0F) : (byte >> 4);",
+                                "q[i] = r < 32 ? (byte >> 4) : (byte & 0x0F);"),
+    "Q4_K top bits of mn read from byte j-4": ("*mn = (b12[j + 4] >> 4) | ((b12[j] >> 6) << 4);",
+                                               "*mn = (b12[j + 4] >> 4) | ((b12[j - 4] >> 6) << 4);"),
+    "Q4_K scale and minimum nibbles swapped": ("*sc = (b12[j + 4] & 0x0F) |", "*sc = (b12[j + 4] >> 4) |"),
+    "Q4_K minimum added, not subtracted": ("b[i] = -(dmin * (double)mn);", "b[i] = dmin * (double)mn;"),
+    "Q4_K chunks 16 bytes apart": ("qs[32 * chunk + (r % 32)]", "qs[16 * chunk + (r % 32)]"),
+    "Q5_1 fifth bit of the high half from bit i-16": ("q[i] = nib | (int)(((qh >> i) & 1u) << 4);",
+                                                      "q[i] = nib | (int)(((qh >> (i % 16)) & 1u) << 4);"),
+    "Q5_1 offset dropped": ("b[i] = m;", "b[i] = 0.0;"),
+    "block bound without the offset term": ("ar[kb * bw + i] = fabs(a[i] * (double)q[i]) + fabs(b[i]);",
+                                            "ar[kb * bw + i] = fabs(a[i] * (double)q[i] + b[i]);"),
+    "fp32 decode drops the offset": ("out[n * K + kb * bw + i] = p + bf;", "out[n * K + kb * bw + i] = p;"),
     "dot product skips the last k": ("for (int64_t k = 0; k < K; ++k) {\n                double p",
                                      "for (int64_t k = 0; k < K - 1; ++k) {\n                double p"),
 }
@@ -46,6 +59,16 @@ def _all_pins():
     yield pins.test_linear_unit_scales_match_numpy_matmul, ()
     yield pins.test_linear_is_linear_in_x, ()
     yield pins.test_grouped_equals_loop_of_dense_calls, ()
+    for fmt in ("q4_k", "q5_1"):
+        yield pins.test_blocks_golden, (fmt,)
+        yield pins.test_blocks_row_bytes_closed_form, (fmt,)
+    yield pins.test_blocks_decode_inverts_an_encoder, ("q4_k", 3, 512)
+    yield pins.test_blocks_decode_inverts_an_encoder, ("q5_1", 4, 96)
+    yield pins.test_blocks_linear_exact_rational, ("q4_k", 2, 3, 256)
+    yield pins.test_blocks_linear_exact_rational, ("q5_1", 3, 2, 64)
+    yield pins.test_blocks_decode_f32_is_the_rounded_exact_value, ("q4_k", 512)
+    yield pins.test_blocks_decode_f32_is_the_rounded_exact_value, ("q5_1", 128)
+    yield pins.test_blocks_q5_1_plain_nibbles_match_numpy_matmul, ()
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))

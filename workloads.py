@@ -18,7 +18,12 @@ the fixed order W, then x, then routing):
   (empty experts allowed);
 * raw packed weights: uniform random bytes (all 16 nibble values, including
   nibble 0, i.e. q = -8, which the quantizer never emits) with fp16 scales
-  drawn as |N(0, 0.02)| / 7.
+  drawn as |N(0, 0.02)| / 7;
+* GGUF block formats (Q4_K: 144-byte blocks of 256 weights; Q5_1: 24-byte
+  blocks of 32): uniform random bytes for every block, then the two fp16
+  fields at the start of each block replaced: Q4_K d ~ U(0.5, 2) 2^-12 and
+  dmin ~ U(0.5, 2) 2^-13 (weights within about [-0.015, 0.46], spread 0.07,
+  with the random 6-bit scales and minimums); Q5_1 d ~ U(0.5, 2) 2^-9 and m ~ -U(0.5, 2) 2^-5.
 """
 from __future__ import annotations
 
@@ -57,6 +62,28 @@ def raw_packed(g: np.random.Generator, N: int, K: int, group: int):
     qw = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
     s = (np.abs(g.normal(0.0, 0.02, size=(N, K // group))) / 7.0).astype(np.float16)
     return qw, s
+
+
+# GGUF block formats: (weights per block, bytes per block), and where the two
+# fp16 fields of a block sit (bytes 0-1 and 2-3 in both formats).
+BLOCK_FORMATS = {"q4_k": (256, 144), "q5_1": (32, 24)}
+
+
+def raw_blocks(g: np.random.Generator, fmt: str, N: int, K: int) -> np.ndarray:
+    """Random block bytes uint8 [N, K / weights_per_block * bytes_per_block]."""
+    bw, bb = BLOCK_FORMATS[fmt]
+    assert K % bw == 0
+    nb = N * (K // bw)
+    raw = g.integers(0, 256, size=(nb, bb), dtype=np.uint8)
+    if fmt == "q4_k":
+        f0 = g.uniform(0.5, 2.0, nb) * 2.0 ** -12
+        f1 = g.uniform(0.5, 2.0, nb) * 2.0 ** -13
+    else:
+        f0 = g.uniform(0.5, 2.0, nb) * 2.0 ** -9
+        f1 = -g.uniform(0.5, 2.0, nb) * 2.0 ** -5
+    raw[:, 0:2] = f0.astype("<f2").view(np.uint8).reshape(nb, 2)
+    raw[:, 2:4] = f1.astype("<f2").view(np.uint8).reshape(nb, 2)
+    return raw.reshape(N, (K // bw) * bb)
 
 
 @dataclass
