@@ -537,6 +537,30 @@ def side_measurements(args, torch, w4, dev, hbm_peak, tc_peak, l2):
         del logits, xt, ys, xs
     except w4.W4A16Error as e:
         out["moe_dispatch"] = {"unavailable": str(e)}
+    # GGUF block formats (Q4_K, Q5_1): the decode GEMV at M = 1 on both decode
+    # shapes, rotated copies so that successive launches miss in L2
+    try:
+        for fmt in ("q4_k", "q5_1"):
+            for K, N in DECODE:
+                gb = workloads.rng(9)
+                blk = torch.from_numpy(workloads.raw_blocks(gb, fmt, N, K)).to(dev)
+                per = blk.numel()
+                nb = max(2, -(-4 * l2 // per))
+                rotb = [blk] + [blk.clone() for _ in range(nb - 1)]
+                xb = torch.from_numpy(workloads.activations(gb, 1, K)).to(dev)
+                yb = torch.empty((1, N), dtype=torch.float16, device=dev)
+                f = lambda i: w4.blocks_linear(fmt, xb, rotb[i % nb], out=yb)  # noqa: E731
+                for i in range(5):
+                    f(i)
+                ms = statistics.median(_time_launches(torch, f, 100))
+                b = per + K * 2 + N * 2
+                out[f"blocks_{fmt}_m1_{K}x{N}"] = {"shape": [1, K, N], "us": ms * 1e3,
+                                                   "GB/s": b / (ms * 1e-3) / 1e9,
+                                                   "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm_peak}
+                del rotb, blk
+        w4.device_status()
+    except w4.W4A16Error as e:
+        out["blocks"] = {"unavailable": str(e)}
     # the whole routed layer (4096 tokens, top-8 of 128 experts, hidden 2048, expert
     # width 512, group 32): route -> dispatch -> gate/up GEMM -> down GEMM -> combine,
     # with the token gather as a separate copy (dispatch writes x_sorted) or fused into
@@ -704,7 +728,8 @@ def oracle_other_configs(oracle):
 # ----------------------------------------------------------------- profile --
 
 PROFILE_CASES = ("decode", "decode_down", "decode_m4", "decode_gated", "prefill", "prefill_m512", "prefill_gated",
-                 "moe_gate_up", "moe_down", "moe_dispatch", "moe_gate_up_gather")
+                 "moe_gate_up", "moe_down", "moe_dispatch", "moe_gate_up_gather", "blocks_q4_k", "blocks_q4_k_down",
+                 "blocks_q5_1", "blocks_q5_1_down")
 
 
 def run_profile(case: str, launches: int):
@@ -755,6 +780,16 @@ def run_profile(case: str, launches: int):
         off, row_of, tok, _ = w4.moe_dispatch(ids, E)
         for _ in range(launches):
             w4.grouped_linear_gather(xt, tok, qm, sm, off, 32)
+    elif case.startswith("blocks_"):
+        # GGUF block-format GEMV, M = 1: blocks_q4_k / blocks_q5_1 on the gate/up
+        # shape, *_down on the down shape
+        fmt = "q4_k" if case.startswith("blocks_q4_k") else "q5_1"
+        K, N = DECODE[1] if case.endswith("_down") else DECODE[0]
+        copies = [torch.from_numpy(workloads.raw_blocks(g, fmt, N, K)).to(dev) for _ in range(4)]
+        x = torch.from_numpy(workloads.activations(g, 1, K)).to(dev)
+        y = torch.empty((1, N), dtype=torch.float16, device=dev)
+        for i in range(launches):
+            w4.blocks_linear(fmt, x, copies[i % 4], out=y)
     elif case.startswith("moe"):
         Km, Nm = (2048, 512) if case == "moe_gate_up" else (512, 2048)
         W, xs, rt = workloads.moe(Km, Nm)

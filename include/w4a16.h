@@ -290,6 +290,63 @@ W4A16_API w4a16_status w4a16_moe_combine(const uint16_t* y_sorted, int64_t R, co
                                          const float* topk_weights, int64_t T, int32_t top_k, int64_t N,
                                          uint16_t* y, void* stream);
 
+/*
+ * GGUF block formats. The infr README lists the block formats its GPU path
+ * decodes byte-identically to the CPU dequant ("Also validated for
+ * correctness", among them Q4_K_M) and stores routed expert banks as Q5_1
+ * (footnote 3); the LLM170 README's status names q4_K and q5_1 MoE tiles. The
+ * pages print no layout; these are ggml's block types as GGUF files carry
+ * them (GGUF specification, ggml repository docs/gguf.md; Q4_K from the
+ * k-quants change, llama.cpp pull request 1684), all fields little-endian:
+ *
+ *   W4A16_FORMAT_Q4_K  256 weights in 144 bytes: fp16 d, fp16 dmin, 12 bytes
+ *     of 6-bit sub-block scales sc[0..7] and minimums mn[0..7] (sc[j], mn[j]
+ *     for j < 4 in the low 6 bits of bytes j and j + 4; for j >= 4 the low
+ *     4 bits in the low and high nibble of byte j + 4 and the top 2 bits in
+ *     the top bits of bytes j - 4 and j), then 128 bytes of nibbles: weight
+ *     64c + l (l < 32) is the low nibble of byte 32c + l, weight 64c + 32 + l
+ *     its high nibble. W^[i] = d * sc[i/32] * q - dmin * mn[i/32].
+ *   W4A16_FORMAT_Q5_1  32 weights in 24 bytes: fp16 d, fp16 m, a 32-bit word
+ *     qh, 16 bytes of nibbles: weight i < 16 is the low nibble of byte i,
+ *     weight i >= 16 the high nibble of byte i - 16, and bit i of qh is its
+ *     fifth bit. W^[i] = d * q + m.
+ *
+ * A matrix of N rows of K weights is uint8 [N, w4a16_blocks_row_bytes(format,
+ * K)]: each row's blocks in k order, rows one after another (K a multiple of
+ * 256 for Q4_K and of 32 for Q5_1).
+ */
+#define W4A16_FORMAT_Q4_K 1
+#define W4A16_FORMAT_Q5_1 2
+
+/* Bytes of one row of K weights, or -1 for an unknown format or a K that is
+ * not a whole number of blocks. */
+W4A16_API int64_t w4a16_blocks_row_bytes(int32_t format, int64_t K);
+
+/*
+ * y = x * W^T for block-format weights: y[m, n] = sum_k x[m, k] * W^[n, k]
+ * with x fp16 [M, K], blocks as above (device) and y fp16 [M, N]. Products of
+ * x and the integer q are exact; each 32-weight sub-block's sums of x q and
+ * of x are accumulated in fp32 and scaled by the block's fp32 step and
+ * offset; y is rounded once to fp16. Element-wise the result stays within
+ * |y - y_ref| <= 2^-9 |y_ref| + 1e-4 sum_k |x[m, k]| (|a q| + |b|) of the
+ * exact value, W^ = a q + b. A decode GEMV: each launch serves up to 8 rows
+ * of x and reads the weights once; larger M runs one launch per 8 rows.
+ * M, N >= 0 (M = 0 or N = 0: nothing to do); K >= 0, whole blocks (K = 0
+ * writes y = 0). x, blocks and y must be 16-byte aligned. No workspace; the
+ * result is deterministic. Unknown format: W4A16_ERR_UNSUPPORTED.
+ */
+W4A16_API w4a16_status w4a16_blocks_linear(int32_t format, const uint16_t* x, const uint8_t* blocks, uint16_t* y,
+                                           int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * W^ as fp32 [N, K] (device, 16-byte aligned): the step and offset of each
+ * sub-block in fp32 (exact), the step times q (exact), plus the offset,
+ * rounded once; bit for bit what a CPU dequantizer forming the same values in
+ * fp32 gets. Same sizes and rules as w4a16_blocks_linear.
+ */
+W4A16_API w4a16_status w4a16_blocks_dequant(int32_t format, const uint8_t* blocks, int64_t N, int64_t K, float* w,
+                                            void* stream);
+
 /* Bytes of workspace w4a16_linear (E = 1) or w4a16_grouped_linear (E experts,
  * M = R rows) needs for this problem on the current device; 0 if none. */
 W4A16_API size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t group, int32_t E);

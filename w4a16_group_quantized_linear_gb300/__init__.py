@@ -21,7 +21,7 @@ import threading
 import torch
 
 __all__ = ["pack", "unpack", "linear", "linear_gated", "grouped_linear", "grouped_linear_gather", "moe_route",
-           "moe_dispatch", "moe_combine",
+           "moe_dispatch", "moe_combine", "blocks_row_bytes", "blocks_linear", "blocks_dequant", "BLOCK_FORMATS",
            "workspace_bytes", "device_status", "STATIC_WEIGHTS",
            "W4A16Error", "lib", "LIB_PATH", "EXPORTS", "STATUS"]
 
@@ -49,6 +49,9 @@ EXPORTS = {
     "w4a16_moe_dispatch_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
     "w4a16_moe_dispatch": (_I32, [_P, _I64, _I32, _I32, _P, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "w4a16_moe_combine": (_I32, [_P, _I64, _P, _P, _I64, _I32, _I64, _P, _P]),
+    "w4a16_blocks_row_bytes": (_I64, [_I32, _I64]),
+    "w4a16_blocks_linear": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "w4a16_blocks_dequant": (_I32, [_I32, _P, _I64, _I64, _P, _P]),
     "w4a16_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32, _I32]),
     "w4a16_workspace_init": (_I32, [_P, _SZ, _P]),
     "w4a16_device_status": (_I32, [_P]),
@@ -60,6 +63,9 @@ EXPORTS = {
 
 # flags of w4a16_linear_ex / w4a16_linear_gated_ex (include/w4a16.h)
 STATIC_WEIGHTS = 1
+
+# GGUF block formats (W4A16_FORMAT_* in include/w4a16.h)
+BLOCK_FORMATS = {"q4_k": 1, "q5_1": 2}
 
 
 class W4A16Error(RuntimeError):
@@ -197,6 +203,48 @@ def linear(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, group: 
                                  _ptr(ws) if ws is not None else None, ws.numel() if ws is not None else 0, st),
            "w4a16_linear")
     return out
+
+
+def _format(fmt) -> int:
+    if isinstance(fmt, str):
+        if fmt not in BLOCK_FORMATS:
+            raise ValueError(f"unknown block format {fmt!r}")
+        return BLOCK_FORMATS[fmt]
+    return int(fmt)
+
+
+def blocks_row_bytes(fmt, K: int) -> int:
+    """Bytes of one row of K weights in a GGUF block format (-1: not whole blocks)."""
+    return int(lib().w4a16_blocks_row_bytes(_format(fmt), K))
+
+
+def blocks_linear(fmt, x: torch.Tensor, blocks: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """y = x W^T for x fp16 [M, K] and GGUF block-format weights ("q4_k" or
+    "q5_1"), blocks uint8 [N, blocks_row_bytes(fmt, K)]."""
+    _need(x, "x", torch.float16, 2)
+    _need(blocks, "blocks", torch.uint8, 2)
+    M, K = x.shape
+    N = blocks.shape[0]
+    f = _format(fmt)
+    if blocks.shape[1] != blocks_row_bytes(f, K):
+        raise ValueError("blocks: expected [N, blocks_row_bytes(fmt, K)] bytes")
+    out = _out(out, (M, N), x.device, K)
+    _check(lib().w4a16_blocks_linear(f, _ptr(x), _ptr(blocks), _ptr(out), M, N, K, _stream(x.device)),
+           "w4a16_blocks_linear")
+    return out
+
+
+def blocks_dequant(fmt, blocks: torch.Tensor, K: int) -> torch.Tensor:
+    """W^ fp32 [N, K] from GGUF block-format weights uint8 [N, row_bytes]."""
+    _need(blocks, "blocks", torch.uint8, 2)
+    f = _format(fmt)
+    N = blocks.shape[0]
+    if blocks.shape[1] != blocks_row_bytes(f, K):
+        raise ValueError("blocks: expected [N, blocks_row_bytes(fmt, K)] bytes")
+    w = torch.empty((N, K), dtype=torch.float32, device=blocks.device)
+    _check(lib().w4a16_blocks_dequant(f, _ptr(blocks), N, K, _ptr(w), _stream(blocks.device)),
+           "w4a16_blocks_dequant")
+    return w
 
 
 def linear_gated(x: torch.Tensor, qweight_gate: torch.Tensor, scales_gate: torch.Tensor,

@@ -143,6 +143,36 @@ const char* w4a16_status_string(w4a16_status status) {
     return "W4A16: unknown status";
 }
 
+int64_t w4a16_blocks_row_bytes(int32_t format, int64_t K) { return blocks_row_bytes(format, K); }
+
+w4a16_status w4a16_blocks_linear(int32_t format, const uint16_t* x, const uint8_t* blocks, uint16_t* y, int64_t M,
+                                 int64_t N, int64_t K, void* stream) {
+    if (format != W4A16_FORMAT_Q4_K && format != W4A16_FORMAT_Q5_1) return W4A16_ERR_UNSUPPORTED;
+    if (M < 0 || N < 0 || blocks_row_bytes(format, K) < 0) return W4A16_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4A16_OK;
+    if (!y || (K > 0 && (!x || !blocks))) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(blocks) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return W4A16_ERR_CUDA;
+    if (dev->cc_major != 10 || dev->cc_minor != 3) return W4A16_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(uint16_t), st));
+    return blocks_linear_launch(*dev, format, x, blocks, y, M, N, K, st);
+}
+
+w4a16_status w4a16_blocks_dequant(int32_t format, const uint8_t* blocks, int64_t N, int64_t K, float* w,
+                                  void* stream) {
+    if (format != W4A16_FORMAT_Q4_K && format != W4A16_FORMAT_Q5_1) return W4A16_ERR_UNSUPPORTED;
+    if (N < 0 || blocks_row_bytes(format, K) < 0) return W4A16_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return W4A16_OK;
+    if (!blocks || !w) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(blocks) || !aligned16(w)) return W4A16_ERR_MISALIGNED;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return W4A16_ERR_CUDA;
+    if (dev->cc_major != 10 || dev->cc_minor != 3) return W4A16_ERR_UNSUPPORTED;
+    return blocks_dequant_launch(format, blocks, N, K, w, (cudaStream_t)stream);
+}
+
 w4a16_status w4a16_pack(const float* w, int64_t N, int64_t K, int32_t group, uint8_t* qweight, uint16_t* scales,
                         void* stream) {
     if (N < 0 || K < 0) return W4A16_ERR_INVALID_ARG;

@@ -175,6 +175,13 @@ w4a16_status moe_dispatch_launch(const DeviceInfo& dev, const int32_t* ids, int6
 w4a16_status moe_combine_launch(const DeviceInfo& dev, const uint16_t* y_sorted, int64_t R, const int32_t* row_of,
                                 const float* weights, int64_t T, int k, int64_t N, uint16_t* y, cudaStream_t st);
 
+// GGUF block formats (Q4_K, Q5_1): decode GEMV and fp32 dequantizer.
+int64_t blocks_row_bytes(int32_t format, int64_t K);
+w4a16_status blocks_linear_launch(const DeviceInfo& dev, int32_t format, const uint16_t* x, const uint8_t* w,
+                                  uint16_t* y, int64_t M, int64_t N, int64_t K, cudaStream_t st);
+w4a16_status blocks_dequant_launch(int32_t format, const uint8_t* w, int64_t N, int64_t K, float* out,
+                                   cudaStream_t st);
+
 #ifdef W4A16_TEST_HOOKS
 // Test-only build (compiled with -DW4A16_TEST_HOOKS into a separate library):
 // the bounded waits give up after a limit the test chooses, and the TMA
