@@ -14,18 +14,19 @@
 //         of nibbles (weight i < 16: low nibble of byte i, else high nibble
 //         of byte i - 16; bit i of qh on top); W^ = d q + m.
 //
-// GEMV design. A warp's unit is 8 weight rows x 256 k (one Q4_K block or
-// eight Q5_1 blocks per row). Every lane loads its own pieces of the unit
-// straight into registers, one unit ahead, and turns nibbles into exact fp16
-// integers. One mma.sync m16n8k16 per 16 k takes weight rows as A rows 0-7,
-// constant ones as A rows 8-15 and up to 8 tokens of x as B: C rows 0-7 are
-// the integer dot products S = sum x q of a 32-weight sub-block and C rows
-// 8-15 the sums X = sum x over the same k, so the sub-block adds a S + b X
-// (W^ = a q + b) in fp32 with no extra pass over x. A block of 4 warps owns a
-// row-block and splits its units over the warps (and, when row-blocks are
-// few, over the 2 or 4 blocks of a thread-block cluster); the partial sums
-// meet in the shared memory of the cluster's first block and are added in a
-// fixed order, so results are deterministic.
+// GEMV design. A warp's unit is 256 k of 16 weight rows (Q4_K: one block a
+// row) or of 8 rows (Q5_1: eight blocks a row). Each warp copies its units
+// with cp.async into a ring of three stages in shared memory, two units ahead
+// of the one it computes; each lane reads its pieces of a stage and turns
+// nibbles into exact fp16 integers. mma.sync m16n8k16 takes them as A and up
+// to 8 tokens of x as B; an A of constant ones (a second mma for Q4_K, A rows
+// 8-15 for Q5_1) gives the sums X = sum x over
+// each 32-weight sub-block beside the integer dot products S = sum x q, so the
+// sub-block adds a S + b X (W^ = a q + b) in fp32 with no extra pass over x.
+// The grid is persistent: each thread-block cluster (1 to 8 blocks of 8 warps)
+// owns a run of whole row-blocks and its warps stream equal shares of their
+// units; the partial sums meet in the shared memory of the cluster's first
+// block and are added in a fixed order, so results are deterministic.
 #include <type_traits>
 
 #include "internal.cuh"
@@ -36,21 +37,11 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBWarps = 4;             // warps per block
+constexpr int kBWarps = 8;             // warps per block
 constexpr int kBThreads = kBWarps * 32;
-constexpr int kBRows = 8;              // weight rows per row-block
 constexpr int kBUnitK = 256;           // k per unit
 constexpr int kBTokens = 8;            // tokens per launch
 
-struct BlocksArgs {
-    const uint16_t* x;   // fp16 [M, K]
-    const uint8_t* w;    // blocks [N, row_bytes]
-    uint16_t* y;         // fp16 [M, N]
-    int64_t N, K, row_bytes;
-    int M;               // tokens of this launch, 1..8
-    int units;           // ceil(K / 256)
-    int tail;            // Q5_1 blocks in the last unit when K % 256 != 0, else 8
-};
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return __byte_perm(a, b, sel);
@@ -88,82 +79,107 @@ __device__ __forceinline__ void x_pairs(uint32_t u0, uint32_t u1, uint32_t& b0, 
     b1 = prmt(u0, u1, 0x7632);
 }
 
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 // Stores into the shared memory of another block of the cluster.
 __device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
 }
 
 // ------------------------------------------------------------------ Q4_K --
+// A Q4_K unit is 16 rows x 256 k: the lane holds rows gid and gid + 8 (A rows
+// of one mma); a second mma with constant-one A rows gives the sub-block sums
+// of x.
 
-struct Q4KUnit {
-    uint4 head;      // d, dmin, 12 scale bytes of the lane's row
+struct Q4KRow {
+    uint4 head;      // d, dmin, 12 scale bytes
     uint2 qs[4];     // bytes 8 t4 .. 8 t4 + 7 of each 32-byte chunk
 };
+struct Q4KUnit {
+    Q4KRow r[2];     // rows gid and gid + 8
+};
 
-__device__ __forceinline__ void load_unit(Q4KUnit& r, const uint8_t* blk, int t4, bool ok, int) {
-    if (ok) {
-        r.head = __ldg(reinterpret_cast<const uint4*>(blk));
-#pragma unroll
-        for (int c = 0; c < 4; ++c) r.qs[c] = __ldg(reinterpret_cast<const uint2*>(blk + 16 + 32 * c + 8 * t4));
+// Scale (sc) and minimum (mn) bytes of a row's eight sub-blocks: j < 4 in the
+// low six bits of scale bytes 0-3 and 4-7; j >= 4 low four bits from bytes
+// 8-11, top two bits from the top of bytes 0-3 (sc) and 4-7 (mn).
+struct Q4KScales {
+    uint32_t s03, m03, s47, m47;
+};
+
+__device__ __forceinline__ Q4KScales q4k_scales(const uint4& h) {
+    Q4KScales q;
+    q.s03 = h.y & 0x3F3F3F3Fu;
+    q.m03 = h.z & 0x3F3F3F3Fu;
+    q.s47 = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
+    q.m47 = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+    return q;
+}
+
+// Nibbles of bytes (0, 2) and (1, 3) of w (low or high nibbles) as exact fp16 pairs.
+template <int HI>
+__device__ __forceinline__ void q4_pairs(uint32_t w, uint32_t w8, uint32_t& p02, uint32_t& p13) {
+    if (HI) {
+        p02 = hfma2_u32(lop3_and_or(w, 0x00F000F0u, kMagic), kSixteenth, kMinus64);
+        p13 = hfma2_u32(lop3_and_or(w8, 0x00F000F0u, kMagic), kSixteenth, kMinus64);
     } else {
-        r.head = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) r.qs[c] = make_uint2(0, 0);
+        p02 = hsub2_u32(lop3_and_or(w, 0x000F000Fu, kMagic), k1024);
+        p13 = hsub2_u32(lop3_and_or(w8, 0x000F000Fu, kMagic), k1024);
     }
 }
 
-// One Q4_K unit: acc[0..1] (row gid, tokens 2 t4 and 2 t4 + 1) += sum over the
+// One Q4_K unit: acc[r][t] (row gid + 8 r, token 2 t4 + t) += sum over the
 // unit's 256 k of x W^.
-__device__ __forceinline__ void compute_unit(const Q4KUnit& r, const uint16_t* xk, bool xok, float (&acc)[2]) {
-    // sub-block scales sc[j] and minimums mn[j] as bytes: j < 4 in the low six
-    // bits of scale bytes 0-3 and 4-7; j >= 4 low four bits from bytes 8-11,
-    // top two bits from the top of bytes 0-3 (sc) and 4-7 (mn)
-    const uint32_t s03 = r.head.y & 0x3F3F3F3Fu, m03 = r.head.z & 0x3F3F3F3Fu;
-    const uint32_t s47 = (r.head.w & 0x0F0F0F0Fu) | ((r.head.y >> 2) & 0x30303030u);
-    const uint32_t m47 = ((r.head.w >> 4) & 0x0F0F0F0Fu) | ((r.head.z >> 2) & 0x30303030u);
-    float sacc[2] = {0.0f, 0.0f}, macc[2] = {0.0f, 0.0f};
+__device__ __forceinline__ void compute_unit(const Q4KUnit& u, const uint16_t* xk, float (&acc)[2][2]) {
+    const Q4KScales q0 = q4k_scales(u.r[0].head), q1 = q4k_scales(u.r[1].head);
+    float sacc[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}}, macc[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         // x for sub-blocks 2c (low nibbles) and 2c + 1 (high nibbles): eight
         // consecutive values each, at 32 j + 8 t4
-        uint4 xl = make_uint4(0, 0, 0, 0), xh = make_uint4(0, 0, 0, 0);
-        if (xok) {
-            xl = *reinterpret_cast<const uint4*>(xk + 64 * c);
-            xh = *reinterpret_cast<const uint4*>(xk + 64 * c + 32);
-        }
+        const uint4 xl = *reinterpret_cast<const uint4*>(xk + 64 * c);
+        const uint4 xh = *reinterpret_cast<const uint4*>(xk + 64 * c + 32);
 #pragma unroll
         for (int hi = 0; hi < 2; ++hi) {
             const uint4 xv = hi ? xh : xl;
-            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f}, xs[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
-                const uint32_t w = s ? r.qs[c].y : r.qs[c].x;
-                const uint32_t w8 = w >> 8;
-                uint32_t a0, a2;
+                const uint32_t w0 = s ? u.r[0].qs[c].y : u.r[0].qs[c].x;
+                const uint32_t w1 = s ? u.r[1].qs[c].y : u.r[1].qs[c].x;
+                uint32_t a0, a1, a2, a3;
                 if (hi) {
-                    a0 = hfma2_u32(lop3_and_or(w, 0x00F000F0u, kMagic), kSixteenth, kMinus64);
-                    a2 = hfma2_u32(lop3_and_or(w8, 0x00F000F0u, kMagic), kSixteenth, kMinus64);
+                    q4_pairs<1>(w0, w0 >> 8, a0, a2);
+                    q4_pairs<1>(w1, w1 >> 8, a1, a3);
                 } else {
-                    a0 = hsub2_u32(lop3_and_or(w, 0x000F000Fu, kMagic), k1024);
-                    a2 = hsub2_u32(lop3_and_or(w8, 0x000F000Fu, kMagic), k1024);
+                    q4_pairs<0>(w0, w0 >> 8, a0, a2);
+                    q4_pairs<0>(w1, w1 >> 8, a1, a3);
                 }
                 uint32_t b0, b1;
                 x_pairs(s ? xv.z : xv.x, s ? xv.w : xv.y, b0, b1);
-                mma_16816(d, a0, kOnes, a2, kOnes, b0, b1);
+                mma_16816(d, a0, a1, a2, a3, b0, b1);
+                mma_16816(xs, kOnes, kOnes, kOnes, kOnes, b0, b1);
             }
-            const int j = 2 * c + hi;
-            const float sc = byte_to_float(j < 4 ? s03 : s47, j & 3);
-            const float mn = byte_to_float(j < 4 ? m03 : m47, j & 3);
-            sacc[0] = fmaf(sc, d[0], sacc[0]);
-            sacc[1] = fmaf(sc, d[1], sacc[1]);
-            macc[0] = fmaf(mn, d[2], macc[0]);
-            macc[1] = fmaf(mn, d[3], macc[1]);
+            const int j = 2 * c + hi, e = j & 3;
+            const float sc0 = byte_to_float(j < 4 ? q0.s03 : q0.s47, e), mn0 = byte_to_float(j < 4 ? q0.m03 : q0.m47, e);
+            const float sc1 = byte_to_float(j < 4 ? q1.s03 : q1.s47, e), mn1 = byte_to_float(j < 4 ? q1.m03 : q1.m47, e);
+            sacc[0][0] = fmaf(sc0, d[0], sacc[0][0]);
+            sacc[0][1] = fmaf(sc0, d[1], sacc[0][1]);
+            sacc[1][0] = fmaf(sc1, d[2], sacc[1][0]);
+            sacc[1][1] = fmaf(sc1, d[3], sacc[1][1]);
+            macc[0][0] = fmaf(mn0, xs[0], macc[0][0]);
+            macc[0][1] = fmaf(mn0, xs[1], macc[0][1]);
+            macc[1][0] = fmaf(mn1, xs[0], macc[1][0]);
+            macc[1][1] = fmaf(mn1, xs[1], macc[1][1]);
         }
     }
-    const __half2 dd = *reinterpret_cast<const __half2*>(&r.head.x);
-    const float2 df = __half22float2(dd);   // (d, dmin)
-    acc[0] = fmaf(df.x, sacc[0], fmaf(-df.y, macc[0], acc[0]));
-    acc[1] = fmaf(df.x, sacc[1], fmaf(-df.y, macc[1], acc[1]));
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const float2 df = __half22float2(*reinterpret_cast<const __half2*>(&u.r[r].head.x));   // (d, dmin)
+        acc[r][0] = fmaf(df.x, sacc[r][0], fmaf(-df.y, macc[r][0], acc[r][0]));
+        acc[r][1] = fmaf(df.x, sacc[r][1], fmaf(-df.y, macc[r][1], acc[r][1]));
+    }
 }
 
 // ------------------------------------------------------------------ Q5_1 --
@@ -172,19 +188,6 @@ struct Q51Unit {
     uint2 head[8];   // d, m, qh of each of the row's eight blocks
     uint32_t qs[8];  // bytes 4 t4 .. 4 t4 + 3 of each block's nibbles
 };
-
-__device__ __forceinline__ void load_unit(Q51Unit& r, const uint8_t* blk, int t4, bool ok, int nb) {
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-        if (ok && b < nb) {
-            r.head[b] = __ldg(reinterpret_cast<const uint2*>(blk + 24 * b));
-            r.qs[b] = __ldg(reinterpret_cast<const uint32_t*>(blk + 24 * b + 8 + 4 * t4));
-        } else {
-            r.head[b] = make_uint2(0, 0);
-            r.qs[b] = 0;
-        }
-    }
-}
 
 // Two fp16 pairs (bytes 0, 2) and (bytes 1, 3) of the nibbles in v (bits
 // 0-3 of each byte) with fifth bits f (bit e = byte e's), as exact integers.
@@ -196,12 +199,12 @@ __device__ __forceinline__ void q5_pairs(uint32_t v, uint32_t f, uint32_t& p02, 
     p13 = hsub2_u32(lop3_and_or(v >> 8, 0x000F000Fu, f13), k1024);
 }
 
-__device__ __forceinline__ void compute_unit(const Q51Unit& r, const uint16_t* xk, int t4, bool xok, int nb,
+__device__ __forceinline__ void compute_unit(const Q51Unit& r, const uint16_t* xk, int t4, int nb,
                                              float (&acc)[2]) {
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
         uint2 xl = make_uint2(0, 0), xh = make_uint2(0, 0);
-        if (xok && b < nb) {
+        if (b < nb) {
             xl = *reinterpret_cast<const uint2*>(xk + 32 * b);        // weights 4 t4 .. + 3
             xh = *reinterpret_cast<const uint2*>(xk + 32 * b + 16);   // weights 16 + 4 t4 .. + 3
         }
@@ -224,59 +227,230 @@ __device__ __forceinline__ void compute_unit(const Q51Unit& r, const uint16_t* x
 
 // ---------------------------------------------------------------- kernel --
 
+template <int FMT>
+struct Fmt;
+template <>
+struct Fmt<W4A16_FORMAT_Q4_K> {
+    using Unit = Q4KUnit;
+    static constexpr int kRows = 16;       // rows per row-block (two per lane)
+    static constexpr int kUnitBytes = 144; // bytes of a unit in one row
+    static constexpr int kPiece = 16;      // bytes per cp.async
+    static constexpr int kStride = 160;    // shared-memory bytes per row of a stage (conflict-free 8-byte reads)
+    static constexpr int kXStep = 8;       // x offset of lane t4 inside a sub-block, per t4
+};
+template <>
+struct Fmt<W4A16_FORMAT_Q5_1> {
+    using Unit = Q51Unit;
+    static constexpr int kRows = 8;        // one row per lane, constant ones in A rows 8-15
+    static constexpr int kUnitBytes = 192;
+    static constexpr int kPiece = 8;       // rows of 24-byte blocks need not start 16-byte aligned
+    static constexpr int kStride = 208;
+    static constexpr int kXStep = 4;
+};
+
+constexpr int kStages = 3;   // units in flight per warp (a ring in shared memory)
+
+template <int FMT>
+constexpr int stage_bytes() {
+    return Fmt<FMT>::kRows * Fmt<FMT>::kStride;
+}
+
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src, uint32_t src_size) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_size) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
+    return r;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 r;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a));
+    return r;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t r;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(a));
+    return r;
+}
+
+// The lane's part of a unit from its shared-memory stage (rows kStride apart).
+__device__ __forceinline__ void read_unit(Q4KUnit& u, uint32_t st, int gid, int t4) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const uint32_t row = st + (uint32_t)(gid + 8 * r) * Fmt<W4A16_FORMAT_Q4_K>::kStride;
+        u.r[r].head = lds128(row);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) u.r[r].qs[c] = lds64(row + 16 + 32 * c + 8 * t4);
+    }
+}
+__device__ __forceinline__ void read_unit(Q51Unit& u, uint32_t st, int gid, int t4) {
+    const uint32_t row = st + (uint32_t)gid * Fmt<W4A16_FORMAT_Q5_1>::kStride;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        u.head[b] = lds64(row + 24 * b);
+        u.qs[b] = lds32(row + 24 * b + 8 + 4 * t4);
+    }
+}
+
+// Work split. Row-block r covers rows [kRows r, kRows (r + 1)); its units are
+// the KU = ceil(K / 256) stretches of 256 k. Cluster cl owns the row-blocks
+// [nrb cl / ncl, nrb (cl + 1) / ncl) and lists their units row-block by
+// row-block; warp v of the cluster's V takes the contiguous run [T v / V,
+// T (v + 1) / V) of that list (T units), so every warp streams the same
+// number of units, give or take one, across row-block boundaries. Each run
+// leaves one partial sum per row-block it touches (at most J) in the shared
+// memory of the cluster's first block.
+struct StreamArgs {
+    const uint16_t* x;   // fp16 [M, K]
+    const uint8_t* w;    // blocks [N, row_bytes]
+    uint16_t* y;         // fp16 [M, N]
+    int64_t N, K, row_bytes;
+    int M;               // tokens of this launch, 1..8
+    int KU;              // units per row-block
+    int tail;            // Q5_1 blocks in a row's last unit (8 when K % 256 == 0)
+    int64_t rb_first;    // first row-block of this launch
+    int nrb, ncl, J;     // row-blocks, clusters, partial slots per warp
+};
+
+__host__ __device__ __forceinline__ int64_t run_begin(int64_t T, int v, int V) { return T * v / V; }
+
 template <int FMT, int C>
-__global__ void __launch_bounds__(kBThreads) blocks_gemv_kernel(const BlocksArgs a) {
-    __shared__ float red[C * kBWarps][32][2];
+__global__ void __launch_bounds__(kBThreads, 2) blocks_gemv_kernel(const StreamArgs a) {
+    using F = Fmt<FMT>;
+    constexpr int RL = F::kRows / 8;   // rows per lane
+    constexpr int V = C * kBWarps;
+    // [V][J][32][2 RL] partial sums (used in the cluster's first block), then
+    // each warp's ring of weight stages
+    extern __shared__ __align__(16) float part[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gid = lane >> 2, t4 = lane & 3;
     const int rank = C > 1 ? (int)cluster_rank() : 0;
-    const int64_t rb = blockIdx.x / C;
-    const int64_t row = rb * kBRows + gid;
-    const bool row_ok = row < a.N;
-    const bool xok = gid < a.M;
-    const int v = rank * kBWarps + warp, V = C * kBWarps;
-    const uint8_t* wrow = a.w + (row_ok ? row : 0) * a.row_bytes;
-    constexpr int kUnitBytes = FMT == W4A16_FORMAT_Q4_K ? 144 : 192;
-    // the lane's x: token gid, at 8 t4 (Q4_K) or 4 t4 (Q5_1) inside each sub-block
-    const uint16_t* xrow = a.x + (int64_t)(xok ? gid : 0) * a.K + (FMT == W4A16_FORMAT_Q4_K ? 8 * t4 : 4 * t4);
+    const int cl = blockIdx.x / C;
+    const int64_t rb0 = a.rb_first + (int64_t)cl * a.nrb / a.ncl, rb1 = a.rb_first + (int64_t)(cl + 1) * a.nrb / a.ncl;
+    const int64_t T = (rb1 - rb0) * a.KU;
+    const int v = rank * kBWarps + warp;
+    const int64_t i0 = run_begin(T, v, V), i1 = run_begin(T, v + 1, V);
+    const int KU = a.KU;
+    // the lane's x: token gid, at kXStep * t4 inside each sub-block. Lanes past
+    // the last token read the last token instead: their columns of the
+    // product are never stored, and no load is predicated.
+    const int tok = gid < a.M ? gid : a.M - 1;
+    const uint16_t* xrow = a.x + (int64_t)tok * a.K + F::kXStep * t4;
+    // this lane's first partial slot, in the shared memory of the cluster's first block
+    const uint32_t own = (uint32_t)(v * a.J * 32 + lane) * (8 * RL);
+    const uint32_t part_base = (C > 1 ? cluster_map(smem_u32(part), 0) : smem_u32(part)) + own;
 
-    float acc[2] = {0.0f, 0.0f};
-    using Unit = typename std::conditional<FMT == W4A16_FORMAT_Q4_K, Q4KUnit, Q51Unit>::type;
-    Unit cur, nxt;
-    const int last = a.units - 1;
-    if (v < a.units) load_unit(cur, wrow + (int64_t)v * kUnitBytes, t4, row_ok, v == last ? a.tail : 8);
-    for (int u = v; u < a.units; u += V) {
-        const int un = u + V;
-        if (un < a.units) load_unit(nxt, wrow + (int64_t)un * kUnitBytes, t4, row_ok, un == last ? a.tail : 8);
-        if constexpr (FMT == W4A16_FORMAT_Q4_K)
-            compute_unit(cur, xrow + (int64_t)u * kBUnitK, xok, acc);
-        else
-            compute_unit(cur, xrow + (int64_t)u * kBUnitK, t4, xok, u == last ? a.tail : 8, acc);
-        cur = nxt;
-    }
-
-    // partial sums of every warp of the cluster meet in the first block
-    if constexpr (C == 1) {
-        red[v][lane][0] = acc[0];
-        red[v][lane][1] = acc[1];
-        __syncthreads();
-    } else {
-        const uint32_t base = cluster_map(smem_u32(&red[v][lane][0]), 0);
-        st_cluster_f32(base, acc[0]);
-        st_cluster_f32(base + 4, acc[1]);
-        cluster_sync();
-    }
-    if (rank != 0 || warp != 0) return;
-    float s0 = 0.0f, s1 = 0.0f;
+    // weights: a ring of kStages units per warp in shared memory, filled by
+    // cp.async kStages - 1 units ahead of the unit being computed; the load
+    // position (row-block lr, unit ls) runs ahead of the compute position (cr, cs)
+    const uint32_t ring = smem_u32(part) + (uint32_t)a.J * V * 32 * (8 * RL) +
+                          (uint32_t)(warp * kStages) * stage_bytes<FMT>();
+    int lr = (int)(i0 / KU), ls = (int)(i0 % KU);
+    int cr = lr, cs = ls;
+    const int first = cr;
+    constexpr int P = F::kUnitBytes / F::kPiece;   // pieces per row of a unit
+    auto issue = [&](int stage) {
+        const uint32_t dst0 = ring + (uint32_t)stage * stage_bytes<FMT>();
+        const int valid = FMT == W4A16_FORMAT_Q4_K ? F::kUnitBytes : (ls == KU - 1 ? a.tail : 8) * 24;
 #pragma unroll
-    for (int i = 0; i < C * kBWarps; ++i) {
-        s0 += red[i][lane][0];
-        s1 += red[i][lane][1];
+        for (int i = 0; i < (F::kRows * P + 31) / 32; ++i) {
+            const int idx = i * 32 + lane;
+            if (idx < F::kRows * P) {
+                const int r = idx / P, pc = idx % P;
+                const int64_t row = (rb0 + lr) * F::kRows + r;
+                const bool ok = row < a.N && pc * F::kPiece < valid;
+                const uint8_t* src = a.w + (ok ? row * a.row_bytes + (int64_t)ls * F::kUnitBytes + pc * F::kPiece : 0);
+                const uint32_t dst = dst0 + (uint32_t)(r * F::kStride + pc * F::kPiece);
+                if constexpr (F::kPiece == 16)
+                    cp_async_16(dst, src, ok ? 16u : 0u);
+                else
+                    cp_async_8(dst, src, ok ? 8u : 0u);
+            }
+        }
+        if (++ls == KU) {
+            ls = 0;
+            ++lr;
+        }
+    };
+#pragma unroll
+    for (int i = 0; i < kStages - 1; ++i) {
+        if (i0 + i < i1) issue(i);
+        cp_async_commit();
     }
-    if (!row_ok) return;
-    const int m0 = 2 * t4;
-    if (m0 < a.M) a.y[(int64_t)m0 * a.N + row] = __half_as_ushort(__float2half_rn(s0));
-    if (m0 + 1 < a.M) a.y[(int64_t)(m0 + 1) * a.N + row] = __half_as_ushort(__float2half_rn(s1));
+    float acc[RL][2] = {};
+    int stage = 0;
+    for (int64_t i = i0; i < i1; ++i) {
+        if (i + kStages - 1 < i1) issue(stage == 0 ? kStages - 1 : stage - 1);
+        cp_async_commit();
+        cp_async_wait<kStages - 1>();
+        __syncwarp();
+        typename F::Unit u;
+        read_unit(u, ring + (uint32_t)stage * stage_bytes<FMT>(), gid, t4);
+        __syncwarp();   // the stage is refilled next round
+        if constexpr (FMT == W4A16_FORMAT_Q4_K)
+            compute_unit(u, xrow + (int64_t)cs * kBUnitK, acc);
+        else
+            compute_unit(u, xrow + (int64_t)cs * kBUnitK, t4, cs == KU - 1 ? a.tail : 8, acc[0]);
+        // the run leaves this row-block: park its partial sum
+        if (cs == KU - 1 || i + 1 == i1) {
+            const uint32_t p = part_base + (uint32_t)((cr - first) * 32) * (8 * RL);
+#pragma unroll
+            for (int r = 0; r < RL; ++r) {
+                if constexpr (C > 1) {
+                    st_cluster_f32(p + 8 * r, acc[r][0]);
+                    st_cluster_f32(p + 8 * r + 4, acc[r][1]);
+                } else {
+                    st_shared_f32(p + 8 * r, acc[r][0]);
+                    st_shared_f32(p + 8 * r + 4, acc[r][1]);
+                }
+                acc[r][0] = acc[r][1] = 0.0f;
+            }
+        }
+        if (++cs == KU) {
+            cs = 0;
+            ++cr;
+        }
+        if (++stage == kStages) stage = 0;
+    }
+    cp_async_wait<0>();
+
+    if constexpr (C > 1)
+        cluster_sync();
+    else
+        __syncthreads();
+    if (rank != 0) return;
+    // the first block adds each row-block's partial sums in warp order
+    for (int64_t r = warp; r < rb1 - rb0; r += kBWarps) {
+        // the warps whose runs touch units [r KU, (r + 1) KU)
+        const int64_t lo = r * KU, hi = (r + 1) * KU;
+        int u = (int)(((lo + 1) * V + T - 1) / T) - 1;   // the run that holds unit lo
+        float s[RL][2] = {};
+        for (; u < V; ++u) {
+            const int64_t b0 = run_begin(T, u, V), b1 = run_begin(T, u + 1, V);
+            if (b0 >= hi) break;
+            if (b1 <= b0 || b1 <= lo) continue;
+            const float* p = part + ((int64_t)(u * a.J + (r - b0 / KU)) * 32 + lane) * (2 * RL);
+#pragma unroll
+            for (int q = 0; q < RL; ++q) {
+                s[q][0] += p[2 * q];
+                s[q][1] += p[2 * q + 1];
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < RL; ++q) {
+            const int64_t n = (rb0 + r) * F::kRows + gid + 8 * q;
+            if (n >= a.N) continue;
+            const int m0 = 2 * t4;
+            if (m0 < a.M) a.y[(int64_t)m0 * a.N + n] = __half_as_ushort(__float2half_rn(s[q][0]));
+            if (m0 + 1 < a.M) a.y[(int64_t)(m0 + 1) * a.N + n] = __half_as_ushort(__float2half_rn(s[q][1]));
+        }
+    }
 }
 
 // ------------------------------------------------------------- dequantize --
@@ -328,33 +502,135 @@ __global__ void __launch_bounds__(256) blocks_dequant_kernel(const uint8_t* __re
     for (int i = 0; i < 8; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
-template <int FMT>
-cudaError_t launch_gemv(const BlocksArgs& a, int c, cudaStream_t st) {
-    const int64_t nrb = (a.N + kBRows - 1) / kBRows;
+template <int FMT, int C>
+cudaError_t launch_c(const StreamArgs& a, size_t smem, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(nrb * c));
+    cfg.gridDim = dim3((unsigned)(a.ncl * C));
     cfg.blockDim = dim3(kBThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = (unsigned)c;
+    at[0].val.clusterDim.x = (unsigned)C;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
-    cfg.numAttrs = c > 1 ? 1 : 0;
-    if (c == 1) return cudaLaunchKernelEx(&cfg, blocks_gemv_kernel<FMT, 1>, a);
-    if (c == 2) return cudaLaunchKernelEx(&cfg, blocks_gemv_kernel<FMT, 2>, a);
-    return cudaLaunchKernelEx(&cfg, blocks_gemv_kernel<FMT, 4>, a);
+    cfg.numAttrs = C > 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, blocks_gemv_kernel<FMT, C>, a);
 }
 
-// Blocks per cluster: 1, or 2 / 4 when row-blocks are too few to give every SM
-// about six blocks and each warp still gets two units or more.
-int cluster_size(const DeviceInfo& dev, int64_t N, int64_t units) {
-    const int64_t nrb = (N + kBRows - 1) / kBRows;
-    int c = 1;
-    while (c < 4 && nrb * c < 6LL * dev.sms && units >= 2LL * kBWarps * 2 * c) c *= 2;
-    return c;
+constexpr size_t kPartSmem = 32 * 1024;   // largest partial-sum area of a block
+
+// Dynamic shared memory of a block: the partial-sum area, then the weight rings.
+template <int FMT>
+constexpr size_t ring_bytes() {
+    return (size_t)kBWarps * kStages * stage_bytes<FMT>();
+}
+constexpr int kClusterSizes[4] = {1, 2, 4, 8};
+
+// Per device and format: the dynamic shared-memory limit set once, and how
+// many clusters of each size fit on the GPU at once with that much memory.
+struct ClusterFit {
+    int count[4];
+};
+
+template <int FMT>
+const ClusterFit& cluster_fit(const DeviceInfo& dev, cudaError_t* err) {
+    static PerDeviceOnce once;
+    static ClusterFit fit[kMaxDevices];
+    *err = once.run(dev.device, [&]() -> cudaError_t {
+        cudaError_t e = cudaSuccess;
+        e = cudaFuncSetAttribute(blocks_gemv_kernel<FMT, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kPartSmem + ring_bytes<FMT>()));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(blocks_gemv_kernel<FMT, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kPartSmem + ring_bytes<FMT>()));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(blocks_gemv_kernel<FMT, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kPartSmem + ring_bytes<FMT>()));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(blocks_gemv_kernel<FMT, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kPartSmem + ring_bytes<FMT>()));
+        if (e != cudaSuccess) return e;
+        for (int i = 0; i < 4; ++i) {
+            const int c = kClusterSizes[i];
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(c * dev.sms));
+            cfg.blockDim = dim3(kBThreads);
+            cfg.dynamicSmemBytes = kPartSmem + ring_bytes<FMT>();
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = (unsigned)c;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            int m = 0;
+            const cudaError_t q =
+                c == 1 ? cudaOccupancyMaxActiveClusters(&m, blocks_gemv_kernel<FMT, 1>, &cfg)
+                : c == 2 ? cudaOccupancyMaxActiveClusters(&m, blocks_gemv_kernel<FMT, 2>, &cfg)
+                : c == 4 ? cudaOccupancyMaxActiveClusters(&m, blocks_gemv_kernel<FMT, 4>, &cfg)
+                         : cudaOccupancyMaxActiveClusters(&m, blocks_gemv_kernel<FMT, 8>, &cfg);
+            if (q != cudaSuccess) {
+                (void)cudaGetLastError();  // not a sticky error: this cluster size is just not used
+                m = 0;
+            }
+            fit[dev.device].count[i] = m;
+        }
+        return cudaSuccess;
+    });
+    return fit[dev.device];
+}
+
+// Runs the GEMV for up to 8 tokens. Rows go in chunks small enough that the
+// partial sums of a cluster fit its first block's shared memory.
+template <int FMT>
+w4a16_status run_gemv(const DeviceInfo& dev, StreamArgs a, cudaStream_t st) {
+    using F = Fmt<FMT>;
+    constexpr int RL = F::kRows / 8;
+    cudaError_t e = cudaSuccess;
+    const ClusterFit& fit = cluster_fit<FMT>(dev, &e);
+    if (e != cudaSuccess) return cuda_status(e, "blocks gemv: set-up");
+    const int64_t nrb_all = (a.N + F::kRows - 1) / F::kRows;
+    // the cluster size that gives the fewest units to the busiest warp
+    int best = -1;
+    double best_load = 0.0;
+    int64_t best_per_cl = 0;
+    for (int i = 0; i < 4; ++i) {
+        const int c = kClusterSizes[i], m = fit.count[i], V = c * kBWarps;
+        const size_t slot = (size_t)V * 32 * 2 * RL * sizeof(float);   // one partial slot of every warp
+        const int64_t jmax = (int64_t)(kPartSmem / slot);
+        // a run of L units touches at most (L - 1) / KU + 2 row-blocks, which
+        // must not exceed jmax: a cluster takes at most per_cl row-blocks a launch
+        const int64_t per_cl = jmax >= 2 ? ((jmax - 1) * a.KU - 1) * V / a.KU : 0;
+        if (m <= 0 || per_cl < 1) continue;
+        const int64_t ncl = nrb_all < m ? nrb_all : m;
+        int64_t rbc = (nrb_all + ncl - 1) / ncl;
+        if (rbc > per_cl) rbc = per_cl;
+        const double load = (double)rbc * a.KU / V;
+        if (best < 0 || load < best_load * 0.97) {
+            best = i;
+            best_load = load;
+            best_per_cl = per_cl;
+        }
+    }
+    if (best < 0) return W4A16_ERR_UNSUPPORTED;
+    const int c = kClusterSizes[best], V = c * kBWarps;
+    const int64_t maxcl = fit.count[best], per_cl = best_per_cl;
+    const size_t slot = (size_t)V * 32 * 2 * RL * sizeof(float);
+    for (int64_t r0 = 0; r0 < nrb_all;) {
+        const int64_t nrb = nrb_all - r0 < maxcl * per_cl ? nrb_all - r0 : maxcl * per_cl;
+        StreamArgs b = a;
+        b.rb_first = r0;
+        b.nrb = (int)nrb;
+        b.ncl = (int)(nrb < maxcl ? nrb : maxcl);
+        const int64_t T = (nrb + b.ncl - 1) / b.ncl * a.KU;   // the most units a cluster gets
+        b.J = (int)((T + V - 1) / V / a.KU + 2);
+        const size_t smem = (size_t)b.J * slot + ring_bytes<FMT>();
+        e = c == 1 ? launch_c<FMT, 1>(b, smem, st)
+            : c == 2 ? launch_c<FMT, 2>(b, smem, st)
+            : c == 4 ? launch_c<FMT, 4>(b, smem, st)
+                     : launch_c<FMT, 8>(b, smem, st);
+        if (e != cudaSuccess) return cuda_status(e, "blocks gemv: kernel launch");
+        r0 += nrb;
+    }
+    return W4A16_OK;
 }
 
 }  // namespace
@@ -369,22 +645,23 @@ int64_t blocks_row_bytes(int32_t format, int64_t K) {
 w4a16_status blocks_linear_launch(const DeviceInfo& dev, int32_t format, const uint16_t* x, const uint8_t* w,
                                   uint16_t* y, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
     const int64_t units = (K + kBUnitK - 1) / kBUnitK;
-    if (units > 0x7fffffffLL || (N + kBRows - 1) / kBRows * 4 > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
-    const int c = cluster_size(dev, N, units);
-    BlocksArgs a;
+    if (units > 0x7fffffffLL || (N + 7) / 8 > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
+    StreamArgs a;
     a.w = w;
     a.N = N;
     a.K = K;
     a.row_bytes = blocks_row_bytes(format, K);
-    a.units = (int)units;
+    a.KU = (int)units;
     a.tail = K % kBUnitK ? (int)(K % kBUnitK) / 32 : 8;
+    a.rb_first = 0;
+    a.nrb = a.ncl = a.J = 0;
     for (int64_t m0 = 0; m0 < M; m0 += kBTokens) {
         a.x = x + m0 * K;
         a.y = y + m0 * N;
         a.M = (int)(M - m0 < kBTokens ? M - m0 : kBTokens);
-        const cudaError_t e = format == W4A16_FORMAT_Q4_K ? launch_gemv<W4A16_FORMAT_Q4_K>(a, c, st)
-                                                          : launch_gemv<W4A16_FORMAT_Q5_1>(a, c, st);
-        if (e != cudaSuccess) return cuda_status(e, "blocks gemv: kernel launch");
+        const w4a16_status r = format == W4A16_FORMAT_Q4_K ? run_gemv<W4A16_FORMAT_Q4_K>(dev, a, st)
+                                                           : run_gemv<W4A16_FORMAT_Q5_1>(dev, a, st);
+        if (r != W4A16_OK) return r;
     }
     return W4A16_OK;
 }
