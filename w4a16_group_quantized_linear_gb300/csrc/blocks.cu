@@ -455,19 +455,21 @@ __global__ void __launch_bounds__(kBThreads, 2) blocks_gemv_kernel(const StreamA
 
 // ------------------------------------------------------------- dequantize --
 
-// One thread per 32 weights (a Q4_K sub-block or a Q5_1 block): W^ in fp32,
-// step and offset exact in fp32, step * q exact, one rounding in the sum.
+// One thread per 4 consecutive weights, so that a warp stores 512 contiguous
+// bytes: W^ in fp32 with the step and offset exact in fp32, step * q exact,
+// one rounding in the sum.
 template <int FMT>
 __global__ void __launch_bounds__(256) blocks_dequant_kernel(const uint8_t* __restrict__ w, float* __restrict__ out,
                                                              int64_t N, int64_t K, int64_t row_bytes) {
-    const int64_t per_row = K / 32;
+    const int64_t per_row = K / 4;
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= N * per_row) return;
-    const int64_t n = t / per_row, g = t % per_row;
-    float v[32];
+    const int64_t n = t / per_row;
+    const int k = (int)(t % per_row) * 4;
+    float v[4];
     if constexpr (FMT == W4A16_FORMAT_Q4_K) {
-        const uint8_t* blk = w + n * row_bytes + (g / 8) * 144;
-        const int j = (int)(g % 8), c = j / 2, hi = j % 2;
+        const uint8_t* blk = w + n * row_bytes + (int64_t)(k / 256) * 144;
+        const int i = k % 256, j = i / 32, c = i / 64, r = i % 64;
         const uint4 head = __ldg(reinterpret_cast<const uint4*>(blk));
         const uint32_t s03 = head.y & 0x3F3F3F3Fu, m03 = head.z & 0x3F3F3F3Fu;
         const uint32_t s47 = (head.w & 0x0F0F0F0Fu) | ((head.y >> 2) & 0x30303030u);
@@ -475,31 +477,23 @@ __global__ void __launch_bounds__(256) blocks_dequant_kernel(const uint8_t* __re
         const float sc = byte_to_float(j < 4 ? s03 : s47, j & 3), mn = byte_to_float(j < 4 ? m03 : m47, j & 3);
         const float2 df = __half22float2(*reinterpret_cast<const __half2*>(&head.x));
         const float step = __fmul_rn(df.x, sc), off = __fmul_rn(df.y, mn);
-        const uint4* qs = reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
-        const uint4 q0 = __ldg(qs), q1 = __ldg(qs + 1);
-        const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        // weights 64c + (r mod 32) .. + 3: four bytes, low nibbles if r < 32, else high
+        const uint32_t q4 = __ldg(reinterpret_cast<const uint32_t*>(blk + 16 + 32 * c + (r % 32))) >> (r < 32 ? 0 : 4);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const uint32_t q = (words[i / 4] >> (8 * (i % 4) + 4 * hi)) & 0xFu;
-            v[i] = __fsub_rn(__fmul_rn(step, (float)q), off);
-        }
+        for (int e = 0; e < 4; ++e) v[e] = __fsub_rn(__fmul_rn(step, (float)((q4 >> (8 * e)) & 0xFu)), off);
     } else {
-        const uint8_t* blk = w + n * row_bytes + g * 24;
+        const uint8_t* blk = w + n * row_bytes + (int64_t)(k / 32) * 24;
+        const int i = k % 32;
         const uint2 head = __ldg(reinterpret_cast<const uint2*>(blk));
-        const uint2 qa = __ldg(reinterpret_cast<const uint2*>(blk + 8)), qb = __ldg(reinterpret_cast<const uint2*>(blk + 16));
-        const uint32_t words[4] = {qa.x, qa.y, qb.x, qb.y};
         const float2 dm = __half22float2(*reinterpret_cast<const __half2*>(&head.x));
+        const uint32_t q4 = __ldg(reinterpret_cast<const uint32_t*>(blk + 8 + (i % 16))) >> (i < 16 ? 0 : 4);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int byte = i % 16;
-            const uint32_t nib = (words[byte / 4] >> (8 * (byte % 4) + (i < 16 ? 0 : 4))) & 0xFu;
-            const uint32_t q = nib | (((head.y >> i) & 1u) << 4);
-            v[i] = __fadd_rn(__fmul_rn(dm.x, (float)q), dm.y);
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t q = ((q4 >> (8 * e)) & 0xFu) | (((head.y >> (i + e)) & 1u) << 4);
+            v[e] = __fadd_rn(__fmul_rn(dm.x, (float)q), dm.y);
         }
     }
-    float4* o = reinterpret_cast<float4*>(out + n * K + g * 32);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    *reinterpret_cast<float4*>(out + n * K + k) = make_float4(v[0], v[1], v[2], v[3]);
 }
 
 template <int FMT, int C>
@@ -668,7 +662,7 @@ w4a16_status blocks_linear_launch(const DeviceInfo& dev, int32_t format, const u
 
 w4a16_status blocks_dequant_launch(int32_t format, const uint8_t* w, int64_t N, int64_t K, float* out,
                                    cudaStream_t st) {
-    const int64_t threads = N * (K / 32);
+    const int64_t threads = N * (K / 4);
     if (threads == 0) return W4A16_OK;
     const int64_t grid = (threads + 255) / 256;
     if (grid > 0x7fffffffLL) return W4A16_ERR_UNSUPPORTED;
