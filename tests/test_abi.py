@@ -127,3 +127,36 @@ def test_grouped_gather_validation(lib):
     assert lib.w4a16_grouped_linear_gather(p, 64, p, p, p, p, p, 4, 16, 8, 100, 32, None) == 1
     # nothing to do
     assert lib.w4a16_grouped_linear_gather(p, 64, p, p, p, p, p, 4, 0, 8, 128, 32, None) == 0
+
+
+def test_blocks_validation(lib):
+    """GGUF block formats: row sizes and the host checks, all before any device work."""
+    import oracle
+
+    p, q = _fake(1 << 20), _fake((1 << 20) + 8)
+    Q4K, Q51 = 1, 2
+    for fmt, name in ((Q4K, "q4_k"), (Q51, "q5_1")):
+        for K in (0, 32, 96, 256, 288, 5120, 17408, 100, -256):
+            assert lib.w4a16_blocks_row_bytes(fmt, K) == oracle.blocks_row_bytes(name, K), (name, K)
+    assert lib.w4a16_blocks_row_bytes(Q4K, 5120) == 20 * 144 and lib.w4a16_blocks_row_bytes(Q51, 5120) == 160 * 24
+    assert lib.w4a16_blocks_row_bytes(3, 256) == -1
+    # unknown format; K not whole blocks; negative sizes; null pointers; misaligned pointers
+    assert lib.w4a16_blocks_linear(3, p, p, p, 1, 8, 256, None) == 2
+    assert lib.w4a16_blocks_linear(Q4K, p, p, p, 1, 8, 288, None) == 1
+    assert lib.w4a16_blocks_linear(Q51, p, p, p, 1, 8, 48, None) == 1
+    assert lib.w4a16_blocks_linear(Q4K, p, p, p, -1, 8, 256, None) == 1
+    assert lib.w4a16_blocks_linear(Q4K, None, p, p, 1, 8, 256, None) == 1
+    assert lib.w4a16_blocks_linear(Q4K, p, p, None, 1, 8, 256, None) == 1
+    assert lib.w4a16_blocks_linear(Q4K, q, p, p, 1, 8, 256, None) == 3
+    assert lib.w4a16_blocks_linear(Q51, p, q, p, 1, 8, 64, None) == 3
+    # nothing to do
+    assert lib.w4a16_blocks_linear(Q4K, p, p, p, 0, 8, 256, None) == 0
+    assert lib.w4a16_blocks_linear(Q4K, p, p, p, 1, 0, 256, None) == 0
+    # the dequantizer
+    assert lib.w4a16_blocks_dequant(3, p, 8, 256, p, None) == 2
+    assert lib.w4a16_blocks_dequant(Q4K, p, 8, 300, p, None) == 1
+    assert lib.w4a16_blocks_dequant(Q4K, p, -1, 256, p, None) == 1
+    assert lib.w4a16_blocks_dequant(Q4K, None, 8, 256, p, None) == 1
+    assert lib.w4a16_blocks_dequant(Q4K, p, 8, 256, q, None) == 3
+    assert lib.w4a16_blocks_dequant(Q4K, p, 0, 256, p, None) == 0
+    assert lib.w4a16_blocks_dequant(Q51, p, 8, 0, p, None) == 0
