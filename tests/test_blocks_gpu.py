@@ -50,8 +50,8 @@ def test_dequant_bit_exact(w4, cuda_device, fmt, N, K):
 @pytest.mark.parametrize("fmt", ["q4_k", "q5_1"])
 @pytest.mark.parametrize("M", [1, 2, 3, 8, 9, 17])
 def test_small_shapes_all_M(w4, cuda_device, fmt, M):
-    # 203 rows: 25 full row-blocks and a ragged one; 11 units of 256 k, split
-    # over 4 warps unevenly
+    # 203 rows: full row-blocks and a ragged last one; 11 units of 256 k a row,
+    # so the warps' runs of units cross row-block boundaries
     print(fmt, M, "max err/bound", _check(w4, cuda_device, fmt, M, 203, 2816, 10 + M))
 
 
@@ -64,7 +64,8 @@ def test_short_and_ragged_k(w4, cuda_device, fmt, K):
 
 @pytest.mark.parametrize("fmt", ["q4_k", "q5_1"])
 def test_cluster_split(w4, cuda_device, fmt):
-    # 125 row-blocks of 32 units: split over clusters of 4 blocks
+    # few row-blocks of 32 units each: every row-block is shared by several warps
+    # and blocks of a cluster
     for M in (1, 4):
         print(fmt, M, "max err/bound", _check(w4, cuda_device, fmt, M, 1000, 8192, 40 + M, threads=8))
 
@@ -129,3 +130,9 @@ def test_edge_cases_and_errors(w4, cuda_device):
     assert lib.w4a16_blocks_row_bytes(Q4K, 512) == 288 and lib.w4a16_blocks_row_bytes(Q51, 64) == 48
     assert lib.w4a16_blocks_row_bytes(Q4K, 100) == -1 and lib.w4a16_blocks_row_bytes(9, 256) == -1
     assert w4.device_status() == 0
+
+
+def test_many_rows_take_several_launches(w4, cuda_device):
+    # 2500 row-blocks at 8 tokens: more than one launch's clusters may hold, so the
+    # rows go in two launches
+    print("q4_k M=8 N=40000 max err/bound", _check(w4, cuda_device, "q4_k", 8, 40000, 5120, 70, threads=8))
