@@ -116,3 +116,16 @@ def test_moe_dispatch_and_combine_write_only_their_outputs(w4, cuda_device):
     assert _tail_intact(y_buf, T * K)
     y_ref, a = oracle.moe_combine(xs.cpu().numpy(), row_of.cpu().numpy(), wts.cpu().numpy())
     assert np.all(np.abs(y_view.cpu().numpy().astype(np.float64) - y_ref) <= oracle.combine_tolerance(y_ref, a, k))
+
+
+@pytest.mark.parametrize("fmt,M,N,K", [("q4_k", 3, 203, 2816), ("q5_1", 9, 77, 1056), ("q4_k", 1, 1000, 8192)])
+def test_blocks_gemv_writes_only_its_output(w4, cuda_device, fmt, M, N, K):
+    r = workloads.rng(M + N + K)
+    wb = workloads.raw_blocks(r, fmt, N, K)
+    x = workloads.activations(r, M, K)
+    buf, out = _guarded(M, N, cuda_device)
+    w4.blocks_linear(fmt, to_dev(x, cuda_device), to_dev(wb, cuda_device), out=out)
+    w4.device_status()
+    assert _tail_intact(buf, M * N)
+    y_ref, a = oracle.blocks_linear(fmt, x, wb)
+    assert_within_bound(out.cpu().numpy(), y_ref, a, f"{fmt} canary")
